@@ -1,0 +1,178 @@
+/*
+ * sse.h -- C ABI of libsse, a GB300 (sm_103a) CUDA library for the Sparse
+ * State Expansion (SSE) linear-attention layer.
+ *
+ * Method: "Scaling Linear Attention with Sparse State Expansion" (arXiv
+ * 2507.16577; close-reading notes, sections 2.3-2.6).  Per token t and head
+ * h, with N routed partition states S_i (each c x d, key rows by value
+ * columns) and one always-on shared state S_N:
+ *
+ *   e_t  = softmax(router_logits_t)              over the N partitions (eq. 9)
+ *   T_t  = the top_k partitions by logit, equal logits ordered by
+ *          ascending partition index                                  (eq. 10)
+ *   a_t  = exp(log_gate_t), one decay per key row (diagonal gate, eq. 6)
+ *   S_i <- diag(a_t) S_i + e_t[i] k_t^T v_t      for i in T_t         (eq. 13)
+ *   S_i    unchanged (no write, no decay)        for i not in T_t
+ *   S_N <- diag(a_t) S_N + ks_t^T v_t            (shared, section 2.5)
+ *   o_t  = sum_{i in T_t} e_t[i] (scale q_t) S_i + (scale qs_t) S_N   (eq. 14)
+ *
+ * e_t is the full-N softmax (not renormalised over T_t).  k_t is taken as
+ * given (the caller applies the key softmax of eq. 12); q is linear.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - All array pointers are DEVICE pointers owned by the caller.  The library
+ *   allocates no device or host memory, keeps no state between calls and
+ *   never synchronizes the stream (except sse_read_device_status).  Calls are
+ *   asynchronous on `stream` (NULL = legacy default stream) and thread-safe.
+ * - Token tensors are packed over all sequences, head-interleaved, row-major:
+ *   q, k, log_gate, q_shared, k_shared : [total_tokens, H, c]
+ *   v, out                             : [total_tokens, H, d]
+ *   router_logits                      : [total_tokens, H, N]
+ *   in the dtype of cfg->dtype (float32 or bfloat16); out has that dtype too.
+ * - States are float32 [num_seqs, H, P, c, d] with P = N + use_shared; slot N
+ *   is the shared partition.
+ * - cu_seqlens is a device int32 array [num_seqs + 1]: cu_seqlens[0] = 0,
+ *   non-decreasing, cu_seqlens[num_seqs] = total_tokens (zero-length
+ *   sequences allowed).  The host passes num_seqs and total_tokens for sizing;
+ *   the device values are trusted, not checked.
+ * - Arguments are validated on the host before any launch; a rejected call
+ *   launches nothing and returns SSE_ERR_INVALID_ARG / SSE_ERR_UNSUPPORTED /
+ *   SSE_ERR_WORKSPACE.  SSE_ERR_CUDA reports a launch error (the CUDA error is
+ *   left to cudaGetLastError of the caller's runtime).
+ * - Every token-tensor pointer must be 16-byte aligned; c and d must make a
+ *   row a multiple of 16 bytes.
+ */
+#ifndef SSE_H
+#define SSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, without including the CUDA headers. */
+typedef struct CUstream_st *sse_stream_t;
+
+typedef enum {
+    SSE_OK = 0,
+    SSE_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, top_k out of range */
+    SSE_ERR_UNSUPPORTED = 2, /* well-formed but not supported (c, d, N, dtype, algo) */
+    SSE_ERR_WORKSPACE = 3,   /* workspace null, misaligned (256 B) or too small */
+    SSE_ERR_CUDA = 4,        /* a kernel launch failed */
+    SSE_ERR_DEVICE = 5       /* a device-side check failed (sse_read_device_status) */
+} sse_status_t;
+
+typedef enum { SSE_F32 = 0, SSE_BF16 = 1 } sse_dtype_t;
+
+/* Forward algorithm selection (cfg->algo). */
+typedef enum {
+    SSE_ALGO_AUTO = 0,      /* tensor-core chunked path where supported, else recurrent */
+    SSE_ALGO_CHUNKED = 1,   /* tcgen05 chunked path: bf16, c in {64,128}, d in {64,128} */
+    SSE_ALGO_RECURRENT = 2  /* CUDA-core per-token recurrence: any supported dtype/shape */
+} sse_algo_t;
+
+typedef struct {
+    int32_t num_heads;      /* H >= 1 */
+    int32_t key_dim;        /* c: query/key width = rows of every state */
+    int32_t value_dim;      /* d: value width = columns of every state */
+    int32_t num_partitions; /* N routed partitions, 1..64 */
+    int32_t top_k;          /* k selected per token and head, 1..min(N, 8) */
+    int32_t use_shared;     /* 0 or 1: the always-on shared partition (slot N) */
+    float scale;            /* multiplies q and q_shared at the read (1.0 = none) */
+    int32_t dtype;          /* sse_dtype_t of all token tensors and of out */
+    int32_t algo;           /* sse_algo_t, forward only */
+} sse_config_t;
+
+/* Version of this ABI (incremented on any incompatible change). */
+int32_t sse_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *sse_status_string(sse_status_t status);
+
+/* ---------------------------------------------------------------------------
+ * sse_route -- router and token->partition grouping (eqs. 9-10; the varlen
+ * grouping of section 2.6 that gathers, per sequence and partition, the
+ * tokens routed to it in their original time order).
+ *
+ * Outputs (device, caller-owned, fully overwritten):
+ *   topk_idx [total_tokens, H, k] int32  selected partitions, descending logit,
+ *                                        equal logits by ascending index
+ *   topk_w   [total_tokens, H, k] float  e_t at those partitions (fp32 softmax)
+ *   seg_off  [num_seqs*H*N + 1]   int32  start of segment s = (b*H + h)*N + i
+ *                                        in perm; seg_off[last] = H*k*total_tokens
+ *   perm     [H*k*total_tokens]   int32  token indices of each segment, ascending
+ * topk_w, seg_off and perm may be NULL (not written).  The grouping is exact
+ * (integer) and deterministic.  Workspace: sse_route_workspace_size bytes,
+ * 256-byte aligned, contents undefined on entry and exit.
+ * ------------------------------------------------------------------------- */
+size_t sse_route_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
+
+sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits,
+                       const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                       int32_t *topk_idx, float *topk_w, int32_t *seg_off, int32_t *perm,
+                       void *workspace, size_t workspace_bytes, sse_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * sse_forward -- the SSE layer over packed varlen sequences (eqs. 9-14 and
+ * the shared partition of section 2.5), computed per (sequence, head,
+ * partition) segment in chunks (section 2.6, varlen schedule), with the
+ * gated sum of the partial read-outs scattered back to token order.
+ *
+ *   q_shared, k_shared  may be NULL: the shared partition then reads q, k.
+ *   initial_state       may be NULL: all states start at zero.
+ *   final_state         may be NULL: not written.  May alias initial_state.
+ *   out                 [total_tokens, H, d] in cfg->dtype.
+ *   topk_idx, topk_w    may be NULL; when given they receive the routing of
+ *                       every token (same contents as sse_route).
+ * Workspace: sse_forward_workspace_size bytes (256-byte aligned).
+ * Numerics: float32 states and accumulation.  The chunked path rounds its
+ * tensor-core operands to bfloat16 and needs the summed log-gate of any 128
+ * consecutive tokens of a segment to stay above -80 per key row (the decay
+ * factors are split around the chunk midpoint); a chunk outside this range
+ * sets the SSE_DEVICE_GATE_RANGE flag read by sse_read_device_status.
+ * ------------------------------------------------------------------------- */
+size_t sse_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
+
+sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                         const void *log_gate, const void *router_logits,
+                         const void *q_shared, const void *k_shared,
+                         const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                         const float *initial_state, float *final_state, void *out,
+                         int32_t *topk_idx, float *topk_w,
+                         void *workspace, size_t workspace_bytes, sse_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * sse_decode_step -- one token per sequence on states resident in device
+ * memory (section 2.6: decoding recurs only on the selected states).  Reads
+ * and rewrites, in place, only the top_k selected states and the shared
+ * state of each (sequence, head); every other state is left untouched.
+ *
+ *   q, k, log_gate, q_shared, k_shared : [batch, H, c]
+ *   v, out                              : [batch, H, d]
+ *   router_logits                       : [batch, H, N]
+ *   state   [batch, H, P, c, d] float32, updated in place
+ *   topk_idx, topk_w  [batch, H, k], may be NULL
+ * No workspace.  cfg->algo is ignored.
+ * ------------------------------------------------------------------------- */
+sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                             const void *log_gate, const void *router_logits,
+                             const void *q_shared, const void *k_shared, int32_t batch,
+                             float *state, void *out, int32_t *topk_idx, float *topk_w,
+                             sse_stream_t stream);
+
+/* Device-side check flags (bit mask). */
+enum { SSE_DEVICE_GATE_RANGE = 1 };
+
+/* Reads (and clears) the device-check flags that the last sse_forward using
+ * `workspace` recorded.  Synchronizes `stream`.  *flags receives the bit mask;
+ * returns SSE_ERR_DEVICE if any flag was set, SSE_ERR_CUDA on a copy failure. */
+sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSE_H */

@@ -1,0 +1,231 @@
+"""Thin ctypes binding of libsse (include/sse.h).
+
+The functions named like the C entry points (``sse_route``, ``sse_forward``,
+``sse_decode_step``, ...) take raw integers (device pointers, sizes, a CUDA
+stream handle) and only marshal arguments.  The ``route`` / ``forward`` /
+``decode_step`` helpers take torch tensors, allocate outputs and the
+workspace with torch (device memory plumbing only) and call the C entry
+points on the current torch stream.  Every step of the layer runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback: if libsse.so is
+missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsse.so")
+
+SSE_OK, SSE_ERR_INVALID_ARG, SSE_ERR_UNSUPPORTED, SSE_ERR_WORKSPACE, SSE_ERR_CUDA, SSE_ERR_DEVICE = range(6)
+SSE_F32, SSE_BF16 = 0, 1
+SSE_ALGO_AUTO, SSE_ALGO_CHUNKED, SSE_ALGO_RECURRENT = 0, 1, 2
+_ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_ALGO_RECURRENT}
+
+# Every extern "C" symbol that include/sse.h declares.
+EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
+            "sse_forward_workspace_size", "sse_forward", "sse_decode_step", "sse_read_device_status")
+
+
+class sse_config_t(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("key_dim", ctypes.c_int32),
+                ("value_dim", ctypes.c_int32), ("num_partitions", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("use_shared", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32)]
+
+
+class SSEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {sse_status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libsse.so.  Raises when the library has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libsse.so not found at {path}; build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    cfgp = ctypes.POINTER(sse_config_t)
+    lib.sse_abi_version.restype = i32
+    lib.sse_abi_version.argtypes = []
+    lib.sse_status_string.restype = ctypes.c_char_p
+    lib.sse_status_string.argtypes = [ctypes.c_int]
+    lib.sse_route_workspace_size.restype = sz
+    lib.sse_route_workspace_size.argtypes = [cfgp, i64, i32]
+    lib.sse_route.restype = ctypes.c_int
+    lib.sse_route.argtypes = [cfgp, P, P, i32, i64, P, P, P, P, P, sz, P]
+    lib.sse_forward_workspace_size.restype = sz
+    lib.sse_forward_workspace_size.argtypes = [cfgp, i64, i32]
+    lib.sse_forward.restype = ctypes.c_int
+    lib.sse_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, sz, P]
+    lib.sse_decode_step.restype = ctypes.c_int
+    lib.sse_decode_step.argtypes = [cfgp, P, P, P, P, P, P, P, i32, P, P, P, P, P]
+    lib.sse_read_device_status.restype = ctypes.c_int
+    lib.sse_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# Raw C entry points (integers in, status out)
+# ---------------------------------------------------------------------------
+def sse_abi_version() -> int:
+    return load().sse_abi_version()
+
+
+def sse_status_string(status: int) -> str:
+    return load().sse_status_string(status).decode()
+
+
+def sse_route_workspace_size(cfg: sse_config_t, total_tokens: int, num_seqs: int) -> int:
+    return load().sse_route_workspace_size(ctypes.byref(cfg), total_tokens, num_seqs)
+
+
+def sse_forward_workspace_size(cfg: sse_config_t, total_tokens: int, num_seqs: int) -> int:
+    return load().sse_forward_workspace_size(ctypes.byref(cfg), total_tokens, num_seqs)
+
+
+def sse_route(cfg, logits, cu_seqlens, num_seqs, total_tokens, topk_idx, topk_w, seg_off, perm,
+              workspace, workspace_bytes, stream) -> int:
+    return load().sse_route(ctypes.byref(cfg), logits, cu_seqlens, num_seqs, total_tokens, topk_idx,
+                            topk_w, seg_off, perm, workspace, workspace_bytes, stream)
+
+
+def sse_forward(cfg, q, k, v, log_gate, logits, q_shared, k_shared, cu_seqlens, num_seqs,
+                total_tokens, initial_state, final_state, out, topk_idx, topk_w, workspace,
+                workspace_bytes, stream) -> int:
+    return load().sse_forward(ctypes.byref(cfg), q, k, v, log_gate, logits, q_shared, k_shared,
+                              cu_seqlens, num_seqs, total_tokens, initial_state, final_state, out,
+                              topk_idx, topk_w, workspace, workspace_bytes, stream)
+
+
+def sse_decode_step(cfg, q, k, v, log_gate, logits, q_shared, k_shared, batch, state, out,
+                    topk_idx, topk_w, stream) -> int:
+    return load().sse_decode_step(ctypes.byref(cfg), q, k, v, log_gate, logits, q_shared, k_shared,
+                                  batch, state, out, topk_idx, topk_w, stream)
+
+
+def sse_read_device_status(workspace, stream):
+    flags = ctypes.c_int32(0)
+    st = load().sse_read_device_status(workspace, ctypes.byref(flags), stream)
+    return st, flags.value
+
+
+# ---------------------------------------------------------------------------
+# torch-tensor helpers (allocation of outputs/workspace + marshalling)
+# ---------------------------------------------------------------------------
+def make_config(num_heads, key_dim, value_dim, num_partitions, top_k, use_shared=1, scale=1.0,
+                dtype="bf16", algo="auto") -> sse_config_t:
+    dt = {"bf16": SSE_BF16, "f32": SSE_F32}[dtype] if isinstance(dtype, str) else dtype
+    return sse_config_t(num_heads, key_dim, value_dim, num_partitions, top_k, int(use_shared),
+                        float(scale), dt, _ALGOS[algo] if isinstance(algo, str) else int(algo))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != SSE_OK:
+        raise SSEError(status, what)
+
+
+def _token_dtype(cfg):
+    import torch
+    return torch.bfloat16 if cfg.dtype == SSE_BF16 else torch.float32
+
+
+def route(cfg, logits, cu_seqlens, group: bool = True, workspace=None):
+    """Returns dict(topk_idx [T,H,k] int32, topk_w [T,H,k] f32, seg_off, perm)."""
+    import torch
+    T = logits.shape[0]
+    S = cu_seqlens.numel() - 1
+    H, k, N = cfg.num_heads, cfg.top_k, cfg.num_partitions
+    dev = logits.device
+    idx = torch.empty((T, H, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, H, k), dtype=torch.float32, device=dev)
+    seg_off = torch.empty(S * H * N + 1, dtype=torch.int32, device=dev) if group else None
+    perm = torch.empty(max(1, H * k * T), dtype=torch.int32, device=dev) if group else None
+    nbytes = sse_route_workspace_size(cfg, T, S)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    _check(sse_route(cfg, _ptr(logits), _ptr(cu_seqlens), S, T, _ptr(idx), _ptr(w), _ptr(seg_off),
+                     _ptr(perm), _ptr(workspace), workspace.numel(), _stream()), "sse_route")
+    return {"topk_idx": idx, "topk_w": w, "seg_off": seg_off,
+            "perm": None if perm is None else perm[:H * k * T]}
+
+
+def forward_workspace(cfg, total_tokens: int, num_seqs: int, device="cuda"):
+    import torch
+    n = sse_forward_workspace_size(cfg, total_tokens, num_seqs)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def forward(cfg, q, k, v, log_gate, logits, cu_seqlens, *, q_shared=None, k_shared=None,
+            initial_state=None, want_final_state=True, out=None, final_state=None,
+            want_routing=False, workspace=None):
+    """SSE forward on device tensors; returns dict(out, final_state, topk_idx, topk_w)."""
+    import torch
+    T = q.shape[0]
+    S = cu_seqlens.numel() - 1
+    H, d, c = cfg.num_heads, cfg.value_dim, cfg.key_dim
+    P = cfg.num_partitions + cfg.use_shared
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, H, d), dtype=_token_dtype(cfg), device=dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((S, H, P, c, d), dtype=torch.float32, device=dev)
+    idx = w = None
+    if want_routing:
+        idx = torch.empty((T, H, cfg.top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, H, cfg.top_k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = forward_workspace(cfg, T, S, dev)
+    _check(sse_forward(cfg, _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(logits), _ptr(q_shared),
+                       _ptr(k_shared), _ptr(cu_seqlens), S, T, _ptr(initial_state), _ptr(final_state),
+                       _ptr(out), _ptr(idx), _ptr(w), _ptr(workspace), workspace.numel(), _stream()),
+           "sse_forward")
+    return {"out": out, "final_state": final_state, "topk_idx": idx, "topk_w": w,
+            "workspace": workspace}
+
+
+def decode_step(cfg, state, q, k, v, log_gate, logits, *, q_shared=None, k_shared=None, out=None,
+                want_routing=False):
+    """One decode step; ``state`` [B,H,P,c,d] float32 is updated in place."""
+    import torch
+    B = q.shape[0]
+    H, d = cfg.num_heads, cfg.value_dim
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, d), dtype=_token_dtype(cfg), device=dev)
+    idx = w = None
+    if want_routing:
+        idx = torch.empty((B, H, cfg.top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((B, H, cfg.top_k), dtype=torch.float32, device=dev)
+    _check(sse_decode_step(cfg, _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(logits),
+                           _ptr(q_shared), _ptr(k_shared), B, _ptr(state), _ptr(out), _ptr(idx),
+                           _ptr(w), _stream()), "sse_decode_step")
+    return {"out": out, "topk_idx": idx, "topk_w": w}
+
+
+def to_device(arr, device="cuda"):
+    """numpy storage array (float32, or bf16 bits in uint16) -> torch tensor."""
+    import numpy as np
+    import torch
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(arr)).to(device)

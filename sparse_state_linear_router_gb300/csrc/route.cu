@@ -1,0 +1,236 @@
+// route.cu -- router (eqs. 9-10 of "Scaling Linear Attention with Sparse
+// State Expansion") and the token->partition grouping of its varlen schedule
+// (section 2.6): a stable counting sort of the routed records by segment
+// s = (b*H + h)*N + i that keeps each segment in time order.
+//
+// Stages (all deterministic, integer-exact):
+//   plan     1 CTA   : routing blocks per sequence (256 tokens, never
+//                      straddling a sequence) -> blk_prefix
+//   count    (blk,H) : route every token of the block, write topk_idx/topk_w,
+//                      per-block histogram over partitions -> cnt
+//   scan     (H*N)   : exclusive scan of cnt over blocks, per (h, i)
+//   seg_off  1 CTA   : segment sizes from the scanned counts; exclusive scan
+//                      over s -> seg_off
+//   scatter  (blk,H) : rank of each record inside its block (per-warp bit
+//                      masks + popc) + block base -> perm / perm_rec
+#include "sse_internal.cuh"
+
+namespace sse {
+
+int64_t route_max_blocks(int64_t total_tokens, int32_t num_seqs) {
+    return (total_tokens + kRouteBlock - 1) / kRouteBlock + num_seqs;
+}
+
+namespace {
+
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of
+// 32, at most 1024).  Returns the exclusive prefix; *total receives the sum.
+__device__ int block_exclusive_scan(int x, int *total) {
+    __shared__ int warp_off[32];
+    __shared__ int s_total;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    __syncthreads();  // previous call's readers are done with warp_off / s_total
+    if (lane == 31) warp_off[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < nwarps ? warp_off[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < nwarps) warp_off[lane] = wi - w;
+        if (lane == 31) s_total = wi;
+    }
+    __syncthreads();
+    *total = s_total;
+    return warp_off[warp] + incl - x;
+}
+
+__global__ void plan_blocks_kernel(const int32_t *__restrict__ cu, int32_t nseq,
+                                   int32_t *__restrict__ blk_prefix) {
+    int carry = 0;
+    for (int base = 0; base < nseq; base += blockDim.x) {
+        const int b = base + threadIdx.x;
+        int nb = 0;
+        if (b < nseq) nb = (cu[b + 1] - cu[b] + kRouteBlock - 1) / kRouteBlock;
+        int tot;
+        const int ex = block_exclusive_scan(nb, &tot);
+        if (b < nseq) blk_prefix[b] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) blk_prefix[nseq] = carry;
+}
+
+// Locates routing block j: its sequence and token range.  Returns false when
+// j is past the last block.
+__device__ __forceinline__ bool find_block(const int32_t *blk_prefix, const int32_t *cu,
+                                           int32_t nseq, int j, int &b, int &t0, int &t1) {
+    if (j >= blk_prefix[nseq]) return false;
+    int lo = 0, hi = nseq - 1;  // largest b with blk_prefix[b] <= j and a non-empty range
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (blk_prefix[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    // zero-length sequences share their prefix with the next one; the largest
+    // b with blk_prefix[b] <= j is the non-empty sequence owning block j.
+    b = lo;
+    t0 = cu[b] + (j - blk_prefix[b]) * kRouteBlock;
+    t1 = min(t0 + kRouteBlock, cu[b + 1]);
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRouteBlock)
+route_count_kernel(const T *__restrict__ logits, const int32_t *__restrict__ cu, int32_t nseq,
+                   const int32_t *__restrict__ blk_prefix, int32_t H, int32_t N, int32_t k,
+                   int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                   int32_t *__restrict__ cnt, int32_t max_blocks) {
+    __shared__ int hist[kMaxPartitions];
+    __shared__ int s_b, s_t0, s_t1, s_ok;
+    const int j = blockIdx.x, h = blockIdx.y;
+    if (threadIdx.x < kMaxPartitions) hist[threadIdx.x] = 0;
+    if (threadIdx.x == 0) {
+        int b = 0, t0 = 0, t1 = 0;
+        s_ok = find_block(blk_prefix, cu, nseq, j, b, t0, t1);
+        s_b = b; s_t0 = t0; s_t1 = t1;
+    }
+    __syncthreads();
+    if (s_ok) {
+        const int t = s_t0 + threadIdx.x;
+        if (t < s_t1) {
+            int idx[kMaxTopK];
+            float w[kMaxTopK];
+            route_token<T>(logits + ((int64_t)t * H + h) * N, N, k, idx, w);
+            const int64_t o = ((int64_t)t * H + h) * k;
+            for (int jj = 0; jj < k; ++jj) {
+                topk_idx[o + jj] = idx[jj];
+                if (topk_w) topk_w[o + jj] = w[jj];
+                atomicAdd(&hist[idx[jj]], 1);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += blockDim.x)
+        cnt[((int64_t)h * N + i) * (max_blocks + 1) + j] = hist[i];
+}
+
+__global__ void __launch_bounds__(1024)
+scan_blocks_kernel(int32_t *__restrict__ cnt, int32_t max_blocks) {
+    int32_t *row = cnt + (int64_t)blockIdx.x * (max_blocks + 1);
+    int carry = 0;
+    for (int base = 0; base < max_blocks; base += blockDim.x) {
+        const int j = base + threadIdx.x;
+        const int x = j < max_blocks ? row[j] : 0;
+        int tot;
+        const int ex = block_exclusive_scan(x, &tot);
+        if (j < max_blocks) row[j] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) row[max_blocks] = carry;
+}
+
+__global__ void __launch_bounds__(1024)
+seg_off_kernel(const int32_t *__restrict__ cnt, int32_t max_blocks,
+               const int32_t *__restrict__ blk_prefix, int32_t nseq, int32_t H, int32_t N,
+               int32_t *__restrict__ seg_off) {
+    const int64_t nseg = (int64_t)nseq * H * N;
+    int carry = 0;
+    for (int64_t base = 0; base < nseg; base += blockDim.x) {
+        const int64_t s = base + threadIdx.x;
+        int x = 0;
+        if (s < nseg) {
+            const int i = (int)(s % N);
+            const int64_t bh = s / N;
+            const int h = (int)(bh % H), b = (int)(bh / H);
+            const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
+            x = row[blk_prefix[b + 1]] - row[blk_prefix[b]];
+        }
+        int tot;
+        const int ex = block_exclusive_scan(x, &tot);
+        if (s < nseg) seg_off[s] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) seg_off[nseg] = carry;
+}
+
+__global__ void __launch_bounds__(kRouteBlock)
+scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ cu, int32_t nseq,
+               const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cnt,
+               int32_t max_blocks, const int32_t *__restrict__ seg_off, int32_t H, int32_t N,
+               int32_t k, int32_t *__restrict__ perm, int32_t *__restrict__ perm_rec) {
+    constexpr int kWarps = kRouteBlock / 32;
+    __shared__ uint32_t wmask[kWarps][kMaxPartitions];
+    __shared__ int s_b, s_t0, s_t1, s_ok;
+    const int j = blockIdx.x, h = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int x = threadIdx.x; x < kWarps * kMaxPartitions; x += blockDim.x)
+        (&wmask[0][0])[x] = 0u;
+    if (threadIdx.x == 0) {
+        int b = 0, t0 = 0, t1 = 0;
+        s_ok = find_block(blk_prefix, cu, nseq, j, b, t0, t1);
+        s_b = b; s_t0 = t0; s_t1 = t1;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    const int b = s_b;
+    const int t = s_t0 + threadIdx.x;
+    const bool valid = t < s_t1;
+    int idx[kMaxTopK];
+    if (valid) {
+        const int64_t o = ((int64_t)t * H + h) * k;
+        for (int jj = 0; jj < k; ++jj) {
+            idx[jj] = topk_idx[o + jj];
+            atomicOr(&wmask[warp][idx[jj]], 1u << lane);
+        }
+    }
+    __syncthreads();
+    if (!valid) return;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int jj = 0; jj < k; ++jj) {
+        const int i = idx[jj];
+        int rank = __popc(wmask[warp][i] & lt);
+        for (int w2 = 0; w2 < warp; ++w2) rank += __popc(wmask[w2][i]);
+        const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
+        const int seg_rank = row[j] - row[blk_prefix[b]] + rank;
+        const int64_t pos = (int64_t)seg_off[((int64_t)b * H + h) * N + i] + seg_rank;
+        if (perm) perm[pos] = t;
+        if (perm_rec) perm_rec[pos] = t * k + jj;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int32_t *cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, const RouteBuffers &rb,
+                         bool group, cudaStream_t stream) {
+    const int H = cfg.num_heads, N = cfg.num_partitions, k = cfg.top_k;
+    const int MB = rb.max_blocks;
+    plan_blocks_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, rb.blk_prefix);
+    dim3 grid(MB, H);
+    if (cfg.dtype == SSE_BF16)
+        route_count_kernel<__nv_bfloat16><<<grid, kRouteBlock, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(logits), cu_seqlens, num_seqs, rb.blk_prefix, H, N, k,
+            rb.topk_idx, rb.topk_w, rb.cnt, MB);
+    else
+        route_count_kernel<float><<<grid, kRouteBlock, 0, stream>>>(
+            static_cast<const float *>(logits), cu_seqlens, num_seqs, rb.blk_prefix, H, N, k,
+            rb.topk_idx, rb.topk_w, rb.cnt, MB);
+    if (!group) return cudaGetLastError();
+    scan_blocks_kernel<<<H * N, 1024, 0, stream>>>(rb.cnt, MB);
+    seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, num_seqs, H, N, rb.seg_off);
+    scatter_kernel<<<grid, kRouteBlock, 0, stream>>>(rb.topk_idx, cu_seqlens, num_seqs, rb.blk_prefix,
+                                                     rb.cnt, MB, rb.seg_off, H, N, k, rb.perm,
+                                                     rb.perm_rec);
+    return cudaGetLastError();
+}
+
+}  // namespace sse

@@ -1,0 +1,237 @@
+// sse_api.cu -- the extern "C" entry points of libsse (declared and
+// documented in include/sse.h): host-side validation, workspace layout and
+// the launch sequence of each call.  No allocation, no synchronization
+// (except sse_read_device_status).
+#include <algorithm>
+#include <cmath>
+#include <initializer_list>
+
+#include "sse_internal.cuh"
+
+namespace {
+
+using sse::Carver;
+using sse::RouteBuffers;
+
+constexpr int32_t kAbiVersion = 1;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(const sse_config_t &c) { return c.dtype == SSE_BF16 ? 2 : 4; }
+
+// Checks shared by every entry point.
+sse_status_t check_config(const sse_config_t *cfg) {
+    if (!cfg) return SSE_ERR_INVALID_ARG;
+    const sse_config_t &c = *cfg;
+    if (c.num_heads < 1 || c.key_dim < 1 || c.value_dim < 1) return SSE_ERR_INVALID_ARG;
+    if (c.num_partitions < 1 || c.top_k < 1 || c.top_k > c.num_partitions) return SSE_ERR_INVALID_ARG;
+    if (c.use_shared != 0 && c.use_shared != 1) return SSE_ERR_INVALID_ARG;
+    if (c.dtype != SSE_F32 && c.dtype != SSE_BF16) return SSE_ERR_INVALID_ARG;
+    if (c.algo < SSE_ALGO_AUTO || c.algo > SSE_ALGO_RECURRENT) return SSE_ERR_INVALID_ARG;
+    if (!std::isfinite(c.scale)) return SSE_ERR_INVALID_ARG;
+    if (c.num_partitions > sse::kMaxPartitions || c.top_k > sse::kMaxTopK) return SSE_ERR_UNSUPPORTED;
+    if ((c.key_dim * elem_bytes(c)) % 16 || (c.value_dim * elem_bytes(c)) % 16) return SSE_ERR_UNSUPPORTED;
+    return SSE_OK;
+}
+
+sse_status_t check_sizes(const sse_config_t &c, int64_t total_tokens, int32_t num_seqs) {
+    if (num_seqs < 0 || total_tokens < 0) return SSE_ERR_INVALID_ARG;
+    if (num_seqs == 0 && total_tokens != 0) return SSE_ERR_INVALID_ARG;
+    const int64_t recs = total_tokens * c.num_heads * c.top_k;
+    if (recs >= (int64_t(1) << 31) || total_tokens * c.top_k >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * c.num_heads * c.num_partitions >= (int64_t(1) << 30)) return SSE_ERR_UNSUPPORTED;
+    return SSE_OK;
+}
+
+// Route-stage buffers carved from the workspace.  User-provided outputs are
+// used in place; missing ones live in the workspace.
+RouteBuffers carve_route(Carver &cv, const sse_config_t &c, int64_t T, int32_t S, int32_t *topk_idx,
+                         float *topk_w, int32_t *seg_off, int32_t *perm, bool need_w, bool need_rec) {
+    RouteBuffers rb{};
+    rb.max_blocks = (int32_t)sse::route_max_blocks(T, S);
+    rb.blk_prefix = cv.take<int32_t>(S + 1);
+    rb.cnt = cv.take<int32_t>((size_t)c.num_heads * c.num_partitions * (rb.max_blocks + 1));
+    int32_t *ws_seg = cv.take<int32_t>((size_t)S * c.num_heads * c.num_partitions + 1);
+    int32_t *ws_idx = cv.take<int32_t>((size_t)T * c.num_heads * c.top_k);
+    float *ws_w = need_w ? cv.take<float>((size_t)T * c.num_heads * c.top_k) : nullptr;
+    int32_t *ws_rec = need_rec ? cv.take<int32_t>((size_t)T * c.num_heads * c.top_k) : nullptr;
+    rb.seg_off = seg_off ? seg_off : ws_seg;
+    rb.topk_idx = topk_idx ? topk_idx : ws_idx;
+    rb.topk_w = topk_w ? topk_w : ws_w;
+    rb.perm = perm;
+    rb.perm_rec = ws_rec;
+    return rb;
+}
+
+bool use_chunked(const sse_config_t &c) {
+    if (c.algo == SSE_ALGO_RECURRENT) return false;
+    if (c.algo == SSE_ALGO_CHUNKED) return true;
+    return sse::chunked_supported(c);
+}
+
+struct ForwardLayout {
+    RouteBuffers rb;
+    float *part_routed, *part_shared;
+    int32_t *flags;
+    void *chunk_ws;
+    size_t bytes;
+};
+
+ForwardLayout carve_forward(void *ws, const sse_config_t &c, int64_t T, int32_t S,
+                            int32_t *topk_idx, float *topk_w) {
+    Carver cv(ws);
+    ForwardLayout L{};
+    L.flags = cv.take<int32_t>(64);
+    L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
+    if (use_chunked(c)) {
+        const size_t extra = sse::chunked_extra_workspace(c, T, S);
+        L.chunk_ws = cv.take<unsigned char>(extra);
+        L.part_routed = nullptr;
+        L.part_shared = nullptr;
+    } else {
+        L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
+        L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
+        L.chunk_ws = nullptr;
+    }
+    L.bytes = (cv.off + 255) & ~size_t(255);
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sse_abi_version(void) { return kAbiVersion; }
+
+const char *sse_status_string(sse_status_t s) {
+    switch (s) {
+    case SSE_OK: return "SSE_OK";
+    case SSE_ERR_INVALID_ARG: return "SSE_ERR_INVALID_ARG: invalid argument";
+    case SSE_ERR_UNSUPPORTED: return "SSE_ERR_UNSUPPORTED: configuration not supported";
+    case SSE_ERR_WORKSPACE: return "SSE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case SSE_ERR_CUDA: return "SSE_ERR_CUDA: kernel launch failed";
+    case SSE_ERR_DEVICE: return "SSE_ERR_DEVICE: a device-side check failed";
+    default: return "unknown sse_status_t";
+    }
+}
+
+size_t sse_route_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs) {
+    if (check_config(cfg) != SSE_OK || check_sizes(*cfg, total_tokens, num_seqs) != SSE_OK) return 0;
+    Carver cv(nullptr);
+    carve_route(cv, *cfg, total_tokens, num_seqs, nullptr, nullptr, nullptr, nullptr, true, false);
+    return (cv.off + 255) & ~size_t(255);
+}
+
+sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits, const int32_t *cu_seqlens,
+                       int32_t num_seqs, int64_t total_tokens, int32_t *topk_idx, float *topk_w,
+                       int32_t *seg_off, int32_t *perm, void *workspace, size_t workspace_bytes,
+                       sse_stream_t stream) {
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
+    if (!cu_seqlens || !topk_idx || (total_tokens > 0 && !router_logits)) return SSE_ERR_INVALID_ARG;
+    if (!aligned16(router_logits)) return SSE_ERR_INVALID_ARG;
+    const bool group = seg_off || perm;
+    if (group && !(seg_off && perm)) return SSE_ERR_INVALID_ARG;
+    const size_t need = sse_route_workspace_size(cfg, total_tokens, num_seqs);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return SSE_ERR_WORKSPACE;
+    if (num_seqs == 0) return SSE_OK;
+    Carver cv(workspace);
+    RouteBuffers rb = carve_route(cv, *cfg, total_tokens, num_seqs, topk_idx, topk_w, seg_off, perm,
+                                  true, false);
+    cudaError_t e = sse::launch_route(*cfg, router_logits, cu_seqlens, num_seqs, total_tokens, rb,
+                                      group, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
+
+size_t sse_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs) {
+    if (check_config(cfg) != SSE_OK || check_sizes(*cfg, total_tokens, num_seqs) != SSE_OK) return 0;
+    return carve_forward(nullptr, *cfg, total_tokens, num_seqs, nullptr, nullptr).bytes;
+}
+
+sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                         const void *log_gate, const void *router_logits, const void *q_shared,
+                         const void *k_shared, const int32_t *cu_seqlens, int32_t num_seqs,
+                         int64_t total_tokens, const float *initial_state, float *final_state,
+                         void *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                         size_t workspace_bytes, sse_stream_t stream) {
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
+    const sse_config_t &c = *cfg;
+    if (!cu_seqlens) return SSE_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !log_gate || !router_logits || !out))
+        return SSE_ERR_INVALID_ARG;
+    for (const void *p : std::initializer_list<const void *>{q, k, v, log_gate, router_logits, q_shared, k_shared, out,
+                          (const void *)initial_state, (const void *)final_state})
+        if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
+    if (use_chunked(c)) {
+        if (!sse::chunked_supported(c)) return SSE_ERR_UNSUPPORTED;
+    } else if (!sse::recurrent_supported(c)) {
+        return SSE_ERR_UNSUPPORTED;
+    }
+    const size_t need = sse_forward_workspace_size(cfg, total_tokens, num_seqs);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return SSE_ERR_WORKSPACE;
+    if (num_seqs == 0) return SSE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ForwardLayout L = carve_forward(workspace, c, total_tokens, num_seqs, topk_idx, topk_w);
+    if (cudaMemsetAsync(L.flags, 0, 64 * sizeof(int32_t), s) != cudaSuccess) return SSE_ERR_CUDA;
+    cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, true, s);
+    if (e != cudaSuccess) return SSE_ERR_CUDA;
+    sse::ForwardArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = log_gate; a.qs = q_shared; a.ks = k_shared;
+    a.cu_seqlens = cu_seqlens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.init = initial_state;
+    a.final_state = final_state;
+    a.out = out;
+    a.seg_off = L.rb.seg_off;
+    a.perm_rec = L.rb.perm_rec;
+    a.topk_w = L.rb.topk_w;
+    a.part_routed = L.part_routed;
+    a.part_shared = L.part_shared;
+    a.flags = L.flags;
+    if (use_chunked(c)) {
+        e = sse::launch_forward_chunked(c, a, s);
+        (void)L.chunk_ws;
+    } else {
+        e = sse::launch_forward_recurrent(c, a, s);
+        if (e == cudaSuccess) e = sse::launch_combine(c, a, s);
+    }
+    return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
+
+sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                             const void *log_gate, const void *router_logits, const void *q_shared,
+                             const void *k_shared, int32_t batch, float *state, void *out,
+                             int32_t *topk_idx, float *topk_w, sse_stream_t stream) {
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if (batch < 0) return SSE_ERR_INVALID_ARG;
+    if ((int64_t)batch * cfg->num_heads >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    if (batch > 0 && (!q || !k || !v || !log_gate || !router_logits || !state || !out))
+        return SSE_ERR_INVALID_ARG;
+    for (const void *p : std::initializer_list<const void *>{q, k, v, log_gate, router_logits, q_shared, k_shared, out, (const void *)state})
+        if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
+    if (!sse::decode_supported(*cfg)) return SSE_ERR_UNSUPPORTED;
+    cudaError_t e = sse::launch_decode(*cfg, q, k, v, log_gate, router_logits, q_shared, k_shared,
+                                       batch, state, out, topk_idx, topk_w,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
+
+sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_t stream) {
+    if (!workspace || !flags || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SSE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    if (cudaMemcpyAsync(&host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SSE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSE_ERR_CUDA;
+    *flags = host;
+    return host ? SSE_ERR_DEVICE : SSE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+// sse_internal.cuh -- device helpers and launcher declarations shared by the
+// translation units of libsse.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/sse.h"
+
+namespace sse {
+
+constexpr int kMaxPartitions = 64;
+constexpr int kMaxTopK = 8;
+constexpr int kRouteBlock = 256;  // tokens per routing block (one thread per token)
+
+// ---------------------------------------------------------------------------
+// Element access for the two storage dtypes.
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
+    static __device__ __forceinline__ void store(float *p, float x) { *p = x; }
+    // four consecutive elements (16-byte aligned for float)
+    static __device__ __forceinline__ float4 load4(const float *p) {
+        return __ldg(reinterpret_cast<const float4 *>(p));
+    }
+    static __device__ __forceinline__ void store4(float *p, float4 x) {
+        *reinterpret_cast<float4 *>(p) = x;
+    }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+    // four consecutive elements (8-byte aligned)
+    static __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+        uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        float4 f;
+        f.x = __uint_as_float(u.x << 16);
+        f.y = __uint_as_float(u.x & 0xffff0000u);
+        f.z = __uint_as_float(u.y << 16);
+        f.w = __uint_as_float(u.y & 0xffff0000u);
+        return f;
+    }
+    static __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 x) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&lo);
+        u.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(p) = u;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Router for one (token, head): softmax over N logits in fp32 and the top-k
+// by logit, equal logits ordered by ascending index (strict comparison while
+// scanning upward keeps the lower index).  idx/w receive k entries in
+// descending-logit order.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void route_token(const T *logit, int N, int k, int *idx, float *w) {
+    float l[kMaxPartitions];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxPartitions; ++i) {
+        if (i < N) {
+            l[i] = Elem<T>::load(logit + i);
+            m = fmaxf(m, l[i]);
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPartitions; ++i)
+        if (i < N) s += expf(l[i] - m);
+    const float inv = 1.f / s;
+    uint64_t taken = 0;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        int bi = -1;
+        float bv = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kMaxPartitions; ++i) {
+            if (i < N && !((taken >> i) & 1ull) && (bi < 0 || l[i] > bv)) {
+                bv = l[i];
+                bi = i;
+            }
+        }
+        taken |= 1ull << bi;
+        idx[j] = bi;
+        w[j] = expf(bv - m) * inv;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Workspace carving (256-byte aligned regions).
+// ---------------------------------------------------------------------------
+struct Carver {
+    uintptr_t base;
+    size_t off = 0;
+    explicit Carver(void *p) : base(reinterpret_cast<uintptr_t>(p)) {}
+    template <typename T> T *take(size_t n) {
+        off = (off + 255) & ~size_t(255);
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += n * sizeof(T);
+        return p;
+    }
+};
+
+// Device buffers of the routing/grouping stage.
+struct RouteBuffers {
+    int32_t *blk_prefix;  // [num_seqs + 1] routing blocks before each sequence
+    int32_t *cnt;         // [H * N * (max_blocks + 1)] per-block counts, scanned in place
+    int32_t *seg_off;     // [num_seqs * H * N + 1]
+    int32_t *topk_idx;    // [T * H * k]
+    float *topk_w;        // [T * H * k]
+    int32_t *perm;        // [H * k * T] token ids (may be null)
+    int32_t *perm_rec;    // [H * k * T] record ids t * k + j (may be null)
+    int32_t max_blocks;
+};
+
+int64_t route_max_blocks(int64_t total_tokens, int32_t num_seqs);
+
+// Launches the routing + grouping kernels; returns cudaGetLastError().
+cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int32_t *cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, const RouteBuffers &rb,
+                         bool group, cudaStream_t stream);
+
+// Recurrent (CUDA-core) forward over all segments; writes fp32 partials.
+struct ForwardArgs {
+    const void *q, *k, *v, *g, *qs, *ks;
+    const int32_t *cu_seqlens;
+    int32_t num_seqs;
+    int64_t total_tokens;
+    const float *init;
+    float *final_state;
+    void *out;
+    const int32_t *seg_off;
+    const int32_t *perm_rec;
+    const float *topk_w;
+    float *part_routed;  // [T, H, k, d] fp32
+    float *part_shared;  // [T, H, d] fp32
+    int32_t *flags;
+};
+
+bool recurrent_supported(const sse_config_t &cfg);
+cudaError_t launch_forward_recurrent(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+
+bool chunked_supported(const sse_config_t &cfg);
+size_t chunked_extra_workspace(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs);
+cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+
+// out[t,h,:] = sum_j part_routed[t,h,j,:] + part_shared[t,h,:]
+cudaError_t launch_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+
+bool decode_supported(const sse_config_t &cfg);
+cudaError_t launch_decode(const sse_config_t &cfg, const void *q, const void *k, const void *v,
+                          const void *g, const void *logits, const void *qs, const void *ks,
+                          int32_t batch, float *state, void *out, int32_t *topk_idx,
+                          float *topk_w, cudaStream_t stream);
+
+}  // namespace sse

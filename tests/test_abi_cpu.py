@@ -1,0 +1,111 @@
+"""CPU-only checks of the C ABI: the library builds, loads and exports every
+symbol include/sse.h declares; host-side validation rejects bad arguments
+before any launch (no GPU needed, no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_state_linear_router_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "sse.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sse_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from sparse_state_linear_router_gb300 import binding
+    declared = _declared_functions()
+    assert declared, "no declarations parsed"
+    assert sorted(binding.EXPORTED) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    from sparse_state_linear_router_gb300 import binding
+    assert binding.sse_abi_version() == 1
+    for s in range(6):
+        assert binding.sse_status_string(s).startswith("SSE_")
+
+
+def _cfg(**kw):
+    from sparse_state_linear_router_gb300 import binding
+    base = dict(num_heads=2, key_dim=64, value_dim=64, num_partitions=8, top_k=2, use_shared=1,
+                scale=1.0, dtype="bf16", algo="auto")
+    base.update(kw)
+    return binding.make_config(**base)
+
+
+FAKE = 1 << 20  # aligned non-null "device" address; never dereferenced
+
+
+def _fwd(cfg, T=16, S=1, ws=FAKE, ws_bytes=1 << 40, q=FAKE, cu=FAKE, out=FAKE):
+    from sparse_state_linear_router_gb300 import binding
+    return binding.sse_forward(cfg, q, FAKE, FAKE, FAKE, FAKE, None, None, cu, S, T, None, None,
+                               out, None, None, ws, ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    from sparse_state_linear_router_gb300 import binding as b
+    assert _fwd(_cfg(top_k=0)) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(top_k=9, num_partitions=8)) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(num_partitions=65, top_k=2)) == b.SSE_ERR_UNSUPPORTED
+    assert _fwd(_cfg(top_k=9, num_partitions=16)) == b.SSE_ERR_UNSUPPORTED
+    assert _fwd(_cfg(use_shared=2)) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(dtype=7)) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(algo=9)) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(scale=float("nan"))) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(key_dim=12)) == b.SSE_ERR_UNSUPPORTED     # 24-byte bf16 rows
+    assert _fwd(_cfg(value_dim=100, dtype="f32")) == b.SSE_ERR_UNSUPPORTED
+    assert _fwd(_cfg(), q=None) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(), cu=None) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(), q=FAKE + 8) == b.SSE_ERR_INVALID_ARG    # misaligned
+    assert _fwd(_cfg(), T=-1) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(), S=0, T=5) == b.SSE_ERR_INVALID_ARG
+    assert _fwd(_cfg(), ws=None) == b.SSE_ERR_WORKSPACE
+    assert _fwd(_cfg(), ws=FAKE + 128) == b.SSE_ERR_WORKSPACE
+    assert _fwd(_cfg(), ws_bytes=64) == b.SSE_ERR_WORKSPACE
+    # empty batch: valid, nothing launched
+    assert _fwd(_cfg(), S=0, T=0) == b.SSE_OK
+
+
+def test_decode_and_route_reject_bad_arguments(lib):
+    from sparse_state_linear_router_gb300 import binding as b
+    cfg = _cfg()
+    assert b.sse_decode_step(cfg, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, -1, FAKE, FAKE, None,
+                             None, None) == b.SSE_ERR_INVALID_ARG
+    assert b.sse_decode_step(cfg, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 4, None, FAKE, None,
+                             None, None) == b.SSE_ERR_INVALID_ARG
+    assert b.sse_decode_step(_cfg(value_dim=24, dtype="f32"), FAKE, FAKE, FAKE, FAKE, FAKE, None, None,
+                             4, FAKE, FAKE, None, None, None) == b.SSE_ERR_UNSUPPORTED
+    # batch 0: valid no-op
+    assert b.sse_decode_step(cfg, None, None, None, None, None, None, None, 0, None, None, None,
+                             None, None) == b.SSE_OK
+    assert b.sse_route(cfg, FAKE, FAKE, 1, 16, None, None, None, None, FAKE, 1 << 30,
+                       None) == b.SSE_ERR_INVALID_ARG
+    assert b.sse_route(cfg, FAKE, FAKE, 1, 16, FAKE, None, FAKE, None, FAKE, 1 << 30,
+                       None) == b.SSE_ERR_INVALID_ARG  # seg_off without perm
+    assert b.sse_route(cfg, FAKE, FAKE, 1, 16, FAKE, None, None, None, FAKE, 8,
+                       None) == b.SSE_ERR_WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    from sparse_state_linear_router_gb300 import binding as b
+    cfg = _cfg()
+    small = b.sse_forward_workspace_size(cfg, 100, 2)
+    big = b.sse_forward_workspace_size(cfg, 10000, 2)
+    assert 0 < small < big and small % 256 == 0
+    assert b.sse_forward_workspace_size(_cfg(top_k=0), 100, 2) == 0
+    assert b.sse_route_workspace_size(cfg, 100, 2) > 0
+    assert b.sse_route_workspace_size(cfg, 0, 1) > 0

@@ -1,0 +1,97 @@
+"""GPU parity of sse_decode_step against the fp64 oracle (marked gpu)."""
+import numpy as np
+import pytest
+
+from sparse_state_linear_router_gb300 import inputs as synth
+from tests import _helpers as H_
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_state_linear_router_gb300 import binding
+    binding.load()
+
+
+def _decode_run(w, batch, steps, init_std=0.1, sample=None):
+    import oracle
+    from sparse_state_linear_router_gb300 import binding
+    cfg = H_.config_of(w)
+    P = w.num_slots
+    rng = np.random.default_rng(77)
+    state0 = (rng.normal(size=(batch, w.num_heads, P, w.key_dim, w.value_dim)) * init_std).astype(np.float32)
+    sample = np.arange(batch) if sample is None else np.asarray(sample)
+    ref_state = np.ascontiguousarray(state0[sample].astype(np.float64))
+    dstate = torch.from_numpy(state0).cuda()
+    for s in range(steps):
+        tok = synth.make_decode_inputs(w, s, batch=batch)
+        before = dstate.clone()
+        dv = {n: binding.to_device(getattr(tok, n)) for n in ("q", "k", "v", "g", "logits")}
+        r = binding.decode_step(cfg, dstate, dv["q"], dv["k"], dv["v"], dv["g"], dv["logits"],
+                                want_routing=True)
+        torch.cuda.synchronize()
+        ref = oracle.decode_step(ref_state, *(getattr(tok, n)[sample] for n in ("q", "k", "v", "g", "logits")),
+                                 top_k=w.top_k, use_shared=w.use_shared)
+        idx = H_.to_numpy(r["topk_idx"])[sample]
+        assert np.array_equal(idx, ref["topk_idx"])
+        np.testing.assert_allclose(H_.to_numpy(r["topk_w"])[sample], ref["topk_w"], rtol=2e-6, atol=1e-7)
+        assert H_.max_abs_rel(H_.to_numpy(r["out"])[sample], ref["out"]) < H_.tol_for(w)
+        assert H_.max_abs_rel(H_.to_numpy(dstate)[sample], ref_state) < H_.tol_for(w)
+        # unselected states: bit-identical after the step
+        changed = (dstate != before).flatten(3).any(-1).cpu().numpy()  # [B,H,P]
+        sel = np.zeros(changed.shape, dtype=bool)
+        all_idx = H_.to_numpy(r["topk_idx"])
+        np.put_along_axis(sel, all_idx.astype(np.int64), True, axis=-1)
+        if w.use_shared:
+            sel[..., w.num_partitions] = True
+        assert not np.any(changed & ~sel)
+
+
+def test_decode_small_f32():
+    w = H_.workload_variant("decode_bf16", dtype="f32", num_heads=2, key_dim=16, value_dim=16,
+                            num_partitions=4, top_k=1)
+    _decode_run(w, batch=5, steps=4)
+
+
+def test_decode_bf16_reduced_batch():
+    w = synth.WORKLOADS["decode_bf16"]
+    _decode_run(w, batch=4, steps=3)
+
+
+def test_decode_noshared_k3_d64():
+    w = H_.workload_variant("decode_bf16", num_heads=3, key_dim=64, value_dim=64, num_partitions=8,
+                            top_k=3, use_shared=0)
+    _decode_run(w, batch=6, steps=3)
+
+
+def test_decode_full_batch_sampled():
+    """Full decode workload (256 sequences x 16 heads, N=16): every sequence
+    is stepped on the GPU, a sample of sequences is recomputed by the oracle."""
+    w = synth.WORKLOADS["decode_bf16"]
+    _decode_run(w, batch=w.decode_batch, steps=2, sample=[0, 17, 128, 255])
+
+
+def test_decode_matches_forward_continuation():
+    """forward over T tokens then decode steps == forward over T + steps
+    tokens (state carry from the chunked prefill into the recurrent decode)."""
+    from sparse_state_linear_router_gb300 import binding
+    w = H_.workload_variant("small_bf16", num_heads=2)
+    T1, extra = 200, 3
+    inp = synth.make_forward_inputs(w, seed=4, lengths=[T1 + extra], with_init=True)
+    first = synth.LayerInputs(w, inp.q[:T1], inp.k[:T1], inp.v[:T1], inp.g[:T1], inp.logits[:T1],
+                              np.array([0, T1], np.int32), inp.init_state)
+    g1 = H_.run_gpu_forward(w, first)
+    full = H_.run_oracle_forward(w, inp)
+    cfg = H_.config_of(w)
+    st = torch.from_numpy(np.ascontiguousarray(g1["final_state"])).cuda()
+    for t in range(T1, T1 + extra):
+        dv = {n: binding.to_device(np.ascontiguousarray(getattr(inp, n)[t:t + 1])) for n in ("q", "k", "v", "g", "logits")}
+        r = binding.decode_step(cfg, st, dv["q"], dv["k"], dv["v"], dv["g"], dv["logits"])
+        torch.cuda.synchronize()
+        assert H_.max_abs_rel(H_.to_numpy(r["out"])[0], full["out"][t]) < H_.TOL_BF16
+    assert H_.max_abs_rel(H_.to_numpy(st), full["final_state"]) < H_.TOL_BF16

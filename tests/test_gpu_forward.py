@@ -1,0 +1,145 @@
+"""GPU parity of sse_route / sse_forward against the fp64 oracle, on the same
+seeded inputs, through the C ABI (marked gpu)."""
+import numpy as np
+import pytest
+
+from sparse_state_linear_router_gb300 import inputs as synth
+from tests import _helpers as H_
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_state_linear_router_gb300 import binding
+    binding.load()
+
+
+def _stable_topk(logits_bits, k):
+    import oracle
+    lg = oracle.to_f64(logits_bits)
+    return np.argsort(-lg, axis=-1, kind="stable")[..., :k].astype(np.int32)
+
+
+# (workload, lengths, with_init, overrides)
+CASES = {
+    "tiny_f32": ("tiny_f32", None, None, {}),
+    "tiny_f32_init_varlen": ("tiny_f32", [23, 0, 64, 1, 40], True, {}),
+    "small_bf16": ("small_bf16", None, None, {}),
+    "layer_bf16_ragged": ("layer_bf16", [300, 1, 0, 517], False, {"num_heads": 3}),
+    "varlen_bf16_init": ("varlen_bf16", [700, 129, 0, 1500], True, {"num_heads": 2}),
+    "N1_k1_noshared": ("small_bf16", [200, 77], True, {"num_partitions": 1, "top_k": 1, "use_shared": 0}),
+    "k_equals_N": ("small_bf16", [250, 3], True, {"num_partitions": 4, "top_k": 4, "num_heads": 2}),
+    "noshared_k3": ("layer_bf16", [333], True, {"num_partitions": 8, "top_k": 3, "use_shared": 0, "num_heads": 2}),
+    "f32_d64": ("tiny_f32", [90, 31], True, {"key_dim": 64, "value_dim": 64, "num_partitions": 8, "top_k": 2}),
+}
+
+
+def _case(name):
+    wname, lengths, with_init, over = CASES[name]
+    w = H_.workload_variant(wname, **over)
+    inp = synth.make_forward_inputs(w, seed=0, lengths=lengths, with_init=with_init)
+    return w, inp
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("algo", ["auto", "recurrent"])
+def test_forward_matches_oracle(name, algo):
+    w, inp = _case(name)
+    gpu = H_.run_gpu_forward(w, inp, algo=algo)
+    ref = H_.run_oracle_forward(w, inp)
+    tol = H_.tol_for(w)
+    assert np.array_equal(gpu["topk_idx"], ref["topk_idx"])
+    np.testing.assert_allclose(gpu["topk_w"], ref["topk_w"], rtol=2e-6, atol=1e-7)
+    assert H_.max_abs_rel(gpu["out"], ref["out"]) < tol
+    assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < tol
+    assert gpu["device_flags"] == 0
+
+
+def test_forward_scale_and_separate_shared_qk():
+    w, inp = _case("layer_bf16_ragged")
+    rng = np.random.default_rng(5)
+    qs = synth.f32_to_bf16_bits(rng.normal(size=inp.q.shape).astype(np.float32) / 8)
+    ks = synth.f32_to_bf16_bits(rng.random(size=inp.k.shape).astype(np.float32) / 64)
+    gpu = H_.run_gpu_forward(w, inp, scale=0.37, q_shared=qs, k_shared=ks)
+    ref = H_.run_oracle_forward(w, inp, scale=0.37, q_shared=qs, k_shared=ks)
+    assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
+    assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
+
+
+def test_unselected_partitions_final_state_bitwise():
+    w = H_.workload_variant("small_bf16", num_partitions=6, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=3, lengths=[300, 45], with_init=True)
+    lg = inp.logits.copy()
+    lg[..., 4:] = synth.f32_to_bf16_bits(np.full(lg[..., 4:].shape, -60.0, np.float32))
+    inp.logits = lg
+    for algo in ("auto", "recurrent"):
+        gpu = H_.run_gpu_forward(w, inp, algo=algo)
+        assert np.array_equal(gpu["final_state"][:, :, 4:6], inp.init_state[:, :, 4:6])
+
+
+def test_all_sequences_empty():
+    w = H_.workload_variant("small_bf16", num_heads=2)
+    inp = synth.make_forward_inputs(w, seed=1, lengths=[0, 0, 0], with_init=True)
+    gpu = H_.run_gpu_forward(w, inp)
+    assert np.array_equal(gpu["final_state"], inp.init_state)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32_init_varlen", "layer_bf16_ragged", "varlen_bf16_init"])
+def test_route_grouping_bit_exact(name):
+    import oracle
+    from sparse_state_linear_router_gb300 import binding
+    w, inp = _case(name)
+    cfg = H_.config_of(w)
+    lg = binding.to_device(inp.logits)
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    r = binding.route(cfg, lg, cu)
+    torch.cuda.synchronize()
+    idx = H_.to_numpy(r["topk_idx"])
+    assert np.array_equal(idx, _stable_topk(inp.logits, w.top_k))
+    seg_off, perm = oracle.group(idx, inp.cu_seqlens, w.num_partitions)
+    assert np.array_equal(H_.to_numpy(r["seg_off"]).astype(np.int64), seg_off)
+    assert np.array_equal(H_.to_numpy(r["perm"]).astype(np.int64), perm)
+
+
+def test_route_ties_bit_exact():
+    """Router logits drawn from a handful of values: many exact ties, broken
+    toward the lower partition index, identical to a stable argsort."""
+    import oracle
+    from sparse_state_linear_router_gb300 import binding
+    w = H_.workload_variant("small_bf16", num_partitions=16, top_k=4, num_heads=3)
+    inp = synth.make_forward_inputs(w, seed=2, lengths=[513, 0, 257])
+    rng = np.random.default_rng(9)
+    inp.logits = synth.f32_to_bf16_bits(rng.integers(-1, 2, size=inp.logits.shape).astype(np.float32))
+    cfg = H_.config_of(w)
+    r = binding.route(cfg, binding.to_device(inp.logits), torch.from_numpy(inp.cu_seqlens).cuda())
+    torch.cuda.synchronize()
+    idx = H_.to_numpy(r["topk_idx"])
+    assert np.array_equal(idx, _stable_topk(inp.logits, w.top_k))
+    seg_off, perm = oracle.group(idx, inp.cu_seqlens, w.num_partitions)
+    assert np.array_equal(H_.to_numpy(r["perm"]).astype(np.int64), perm)
+    assert np.array_equal(H_.to_numpy(r["seg_off"]).astype(np.int64), seg_off)
+
+
+@pytest.mark.parametrize("wname", ["layer_bf16", "varlen_bf16"])
+def test_full_size_sampled_pairs(wname):
+    """Full workload size in the benchmark's launch configuration; the oracle
+    recomputes a sample of (sequence, head) pairs; routing is checked on every
+    token against a stable argsort."""
+    w = synth.WORKLOADS[wname]
+    inp = synth.make_forward_inputs(w, seed=0)
+    gpu = H_.run_gpu_forward(w, inp)
+    assert gpu["device_flags"] == 0
+    assert np.array_equal(gpu["topk_idx"], _stable_topk(inp.logits, w.top_k))
+    S, H = inp.num_seqs, w.num_heads
+    rng = np.random.default_rng(123)
+    pairs = sorted(set(rng.choice(S * H, size=6, replace=False).tolist()) | {S * H - 1})
+    ref = H_.run_oracle_forward(w, inp, pairs=pairs)
+    for (rows, h), p in zip(H_.pair_rows(inp, H, pairs), pairs):
+        b = p // H
+        assert H_.max_abs_rel(gpu["out"][rows, h], ref["out"][rows, h]) < H_.TOL_BF16
+        assert H_.max_abs_rel(gpu["final_state"][b, h], ref["final_state"][b, h]) < H_.TOL_BF16
