@@ -144,6 +144,21 @@ sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, 
                          int32_t *topk_idx, float *topk_w,
                          void *workspace, size_t workspace_bytes, sse_stream_t stream);
 
+/* sse_forward with timing hooks and a launch count (for benchmarks).
+ * stage_events (NULL = none): four caller-created cudaEvent_t handles, each
+ * recorded on `stream`: [0] before the first launch, [1] after the routing and
+ * grouping kernels, [2] after the main segment kernel, [3] after the last
+ * kernel.  num_launches (NULL = none) receives the number of kernels the call
+ * launched.  Everything else is exactly sse_forward. */
+sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                               const void *log_gate, const void *router_logits,
+                               const void *q_shared, const void *k_shared,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                               const float *initial_state, float *final_state, void *out,
+                               int32_t *topk_idx, float *topk_w,
+                               void *workspace, size_t workspace_bytes, sse_stream_t stream,
+                               void *const *stage_events, int32_t *num_launches);
+
 /* ---------------------------------------------------------------------------
  * sse_decode_step -- one token per sequence on states resident in device
  * memory (section 2.6: decoding recurs only on the selected states).  Reads
@@ -166,9 +181,10 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
 /* Device-side check flags (bit mask). */
 enum { SSE_DEVICE_GATE_RANGE = 1 };
 
-/* Reads (and clears) the device-check flags that the last sse_forward using
- * `workspace` recorded.  Synchronizes `stream`.  *flags receives the bit mask;
- * returns SSE_ERR_DEVICE if any flag was set, SSE_ERR_CUDA on a copy failure. */
+/* Reads the device-check flags recorded by the last sse_forward that used
+ * `workspace` (each sse_forward clears them first).  Synchronizes `stream`.
+ * *flags receives the bit mask; returns SSE_ERR_DEVICE if any flag is set,
+ * SSE_ERR_CUDA if the copy fails. */
 sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_t stream);
 
 #ifdef __cplusplus

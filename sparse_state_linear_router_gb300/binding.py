@@ -25,7 +25,8 @@ _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_A
 
 # Every extern "C" symbol that include/sse.h declares.
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
-            "sse_forward_workspace_size", "sse_forward", "sse_decode_step", "sse_read_device_status")
+            "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
+            "sse_read_device_status")
 
 
 class sse_config_t(ctypes.Structure):
@@ -67,6 +68,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sse_forward_workspace_size.argtypes = [cfgp, i64, i32]
     lib.sse_forward.restype = ctypes.c_int
     lib.sse_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, sz, P]
+    lib.sse_forward_timed.restype = ctypes.c_int
+    lib.sse_forward_timed.argtypes = [cfgp, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, sz, P,
+                                      P, ctypes.POINTER(i32)]
     lib.sse_decode_step.restype = ctypes.c_int
     lib.sse_decode_step.argtypes = [cfgp, P, P, P, P, P, P, P, i32, P, P, P, P, P]
     lib.sse_read_device_status.restype = ctypes.c_int
@@ -106,6 +110,21 @@ def sse_forward(cfg, q, k, v, log_gate, logits, q_shared, k_shared, cu_seqlens, 
     return load().sse_forward(ctypes.byref(cfg), q, k, v, log_gate, logits, q_shared, k_shared,
                               cu_seqlens, num_seqs, total_tokens, initial_state, final_state, out,
                               topk_idx, topk_w, workspace, workspace_bytes, stream)
+
+
+def sse_forward_timed(cfg, q, k, v, log_gate, logits, q_shared, k_shared, cu_seqlens, num_seqs,
+                      total_tokens, initial_state, final_state, out, topk_idx, topk_w, workspace,
+                      workspace_bytes, stream, stage_events=None):
+    """Returns (status, kernels launched).  stage_events: 4 raw cudaEvent_t handles or None."""
+    ev = None
+    if stage_events is not None:
+        ev = (ctypes.c_void_p * 4)(*stage_events)
+    n = ctypes.c_int32(0)
+    st = load().sse_forward_timed(ctypes.byref(cfg), q, k, v, log_gate, logits, q_shared, k_shared,
+                                  cu_seqlens, num_seqs, total_tokens, initial_state, final_state, out,
+                                  topk_idx, topk_w, workspace, workspace_bytes, stream, ev,
+                                  ctypes.byref(n))
+    return st, n.value
 
 
 def sse_decode_step(cfg, q, k, v, log_gate, logits, q_shared, k_shared, batch, state, out,

@@ -150,12 +150,14 @@ size_t sse_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens,
     return carve_forward(nullptr, *cfg, total_tokens, num_seqs, nullptr, nullptr).bytes;
 }
 
-sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
-                         const void *log_gate, const void *router_logits, const void *q_shared,
-                         const void *k_shared, const int32_t *cu_seqlens, int32_t num_seqs,
-                         int64_t total_tokens, const float *initial_state, float *final_state,
-                         void *out, int32_t *topk_idx, float *topk_w, void *workspace,
-                         size_t workspace_bytes, sse_stream_t stream) {
+sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                               const void *log_gate, const void *router_logits, const void *q_shared,
+                               const void *k_shared, const int32_t *cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, const float *initial_state, float *final_state,
+                               void *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                               size_t workspace_bytes, sse_stream_t stream, void *const *stage_events,
+                               int32_t *num_launches) {
+    if (num_launches) *num_launches = 0;
     sse_status_t st = check_config(cfg);
     if (st != SSE_OK) return st;
     if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
@@ -163,8 +165,9 @@ sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, 
     if (!cu_seqlens) return SSE_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !log_gate || !router_logits || !out))
         return SSE_ERR_INVALID_ARG;
-    for (const void *p : std::initializer_list<const void *>{q, k, v, log_gate, router_logits, q_shared, k_shared, out,
-                          (const void *)initial_state, (const void *)final_state})
+    for (const void *p : std::initializer_list<const void *>{q, k, v, log_gate, router_logits, q_shared,
+                                                             k_shared, out, (const void *)initial_state,
+                                                             (const void *)final_state})
         if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
     if (use_chunked(c)) {
         if (!sse::chunked_supported(c)) return SSE_ERR_UNSUPPORTED;
@@ -176,10 +179,16 @@ sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, 
         return SSE_ERR_WORKSPACE;
     if (num_seqs == 0) return SSE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    auto mark = [&](int i) {
+        return stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s) : cudaSuccess;
+    };
     ForwardLayout L = carve_forward(workspace, c, total_tokens, num_seqs, topk_idx, topk_w);
+    if (mark(0) != cudaSuccess) return SSE_ERR_CUDA;
     if (cudaMemsetAsync(L.flags, 0, 64 * sizeof(int32_t), s) != cudaSuccess) return SSE_ERR_CUDA;
     cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, true, s);
     if (e != cudaSuccess) return SSE_ERR_CUDA;
+    int launches = sse::kRouteLaunches;
+    if (mark(1) != cudaSuccess) return SSE_ERR_CUDA;
     sse::ForwardArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = log_gate; a.qs = q_shared; a.ks = k_shared;
     a.cu_seqlens = cu_seqlens;
@@ -194,14 +203,32 @@ sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, 
     a.part_routed = L.part_routed;
     a.part_shared = L.part_shared;
     a.flags = L.flags;
+    a.chunk_ws = L.chunk_ws;
     if (use_chunked(c)) {
-        e = sse::launch_forward_chunked(c, a, s);
-        (void)L.chunk_ws;
+        e = sse::launch_forward_chunked(c, a, s, &launches);
+        if (e == cudaSuccess && mark(2) != cudaSuccess) return SSE_ERR_CUDA;
     } else {
         e = sse::launch_forward_recurrent(c, a, s);
+        launches += 1;
+        if (e == cudaSuccess && mark(2) != cudaSuccess) return SSE_ERR_CUDA;
         if (e == cudaSuccess) e = sse::launch_combine(c, a, s);
+        launches += 1;
     }
-    return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+    if (e != cudaSuccess) return SSE_ERR_CUDA;
+    if (mark(3) != cudaSuccess) return SSE_ERR_CUDA;
+    if (num_launches) *num_launches = launches;
+    return SSE_OK;
+}
+
+sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                         const void *log_gate, const void *router_logits, const void *q_shared,
+                         const void *k_shared, const int32_t *cu_seqlens, int32_t num_seqs,
+                         int64_t total_tokens, const float *initial_state, float *final_state,
+                         void *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                         size_t workspace_bytes, sse_stream_t stream) {
+    return sse_forward_timed(cfg, q, k, v, log_gate, router_logits, q_shared, k_shared, cu_seqlens,
+                             num_seqs, total_tokens, initial_state, final_state, out, topk_idx, topk_w,
+                             workspace, workspace_bytes, stream, nullptr, nullptr);
 }
 
 sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void *k, const void *v,

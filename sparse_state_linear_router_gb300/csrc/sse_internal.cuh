@@ -13,6 +13,7 @@ namespace sse {
 constexpr int kMaxPartitions = 64;
 constexpr int kMaxTopK = 8;
 constexpr int kRouteBlock = 256;  // tokens per routing block (one thread per token)
+constexpr int kRouteLaunches = 5; // kernels launch_route issues when grouping
 
 // ---------------------------------------------------------------------------
 // Element access for the two storage dtypes.
@@ -145,6 +146,7 @@ struct ForwardArgs {
     float *part_routed;  // [T, H, k, d] fp32
     float *part_shared;  // [T, H, d] fp32
     int32_t *flags;
+    void *chunk_ws;      // chunked path scratch
 };
 
 bool recurrent_supported(const sse_config_t &cfg);
@@ -152,7 +154,9 @@ cudaError_t launch_forward_recurrent(const sse_config_t &cfg, const ForwardArgs 
 
 bool chunked_supported(const sse_config_t &cfg);
 size_t chunked_extra_workspace(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs);
-cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+// Adds the number of kernels it launched to *launches.
+cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream,
+                                   int *launches);
 
 // out[t,h,:] = sum_j part_routed[t,h,j,:] + part_shared[t,h,:]
 cudaError_t launch_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
