@@ -178,8 +178,11 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
                              float *state, void *out, int32_t *topk_idx, float *topk_w,
                              sse_stream_t stream);
 
-/* Device-side check flags (bit mask). */
-enum { SSE_DEVICE_GATE_RANGE = 1 };
+/* Device-side check flags (bit mask).
+ *   SSE_DEVICE_GATE_RANGE: a chunk's log-gate sum left the chunked path's range
+ *   SSE_DEVICE_TIMEOUT:    a bounded wait on the tensor core expired; the
+ *                          affected segments stopped early (results invalid) */
+enum { SSE_DEVICE_GATE_RANGE = 1, SSE_DEVICE_TIMEOUT = 2 };
 
 /* Reads the device-check flags recorded by the last sse_forward that used
  * `workspace` (each sse_forward clears them first).  Synchronizes `stream`.

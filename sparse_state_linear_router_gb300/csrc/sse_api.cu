@@ -83,16 +83,9 @@ ForwardLayout carve_forward(void *ws, const sse_config_t &c, int64_t T, int32_t 
     ForwardLayout L{};
     L.flags = cv.take<int32_t>(64);
     L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
-    if (use_chunked(c)) {
-        const size_t extra = sse::chunked_extra_workspace(c, T, S);
-        L.chunk_ws = cv.take<unsigned char>(extra);
-        L.part_routed = nullptr;
-        L.part_shared = nullptr;
-    } else {
-        L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
-        L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
-        L.chunk_ws = nullptr;
-    }
+    L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
+    L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
+    L.chunk_ws = use_chunked(c) ? cv.take<unsigned char>(sse::chunked_extra_workspace(c, T, S)) : nullptr;
     L.bytes = (cv.off + 255) & ~size_t(255);
     return L;
 }

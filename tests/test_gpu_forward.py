@@ -36,6 +36,9 @@ CASES = {
     "k_equals_N": ("small_bf16", [250, 3], True, {"num_partitions": 4, "top_k": 4, "num_heads": 2}),
     "noshared_k3": ("layer_bf16", [333], True, {"num_partitions": 8, "top_k": 3, "use_shared": 0, "num_heads": 2}),
     "f32_d64": ("tiny_f32", [90, 31], True, {"key_dim": 64, "value_dim": 64, "num_partitions": 8, "top_k": 2}),
+    "c128_d64": ("layer_bf16", [129, 255, 1], True, {"value_dim": 64, "num_heads": 2}),
+    "c64_d128": ("layer_bf16", [128, 383], True, {"key_dim": 64, "num_heads": 2}),
+    "long_single": ("layer_bf16", [2000], True, {"num_heads": 1, "num_partitions": 2, "top_k": 1}),
 }
 
 
@@ -46,10 +49,16 @@ def _case(name):
     return w, inp
 
 
+def _chunked_ok(w):
+    return w.dtype == "bf16" and w.key_dim in (64, 128) and w.value_dim in (64, 128)
+
+
 @pytest.mark.parametrize("name", sorted(CASES))
-@pytest.mark.parametrize("algo", ["auto", "recurrent"])
+@pytest.mark.parametrize("algo", ["auto", "recurrent", "chunked"])
 def test_forward_matches_oracle(name, algo):
     w, inp = _case(name)
+    if algo == "chunked" and not _chunked_ok(w):
+        pytest.skip("shape/dtype outside the tensor-core path")
     gpu = H_.run_gpu_forward(w, inp, algo=algo)
     ref = H_.run_oracle_forward(w, inp)
     tol = H_.tol_for(w)
@@ -77,7 +86,7 @@ def test_unselected_partitions_final_state_bitwise():
     lg = inp.logits.copy()
     lg[..., 4:] = synth.f32_to_bf16_bits(np.full(lg[..., 4:].shape, -60.0, np.float32))
     inp.logits = lg
-    for algo in ("auto", "recurrent"):
+    for algo in ("recurrent", "chunked"):
         gpu = H_.run_gpu_forward(w, inp, algo=algo)
         assert np.array_equal(gpu["final_state"][:, :, 4:6], inp.init_state[:, :, 4:6])
 
