@@ -115,6 +115,27 @@ sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits,
                        int32_t *topk_idx, float *topk_w, int32_t *seg_off, int32_t *perm,
                        void *workspace, size_t workspace_bytes, sse_stream_t stream);
 
+/* sse_route_noalloc -- sse_route for callers that cannot allocate device
+ * memory (a plugin inside a host application that owns every device
+ * allocation, a latency-critical loop that cannot afford the device-wide
+ * synchronisation of cudaMalloc, a language without a CUDA allocator
+ * binding).  The source paper has no counterpart; this is an interface
+ * convenience.  Same arguments, outputs and results as sse_route, without the
+ * workspace: the routing scratch lives in a 4 MiB array inside the library's
+ * device image, reserved on every GPU that loads the library until the
+ * process exits.  Limit: (num_seqs + 1) + H * N * (ceil(total_tokens / 256)
+ * + num_seqs + 1) int32 entries (plus 256-byte alignment padding) must fit in
+ * 4 MiB -- about one million tokens at H = 16, N = 16; larger calls return
+ * SSE_ERR_WORKSPACE before any launch.  The first call on each device looks
+ * up the array's device address (make that first call before any stream
+ * capture).  Nothing is allocated or freed.  All calls on a device share the
+ * array and it keeps the previous call's contents (no entry needs to start
+ * at zero); calls that overlap on the GPU race on it and must be serialised. */
+sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *router_logits,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                               int32_t *topk_idx, float *topk_w, int32_t *seg_off, int32_t *perm,
+                               sse_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * sse_forward -- the SSE layer over packed varlen sequences (eqs. 9-14 and
  * the shared partition of section 2.5), computed per (sequence, head,

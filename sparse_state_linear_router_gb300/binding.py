@@ -25,7 +25,7 @@ _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_A
 
 # Every extern "C" symbol that include/sse.h declares.
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
-            "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
+            "sse_route_noalloc", "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
             "sse_read_device_status")
 
 
@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sse_route_workspace_size.argtypes = [cfgp, i64, i32]
     lib.sse_route.restype = ctypes.c_int
     lib.sse_route.argtypes = [cfgp, P, P, i32, i64, P, P, P, P, P, sz, P]
+    lib.sse_route_noalloc.restype = ctypes.c_int
+    lib.sse_route_noalloc.argtypes = [cfgp, P, P, i32, i64, P, P, P, P, P]
     lib.sse_forward_workspace_size.restype = sz
     lib.sse_forward_workspace_size.argtypes = [cfgp, i64, i32]
     lib.sse_forward.restype = ctypes.c_int

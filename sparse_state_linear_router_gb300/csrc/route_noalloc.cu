@@ -1,0 +1,103 @@
+// route_noalloc.cu -- sse_route_noalloc: the router and token->partition
+// grouping of sse_route for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain a workspace: a plugin running inside a
+// host application that owns every device allocation and hands out only the
+// tensors it manages, a serving loop that must never pay the device-wide
+// synchronisation a cudaMalloc can cause, or code written in a language with
+// no binding to the CUDA allocator.  This entry point needs only the caller's
+// inputs and outputs; the routing stage's scratch (per-sequence block
+// prefixes and per-block partition counts) lives in a fixed array that is
+// part of the library's own device image.
+//
+// That array exists once on every GPU that loads the library and stays
+// reserved there until the process exits.  All calls on a device share it,
+// and it keeps whatever the previous call left: nothing in it has to start
+// at zero, because each call writes every entry it reads before reading it.
+// Two calls whose kernels overlap on the same GPU (different streams, or
+// different host threads) race on the array and corrupt each other's
+// results; serialise them.
+#include <mutex>
+
+#include "sse_internal.cuh"
+
+namespace {
+
+// 4 MiB: room for (num_seqs + 1) + H * N * (ceil(T / 256) + num_seqs + 1)
+// int32 entries plus the 256-byte alignment of the two regions; with 16 heads
+// and 16 partitions that is about one million tokens per call.
+constexpr size_t kScratchBytes = size_t(4) << 20;
+
+static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void *g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mutex;
+
+// Device address of g_route_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// (once per device, with that device current) through the runtime.
+cudaError_t scratch_address(void **addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *router_logits,
+                                          const int32_t *cu_seqlens, int32_t num_seqs,
+                                          int64_t total_tokens, int32_t *topk_idx, float *topk_w,
+                                          int32_t *seg_off, int32_t *perm, sse_stream_t stream) {
+    // Argument checks: the same rules as sse_route, minus the workspace.
+    if (!cfg) return SSE_ERR_INVALID_ARG;
+    const sse_config_t &c = *cfg;
+    if (c.num_heads < 1 || c.key_dim < 1 || c.value_dim < 1) return SSE_ERR_INVALID_ARG;
+    if (c.num_partitions < 1 || c.top_k < 1 || c.top_k > c.num_partitions) return SSE_ERR_INVALID_ARG;
+    if (c.use_shared != 0 && c.use_shared != 1) return SSE_ERR_INVALID_ARG;
+    if (c.dtype != SSE_F32 && c.dtype != SSE_BF16) return SSE_ERR_INVALID_ARG;
+    if (c.num_partitions > sse::kMaxPartitions || c.top_k > sse::kMaxTopK) return SSE_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || (num_seqs == 0 && total_tokens != 0)) return SSE_ERR_INVALID_ARG;
+    if (total_tokens * c.num_heads * c.top_k >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    if (!cu_seqlens || !topk_idx || (total_tokens > 0 && !router_logits)) return SSE_ERR_INVALID_ARG;
+    if (!aligned16(router_logits)) return SSE_ERR_INVALID_ARG;
+    const bool group = seg_off || perm;
+    if (group && !(seg_off && perm)) return SSE_ERR_INVALID_ARG;
+
+    // Scratch layout and the size limit, checked before any CUDA call.
+    const int64_t max_blocks = sse::route_max_blocks(total_tokens, num_seqs);
+    const int64_t cnt_entries = (int64_t)c.num_heads * c.num_partitions * (max_blocks + 1);
+    sse::Carver cv(nullptr);
+    cv.take<int32_t>((size_t)num_seqs + 1);
+    cv.take<int32_t>((size_t)cnt_entries);
+    if (cv.off > kScratchBytes) return SSE_ERR_WORKSPACE;
+    if (num_seqs == 0) return SSE_OK;
+
+    void *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return SSE_ERR_CUDA;
+    sse::Carver sc(scratch);
+    sse::RouteBuffers rb{};
+    rb.max_blocks = (int32_t)max_blocks;
+    rb.blk_prefix = sc.take<int32_t>((size_t)num_seqs + 1);
+    rb.cnt = sc.take<int32_t>((size_t)cnt_entries);
+    rb.seg_off = seg_off;
+    rb.topk_idx = topk_idx;
+    rb.topk_w = topk_w;
+    rb.perm = perm;
+    rb.perm_rec = nullptr;
+    cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, rb, group,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
