@@ -225,11 +225,13 @@ def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
-    w_fwd, w_dec = synth.WORKLOADS[FWD_WORKLOAD], synth.WORKLOADS[DEC_WORKLOAD]
+    w_fwd, w_dec = synth.WORKLOADS[args.fwd_workload], synth.WORKLOADS[DEC_WORKLOAD]
     fwd_inp = synth.make_forward_inputs(w_fwd, seed=0)
     dec_steps = [synth.make_decode_inputs(w_dec, s, batch=16) for s in range(4)]
     T = fwd_inp.total_tokens
     B = w_dec.decode_batch
+    do_fwd = args.part in ("both", "forward")
+    do_dec = args.part in ("both", "decode")
     smp = OracleSampler(fwd_inp, w_fwd, dec_steps, w_dec, dec_seqs=16)
     for _ in range(args.warmup):
         smp.once()
@@ -239,23 +241,39 @@ def run_reference(args):
         smp.once()
     wall = time.perf_counter() - t0
     fwd_tps, dec_tps = smp.rates()
-    value = step_equivalent_tps(T, B, fwd_tps, dec_tps)
-    threads = smp.threads
+    if do_fwd and do_dec:
+        value = step_equivalent_tps(T, B, fwd_tps, dec_tps)
+    else:
+        value = fwd_tps if do_fwd else dec_tps
+    parts = ([describe_forward(w_fwd, fwd_inp)] if do_fwd else []) + ([describe_decode(w_dec)] if do_dec else [])
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{FWD_WORKLOAD} forward (8x4096 tokens, H16, c=d=128, N8, k2, shared) + "
-                               f"{DEC_WORKLOAD} step (256 seqs, H16, c=d=128, N16, k2, shared)",
-                   "fwd_tokens_per_step": T, "decode_tokens_per_step": B},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "config": {"workload": " + ".join(parts), "fwd_tokens_per_step": T if do_fwd else 0,
+                   "decode_tokens_per_step": B if do_dec else 0},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
                          "sample": "per step: " + smp.sample_text() + "; value = tokens/s of one full step "
                                                                        "at the measured forward and decode rates"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def describe_forward(w, inp):
+    lens = np.diff(inp.cu_seqlens)
+    shape = (f"{inp.num_seqs} seqs x {int(lens[0])} tokens" if np.all(lens == lens[0])
+             else f"{inp.num_seqs} varlen seqs, {inp.total_tokens} tokens")
+    return (f"{w.name} forward ({shape}, H{w.num_heads}, c={w.key_dim}, d={w.value_dim}, "
+            f"N{w.num_partitions}, top-{w.top_k}{', shared' if w.use_shared else ''}, {w.dtype} in, fp32 state"
+            f"{', random initial state' if inp.init_state is not None else ''})")
+
+
+def describe_decode(w):
+    return (f"{w.name} step ({w.decode_batch} seqs x H{w.num_heads}, c={w.key_dim}, d={w.value_dim}, "
+            f"N{w.num_partitions}, top-{w.top_k}{', shared' if w.use_shared else ''}, fp32 states resident)")
 
 
 def run_native(args):
@@ -271,33 +289,38 @@ def run_native(args):
         from sparse_state_linear_router_gb300 import build as libbuild
         libbuild.build()
     binding.load()
-
-    w_fwd, w_dec = synth.WORKLOADS[FWD_WORKLOAD], synth.WORKLOADS[DEC_WORKLOAD]
-    fwd_inp = synth.make_forward_inputs(w_fwd, seed=rank)
-    T, S = fwd_inp.total_tokens, fwd_inp.num_seqs
-    B = w_dec.decode_batch
-    nsteps = args.warmup + args.steps
-    pool = min(nsteps, 64)
-    dec_host = [synth.make_decode_inputs(w_dec, s) for s in range(pool)]
-    cfg_f = binding.make_config(w_fwd.num_heads, w_fwd.key_dim, w_fwd.value_dim, w_fwd.num_partitions,
-                                w_fwd.top_k, w_fwd.use_shared, 1.0, w_fwd.dtype, args.algo)
-    cfg_d = binding.make_config(w_dec.num_heads, w_dec.key_dim, w_dec.value_dim, w_dec.num_partitions,
-                                w_dec.top_k, w_dec.use_shared, 1.0, w_dec.dtype)
+    do_fwd = args.part in ("both", "forward")
+    do_dec = args.part in ("both", "decode")
     names = ("q", "k", "v", "g", "logits")
-    f = {n: binding.to_device(getattr(fwd_inp, n), dev) for n in names}
-    cu = torch.from_numpy(fwd_inp.cu_seqlens).to(dev)
-    H, d = w_fwd.num_heads, w_fwd.value_dim
-    P = w_fwd.num_slots
-    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
-    fin = torch.empty((S, H, P, w_fwd.key_dim, d), dtype=torch.float32, device=dev)
-    wsp = binding.forward_workspace(cfg_f, T, S, dev)
-    dq = [{n: binding.to_device(getattr(x, n), dev) for n in names} for x in dec_host]
-    state = torch.zeros((B, w_dec.num_heads, w_dec.num_slots, w_dec.key_dim, w_dec.value_dim),
-                        dtype=torch.float32, device=dev)
-    dout = torch.empty((B, w_dec.num_heads, w_dec.value_dim), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     P_ = binding._ptr
+    launches = {"n": 0}
+
+    w_fwd, w_dec = synth.WORKLOADS[args.fwd_workload], synth.WORKLOADS[DEC_WORKLOAD]
+    fwd_inp = synth.make_forward_inputs(w_fwd, seed=rank)   # also the CPU-baseline sample
+    T, S = fwd_inp.total_tokens, fwd_inp.num_seqs
+    B = w_dec.decode_batch
+    pool = min(args.warmup + args.steps, 64)
+    dec_host = [synth.make_decode_inputs(w_dec, s) for s in range(pool if do_dec else 4)]
+
+    if do_fwd:
+        cfg_f = binding.make_config(w_fwd.num_heads, w_fwd.key_dim, w_fwd.value_dim, w_fwd.num_partitions,
+                                    w_fwd.top_k, w_fwd.use_shared, 1.0, w_fwd.dtype, args.algo)
+        f = {n: binding.to_device(getattr(fwd_inp, n), dev) for n in names}
+        cu = torch.from_numpy(fwd_inp.cu_seqlens).to(dev)
+        init = None if fwd_inp.init_state is None else torch.from_numpy(fwd_inp.init_state).to(dev)
+        out = torch.empty((T, w_fwd.num_heads, w_fwd.value_dim), dtype=torch.bfloat16, device=dev)
+        fin = torch.empty((S, w_fwd.num_heads, w_fwd.num_slots, w_fwd.key_dim, w_fwd.value_dim),
+                          dtype=torch.float32, device=dev)
+        wsp = binding.forward_workspace(cfg_f, T, S, dev)
+    if do_dec:
+        cfg_d = binding.make_config(w_dec.num_heads, w_dec.key_dim, w_dec.value_dim, w_dec.num_partitions,
+                                    w_dec.top_k, w_dec.use_shared, 1.0, w_dec.dtype)
+        dq = [{n: binding.to_device(getattr(x, n), dev) for n in names} for x in dec_host]
+        state = torch.zeros((B, w_dec.num_heads, w_dec.num_slots, w_dec.key_dim, w_dec.value_dim),
+                            dtype=torch.float32, device=dev)
+        dout = torch.empty((B, w_dec.num_heads, w_dec.value_dim), dtype=torch.bfloat16, device=dev)
 
     def new_events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -305,18 +328,15 @@ def run_native(args):
             e.record(stream)   # materialise the handles
         return evs
 
-    launches = {"n": 0}
-
-    def forward_call(fin_t, out_t, stage_events=None):
-        st, n = binding.sse_forward_timed(cfg_f, P_(f["q"]), P_(f["k"]), P_(f["v"]), P_(f["g"]),
-                                          P_(f["logits"]), None, None, P_(cu), S, T, None, P_(fin_t),
-                                          P_(out_t), None, None, P_(wsp), wsp.numel(), sh,
+    def forward_call(src, stage_events=None):
+        st, n = binding.sse_forward_timed(cfg_f, P_(src["q"]), P_(src["k"]), P_(src["v"]), P_(src["g"]),
+                                          P_(src["logits"]), None, None, P_(cu), S, T, P_(init), P_(fin),
+                                          P_(out), None, None, P_(wsp), wsp.numel(), sh,
                                           None if stage_events is None else [e.cuda_event for e in stage_events])
         binding._check(st, "sse_forward_timed")
         launches["n"] += n
 
-    def decode_call(i, inputs=None):
-        x = dq[i % pool] if inputs is None else inputs
+    def decode_call(x):
         st = binding.sse_decode_step(cfg_d, P_(x["q"]), P_(x["k"]), P_(x["v"]), P_(x["g"]),
                                      P_(x["logits"]), None, None, B, P_(state), P_(dout), None, None, sh)
         binding._check(st, "sse_decode_step")
@@ -327,13 +347,23 @@ def run_native(args):
             import torch.distributed as dist
             dist.barrier()
 
+    def max_over_ranks(x):
+        if ws > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([x], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            return float(tt.item())
+        return x
+
     # ---- device-resident timing -------------------------------------------
     for i in range(args.warmup):
-        forward_call(fin, out)
-        decode_call(i)
+        if do_fwd:
+            forward_call(f)
+        if do_dec:
+            decode_call(dq[i % pool])
     torch.cuda.synchronize()
-    fwd_ev = [new_events(4) for _ in range(args.steps)]
-    dec_ev = [new_events(2) for _ in range(args.steps)]
+    fwd_ev = [new_events(4) for _ in range(args.steps)] if do_fwd else []
+    dec_ev = [new_events(2) for _ in range(args.steps)] if do_dec else []
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier()
@@ -342,88 +372,96 @@ def run_native(args):
         time.sleep(0.15)
         t_start.record(stream)
         for i in range(args.steps):
-            forward_call(fin, out, fwd_ev[i])
-            dec_ev[i][0].record(stream)
-            decode_call(args.warmup + i)
-            dec_ev[i][1].record(stream)
+            if do_fwd:
+                forward_call(f, fwd_ev[i])
+            if do_dec:
+                dec_ev[i][0].record(stream)
+                decode_call(dq[(args.warmup + i) % pool])
+                dec_ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         time.sleep(0.15)
     barrier()
     timed_launches = launches["n"]
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-    ms_step = elapsed_ms / args.steps
-    fwd_main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in fwd_ev)
-    fwd_route_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in fwd_ev)
-    fwd_tail_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in fwd_ev)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in fwd_ev)
-    dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in dec_ev)
-    tokens_step = T + B
+    ms_step = max_over_ranks(t_start.elapsed_time(t_end)) / args.steps
+    tokens_step = (T if do_fwd else 0) + (B if do_dec else 0)
     value = ws * tokens_step / (ms_step * 1e-3)
 
     peaks = _peaks()
     hbm = peaks["hbm_gbs"]
-    b_main = forward_main_bytes(w_fwd, T, S)
-    b_dec = decode_bytes(w_dec, B)
-    kernels = {
-        "forward_main": {"ms": fwd_main_ms, "bytes": b_main, "gbs": b_main / (fwd_main_ms * 1e6)},
-        "decode": {"ms": dec_ms, "bytes": b_dec, "gbs": b_dec / (dec_ms * 1e6)},
-    }
+    has_init = fwd_inp.init_state is not None
+    kernels, extra = {}, {}
+    step_bytes = step_flops = 0
+    if do_fwd:
+        fwd_main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in fwd_ev)
+        fwd_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in fwd_ev)
+        b_main = forward_main_bytes(w_fwd, T, S, init=has_init)
+        kernels["forward_main"] = {"ms": fwd_main_ms, "bytes": b_main, "gbs": b_main / (fwd_main_ms * 1e6)}
+        fb = forward_step_bytes(w_fwd, T, S, init=has_init)
+        ff = forward_flops(w_fwd, T)
+        step_bytes += fb
+        step_flops += ff
+        extra["forward"] = {
+            "ms": fwd_ms, "route_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in fwd_ev),
+            "main_ms": fwd_main_ms, "tail_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in fwd_ev),
+            "tokens_per_s": T / (fwd_ms * 1e-3),
+            "roofline_frac": max(ff / (peaks["bf16_tflops"] * 1e12), fb / (hbm * 1e9)) / (fwd_ms * 1e-3)}
+    if do_dec:
+        dec_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in dec_ev)
+        b_dec = decode_bytes(w_dec, B)
+        kernels["decode"] = {"ms": dec_ms, "bytes": b_dec, "gbs": b_dec / (dec_ms * 1e6)}
+        step_bytes += b_dec
+        step_flops += decode_flops(w_dec, B)
+        extra["decode"] = {"ms": dec_ms, "tokens_per_s": B / (dec_ms * 1e-3),
+                           "hbm_frac": (b_dec / (dec_ms * 1e-3)) / (hbm * 1e9)}
     dom_name = max(kernels, key=lambda kname: kernels[kname]["ms"])
     dom = kernels[dom_name]
-    step_bytes = forward_step_bytes(w_fwd, T, S) + b_dec
-    step_flops = forward_flops(w_fwd, T) + decode_flops(w_dec, B)
     t_bind = max(step_flops / (peaks["bf16_tflops"] * 1e12), step_bytes / (hbm * 1e9))
 
     # ---- end to end through the C ABI with host buffers ---------------------
     e2e = None
     if not args.no_e2e:
-        hf = {n: f[n].cpu().pin_memory() for n in names}
-        hd = [{n: dq[i][n].cpu().pin_memory() for n in names} for i in range(min(pool, 8))]
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
-        df = {n: torch.empty_like(f[n]) for n in names}
-        dd = {n: torch.empty_like(dq[0][n]) for n in names}
-        h2d = sum(hf[n].numel() * hf[n].element_size() for n in names) + \
-            sum(hd[0][n].numel() * hd[0][n].element_size() for n in names)
-        d2h = hout.numel() * hout.element_size() + hdout.numel() * hdout.element_size()
+        h2d = d2h = 0
+        if do_fwd:
+            hf = {n: f[n].cpu().pin_memory() for n in names}
+            df = {n: torch.empty_like(f[n]) for n in names}
+            hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            h2d += sum(hf[n].numel() * hf[n].element_size() for n in names)
+            d2h += hout.numel() * hout.element_size()
+        if do_dec:
+            hd = [{n: dq[i][n].cpu().pin_memory() for n in names} for i in range(min(pool, 8))]
+            dd = {n: torch.empty_like(dq[0][n]) for n in names}
+            hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+            h2d += sum(hd[0][n].numel() * hd[0][n].element_size() for n in names)
+            d2h += hdout.numel() * hdout.element_size()
 
         def e2e_step(i):
-            for n in names:
-                df[n].copy_(hf[n], non_blocking=True)
-            st, _ = binding.sse_forward_timed(cfg_f, P_(df["q"]), P_(df["k"]), P_(df["v"]), P_(df["g"]),
-                                              P_(df["logits"]), None, None, P_(cu), S, T, None, P_(fin),
-                                              P_(out), None, None, P_(wsp), wsp.numel(), sh, None)
-            binding._check(st, "sse_forward_timed")
-            x = hd[i % len(hd)]
-            for n in names:
-                dd[n].copy_(x[n], non_blocking=True)
-            decode_call(0, dd)
-            hout.copy_(out, non_blocking=True)
-            hdout.copy_(dout, non_blocking=True)
+            if do_fwd:
+                for n in names:
+                    df[n].copy_(hf[n], non_blocking=True)
+                forward_call(df)
+            if do_dec:
+                x = hd[i % len(hd)]
+                for n in names:
+                    dd[n].copy_(x[n], non_blocking=True)
+                decode_call(dd)
+            if do_fwd:
+                hout.copy_(out, non_blocking=True)
+            if do_dec:
+                hdout.copy_(dout, non_blocking=True)
 
         for i in range(args.warmup):
             e2e_step(i)
         torch.cuda.synchronize()
         barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
         for i in range(args.steps):
             e2e_step(i)
-        b.record(stream)
+        eb.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = a.elapsed_time(b) / args.steps
-        if ws > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(ea.elapsed_time(eb) / args.steps)
         e2e = {"value": ws * tokens_step / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
@@ -434,23 +472,26 @@ def run_native(args):
         t0 = time.perf_counter()
         smp.run_for(args.cpu_seconds)
         fwd_tps, dec_tps = smp.rates()
-        cpu = {"value": step_equivalent_tps(T, B, fwd_tps, dec_tps), "unit": "tokens/s",
-               "cores": smp.threads, "kind": "oracle",
+        if do_fwd and do_dec:
+            cv = step_equivalent_tps(T, B, fwd_tps, dec_tps)
+        else:
+            cv = fwd_tps if do_fwd else dec_tps
+        cpu = {"value": cv, "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
                "sample": smp.sample_text() + "; value = tokens/s of one full step at the measured rates",
                "seconds": round(time.perf_counter() - t0, 1)}
 
     if rank != 0:
         return 0
+    parts = ([describe_forward(w_fwd, fwd_inp)] if do_fwd else []) + ([describe_decode(w_dec)] if do_dec else [])
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
-            "workload": f"{FWD_WORKLOAD} forward (8 seqs x 4096 tokens, H16, c=d=128, N8, top-2, shared, "
-                        f"bf16 in, fp32 state) + {DEC_WORKLOAD} step (256 seqs x H16, c=d=128, N16, top-2, "
-                        f"shared, fp32 states resident)",
-            "fwd_tokens_per_step": T, "decode_tokens_per_step": B, "algo": args.algo,
-            "l2": "inputs larger than L2 (545 MB forward token tensors, 4.6 GB decode states); no flush",
+            "workload": " + ".join(parts),
+            "fwd_tokens_per_step": T if do_fwd else 0, "decode_tokens_per_step": B if do_dec else 0,
+            "algo": args.algo,
+            "l2": "inputs larger than L2 (forward token tensors >= 545 MB, 4.6 GB decode states); no flush",
         },
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": dom["gbs"], "peak": hbm,
                      "unit": "GB/s", "frac": dom["gbs"] / hbm, "traffic": None,
@@ -458,12 +499,7 @@ def run_native(args):
                      "algorithmic_bytes_per_launch": dom["bytes"], "avg_launch_ms": dom["ms"]},
         "kernels": {k_: {"avg_ms": v["ms"], "algorithmic_bytes": v["bytes"], "gbs": v["gbs"],
                          "frac_of_hbm_peak": v["gbs"] / hbm} for k_, v in kernels.items()},
-        "forward": {"ms": fwd_ms, "route_ms": fwd_route_ms, "main_ms": fwd_main_ms, "tail_ms": fwd_tail_ms,
-                    "tokens_per_s": T / (fwd_ms * 1e-3),
-                    "roofline_frac": max(forward_flops(w_fwd, T) / (peaks["bf16_tflops"] * 1e12),
-                                         forward_step_bytes(w_fwd, T, S) / (hbm * 1e9)) / (fwd_ms * 1e-3)},
-        "decode": {"ms": dec_ms, "tokens_per_s": B / (dec_ms * 1e-3),
-                   "hbm_frac": (b_dec / (dec_ms * 1e-3)) / (hbm * 1e9)},
+        **extra,
         "step_roofline_frac": t_bind / (ms_step * 1e-3),
         "gpu_launches": timed_launches,
         "clocks": clk.summary(),
@@ -487,6 +523,10 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--part", choices=["both", "forward", "decode"], default="both",
+                    help="time the whole step (default) or only one of its two calls")
+    ap.add_argument("--fwd-workload", choices=["layer_bf16", "varlen_bf16", "small_bf16"],
+                    default=FWD_WORKLOAD, help="forward batch of the step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -20,14 +20,22 @@
 // place (also producing the bf16 copy used by Qt S), lets the tensor core
 // accumulate Kt^T V into it, and sets p = exp(G_last - G_m).
 //
-// One CTA per segment (routed (b,h,i) or shared (b,h); shared first as they
-// are the longest); 8 warps.  Per chunk: all threads build Qt, Kt, V in
-// shared memory (128B-swizzled, see umma.cuh); the state rows are rescaled
-// from TMEM; thread 0 issues A = Qt Kt^T, S += Kt^T V and O = Qt S'; the
-// threads turn A into the masked bf16 P; thread 0 issues O += P V; the
-// threads write O (already e-weighted) as the segment's fp32 partial rows.
-// Waits on the tensor core are bounded; a timeout sets SSE_DEVICE_TIMEOUT
-// in the flags word and the CTA stops after releasing its TMEM.
+// Persistent CTAs (one per SM) take segments from an atomic queue (shared
+// segments first: they are the longest).  Inside a CTA two warp roles run a
+// pipeline synchronised by mbarriers:
+//   transform (8 warps): prefetch the raw q, k, g rows of the next chunk into
+//       registers, gather V rows with cp.async into a double buffer, build
+//       Qt and Kt (128B-swizzled, see umma.cuh) and the per-row scales;
+//   epilogue (4 warps, one TMEM lane each): rescale the state rows and
+//       write S'; turn A into the masked bf16 P; write O (already e-weighted)
+//       as bf16 partial rows; final state at the end of the segment.  Lane 0
+//       of warp 0 also issues the tensor-core work of each chunk at the
+//       points of its loop where the operands become ready:
+//       A = Qt Kt^T; S += Kt^T V; O = Qt S' (after the state rows), then
+//       O += P V (after P).  Twelve warps keep three warps per SM
+//       sub-partition, which leaves 168 registers per thread.
+// All waits are bounded: a timeout sets SSE_DEVICE_TIMEOUT in the flags word
+// and the CTA stops after releasing its TMEM.
 #include "sse_internal.cuh"
 #include "umma.cuh"
 
@@ -37,31 +45,32 @@ namespace {
 using namespace umma;
 
 constexpr int kC = 128;          // chunk rows
-constexpr int kThreads = 256;    // 8 warps, two warpgroups
 constexpr int kMid = kC / 2 - 1; // midpoint row of the decay split
+constexpr int kEpiWarps = 4, kTrfWarps = 8;
+constexpr int kThreads = 32 * (kEpiWarps + kTrfWarps);  // 384: 3 warps per SM sub-partition
+constexpr int kTrfThreads = 32 * kTrfWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-// |G_r - G_m| limit in log2 units (~ 80 in natural-log units)
-constexpr float kGateRangeLog2 = 80.f * kLog2e;
+constexpr float kGateRangeLog2 = 80.f * kLog2e;  // |G_r - G_m| limit (~80 natural-log units)
 
 constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
+
+enum Bar { kBarT = 0, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1, kNumBars };
 
 // Shared-memory layout (offsets from a 1024-aligned base).
 struct Smem {
     static constexpr uint32_t Q = 0;
     static constexpr uint32_t K = Q + kTile;
-    static constexpr uint32_t V = K + kTile;
-    static constexpr uint32_t P = V + kTile;
+    static constexpr uint32_t V0 = K + kTile;
+    static constexpr uint32_t V1 = V0 + kTile;
+    static constexpr uint32_t P = V1 + kTile;
     static constexpr uint32_t S = P + kTile;
-    static constexpr uint32_t TOT = S + kTile;            // [33][128] f32 block prefixes; row 32: G_m
-    static constexpr uint32_t FMID = TOT + 33 * 128 * 4;  // [128] exp(G_m) per key row
-    static constexpr uint32_t BETA = FMID + 128 * 4;      // [128] exp(G_last - G_m)
-    static constexpr uint32_t TOK = BETA + 128 * 4;       // [128] int token index (-1: padding)
-    static constexpr uint32_t EW = TOK + 128 * 4;         // [128] float e weight
-    static constexpr uint32_t DST = EW + 128 * 4;         // [128] int64 partial row offset
-    static constexpr uint32_t BAR = DST + 128 * 8;        // 2 mbarriers
-    static constexpr uint32_t SLOT = BAR + 16;            // TMEM base address
-    static constexpr uint32_t MISC = SLOT + 16;           // abort flag
+    static constexpr uint32_t TOT = S + kTile;             // [33][128] f32 block prefixes; row 32: G_m
+    static constexpr uint32_t SCALE = TOT + 33 * 128 * 4;  // [2 stages][2][128] f32: exp(G_m), exp(G_last-G_m)
+    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [3 stages] x {tok int[128], e f32[128], dst i64[128]}
+    static constexpr uint32_t META_STAGE = 128 * (4 + 4 + 8);
+    static constexpr uint32_t BAR = META + 3 * META_STAGE;
+    static constexpr uint32_t MISC = BAR + 8 * kNumBars;   // TMEM slot, work item
     static constexpr uint32_t END = MISC + 16;
 };
 constexpr size_t kSmemBytes = Smem::END + 1024;  // + alignment slack
@@ -73,86 +82,117 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+__device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
 }
 
-// Stores 8 consecutive bf16 columns (one 16-byte chunk) of row `row` of a
-// swizzled tile.
-__device__ __forceinline__ void st_tile8(unsigned char *tile, int row, int col, uint4 v) {
-    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, col, 2)) = v;
+__device__ __forceinline__ uint32_t tile_off(int row, int col) { return sw128_offset(row, col, 2); }
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(mbar) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+// Named barrier that also ORs a predicate over the participating threads,
+// so that every participant takes the same branch afterwards.
+__device__ __forceinline__ bool named_sync_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+struct Segment {
+    int b, h, slot, base, len;
+    bool shared;
+};
+
+__device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item, int H, int N,
+                                                  int use_shared) {
+    Segment s;
+    const int nshared = use_shared ? a.num_seqs * H : 0;
+    s.shared = item < nshared;
+    if (s.shared) {
+        s.b = item / H;
+        s.h = item % H;
+        s.slot = N;
+        s.base = a.cu_seqlens[s.b];
+        s.len = a.cu_seqlens[s.b + 1] - s.base;
+    } else {
+        const int r = item - nshared;
+        s.slot = r % N;
+        s.h = (r / N) % H;
+        s.b = r / (N * H);
+        s.base = a.seg_off[r];
+        s.len = a.seg_off[r + 1] - s.base;
+    }
+    return s;
 }
 
 template <int KC, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-chunked_segment_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared,
-                       float scale) {
+chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared,
+                       float scale, int32_t num_items, int32_t *work_counter) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    unsigned char *sQ = sm + Smem::Q, *sK = sm + Smem::K, *sV = sm + Smem::V;
-    unsigned char *sP = sm + Smem::P, *sS = sm + Smem::S;
     float *s_tot = reinterpret_cast<float *>(sm + Smem::TOT);
-    float *s_fmid = reinterpret_cast<float *>(sm + Smem::FMID);
-    float *s_beta = reinterpret_cast<float *>(sm + Smem::BETA);
-    int *s_tok = reinterpret_cast<int *>(sm + Smem::TOK);
-    float *s_e = reinterpret_cast<float *>(sm + Smem::EW);
-    long long *s_dst = reinterpret_cast<long long *>(sm + Smem::DST);
-    const uint32_t barA = smem_u32(sm + Smem::BAR), barO = barA + 8;
-    uint32_t *s_slot = reinterpret_cast<uint32_t *>(sm + Smem::SLOT);
-    int *s_abort = reinterpret_cast<int *>(sm + Smem::MISC);
+    float *s_scale = reinterpret_cast<float *>(sm + Smem::SCALE);
+    const uint32_t bar0 = smem_u32(sm + Smem::BAR);
+    auto bar = [&](int i) { return bar0 + 8u * i; };
+    uint32_t *s_slot = reinterpret_cast<uint32_t *>(sm + Smem::MISC);
+    int *s_item = reinterpret_cast<int *>(sm + Smem::MISC + 4);
+    int *s_abort = reinterpret_cast<int *>(sm + Smem::MISC + 8);
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = warp >> 2;                       // warpgroup: column half of TMEM tiles
-    const int trow = 32 * (warp & 3) + lane;        // this thread's TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const __nv_bfloat16 *kk = static_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.g);
-    const __nv_bfloat16 *qsb = static_cast<const __nv_bfloat16 *>(a.qs ? a.qs : a.q);
-    const __nv_bfloat16 *ksb = static_cast<const __nv_bfloat16 *>(a.ks ? a.ks : a.k);
-
-    // ---- segment ---------------------------------------------------------
-    const int nshared = use_shared ? a.num_seqs * H : 0;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.v);
+    const __nv_bfloat16 *gg = static_cast<const __nv_bfloat16 *>(a.g);
+    const __nv_bfloat16 *gqs = static_cast<const __nv_bfloat16 *>(a.qs ? a.qs : a.q);
+    const __nv_bfloat16 *gks = static_cast<const __nv_bfloat16 *>(a.ks ? a.ks : a.k);
+    __nv_bfloat16 *part_routed = static_cast<__nv_bfloat16 *>(a.part_routed);  // bf16 partials
+    __nv_bfloat16 *part_shared = static_cast<__nv_bfloat16 *>(a.part_shared);
     const int P = N + use_shared;
-    const bool is_shared = (int)blockIdx.x < nshared;
-    int b, h, slot, len, base;
-    if (is_shared) {
-        b = blockIdx.x / H;
-        h = blockIdx.x % H;
-        slot = N;
-        base = a.cu_seqlens[b];
-        len = a.cu_seqlens[b + 1] - base;
-    } else {
-        const int s = blockIdx.x - nshared;
-        slot = s % N;
-        h = (s / N) % H;
-        b = s / (N * H);
-        base = a.seg_off[s];
-        len = a.seg_off[s + 1] - base;
-    }
-    const __nv_bfloat16 *qsrc = is_shared ? qsb : q;
-    const __nv_bfloat16 *ksrc = is_shared ? ksb : kk;
-    const int64_t state_off = (((int64_t)b * H + h) * P + slot) * (int64_t)KC * DV;
 
-    // ---- set-up: TMEM, barriers, zero padding atoms ----------------------
+    auto meta_tok = [&](int stage) { return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE); };
+    auto meta_e = [&](int stage) {
+        return reinterpret_cast<float *>(sm + Smem::META + stage * Smem::META_STAGE + 512);
+    };
+    auto meta_dst = [&](int stage) {
+        return reinterpret_cast<long long *>(sm + Smem::META + stage * Smem::META_STAGE + 1024);
+    };
+
+    // ---- set-up ------------------------------------------------------------
     if (warp == 0) tmem_alloc(smem_u32(s_slot), kTmemCols);
     if (tid == 0) {
-        mbar_init(barA, 1);
-        mbar_init(barO, 1);
+        mbar_init(bar(kBarT), kTrfThreads);
+        mbar_init(bar(kBarS), 32 * kEpiWarps);
+        mbar_init(bar(kBarA), 1);
+        mbar_init(bar(kBarQK), 1);
+        mbar_init(bar(kBarP), 32 * kEpiWarps);
+        mbar_init(bar(kBarO), 1);
+        mbar_init(bar(kBarOf), 32 * kEpiWarps);
+        mbar_init(bar(kBarV0), 1);
+        mbar_init(bar(kBarV1), 1);
         mbar_fence_init();
         *s_abort = 0;
     }
     if (KC < 128) {  // Kt is also the M = 128 operand of the state pass: its second atom stays 0
         for (int x = tid; x < kC * 8; x += kThreads) {
             const int r = x / 8, chunk = x % 8;
-            *reinterpret_cast<uint4 *>(sK + (r >> 3) * 2048 + 1024 + (r & 7) * 128 + chunk * 16) =
+            *reinterpret_cast<uint4 *>(sm + Smem::K + (r >> 3) * 2048 + 1024 + (r & 7) * 128 + chunk * 16) =
                 make_uint4(0, 0, 0, 0);
         }
     }
@@ -160,293 +200,379 @@ chunked_segment_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_slot;
-    const uint32_t tA = tmem + lane_base + kTmemA, tO = tmem + lane_base + kTmemO;
-    const uint32_t tS = tmem + lane_base + kTmemS;
 
-    // initial state -> TMEM (rows = key index = TMEM lane, fp32 columns)
-    constexpr int kHalf = DV / 2;  // columns per warpgroup
-    if (trow < KC) {
-#pragma unroll
-        for (int cb = 0; cb < kHalf; cb += 32) {
-            uint32_t r[32];
-            const int col0 = wg * kHalf + cb;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                r[i] = a.init ? __float_as_uint(a.init[state_off + (int64_t)trow * DV + col0 + i]) : 0u;
-            tmem_st32(tS + col0, r);
-        }
-    }
-    tmem_wait_st();
-    float p_pending = 1.f;  // S_true[trow] = p_pending * S_stored[trow]
+    uint32_t gch = 0;  // chunks processed by this CTA so far: barrier phase parity
+    for (;;) {
+        if (tid == 0) *s_item = atomicAdd(work_counter, 1);
+        __syncthreads();
+        const int item = *s_item;
+        const bool stop = item >= num_items || *s_abort;
+        __syncthreads();
+        if (stop) break;
+        const Segment seg = decode_segment(a, item, H, N, use_shared);
+        const int nch = (seg.len + kC - 1) / kC;
+        const int64_t state_off = (((int64_t)seg.b * H + seg.h) * P + seg.slot) * (int64_t)KC * DV;
+        bool failed = false;
 
-    const int nchunks = (len + kC - 1) / kC;
-    for (int ch = 0; ch < nchunks; ++ch) {
-        const uint32_t parity = ch & 1;
-        // ---- row metadata --------------------------------------------------
-        if (tid < kC) {
-            const int n = ch * kC + tid;
-            int t = -1;
-            float e = 0.f;
-            long long dst = -1;
-            if (n < len) {
-                if (is_shared) {
-                    t = base + n;
-                    e = 1.f;
-                    dst = ((long long)t * H + h) * DV;
-                } else {
-                    const int rec = a.perm_rec[base + n];
-                    t = rec / topk;
-                    const int jj = rec - t * topk;
-                    e = a.topk_w[((int64_t)t * H + h) * topk + jj];
-                    dst = (((long long)t * H + h) * topk + jj) * DV;
+        if (warp >= kEpiWarps) {
+            // =================== transform warps ===================
+            const int tt = tid - 32 * kEpiWarps;              // 0..255
+            constexpr int CG = KC / 8, NRB = kTrfThreads / CG, RPT = kC / NRB;
+            const int cg = tt % CG, rb = tt / CG, col0 = cg * 8;
+            const __nv_bfloat16 *qsrc = seg.shared ? gqs : gq;
+            const __nv_bfloat16 *ksrc = seg.shared ? gks : gk;
+
+            auto fill_meta = [&](int n) {  // rows of chunk n -> meta stage n % 3
+                if (tt < kC) {
+                    const int st = n % 3;
+                    const int idx = n * kC + tt;
+                    int t = -1;
+                    float e = 0.f;
+                    long long dst = -1;
+                    if (idx < seg.len) {
+                        if (seg.shared) {
+                            t = seg.base + idx;
+                            e = 1.f;
+                            dst = ((long long)t * H + seg.h) * DV;
+                        } else {
+                            const int rec = a.perm_rec[seg.base + idx];
+                            t = rec / topk;
+                            const int jj = rec - t * topk;
+                            e = a.topk_w[((int64_t)t * H + seg.h) * topk + jj];
+                            dst = (((long long)t * H + seg.h) * topk + jj) * DV;
+                        }
+                    }
+                    meta_tok(st)[tt] = t;
+                    meta_e(st)[tt] = e;
+                    meta_dst(st)[tt] = dst;
                 }
-            }
-            s_tok[tid] = t;
-            s_e[tid] = e;
-            s_dst[tid] = dst;
-        }
-        fence_before();
-        __syncthreads();
-        fence_after();
-
-        // ---- transform: G cumsum, Qt, Kt (thread: 8 columns x RPT rows) ----
-        constexpr int CG = KC / 8;              // column groups
-        constexpr int NRB = kThreads / CG;      // row blocks
-        constexpr int RPT = kC / NRB;           // rows per thread
-        const int cg = tid % CG, rb = tid / CG;
-        const int col0 = cg * 8;
-        float G[RPT][8];
-        {
-            float run[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            };
+            uint4 rq[RPT], rk[RPT], rg[RPT];
+            auto prefetch = [&](int n) {
+                const int *tok = meta_tok(n % 3);
 #pragma unroll
-            for (int i = 0; i < RPT; ++i) {
-                const int r = rb * RPT + i;
-                const int t = s_tok[r];
-                if (t >= 0) {
-                    float f[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(g + ((int64_t)t * H + h) * KC + col0)), f);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) run[j] += f[j] * kLog2e;
+                for (int i = 0; i < RPT; ++i) {
+                    const int t = tok[rb * RPT + i];
+                    if (t >= 0) {
+                        const int64_t ro = ((int64_t)t * H + seg.h) * KC + col0;
+                        rg[i] = __ldg(reinterpret_cast<const uint4 *>(gg + ro));
+                        rq[i] = __ldg(reinterpret_cast<const uint4 *>(qsrc + ro));
+                        rk[i] = __ldg(reinterpret_cast<const uint4 *>(ksrc + ro));
+                    } else {
+                        rg[i] = rq[i] = rk[i] = make_uint4(0, 0, 0, 0);
+                    }
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) G[i][j] = run[j];
+            };
+            if (nch > 0) {
+                fill_meta(0);
+                named_sync(1, kTrfThreads);
+                prefetch(0);
             }
+            for (int n = 0; n < nch; ++n) {
+                const uint32_t g_n = gch + n;
+                const int mst = n % 3;
+                const int vb = g_n & 1;
+                unsigned char *sV = sm + (vb ? Smem::V1 : Smem::V0);
+                bool bad = false;
+                // V buffer vb was last read by chunk g_n - 2
+                if (n >= 2) bad = !mbar_wait_bounded(bar(vb ? kBarV1 : kBarV0), ((g_n - 2) >> 1) & 1, kWaitNs);
+                {   // gather V rows of chunk n with cp.async
+                    constexpr int VCG = DV / 8, VNRB = kTrfThreads / VCG, VRPT = kC / VNRB;
+                    const int vcg = tt % VCG, vrb = tt / VCG;
+                    const int *tok = meta_tok(mst);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s_tot[rb * 128 + col0 + j] = run[j];
-        }
-        __syncthreads();
-        // per-column exclusive scan over row blocks; midpoint and last values
-        if (tid < KC) {
-            float acc = 0.f, gmid = 0.f;
-            for (int r2 = 0; r2 < NRB; ++r2) {
-                const float x = s_tot[r2 * 128 + tid];
-                s_tot[r2 * 128 + tid] = acc;
-                acc += x;
-                if ((r2 + 1) * RPT - 1 == kMid) gmid = acc;
-            }
-            s_fmid[tid] = exp2f(gmid);
-            s_beta[tid] = exp2f(acc - gmid);
-            s_tot[32 * 128 + tid] = gmid;
-        }
-        __syncthreads();
-        {
-            float off[8], gm[8];
+                    for (int i = 0; i < VRPT; ++i) {
+                        const int r = vrb * VRPT + i;
+                        const int t = tok[r];
+                        unsigned char *dst = sV + tile_off(r, vcg * 8);
+                        if (t >= 0)
+                            cp_async16(smem_u32(dst), gv + ((int64_t)t * H + seg.h) * DV + vcg * 8);
+                        else
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                // pass 1: per-thread running sums of g over its rows -> block totals
+                {
+                    float run[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                off[j] = s_tot[rb * 128 + col0 + j];
-                gm[j] = s_tot[32 * 128 + col0 + j];
-            }
-            bool range_bad = false;
+                    for (int i = 0; i < RPT; ++i) {
+                        const uint32_t w[4] = {rg[i].x, rg[i].y, rg[i].z, rg[i].w};
 #pragma unroll
-            for (int i = 0; i < RPT; ++i) {
-                const int r = rb * RPT + i;
-                const int t = s_tok[r];
-                uint4 qo = make_uint4(0, 0, 0, 0), ko = make_uint4(0, 0, 0, 0);
-                if (t >= 0) {
-                    const int64_t rowoff = ((int64_t)t * H + h) * KC + col0;
-                    float fq[8], fk[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(qsrc + rowoff)), fq);
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(ksrc + rowoff)), fk);
-                    const float e = s_e[r];
-                    const float eq = e * scale;
-                    float qt[8], kt[8];
+                        for (int j = 0; j < 4; ++j) {
+                            float lo, hi;
+                            unpack2(w[j], lo, hi);
+                            run[2 * j] += lo;
+                            run[2 * j + 1] += hi;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) s_tot[rb * 128 + col0 + j] = run[j];
+                }
+                if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
+                float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
+                if (tt < KC) {  // per-column exclusive scan over row blocks
+                    float acc = 0.f, gmid = 0.f;
+                    for (int r2 = 0; r2 < NRB; ++r2) {
+                        const float x = s_tot[r2 * 128 + tt];
+                        s_tot[r2 * 128 + tt] = acc;
+                        acc += x;
+                        if ((r2 + 1) * RPT - 1 == kMid) gmid = acc;
+                    }
+                    s_fmid[tt] = expf(gmid);
+                    s_beta[tt] = expf(acc - gmid);
+                    s_tot[32 * 128 + tt] = gmid;
+                }
+                named_sync(1, kTrfThreads);
+                // Qt / Kt buffers are free once the first three MMAs of chunk n-1 completed
+                if (n >= 1) bad = !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
+                // pass 2: Qt, Kt rows (bf16) straight into their tiles
+                {
+                    float run[8], gm[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float dlt = G[i][j] + off[j] - gm[j];
-                        range_bad |= fabsf(dlt) > kGateRangeLog2;
-                        qt[j] = eq * fq[j] * exp2f(dlt);
-                        kt[j] = e * fk[j] * exp2f(-dlt);
+                        run[j] = s_tot[rb * 128 + col0 + j];
+                        gm[j] = s_tot[32 * 128 + col0 + j];
                     }
-                    qo = make_uint4(pack_bf16x2(qt[0], qt[1]), pack_bf16x2(qt[2], qt[3]),
-                                    pack_bf16x2(qt[4], qt[5]), pack_bf16x2(qt[6], qt[7]));
-                    ko = make_uint4(pack_bf16x2(kt[0], kt[1]), pack_bf16x2(kt[2], kt[3]),
-                                    pack_bf16x2(kt[4], kt[5]), pack_bf16x2(kt[6], kt[7]));
+                    const float *me = meta_e(mst);
+                    bool range_bad = false;
+#pragma unroll
+                    for (int i = 0; i < RPT; ++i) {
+                        const int r = rb * RPT + i;
+                        const float e = me[r];
+                        const float eq = e * scale;
+                        const uint32_t wg4[4] = {rg[i].x, rg[i].y, rg[i].z, rg[i].w};
+                        const uint32_t wq4[4] = {rq[i].x, rq[i].y, rq[i].z, rq[i].w};
+                        const uint32_t wk4[4] = {rk[i].x, rk[i].y, rk[i].z, rk[i].w};
+                        uint32_t pq[4], pk[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float g0, g1, q0, q1, k0, k1;
+                            unpack2(wg4[j], g0, g1);
+                            unpack2(wq4[j], q0, q1);
+                            unpack2(wk4[j], k0, k1);
+                            run[2 * j] += g0;
+                            run[2 * j + 1] += g1;
+                            const float d0 = (run[2 * j] - gm[2 * j]) * kLog2e;
+                            const float d1 = (run[2 * j + 1] - gm[2 * j + 1]) * kLog2e;
+                            range_bad |= fabsf(d0) > kGateRangeLog2 || fabsf(d1) > kGateRangeLog2;
+                            pq[j] = pack_bf16x2(eq * q0 * exp2f(d0), eq * q1 * exp2f(d1));
+                            pk[j] = pack_bf16x2(e * k0 * exp2f(-d0), e * k1 * exp2f(-d1));
+                        }
+                        *reinterpret_cast<uint4 *>(sm + Smem::Q + tile_off(r, col0)) =
+                            make_uint4(pq[0], pq[1], pq[2], pq[3]);
+                        *reinterpret_cast<uint4 *>(sm + Smem::K + tile_off(r, col0)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                    if (range_bad) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
                 }
-                st_tile8(sQ, r, col0, qo);
-                st_tile8(sK, r, col0, ko);
+                cp_async_wait_all();
+                fence_proxy_async();
+                if (n + 1 < nch) fill_meta(n + 1);
+                if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
+                mbar_arrive(bar(kBarT));
+                if (n + 1 < nch) prefetch(n + 1);
             }
-            if (range_bad) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
-        }
-        // V rows (raw bf16): thread covers 8 columns x VRPT rows
-        {
-            constexpr int VCG = DV / 8, VNRB = kThreads / VCG, VRPT = kC / VNRB;
-            const int vcg = tid % VCG, vrb = tid / VCG;
+        } else {
+            // =================== epilogue warps ===================
+            const int row = tid;  // TMEM lane
+            const uint32_t lb = (uint32_t)(32 * warp) << 16;
+            const uint32_t tA = tmem + lb + kTmemA, tO = tmem + lb + kTmemO, tS = tmem + lb + kTmemS;
+            // initial state -> TMEM
+            if (row < KC) {
 #pragma unroll
-            for (int i = 0; i < VRPT; ++i) {
-                const int r = vrb * VRPT + i;
-                const int t = s_tok[r];
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (t >= 0) u = __ldg(reinterpret_cast<const uint4 *>(v + ((int64_t)t * H + h) * DV + vcg * 8));
-                st_tile8(sV, r, vcg * 8, u);
-            }
-        }
-        // ---- state rows: S_stored *= exp(G_m) * p, bf16 copy -> sS ----------
-        if (trow < KC) {
-            const float f = s_fmid[trow] * p_pending;
+                for (int c0 = 0; c0 < DV; c0 += 32) {
+                    uint32_t r[32];
+                    const float *src = a.init ? a.init + state_off + (int64_t)row * DV + c0 : nullptr;
 #pragma unroll
-            for (int cb = 0; cb < kHalf; cb += 32) {
-                const int c0 = wg * kHalf + cb;
-                uint32_t r[32];
-                tmem_ld32(tS + c0, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-                tmem_st32(tS + c0, r);
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 u = make_uint4(
-                        pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
-                        pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
-                        pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
-                        pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
-                    st_tile8(sS, trow, c0 + i, u);
+                    for (int i = 0; i < 32; i += 4) {
+                        float4 f = src ? *reinterpret_cast<const float4 *>(src + i) : make_float4(0, 0, 0, 0);
+                        r[i] = __float_as_uint(f.x);
+                        r[i + 1] = __float_as_uint(f.y);
+                        r[i + 2] = __float_as_uint(f.z);
+                        r[i + 3] = __float_as_uint(f.w);
+                    }
+                    tmem_st32(tS + c0, r);
                 }
+                tmem_wait_st();
             }
-            tmem_wait_st();
-            p_pending = s_beta[trow];
-        }
-        fence_proxy_async();
-        fence_before();
-        __syncthreads();
-
-        // ---- MMAs: A = Qt Kt^T; S += Kt^T V; O = Qt S' ------------------------
-        if (tid == 0) {
-            fence_after();
-            const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV), s0 = smem_u32(sS);
+            float p_pending = 1.f;
+            __nv_bfloat16 *outp = seg.shared ? part_shared : part_routed;
+            const bool issuer = tid == 0;
+            const uint32_t q0 = smem_u32(sm + Smem::Q), k0 = smem_u32(sm + Smem::K);
+            const uint32_t p0 = smem_u32(sm + Smem::P), s0 = smem_u32(sm + Smem::S);
             constexpr uint32_t idA = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idS = idesc_bf16(128, DV, 1, 1);
-            constexpr uint32_t idO1 = idesc_bf16(128, DV, 0, 1);
+            constexpr uint32_t idO = idesc_bf16(128, DV, 0, 1);
+            auto write_out = [&](uint32_t g_o, int n_o) {  // O of chunk n_o -> bf16 partial rows
+                const long long dst = meta_dst(n_o % 3)[row];
+                uint4 packed[DV / 8];
 #pragma unroll
-            for (int k16 = 0; k16 < KC; k16 += 16) {
-                const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                mma_bf16(tmem + kTmemA, desc_sw128(q0 + ko, 16, 2048), desc_sw128(k0 + ko, 16, 2048), idA,
-                         k16 > 0);
-            }
-            commit(barA);
+                for (int c0 = 0; c0 < DV; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c0, r);
+                    tmem_wait_ld();
 #pragma unroll
-            for (int k16 = 0; k16 < kC; k16 += 16) {
-                const uint32_t ro = (k16 / 8) * 2048;
-                mma_bf16(tmem + kTmemS, desc_sw128(k0 + ro, 1024, 2048), desc_sw128(v0 + ro, 1024, 2048), idS,
-                         1);
-            }
-#pragma unroll
-            for (int k16 = 0; k16 < KC; k16 += 16) {
-                const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                mma_bf16(tmem + kTmemO, desc_sw128(q0 + ko, 16, 2048),
-                         desc_sw128(s0 + (k16 / 8) * 2048, 1024, 2048), idO1, k16 > 0);
-            }
-        }
-        __syncwarp();
-
-        // ---- P = mask(A) (bf16) ------------------------------------------------
-        bool ok = mbar_wait_bounded(barA, parity, kWaitNs);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
-            break;
-        }
-        fence_after();
-#pragma unroll
-        for (int cb = 0; cb < 64; cb += 32) {
-            const int c0 = wg * 64 + cb;
-            uint32_t r[32];
-            tmem_ld32(tA + c0, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = (c0 + i + j <= trow) ? __uint_as_float(r[i + j]) : 0.f;
-                st_tile8(sP, trow, c0 + i,
-                         make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7])));
-            }
-        }
-        fence_proxy_async();
-        fence_before();
-        __syncthreads();
-
-        // ---- O += P V ------------------------------------------------------------
-        if (tid == 0) {
-            fence_after();
-            const uint32_t p0 = smem_u32(sP), v0 = smem_u32(sV);
-            constexpr uint32_t idO2 = idesc_bf16(128, DV, 0, 1);
-#pragma unroll
-            for (int k16 = 0; k16 < kC; k16 += 16) {
-                const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                mma_bf16(tmem + kTmemO, desc_sw128(p0 + ko, 16, 2048),
-                         desc_sw128(v0 + (k16 / 8) * 2048, 1024, 2048), idO2, 1);
-            }
-            commit(barO);
-        }
-        __syncwarp();
-        ok = mbar_wait_bounded(barO, parity, kWaitNs);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
-            break;
-        }
-        fence_after();
-
-        // ---- O rows -> fp32 partials ------------------------------------------
-        {
-            const long long dst = s_dst[trow];
-            float *outp = is_shared ? a.part_shared : a.part_routed;
-#pragma unroll
-            for (int cb = 0; cb < kHalf; cb += 32) {
-                const int c0 = wg * kHalf + cb;
-                uint32_t r[32];
-                tmem_ld32(tO + c0, r);
-                tmem_wait_ld();
+                    for (int i = 0; i < 4; ++i)
+                        packed[c0 / 8 + i] = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                            pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                            pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                            pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+                }
+                fence_before();
+                mbar_arrive(bar(kBarOf));  // O may be overwritten now
+                (void)g_o;
                 if (dst >= 0) {
-                    float4 *o4 = reinterpret_cast<float4 *>(outp + dst + c0);
+                    uint4 *o4 = reinterpret_cast<uint4 *>(outp + dst);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        o4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                    for (int i = 0; i < DV / 8; ++i) o4[i] = packed[i];
+                }
+            };
+            for (int n = 0; n < nch; ++n) {
+                const uint32_t g_n = gch + n;
+                if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarT), g_n & 1, kWaitNs))) { failed = true; break; }
+                if (n >= 1) {
+                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarO), (g_n - 1) & 1, kWaitNs))) {
+                        failed = true;
+                        break;
+                    }
+                    fence_after();
+                    write_out(g_n - 1, n - 1);
+                }
+                // state rows: S_stored *= exp(G_m) * p; bf16 copy -> S' tile
+                const float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
+                if (row < KC) {
+                    const float f = s_fmid[row] * p_pending;
+#pragma unroll
+                    for (int c0 = 0; c0 < DV; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tS + c0, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+                        tmem_st32(tS + c0, r);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8)
+                            *reinterpret_cast<uint4 *>(sm + Smem::S + tile_off(row, c0 + i)) = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                pack_bf16x2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                pack_bf16x2(__uint_as_float(r[i + 4]), __uint_as_float(r[i + 5])),
+                                pack_bf16x2(__uint_as_float(r[i + 6]), __uint_as_float(r[i + 7])));
+                    }
+                    tmem_wait_st();
+                    p_pending = s_beta[row];
+                }
+                fence_proxy_async();
+                fence_before();
+                mbar_arrive(bar(kBarS));
+                const uint32_t v0 = smem_u32(sm + ((g_n & 1) ? Smem::V1 : Smem::V0));
+                if (issuer) {
+                    // A = Qt Kt^T; S += Kt^T V; O = Qt S'
+                    bool ok = mbar_wait_bounded(bar(kBarS), g_n & 1, kWaitNs);
+                    if (ok) {
+                        fence_after();
+#pragma unroll
+                        for (int k16 = 0; k16 < KC; k16 += 16) {
+                            const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                            mma_bf16(tmem + kTmemA, desc_sw128(q0 + ko, 16, 2048),
+                                     desc_sw128(k0 + ko, 16, 2048), idA, k16 > 0);
+                        }
+                        commit(bar(kBarA));
+#pragma unroll
+                        for (int k16 = 0; k16 < kC; k16 += 16) {
+                            const uint32_t ro = (k16 / 8) * 2048;
+                            mma_bf16(tmem + kTmemS, desc_sw128(k0 + ro, 1024, 2048),
+                                     desc_sw128(v0 + ro, 1024, 2048), idS, 1);
+                        }
+                        if (n >= 1) ok = mbar_wait_bounded(bar(kBarOf), (g_n - 1) & 1, kWaitNs);
+                    }
+                    if (ok) {
+                        fence_after();
+#pragma unroll
+                        for (int k16 = 0; k16 < KC; k16 += 16) {
+                            const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                            mma_bf16(tmem + kTmemO, desc_sw128(q0 + ko, 16, 2048),
+                                     desc_sw128(s0 + (k16 / 8) * 2048, 1024, 2048), idO, k16 > 0);
+                        }
+                        commit(bar(kBarQK));
+                    }
+                    failed = !ok;
+                }
+                if (__any_sync(0xffffffffu, failed)) { failed = true; break; }
+                // P = causal mask of A, bf16
+                if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarA), g_n & 1, kWaitNs))) { failed = true; break; }
+                fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < kC; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tA + c0, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        float f[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) f[j] = (c0 + i + j <= row) ? __uint_as_float(r[i + j]) : 0.f;
+                        *reinterpret_cast<uint4 *>(sm + Smem::P + tile_off(row, c0 + i)) =
+                            make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                    }
+                }
+                fence_proxy_async();
+                fence_before();
+                mbar_arrive(bar(kBarP));
+                if (issuer) {
+                    // O += P V once every epilogue thread has written its row of P
+                    const bool ok = mbar_wait_bounded(bar(kBarP), g_n & 1, kWaitNs);
+                    if (ok) {
+                        fence_after();
+#pragma unroll
+                        for (int k16 = 0; k16 < kC; k16 += 16) {
+                            const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                            mma_bf16(tmem + kTmemO, desc_sw128(p0 + ko, 16, 2048),
+                                     desc_sw128(v0 + (k16 / 8) * 2048, 1024, 2048), idO, 1);
+                        }
+                        commit(bar(kBarO));
+                        commit(bar((g_n & 1) ? kBarV1 : kBarV0));
+                    }
+                    failed = !ok;
+                }
+                if (__any_sync(0xffffffffu, failed)) { failed = true; break; }
+            }
+            if (!failed && nch > 0) {
+                const uint32_t g_l = gch + nch - 1;
+                if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarO), g_l & 1, kWaitNs))) failed = true;
+                else {
+                    fence_after();
+                    write_out(g_l, nch - 1);
                 }
             }
+            // final state = p * S_stored
+            if (!failed && a.final_state && row < KC) {
+#pragma unroll
+                for (int c0 = 0; c0 < DV; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + c0, r);
+                    tmem_wait_ld();
+                    float4 *o4 = reinterpret_cast<float4 *>(a.final_state + state_off + (int64_t)row * DV + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        o4[i] = make_float4(__uint_as_float(r[4 * i]) * p_pending,
+                                            __uint_as_float(r[4 * i + 1]) * p_pending,
+                                            __uint_as_float(r[4 * i + 2]) * p_pending,
+                                            __uint_as_float(r[4 * i + 3]) * p_pending);
+                }
+            }
+            fence_before();
         }
-        fence_before();
+        if (failed) {
+            atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
+            *s_abort = 1;
+        }
         __syncthreads();
         fence_after();
+        gch += nch;
+        if (*s_abort) break;
     }
-
-    // ---- final state = p * S_stored --------------------------------------------
-    if (a.final_state && trow < KC) {
-#pragma unroll
-        for (int cb = 0; cb < kHalf; cb += 32) {
-            const int c0 = wg * kHalf + cb;
-            uint32_t r[32];
-            tmem_ld32(tS + c0, r);
-            tmem_wait_ld();
-            float4 *o4 = reinterpret_cast<float4 *>(a.final_state + state_off + (int64_t)trow * DV + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                o4[i] = make_float4(__uint_as_float(r[4 * i]) * p_pending, __uint_as_float(r[4 * i + 1]) * p_pending,
-                                    __uint_as_float(r[4 * i + 2]) * p_pending,
-                                    __uint_as_float(r[4 * i + 3]) * p_pending);
-        }
-    }
-    fence_before();
     __syncthreads();
     if (warp == 0) {
         fence_after();
@@ -456,17 +582,24 @@ chunked_segment_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
 
 template <int KC, int DV>
 cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {
-    static bool attr_set = false;  // benign race: the attribute value is the same for every caller
+    static bool attr_set = false;  // benign race: every caller sets the same value
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunked_segment_kernel<KC, DV>,
+        cudaError_t e = cudaFuncSetAttribute(chunked_forward_kernel<KC, DV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int64_t nseg = (int64_t)a.num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
     if (nseg == 0) return cudaSuccess;
-    chunked_segment_kernel<KC, DV><<<(unsigned)nseg, kThreads, kSmemBytes, stream>>>(
-        a, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int32_t *counter = static_cast<int32_t *>(a.chunk_ws);
+    cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
+    chunked_forward_kernel<KC, DV><<<grid, kThreads, kSmemBytes, stream>>>(
+        a, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
     return cudaGetLastError();
 }
 
@@ -478,7 +611,7 @@ bool chunked_supported(const sse_config_t &cfg) {
     return cfg.dtype == SSE_BF16 && c_ok && d_ok;
 }
 
-size_t chunked_extra_workspace(const sse_config_t &, int64_t, int32_t) { return 0; }
+size_t chunked_extra_workspace(const sse_config_t &, int64_t, int32_t) { return 256; }
 
 cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream,
                                    int *launches) {
@@ -488,9 +621,6 @@ cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a
     else if (cfg.key_dim == 64 && cfg.value_dim == 128) e = launch_t<64, 128>(cfg, a, stream);
     else if (cfg.key_dim == 64 && cfg.value_dim == 64) e = launch_t<64, 64>(cfg, a, stream);
     else return cudaErrorInvalidValue;
-    *launches += 1;
-    if (e != cudaSuccess) return e;
-    e = launch_combine(cfg, a, stream);
     *launches += 1;
     return e;
 }

@@ -11,6 +11,8 @@
 //   routed segment (b,h,i): part_routed[t,h,j,:] = e_t[i] * scale * q_t S_i
 //   shared segment (b,h):   part_shared[t,h,:]   = scale * qs_t S_N
 // The combine kernel sums the partials into out (the gated scatter-sum).
+#include <algorithm>
+
 #include "sse_internal.cuh"
 
 namespace sse {
@@ -109,7 +111,8 @@ segment_recurrent_kernel(ForwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
         }
         *reinterpret_cast<float4 *>(s_red + rg * d + col) = acc;
         __syncthreads();
-        float *dst = is_shared ? a.part_shared + th * d : a.part_routed + (th * topk + jj) * d;
+        float *dst = is_shared ? static_cast<float *>(a.part_shared) + th * d
+                               : static_cast<float *>(a.part_routed) + (th * topk + jj) * d;
         for (int cc = threadIdx.x; cc < d; cc += kRecThreads) {
             float o = 0.f;
             for (int r = 0; r < R; ++r) o += s_red[r * d + cc];
@@ -150,25 +153,45 @@ cudaError_t dispatch_d(const sse_config_t &cfg, const ForwardArgs &a, cudaStream
     }
 }
 
+template <typename P> struct PartLoad;
+template <> struct PartLoad<float> {
+    static __device__ __forceinline__ float4 load4(const float *p) {
+        return *reinterpret_cast<const float4 *>(p);
+    }
+};
+template <> struct PartLoad<__nv_bfloat16> {
+    static __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+};
+
 // out[t,h,:] = sum_j part_routed[t,h,j,:] + part_shared[t,h,:], four columns per thread
-template <typename T>
-__global__ void combine_kernel(const float *__restrict__ part_routed,
-                               const float *__restrict__ part_shared, int64_t rows, int32_t d,
-                               int32_t topk, T *__restrict__ out) {
+template <typename T, typename P>
+__global__ void combine_kernel(const P *__restrict__ part_routed, const P *__restrict__ part_shared,
+                               int64_t rows, int32_t d, int32_t topk, T *__restrict__ out) {
     const int d4 = d / 4;
     const int64_t total = rows * d4;
     for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
          x += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = x / d4;
         const int col = (int)(x - row * d4) * 4;
-        float4 o = part_shared ? *reinterpret_cast<const float4 *>(part_shared + row * d + col)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 o = part_shared ? PartLoad<P>::load4(part_shared + row * d + col) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < topk; ++j) {
-            const float4 p = *reinterpret_cast<const float4 *>(part_routed + (row * topk + j) * d + col);
+            const float4 p = PartLoad<P>::load4(part_routed + (row * topk + j) * d + col);
             o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
         }
         Elem<T>::store4(out + row * d + col, o);
     }
+}
+
+template <typename T, typename P>
+void launch_combine_t(const sse_config_t &cfg, const ForwardArgs &a, int64_t rows, unsigned blocks,
+                      cudaStream_t stream) {
+    const P *ps = cfg.use_shared ? static_cast<const P *>(a.part_shared) : nullptr;
+    combine_kernel<T, P><<<blocks, 256, 0, stream>>>(static_cast<const P *>(a.part_routed), ps, rows,
+                                                     cfg.value_dim, cfg.top_k, static_cast<T *>(a.out));
 }
 
 }  // namespace
@@ -190,15 +213,14 @@ cudaError_t launch_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaSt
     const int64_t rows = a.total_tokens * cfg.num_heads;
     if (rows == 0) return cudaSuccess;
     const int64_t work = rows * (cfg.value_dim / 4);
-    const int threads = 256;
-    const int64_t blocks = std::min<int64_t>((work + threads - 1) / threads, 152 * 16);
-    const float *ps = cfg.use_shared ? a.part_shared : nullptr;
-    if (cfg.dtype == SSE_BF16)
-        combine_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
-            a.part_routed, ps, rows, cfg.value_dim, cfg.top_k, static_cast<__nv_bfloat16 *>(a.out));
-    else
-        combine_kernel<float><<<(unsigned)blocks, threads, 0, stream>>>(
-            a.part_routed, ps, rows, cfg.value_dim, cfg.top_k, static_cast<float *>(a.out));
+    const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 152 * 16);
+    if (cfg.dtype == SSE_BF16) {
+        if (a.part_bf16) launch_combine_t<__nv_bfloat16, __nv_bfloat16>(cfg, a, rows, blocks, stream);
+        else launch_combine_t<__nv_bfloat16, float>(cfg, a, rows, blocks, stream);
+    } else {
+        if (a.part_bf16) launch_combine_t<float, __nv_bfloat16>(cfg, a, rows, blocks, stream);
+        else launch_combine_t<float, float>(cfg, a, rows, blocks, stream);
+    }
     return cudaGetLastError();
 }
 

@@ -71,7 +71,7 @@ bool use_chunked(const sse_config_t &c) {
 
 struct ForwardLayout {
     RouteBuffers rb;
-    float *part_routed, *part_shared;
+    void *part_routed, *part_shared;
     int32_t *flags;
     void *chunk_ws;
     size_t bytes;
@@ -83,8 +83,10 @@ ForwardLayout carve_forward(void *ws, const sse_config_t &c, int64_t T, int32_t 
     ForwardLayout L{};
     L.flags = cv.take<int32_t>(64);
     L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
-    L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
-    L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
+    // partial read-outs: bf16 on the tensor-core path, fp32 on the recurrent path
+    const size_t pe = use_chunked(c) ? 2 : 4;
+    L.part_routed = cv.take<unsigned char>((size_t)T * c.num_heads * c.top_k * c.value_dim * pe);
+    L.part_shared = c.use_shared ? cv.take<unsigned char>((size_t)T * c.num_heads * c.value_dim * pe) : nullptr;
     L.chunk_ws = use_chunked(c) ? cv.take<unsigned char>(sse::chunked_extra_workspace(c, T, S)) : nullptr;
     L.bytes = (cv.off + 255) & ~size_t(255);
     return L;
@@ -195,18 +197,18 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     a.topk_w = L.rb.topk_w;
     a.part_routed = L.part_routed;
     a.part_shared = L.part_shared;
+    a.part_bf16 = use_chunked(c) ? 1 : 0;
     a.flags = L.flags;
     a.chunk_ws = L.chunk_ws;
     if (use_chunked(c)) {
         e = sse::launch_forward_chunked(c, a, s, &launches);
-        if (e == cudaSuccess && mark(2) != cudaSuccess) return SSE_ERR_CUDA;
     } else {
         e = sse::launch_forward_recurrent(c, a, s);
         launches += 1;
-        if (e == cudaSuccess && mark(2) != cudaSuccess) return SSE_ERR_CUDA;
-        if (e == cudaSuccess) e = sse::launch_combine(c, a, s);
-        launches += 1;
     }
+    if (e != cudaSuccess || mark(2) != cudaSuccess) return SSE_ERR_CUDA;
+    e = sse::launch_combine(c, a, s);
+    launches += 1;
     if (e != cudaSuccess) return SSE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return SSE_ERR_CUDA;
     if (num_launches) *num_launches = launches;

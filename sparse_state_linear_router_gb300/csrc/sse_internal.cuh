@@ -132,6 +132,7 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
                          bool group, cudaStream_t stream);
 
 // Recurrent (CUDA-core) forward over all segments; writes fp32 partials.
+// The chunked path writes bf16 partials.
 struct ForwardArgs {
     const void *q, *k, *v, *g, *qs, *ks;
     const int32_t *cu_seqlens;
@@ -143,8 +144,9 @@ struct ForwardArgs {
     const int32_t *seg_off;
     const int32_t *perm_rec;
     const float *topk_w;
-    float *part_routed;  // [T, H, k, d] fp32
-    float *part_shared;  // [T, H, d] fp32
+    void *part_routed;   // [T, H, k, d] partial read-outs (fp32, or bf16 if part_bf16)
+    void *part_shared;   // [T, H, d]
+    int32_t part_bf16;
     int32_t *flags;
     void *chunk_ws;      // chunked path scratch
 };
