@@ -8,9 +8,9 @@
 // C = 128 rows.  With G_r the running sum of g inside the chunk (rows
 // 0..r) and m the midpoint row (63):
 //
-//   Qt_r = e_r scale q_r * exp(G_r - G_m)       Kt_s = e_s k_s * exp(G_m - G_s)
+//   Qt_r = q_r * exp(G_r - G_m)                  Kt_s = e_s k_s * exp(G_m - G_s)
 //   A    = Qt Kt^T, causally masked (s <= r) -> P (bf16)
-//   O    = Qt (exp(G_m) * S) + P V                   (inter- + intra-chunk)
+//   O_r  = e_r scale [Qt (exp(G_m) * S) + P V]_r     (inter- + intra-chunk)
 //   S'   = exp(G_last) * S + exp(G_last - G_m) * Kt^T V   (state pass)
 //
 // Every factor exp(+-(G_r - G_m)) is bounded by exp(|G| over half a chunk),
@@ -23,9 +23,11 @@
 // Persistent CTAs (one per SM) take segments from an atomic queue (shared
 // segments first: they are the longest).  Inside a CTA two warp roles run a
 // pipeline synchronised by mbarriers:
-//   transform (8 warps): prefetch the raw q, k, g rows of the next chunk into
-//       registers, gather V rows with cp.async into a double buffer, build
-//       Qt and Kt (128B-swizzled, see umma.cuh) and the per-row scales;
+//   transform (8 warps): load the raw g rows of the next chunk into registers
+//       while the current one finishes, then its q and k rows and row
+//       metadata one step ahead; gather V rows with cp.async into a double
+//       buffer; build Qt and Kt (128B-swizzled, see umma.cuh) and the
+//       per-row scales;
 //   epilogue (4 warps, one TMEM lane each): rescale the state rows and
 //       write S'; turn A into the masked bf16 P; write O (already e-weighted)
 //       as bf16 partial rows; final state at the end of the segment.  Lane 0
@@ -36,6 +38,8 @@
 //       sub-partition, which leaves 168 registers per thread.
 // All waits are bounded: a timeout sets SSE_DEVICE_TIMEOUT in the flags word
 // and the CTA stops after releasing its TMEM.
+#include <algorithm>
+
 #include "sse_internal.cuh"
 #include "umma.cuh"
 
@@ -54,6 +58,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGateRangeLog2 = 80.f * kLog2e;  // |G_r - G_m| limit (~80 natural-log units)
 
 constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
+constexpr int kMetaStages = 4;          // row metadata ring (chunk n in stage n % 4)
 
 enum Bar { kBarT = 0, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1, kNumBars };
 
@@ -67,9 +72,9 @@ struct Smem {
     static constexpr uint32_t S = P + kTile;
     static constexpr uint32_t TOT = S + kTile;             // [33][128] f32 block prefixes; row 32: G_m
     static constexpr uint32_t SCALE = TOT + 33 * 128 * 4;  // [2 stages][2][128] f32: exp(G_m), exp(G_last-G_m)
-    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [3 stages] x {tok int[128], e f32[128], dst i64[128]}
-    static constexpr uint32_t META_STAGE = 128 * (4 + 4 + 8);
-    static constexpr uint32_t BAR = META + 3 * META_STAGE;
+    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [4 stages] x {tok, e, partial slot}[128]
+    static constexpr uint32_t META_STAGE = 128 * (4 + 4 + 4);
+    static constexpr uint32_t BAR = META + kMetaStages * META_STAGE;
     static constexpr uint32_t MISC = BAR + 8 * kNumBars;   // TMEM slot, work item
     static constexpr uint32_t END = MISC + 16;
 };
@@ -82,12 +87,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Product of two bf16x2 words (round to nearest).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
+    __nv_bfloat162 z = __hmul2(x, y);
+    return *reinterpret_cast<uint32_t *>(&z);
+}
+
 __device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
     lo = __uint_as_float(w << 16);
     hi = __uint_as_float(w & 0xffff0000u);
 }
 
 __device__ __forceinline__ uint32_t tile_off(int row, int col) { return sw128_offset(row, col, 2); }
+
+// 2^x with the SFU instruction (relative error ~2^-22, flushes denormals);
+// its operands are rounded to bf16 right after.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(mbar) : "memory");
@@ -119,6 +140,8 @@ struct Segment {
     bool shared;
 };
 
+// Work items: the shared segments first (the longest, so the persistent CTAs
+// start them early), then the routed segments s = (b * H + h) * N + i.
 __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item, int H, int N,
                                                   int use_shared) {
     Segment s;
@@ -162,16 +185,18 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
     const __nv_bfloat16 *gg = static_cast<const __nv_bfloat16 *>(a.g);
     const __nv_bfloat16 *gqs = static_cast<const __nv_bfloat16 *>(a.qs ? a.qs : a.q);
     const __nv_bfloat16 *gks = static_cast<const __nv_bfloat16 *>(a.ks ? a.ks : a.k);
-    __nv_bfloat16 *part_routed = static_cast<__nv_bfloat16 *>(a.part_routed);  // bf16 partials
-    __nv_bfloat16 *part_shared = static_cast<__nv_bfloat16 *>(a.part_shared);
+    // Partial read-outs [T*H][ncon][DV] (bf16), summed by the slot-combine kernel.
+    __nv_bfloat16 *part = static_cast<__nv_bfloat16 *>(a.part_routed);
+    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
+    const int ncon = topk + use_shared;  // contributions per (token, head) row
     const int P = N + use_shared;
 
     auto meta_tok = [&](int stage) { return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE); };
     auto meta_e = [&](int stage) {
         return reinterpret_cast<float *>(sm + Smem::META + stage * Smem::META_STAGE + 512);
     };
-    auto meta_dst = [&](int stage) {
-        return reinterpret_cast<long long *>(sm + Smem::META + stage * Smem::META_STAGE + 1024);
+    auto meta_slot = [&](int stage) {
+        return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE + 1024);
     };
 
     // ---- set-up ------------------------------------------------------------
@@ -222,58 +247,77 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             const __nv_bfloat16 *qsrc = seg.shared ? gqs : gq;
             const __nv_bfloat16 *ksrc = seg.shared ? gks : gk;
 
-            auto fill_meta = [&](int n) {  // rows of chunk n -> meta stage n % 3
-                if (tt < kC) {
-                    const int st = n % 3;
-                    const int idx = n * kC + tt;
-                    int t = -1;
-                    float e = 0.f;
-                    long long dst = -1;
-                    if (idx < seg.len) {
-                        if (seg.shared) {
-                            t = seg.base + idx;
-                            e = 1.f;
-                            dst = ((long long)t * H + seg.h) * DV;
-                        } else {
-                            const int rec = a.perm_rec[seg.base + idx];
-                            t = rec / topk;
-                            const int jj = rec - t * topk;
-                            e = a.topk_w[((int64_t)t * H + seg.h) * topk + jj];
-                            dst = (((long long)t * H + seg.h) * topk + jj) * DV;
-                        }
+            // Row metadata of chunk n: token index, router weight and partial-row
+            // offset.  Loaded into registers two chunks ahead, stored into stage
+            // n % 4 one chunk ahead.
+            struct RowMeta { int t; float e; int slot; };
+            auto load_meta = [&](int n) {
+                RowMeta m{-1, 0.f, 0};
+                const int idx = n * kC + tt;
+                if (tt < kC && idx < seg.len) {
+                    if (seg.shared) {
+                        m.t = seg.base + idx;
+                        m.e = 1.f;
+                        m.slot = topk;
+                    } else {
+                        const int rec = a.perm_rec[seg.base + idx];
+                        m.e = a.perm_e[seg.base + idx];
+                        m.t = rec / topk;
+                        m.slot = rec - m.t * topk;
                     }
-                    meta_tok(st)[tt] = t;
-                    meta_e(st)[tt] = e;
-                    meta_dst(st)[tt] = dst;
+                }
+                return m;
+            };
+            auto store_meta = [&](int n, const RowMeta &m) {
+                if (tt < kC) {
+                    const int st = n % kMetaStages;
+                    meta_tok(st)[tt] = m.t;
+                    meta_e(st)[tt] = m.e;
+                    meta_slot(st)[tt] = m.slot;
                 }
             };
-            uint4 rq[RPT], rk[RPT], rg[RPT];
-            auto prefetch = [&](int n) {
-                const int *tok = meta_tok(n % 3);
+            uint4 rq[RPT], rk[RPT], rg[RPT], rg_next[RPT];
+            auto load_g = [&](int n, uint4 (&dst)[RPT]) {
+                const int *tok = meta_tok(n % kMetaStages);
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const int t = tok[rb * RPT + i];
+                    dst[i] = t >= 0 ? __ldg(reinterpret_cast<const uint4 *>(gg + ((int64_t)t * H + seg.h) * KC + col0))
+                                    : make_uint4(0, 0, 0, 0);
+                }
+            };
+            auto load_qk = [&](int n) {
+                const int *tok = meta_tok(n % kMetaStages);
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) {
                     const int t = tok[rb * RPT + i];
                     if (t >= 0) {
                         const int64_t ro = ((int64_t)t * H + seg.h) * KC + col0;
-                        rg[i] = __ldg(reinterpret_cast<const uint4 *>(gg + ro));
                         rq[i] = __ldg(reinterpret_cast<const uint4 *>(qsrc + ro));
                         rk[i] = __ldg(reinterpret_cast<const uint4 *>(ksrc + ro));
                     } else {
-                        rg[i] = rq[i] = rk[i] = make_uint4(0, 0, 0, 0);
+                        rq[i] = rk[i] = make_uint4(0, 0, 0, 0);
                     }
                 }
             };
+            RowMeta meta_ahead{-1, 0.f, 0};  // metadata of chunk n + 1 while processing chunk n
             if (nch > 0) {
-                fill_meta(0);
+                store_meta(0, load_meta(0));
+                if (nch > 1) meta_ahead = load_meta(1);
                 named_sync(1, kTrfThreads);
-                prefetch(0);
+                load_g(0, rg);
             }
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
-                const int mst = n % 3;
+                const int mst = n % kMetaStages;
                 const int vb = g_n & 1;
                 unsigned char *sV = sm + (vb ? Smem::V1 : Smem::V0);
                 bool bad = false;
+                // stage (n+1) % 4 last held chunk n-3, whose output rows the epilogue
+                // wrote before the state rows of chunk n-2 (which precede this chunk)
+                if (n + 1 < nch) store_meta(n + 1, meta_ahead);
+                if (n + 2 < nch) meta_ahead = load_meta(n + 2);
+                load_qk(n);
                 // V buffer vb was last read by chunk g_n - 2
                 if (n >= 2) bad = !mbar_wait_bounded(bar(vb ? kBarV1 : kBarV0), ((g_n - 2) >> 1) & 1, kWaitNs);
                 {   // gather V rows of chunk n with cp.async
@@ -309,6 +353,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                     for (int j = 0; j < 8; ++j) s_tot[rb * 128 + col0 + j] = run[j];
                 }
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
+                if (n + 1 < nch) load_g(n + 1, rg_next);  // a whole chunk of latency hiding
                 float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (tt < KC) {  // per-column exclusive scan over row blocks
                     float acc = 0.f, gmid = 0.f;
@@ -320,57 +365,57 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                     }
                     s_fmid[tt] = expf(gmid);
                     s_beta[tt] = expf(acc - gmid);
-                    s_tot[32 * 128 + tt] = gmid;
+                    s_tot[32 * 128 + tt] = gmid * kLog2e;
                 }
                 named_sync(1, kTrfThreads);
                 // Qt / Kt buffers are free once the first three MMAs of chunk n-1 completed
                 if (n >= 1) bad = !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
-                // pass 2: Qt, Kt rows (bf16) straight into their tiles
+                // pass 2: Qt, Kt rows (bf16) straight into their tiles.  The read
+                // weight e * scale is applied to the output rows by the epilogue.
+                // The decay factors are rounded to bf16 and multiplied into the bf16
+                // q / k pairs with packed bf16 products.
                 {
-                    float run[8], gm[8];
+                    float run[8], gm2[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        run[j] = s_tot[rb * 128 + col0 + j];
-                        gm[j] = s_tot[32 * 128 + col0 + j];
+                        run[j] = s_tot[rb * 128 + col0 + j] * kLog2e;
+                        gm2[j] = s_tot[32 * 128 + col0 + j];
                     }
                     const float *me = meta_e(mst);
-                    bool range_bad = false;
+                    float maxdev = 0.f;
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
                         const int r = rb * RPT + i;
                         const float e = me[r];
-                        const float eq = e * scale;
                         const uint32_t wg4[4] = {rg[i].x, rg[i].y, rg[i].z, rg[i].w};
                         const uint32_t wq4[4] = {rq[i].x, rq[i].y, rq[i].z, rq[i].w};
                         const uint32_t wk4[4] = {rk[i].x, rk[i].y, rk[i].z, rk[i].w};
                         uint32_t pq[4], pk[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            float g0, g1, q0, q1, k0, k1;
+                            float g0, g1;
                             unpack2(wg4[j], g0, g1);
-                            unpack2(wq4[j], q0, q1);
-                            unpack2(wk4[j], k0, k1);
-                            run[2 * j] += g0;
-                            run[2 * j + 1] += g1;
-                            const float d0 = (run[2 * j] - gm[2 * j]) * kLog2e;
-                            const float d1 = (run[2 * j + 1] - gm[2 * j + 1]) * kLog2e;
-                            range_bad |= fabsf(d0) > kGateRangeLog2 || fabsf(d1) > kGateRangeLog2;
-                            pq[j] = pack_bf16x2(eq * q0 * exp2f(d0), eq * q1 * exp2f(d1));
-                            pk[j] = pack_bf16x2(e * k0 * exp2f(-d0), e * k1 * exp2f(-d1));
+                            run[2 * j] = fmaf(g0, kLog2e, run[2 * j]);
+                            run[2 * j + 1] = fmaf(g1, kLog2e, run[2 * j + 1]);
+                            const float d0 = run[2 * j] - gm2[2 * j];
+                            const float d1 = run[2 * j + 1] - gm2[2 * j + 1];
+                            maxdev = fmaxf(maxdev, fmaxf(fabsf(d0), fabsf(d1)));
+                            pq[j] = bf16x2_mul(wq4[j], pack_bf16x2(ex2(d0), ex2(d1)));
+                            pk[j] = bf16x2_mul(wk4[j], pack_bf16x2(e * ex2(-d0), e * ex2(-d1)));
                         }
                         *reinterpret_cast<uint4 *>(sm + Smem::Q + tile_off(r, col0)) =
                             make_uint4(pq[0], pq[1], pq[2], pq[3]);
                         *reinterpret_cast<uint4 *>(sm + Smem::K + tile_off(r, col0)) =
                             make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
-                    if (range_bad) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
+                    if (maxdev > kGateRangeLog2) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
                 }
                 cp_async_wait_all();
                 fence_proxy_async();
-                if (n + 1 < nch) fill_meta(n + 1);
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
                 mbar_arrive(bar(kBarT));
-                if (n + 1 < nch) prefetch(n + 1);
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) rg[i] = rg_next[i];
             }
         } else {
             // =================== epilogue warps ===================
@@ -396,36 +441,51 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                 tmem_wait_st();
             }
             float p_pending = 1.f;
-            __nv_bfloat16 *outp = seg.shared ? part_shared : part_routed;
             const bool issuer = tid == 0;
             const uint32_t q0 = smem_u32(sm + Smem::Q), k0 = smem_u32(sm + Smem::K);
             const uint32_t p0 = smem_u32(sm + Smem::P), s0 = smem_u32(sm + Smem::S);
             constexpr uint32_t idA = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idS = idesc_bf16(128, DV, 1, 1);
             constexpr uint32_t idO = idesc_bf16(128, DV, 0, 1);
-            auto write_out = [&](uint32_t g_o, int n_o) {  // O of chunk n_o -> bf16 partial rows
-                const long long dst = meta_dst(n_o % 3)[row];
-                uint4 packed[DV / 8];
+            // Output of chunk n_o: each thread scales its TMEM row of O by the read
+            // weight e * scale and stages it as bf16 in the P tile (free until
+            // the next P); then each warp copies its 32 staged rows to their
+            // partial slots with coalesced 16-byte stores (straight to out when
+            // a row has a single contribution).
+            constexpr int CPR = DV / 8;        // 16-byte chunks per row
+            constexpr int RPI = 32 / CPR;      // rows per warp-wide copy step
+            const int lane = tid & 31;
+            auto write_out = [&](int n_o) {
+                const int st = n_o % kMetaStages;
+                const float w = meta_e(st)[row] * scale;
 #pragma unroll
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        packed[c0 / 8 + i] = make_uint4(
-                            pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                            pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                            pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                            pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+                    for (int i = 0; i < 32; i += 8)
+                        *reinterpret_cast<uint4 *>(sm + Smem::P + tile_off(row, c0 + i)) = make_uint4(
+                            pack_bf16x2(w * __uint_as_float(r[i]), w * __uint_as_float(r[i + 1])),
+                            pack_bf16x2(w * __uint_as_float(r[i + 2]), w * __uint_as_float(r[i + 3])),
+                            pack_bf16x2(w * __uint_as_float(r[i + 4]), w * __uint_as_float(r[i + 5])),
+                            pack_bf16x2(w * __uint_as_float(r[i + 6]), w * __uint_as_float(r[i + 7])));
                 }
                 fence_before();
                 mbar_arrive(bar(kBarOf));  // O may be overwritten now
-                (void)g_o;
-                if (dst >= 0) {
-                    uint4 *o4 = reinterpret_cast<uint4 *>(outp + dst);
-#pragma unroll
-                    for (int i = 0; i < DV / 8; ++i) o4[i] = packed[i];
+                __syncwarp();
+                const int *tok = meta_tok(st), *slt = meta_slot(st);
+                const int ch = lane % CPR;
+#pragma unroll 4
+                for (int it = 0; it < 32 / RPI; ++it) {
+                    const int r = 32 * warp + it * RPI + lane / CPR;
+                    const int t = tok[r];
+                    if (t >= 0) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(sm + Smem::P + tile_off(r, ch * 8));
+                        const int64_t th = (int64_t)t * H + seg.h;
+                        __nv_bfloat16 *dst = ncon == 1 ? gout + th * DV : part + (th * ncon + slt[r]) * DV;
+                        *reinterpret_cast<uint4 *>(dst + ch * 8) = u;
+                    }
                 }
             };
             for (int n = 0; n < nch; ++n) {
@@ -437,7 +497,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                         break;
                     }
                     fence_after();
-                    write_out(g_n - 1, n - 1);
+                    write_out(n - 1);
                 }
                 // state rows: S_stored *= exp(G_m) * p; bf16 copy -> S' tile
                 const float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
@@ -502,16 +562,26 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                 // P = causal mask of A, bf16
                 if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarA), g_n & 1, kWaitNs))) { failed = true; break; }
                 fence_after();
+                // warp w holds rows 32w..32w+31: column blocks left of the diagonal
+                // block are copied, the diagonal block is masked, the rest is 0
 #pragma unroll
                 for (int c0 = 0; c0 < kC; c0 += 32) {
+                    if (c0 > 32 * warp) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8)
+                            *reinterpret_cast<uint4 *>(sm + Smem::P + tile_off(row, c0 + i)) = make_uint4(0, 0, 0, 0);
+                        continue;
+                    }
                     uint32_t r[32];
                     tmem_ld32(tA + c0, r);
                     tmem_wait_ld();
+                    const bool diag = c0 == 32 * warp;
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
                         float f[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) f[j] = (c0 + i + j <= row) ? __uint_as_float(r[i + j]) : 0.f;
+                        for (int j = 0; j < 8; ++j)
+                            f[j] = (!diag || c0 + i + j <= row) ? __uint_as_float(r[i + j]) : 0.f;
                         *reinterpret_cast<uint4 *>(sm + Smem::P + tile_off(row, c0 + i)) =
                             make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                        pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
@@ -543,7 +613,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                 if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarO), g_l & 1, kWaitNs))) failed = true;
                 else {
                     fence_after();
-                    write_out(g_l, nch - 1);
+                    write_out(nch - 1);
                 }
             }
             // final state = p * S_stored
@@ -580,6 +650,36 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
     }
 }
 
+// out[row, :] = sum over the row's ncon bf16 partial slots (routed slots
+// 0..k-1, then the shared slot), 8 columns per thread, fp32 accumulation.
+__global__ void __launch_bounds__(256)
+slot_combine_kernel(const __nv_bfloat16 *__restrict__ part, int64_t rows, int32_t d, int32_t ncon,
+                    __nv_bfloat16 *__restrict__ out) {
+    const int cpr = d / 8;
+    const int64_t total = rows * cpr;
+    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = x / cpr;
+        const int ch = (int)(x - row * cpr);
+        const __nv_bfloat16 *src = part + row * ncon * d + ch * 8;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < ncon; ++j) {
+            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)j * d));
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo, hi;
+                unpack2(wv[i], lo, hi);
+                acc[2 * i] += lo;
+                acc[2 * i + 1] += hi;
+            }
+        }
+        *reinterpret_cast<uint4 *>(out + row * d + ch * 8) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+}
+
 template <int KC, int DV>
 cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {
     static bool attr_set = false;  // benign race: every caller sets the same value
@@ -597,6 +697,7 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     int32_t *counter = static_cast<int32_t *>(a.chunk_ws);
     cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
+
     const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
     chunked_forward_kernel<KC, DV><<<grid, kThreads, kSmemBytes, stream>>>(
         a, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
@@ -623,6 +724,17 @@ cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a
     else return cudaErrorInvalidValue;
     *launches += 1;
     return e;
+}
+
+cudaError_t launch_slot_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {
+    const int ncon = cfg.top_k + cfg.use_shared;
+    const int64_t rows = a.total_tokens * cfg.num_heads;
+    if (ncon == 1 || rows == 0) return cudaSuccess;  // the main kernel wrote out directly
+    const int64_t work = rows * (cfg.value_dim / 8);
+    const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 152 * 16);
+    slot_combine_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(a.part_routed), rows,
+                                                    cfg.value_dim, ncon, static_cast<__nv_bfloat16 *>(a.out));
+    return cudaGetLastError();
 }
 
 }  // namespace sse

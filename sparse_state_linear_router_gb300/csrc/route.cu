@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kRouteBlock)
 scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ cu, int32_t nseq,
                const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cnt,
                int32_t max_blocks, const int32_t *__restrict__ seg_off, int32_t H, int32_t N,
-               int32_t k, int32_t *__restrict__ perm, int32_t *__restrict__ perm_rec) {
+               int32_t k, const float *__restrict__ topk_w, int32_t *__restrict__ perm,
+               int32_t *__restrict__ perm_rec, float *__restrict__ perm_e) {
     constexpr int kWarps = kRouteBlock / 32;
     __shared__ uint32_t wmask[kWarps][kMaxPartitions];
     __shared__ int s_b, s_t0, s_t1, s_ok;
@@ -204,6 +205,7 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
         const int64_t pos = (int64_t)seg_off[((int64_t)b * H + h) * N + i] + seg_rank;
         if (perm) perm[pos] = t;
         if (perm_rec) perm_rec[pos] = t * k + jj;
+        if (perm_e) perm_e[pos] = topk_w[((int64_t)t * H + h) * k + jj];
     }
 }
 
@@ -228,8 +230,8 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
     scan_blocks_kernel<<<H * N, 1024, 0, stream>>>(rb.cnt, MB);
     seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, num_seqs, H, N, rb.seg_off);
     scatter_kernel<<<grid, kRouteBlock, 0, stream>>>(rb.topk_idx, cu_seqlens, num_seqs, rb.blk_prefix,
-                                                     rb.cnt, MB, rb.seg_off, H, N, k, rb.perm,
-                                                     rb.perm_rec);
+                                                     rb.cnt, MB, rb.seg_off, H, N, k, rb.topk_w,
+                                                     rb.perm, rb.perm_rec, rb.perm_e);
     return cudaGetLastError();
 }
 

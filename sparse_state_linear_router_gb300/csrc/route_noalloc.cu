@@ -97,6 +97,7 @@ extern "C" sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *r
     rb.topk_w = topk_w;
     rb.perm = perm;
     rb.perm_rec = nullptr;
+    rb.perm_e = nullptr;
     cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, rb, group,
                                       reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;

@@ -55,11 +55,13 @@ RouteBuffers carve_route(Carver &cv, const sse_config_t &c, int64_t T, int32_t S
     int32_t *ws_idx = cv.take<int32_t>((size_t)T * c.num_heads * c.top_k);
     float *ws_w = need_w ? cv.take<float>((size_t)T * c.num_heads * c.top_k) : nullptr;
     int32_t *ws_rec = need_rec ? cv.take<int32_t>((size_t)T * c.num_heads * c.top_k) : nullptr;
+    float *ws_pe = need_rec ? cv.take<float>((size_t)T * c.num_heads * c.top_k) : nullptr;
     rb.seg_off = seg_off ? seg_off : ws_seg;
     rb.topk_idx = topk_idx ? topk_idx : ws_idx;
     rb.topk_w = topk_w ? topk_w : ws_w;
     rb.perm = perm;
     rb.perm_rec = ws_rec;
+    rb.perm_e = ws_pe;
     return rb;
 }
 
@@ -83,11 +85,17 @@ ForwardLayout carve_forward(void *ws, const sse_config_t &c, int64_t T, int32_t 
     ForwardLayout L{};
     L.flags = cv.take<int32_t>(64);
     L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
-    // partial read-outs: bf16 on the tensor-core path, fp32 on the recurrent path
-    const size_t pe = use_chunked(c) ? 2 : 4;
-    L.part_routed = cv.take<unsigned char>((size_t)T * c.num_heads * c.top_k * c.value_dim * pe);
-    L.part_shared = c.use_shared ? cv.take<unsigned char>((size_t)T * c.num_heads * c.value_dim * pe) : nullptr;
-    L.chunk_ws = use_chunked(c) ? cv.take<unsigned char>(sse::chunked_extra_workspace(c, T, S)) : nullptr;
+    if (use_chunked(c)) {
+        // bf16 partial read-outs, one slot per contribution of each output row
+        L.part_routed = cv.take<unsigned char>((size_t)T * c.num_heads * (c.top_k + c.use_shared) * c.value_dim * 2);
+        L.part_shared = nullptr;
+        L.chunk_ws = cv.take<unsigned char>(sse::chunked_extra_workspace(c, T, S));
+    } else {
+        // fp32 partial read-outs for the combine kernel
+        L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
+        L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
+        L.chunk_ws = nullptr;
+    }
     L.bytes = (cv.off + 255) & ~size_t(255);
     return L;
 }
@@ -194,6 +202,7 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     a.out = out;
     a.seg_off = L.rb.seg_off;
     a.perm_rec = L.rb.perm_rec;
+    a.perm_e = L.rb.perm_e;
     a.topk_w = L.rb.topk_w;
     a.part_routed = L.part_routed;
     a.part_shared = L.part_shared;
@@ -202,14 +211,18 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     a.chunk_ws = L.chunk_ws;
     if (use_chunked(c)) {
         e = sse::launch_forward_chunked(c, a, s, &launches);
+        if (e != cudaSuccess || mark(2) != cudaSuccess) return SSE_ERR_CUDA;
+        e = sse::launch_slot_combine(c, a, s);
+        if (c.top_k + c.use_shared > 1) launches += 1;
+        if (e != cudaSuccess) return SSE_ERR_CUDA;
     } else {
         e = sse::launch_forward_recurrent(c, a, s);
         launches += 1;
+        if (e != cudaSuccess || mark(2) != cudaSuccess) return SSE_ERR_CUDA;
+        e = sse::launch_combine(c, a, s);
+        launches += 1;
+        if (e != cudaSuccess) return SSE_ERR_CUDA;
     }
-    if (e != cudaSuccess || mark(2) != cudaSuccess) return SSE_ERR_CUDA;
-    e = sse::launch_combine(c, a, s);
-    launches += 1;
-    if (e != cudaSuccess) return SSE_ERR_CUDA;
     if (mark(3) != cudaSuccess) return SSE_ERR_CUDA;
     if (num_launches) *num_launches = launches;
     return SSE_OK;

@@ -121,6 +121,7 @@ struct RouteBuffers {
     float *topk_w;        // [T * H * k]
     int32_t *perm;        // [H * k * T] token ids (may be null)
     int32_t *perm_rec;    // [H * k * T] record ids t * k + j (may be null)
+    float *perm_e;        // [H * k * T] router weight of each record (may be null)
     int32_t max_blocks;
 };
 
@@ -131,8 +132,8 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
                          int32_t num_seqs, int64_t total_tokens, const RouteBuffers &rb,
                          bool group, cudaStream_t stream);
 
-// Recurrent (CUDA-core) forward over all segments; writes fp32 partials.
-// The chunked path writes bf16 partials.
+// Recurrent (CUDA-core) forward over all segments; writes fp32 partials that
+// launch_combine sums.  The chunked path writes bf16 slots for launch_slot_combine.
 struct ForwardArgs {
     const void *q, *k, *v, *g, *qs, *ks;
     const int32_t *cu_seqlens;
@@ -143,9 +144,10 @@ struct ForwardArgs {
     void *out;
     const int32_t *seg_off;
     const int32_t *perm_rec;
+    const float *perm_e;
     const float *topk_w;
-    void *part_routed;   // [T, H, k, d] partial read-outs (fp32, or bf16 if part_bf16)
-    void *part_shared;   // [T, H, d]
+    void *part_routed;   // recurrent: [T, H, k, d] fp32; chunked: [T, H, k + shared, d] bf16
+    void *part_shared;   // recurrent: [T, H, d] fp32; chunked: unused
     int32_t part_bf16;
     int32_t *flags;
     void *chunk_ws;      // chunked path scratch
@@ -160,8 +162,10 @@ size_t chunked_extra_workspace(const sse_config_t &cfg, int64_t total_tokens, in
 cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream,
                                    int *launches);
 
-// out[t,h,:] = sum_j part_routed[t,h,j,:] + part_shared[t,h,:]
+// out[t,h,:] = sum_j part_routed[t,h,j,:] + part_shared[t,h,:]   (recurrent path)
 cudaError_t launch_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+// out[t,h,:] = sum of the bf16 slots part_routed[t,h,0..k+shared-1,:]   (chunked path)
+cudaError_t launch_slot_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
 
 bool decode_supported(const sse_config_t &cfg);
 cudaError_t launch_decode(const sse_config_t &cfg, const void *q, const void *k, const void *v,
