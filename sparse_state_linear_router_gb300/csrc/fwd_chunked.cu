@@ -58,7 +58,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGateRangeLog2 = 80.f * kLog2e;  // |G_r - G_m| limit (~80 natural-log units)
 
 constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
-constexpr int kMetaStages = 4;          // row metadata ring (chunk n in stage n % 4)
+// Row metadata ring (chunk n in stage n % 6).  The epilogue reads chunk
+// n-1's rows at the end of its chunk-n step, by which time the transform warps
+// may have stored the metadata of chunks up to n+3: five live stages.
+constexpr int kMetaStages = 6;
 
 enum Bar { kBarT = 0, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1, kNumBars };
 
@@ -70,9 +73,12 @@ struct Smem {
     static constexpr uint32_t V1 = V0 + kTile;
     static constexpr uint32_t P = V1 + kTile;
     static constexpr uint32_t S = P + kTile;
-    static constexpr uint32_t TOT = S + kTile;             // [33][128] f32 block prefixes; row 32: G_m
+    // output staging reuses the S' tile with a padded row pitch; it spills
+    // into this extension (128 rows x 272 bytes > 32 KB)
+    static constexpr uint32_t SEXT = S + kTile;
+    static constexpr uint32_t TOT = SEXT + 2048;           // [33][128] f32 block prefixes; row 32: G_m
     static constexpr uint32_t SCALE = TOT + 33 * 128 * 4;  // [2 stages][2][128] f32: exp(G_m), exp(G_last-G_m)
-    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [4 stages] x {tok, e, partial slot}[128]
+    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [kMetaStages] x {tok, e, partial slot}[128]
     static constexpr uint32_t META_STAGE = 128 * (4 + 4 + 4);
     static constexpr uint32_t BAR = META + kMetaStages * META_STAGE;
     static constexpr uint32_t MISC = BAR + 8 * kNumBars;   // TMEM slot, work item
@@ -80,7 +86,8 @@ struct Smem {
 };
 constexpr size_t kSmemBytes = Smem::END + 1024;  // + alignment slack
 
-constexpr uint32_t kTmemA = 0, kTmemO = 128, kTmemS = 256, kTmemCols = 512;
+// TMEM columns: A (Qt Kt^T), two O buffers (chunk parity), the state S.
+constexpr uint32_t kTmemA = 0, kTmemO0 = 128, kTmemS = 256, kTmemO1 = 384, kTmemCols = 512;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -134,6 +141,15 @@ __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Bulk (TMA engine) copy of `bytes` contiguous bytes, shared -> global.
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until this thread's bulk copies have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct Segment {
     int b, h, slot, base, len;
@@ -247,9 +263,9 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             const __nv_bfloat16 *qsrc = seg.shared ? gqs : gq;
             const __nv_bfloat16 *ksrc = seg.shared ? gks : gk;
 
-            // Row metadata of chunk n: token index, router weight and partial-row
-            // offset.  Loaded into registers two chunks ahead, stored into stage
-            // n % 4 one chunk ahead.
+            // Row metadata of chunk n: token index, router weight and partial slot.
+            // Loaded into registers two chunks ahead, stored into its ring stage
+            // one chunk ahead.
             struct RowMeta { int t; float e; int slot; };
             auto load_meta = [&](int n) {
                 RowMeta m{-1, 0.f, 0};
@@ -313,8 +329,8 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                 const int vb = g_n & 1;
                 unsigned char *sV = sm + (vb ? Smem::V1 : Smem::V0);
                 bool bad = false;
-                // stage (n+1) % 4 last held chunk n-3, whose output rows the epilogue
-                // wrote before the state rows of chunk n-2 (which precede this chunk)
+                // the stage of chunk n+1 last held chunk n-5, whose output rows are
+                // long written (see kMetaStages)
                 if (n + 1 < nch) store_meta(n + 1, meta_ahead);
                 if (n + 2 < nch) meta_ahead = load_meta(n + 2);
                 load_qk(n);
@@ -421,7 +437,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             // =================== epilogue warps ===================
             const int row = tid;  // TMEM lane
             const uint32_t lb = (uint32_t)(32 * warp) << 16;
-            const uint32_t tA = tmem + lb + kTmemA, tO = tmem + lb + kTmemO, tS = tmem + lb + kTmemS;
+            const uint32_t tA = tmem + lb + kTmemA, tS = tmem + lb + kTmemS;
             // initial state -> TMEM
             if (row < KC) {
 #pragma unroll
@@ -447,46 +463,47 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             constexpr uint32_t idA = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idS = idesc_bf16(128, DV, 1, 1);
             constexpr uint32_t idO = idesc_bf16(128, DV, 0, 1);
-            // Output of chunk n_o: each thread scales its TMEM row of O by the read
-            // weight e * scale and stages it as bf16 in the P tile (free until
-            // the next P); then each warp copies its 32 staged rows to their
-            // partial slots with coalesced 16-byte stores (straight to out when
-            // a row has a single contribution).
-            constexpr int CPR = DV / 8;        // 16-byte chunks per row
-            constexpr int RPI = 32 / CPR;      // rows per warp-wide copy step
-            const int lane = tid & 31;
+            // Output of chunk n_o (O buffer of its parity), written one chunk late so
+            // that it overlaps the transform's compute: each thread scales its TMEM
+            // row of O by the read weight e * scale, stages it as a contiguous bf16
+            // row in the S' tile (free once the O = Qt S' product of the following
+            // chunk has completed; row pitch DV*2 + 16 bytes keeps the 16-byte
+            // stores of a warp at the minimum 4-way bank conflict) and hands the
+            // row to the bulk copy engine: one asynchronous shared->global copy per
+            // row into its partial slot (straight to out when a row has a single
+            // contribution).  The staging rows are reused only after
+            // bulk_wait_read().
+            constexpr int CPR = DV / 8;             // 16-byte chunks per row
+            constexpr uint32_t kPitch = DV * 2 + 16;
+            static_assert(128 * kPitch <= kTile + 2048, "staging exceeds S' + extension");
             auto write_out = [&](int n_o) {
                 const int st = n_o % kMetaStages;
                 const float w = meta_e(st)[row] * scale;
+                const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
+                unsigned char *srow = sm + Smem::S + row * kPitch;
 #pragma unroll
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8)
-                        *reinterpret_cast<uint4 *>(sm + Smem::P + tile_off(row, c0 + i)) = make_uint4(
-                            pack_bf16x2(w * __uint_as_float(r[i]), w * __uint_as_float(r[i + 1])),
-                            pack_bf16x2(w * __uint_as_float(r[i + 2]), w * __uint_as_float(r[i + 3])),
-                            pack_bf16x2(w * __uint_as_float(r[i + 4]), w * __uint_as_float(r[i + 5])),
-                            pack_bf16x2(w * __uint_as_float(r[i + 6]), w * __uint_as_float(r[i + 7])));
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<uint4 *>(srow + (c0 / 8 + i) * 16) = make_uint4(
+                            pack_bf16x2(w * __uint_as_float(r[8 * i]), w * __uint_as_float(r[8 * i + 1])),
+                            pack_bf16x2(w * __uint_as_float(r[8 * i + 2]), w * __uint_as_float(r[8 * i + 3])),
+                            pack_bf16x2(w * __uint_as_float(r[8 * i + 4]), w * __uint_as_float(r[8 * i + 5])),
+                            pack_bf16x2(w * __uint_as_float(r[8 * i + 6]), w * __uint_as_float(r[8 * i + 7])));
                 }
                 fence_before();
                 mbar_arrive(bar(kBarOf));  // O may be overwritten now
-                __syncwarp();
-                const int *tok = meta_tok(st), *slt = meta_slot(st);
-                const int ch = lane % CPR;
-#pragma unroll 4
-                for (int it = 0; it < 32 / RPI; ++it) {
-                    const int r = 32 * warp + it * RPI + lane / CPR;
-                    const int t = tok[r];
-                    if (t >= 0) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(sm + Smem::P + tile_off(r, ch * 8));
-                        const int64_t th = (int64_t)t * H + seg.h;
-                        __nv_bfloat16 *dst = ncon == 1 ? gout + th * DV : part + (th * ncon + slt[r]) * DV;
-                        *reinterpret_cast<uint4 *>(dst + ch * 8) = u;
-                    }
+                fence_proxy_async();
+                const int t = meta_tok(st)[row];
+                if (t >= 0) {
+                    const int64_t th = (int64_t)t * H + seg.h;
+                    __nv_bfloat16 *dst = ncon == 1 ? gout + th * DV : part + (th * ncon + meta_slot(st)[row]) * DV;
+                    bulk_store(dst, smem_u32(srow), DV * 2);
                 }
+                bulk_commit();
             };
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
@@ -497,9 +514,11 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                         break;
                     }
                     fence_after();
-                    write_out(n - 1);
                 }
-                // state rows: S_stored *= exp(G_m) * p; bf16 copy -> S' tile
+                // state rows: S_stored *= exp(G_m) * p; bf16 copy -> S' tile, once the
+                // bulk copies of every epilogue thread have read their staged rows
+                bulk_wait_read();
+                named_sync(2, 32 * kEpiWarps);
                 const float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (row < KC) {
                     const float f = s_fmid[row] * p_pending;
@@ -544,14 +563,15 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                             mma_bf16(tmem + kTmemS, desc_sw128(k0 + ro, 1024, 2048),
                                      desc_sw128(v0 + ro, 1024, 2048), idS, 1);
                         }
-                        if (n >= 1) ok = mbar_wait_bounded(bar(kBarOf), (g_n - 1) & 1, kWaitNs);
+                        // O buffer g_n & 1 was last read out for chunk g_n - 2
+                        if (n >= 2) ok = mbar_wait_bounded(bar(kBarOf), g_n & 1, kWaitNs);
                     }
                     if (ok) {
                         fence_after();
 #pragma unroll
                         for (int k16 = 0; k16 < KC; k16 += 16) {
                             const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                            mma_bf16(tmem + kTmemO, desc_sw128(q0 + ko, 16, 2048),
+                            mma_bf16(tmem + ((g_n & 1) ? kTmemO1 : kTmemO0), desc_sw128(q0 + ko, 16, 2048),
                                      desc_sw128(s0 + (k16 / 8) * 2048, 1024, 2048), idO, k16 > 0);
                         }
                         commit(bar(kBarQK));
@@ -598,7 +618,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
 #pragma unroll
                         for (int k16 = 0; k16 < kC; k16 += 16) {
                             const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                            mma_bf16(tmem + kTmemO, desc_sw128(p0 + ko, 16, 2048),
+                            mma_bf16(tmem + ((g_n & 1) ? kTmemO1 : kTmemO0), desc_sw128(p0 + ko, 16, 2048),
                                      desc_sw128(v0 + (k16 / 8) * 2048, 1024, 2048), idO, 1);
                         }
                         commit(bar(kBarO));
@@ -607,6 +627,14 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                     failed = !ok;
                 }
                 if (__any_sync(0xffffffffu, failed)) { failed = true; break; }
+                if (n >= 1) {  // output of the previous chunk, staged in S' once O = Qt S' of this one is done
+                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarQK), g_n & 1, kWaitNs))) {
+                        failed = true;
+                        break;
+                    }
+                    fence_after();
+                    write_out(n - 1);
+                }
             }
             if (!failed && nch > 0) {
                 const uint32_t g_l = gch + nch - 1;
@@ -616,6 +644,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                     write_out(nch - 1);
                 }
             }
+            bulk_wait_all();
             // final state = p * S_stored
             if (!failed && a.final_state && row < KC) {
 #pragma unroll
