@@ -221,6 +221,31 @@ def _dist():
     return ws, rank, local
 
 
+def rank_barrier(ws):
+    """Barrier over all ranks of the job (no-op for one process)."""
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks_of(x, ws, dev):
+    """Largest value of the scalar x over all ranks (the slowest rank's time)."""
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        tt = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+    return x
+
+
+def whole_job_tokens_per_s(ws, tokens_per_rank_step, ms_per_step):
+    """Weak scaling: every rank processes its own batch of tokens_per_rank_step
+    tokens per step; the job rate is all ranks' tokens over the slowest rank's
+    step time."""
+    return ws * tokens_per_rank_step / (ms_per_step * 1e-3)
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -343,17 +368,10 @@ def run_native(args):
         launches["n"] += 1
 
     def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        rank_barrier(ws)
 
     def max_over_ranks(x):
-        if ws > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([x], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            return float(tt.item())
-        return x
+        return max_over_ranks_of(x, ws, dev)
 
     # ---- device-resident timing -------------------------------------------
     for i in range(args.warmup):
@@ -385,7 +403,7 @@ def run_native(args):
     timed_launches = launches["n"]
     ms_step = max_over_ranks(t_start.elapsed_time(t_end)) / args.steps
     tokens_step = (T if do_fwd else 0) + (B if do_dec else 0)
-    value = ws * tokens_step / (ms_step * 1e-3)
+    value = whole_job_tokens_per_s(ws, tokens_step, ms_step)
 
     peaks = _peaks()
     hbm = peaks["hbm_gbs"]
@@ -462,7 +480,7 @@ def run_native(args):
         torch.cuda.synchronize()
         barrier()
         e2e_ms = max_over_ranks(ea.elapsed_time(eb) / args.steps)
-        e2e = {"value": ws * tokens_step / (e2e_ms * 1e-3), "unit": "tokens/s",
+        e2e = {"value": whole_job_tokens_per_s(ws, tokens_step, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------
