@@ -3,8 +3,8 @@
 // only on the selected states; update and read-out of eqs. 13-14 and the
 // shared partition of section 2.5).
 //
-// One CTA per (sequence, head).  Thread 0 routes the token (softmax + top-k
-// over N logits); the token vectors go to shared memory; then the CTA streams
+// One CTA per (sequence, head).  Warp 0 routes the token (softmax + top-k
+// over N logits, by shuffles); the token vectors go to shared memory; then the CTA streams
 // exactly k + use_shared states (c x d float32 each) through registers:
 //   S <- diag(exp g) S + w_write k^T v   (read-modify-write, 16-byte vectors)
 //   o += w_read q S                      (partial per thread, reduced in smem)
@@ -17,6 +17,7 @@ namespace sse {
 namespace {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kBatch = 8;  // state rows per thread in flight
 
 template <typename T, int D4>
 __global__ void __launch_bounds__(kDecodeThreads)
@@ -50,18 +51,18 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ kk, const T *__rest
         s_qs[r] = Elem<T>::load(qsrow + r);
     }
     for (int col = tid; col < d; col += kDecodeThreads) s_v[col] = Elem<T>::load(v + bh * d + col);
-    if (tid == 0) {
+    if (tid < 32) {  // warp 0 routes the token
         int idx[kMaxTopK];
         float w[kMaxTopK];
-        route_token<T>(logits + bh * N, N, topk, idx, w);
-        for (int j = 0; j < topk; ++j) {
+        route_token_warp<T>(logits + bh * N, N, topk, tid, idx, w);
+        for (int j = 0; j < topk && tid == 0; ++j) {
             s_slot[j] = idx[j];
             s_ww[j] = w[j];
             s_wr[j] = w[j] * scale;
             if (topk_idx) topk_idx[bh * topk + j] = idx[j];
             if (topk_w) topk_w[bh * topk + j] = w[j];
         }
-        if (use_shared) {
+        if (use_shared && tid == 0) {
             s_slot[topk] = N;
             s_ww[topk] = 1.f;
             s_wr[topk] = scale;
@@ -82,20 +83,32 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ kk, const T *__rest
         const float *qvec = shared_slot ? s_qs : s_q;
         const float ww = s_ww[sl], wr = s_wr[sl];
         float *S = state + (bh * P + s_slot[sl]) * (int64_t)c * d;
-#pragma unroll 4
-        for (int r = rg; r < c; r += R) {
-            float4 *p = reinterpret_cast<float4 *>(S + (int64_t)r * d + col);
-            float4 s = __ldcs(p);
-            const float a = s_a[r], kw = ww * kvec[r], qw = wr * qvec[r];
-            s.x = fmaf(a, s.x, kw * v4.x);
-            s.y = fmaf(a, s.y, kw * v4.y);
-            s.z = fmaf(a, s.z, kw * v4.z);
-            s.w = fmaf(a, s.w, kw * v4.w);
-            __stcs(p, s);
-            acc.x = fmaf(qw, s.x, acc.x);
-            acc.y = fmaf(qw, s.y, acc.y);
-            acc.z = fmaf(qw, s.z, acc.z);
-            acc.w = fmaf(qw, s.w, acc.w);
+        // kBatch rows per thread in flight: all loads of a batch are issued
+        // before its first store
+        for (int r0 = rg; r0 < c; r0 += kBatch * R) {
+            float4 sv[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int r = r0 + u * R;
+                if (r < c) sv[u] = __ldcs(reinterpret_cast<const float4 *>(S + (int64_t)r * d + col));
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int r = r0 + u * R;
+                if (r < c) {
+                    float4 s = sv[u];
+                    const float a = s_a[r], kw = ww * kvec[r], qw = wr * qvec[r];
+                    s.x = fmaf(a, s.x, kw * v4.x);
+                    s.y = fmaf(a, s.y, kw * v4.y);
+                    s.z = fmaf(a, s.z, kw * v4.z);
+                    s.w = fmaf(a, s.w, kw * v4.w);
+                    __stcs(reinterpret_cast<float4 *>(S + (int64_t)r * d + col), s);
+                    acc.x = fmaf(qw, s.x, acc.x);
+                    acc.y = fmaf(qw, s.y, acc.y);
+                    acc.z = fmaf(qw, s.z, acc.z);
+                    acc.w = fmaf(qw, s.w, acc.w);
+                }
+            }
         }
     }
     *reinterpret_cast<float4 *>(s_red + rg * d + col) = acc;

@@ -88,10 +88,10 @@ __device__ __forceinline__ bool find_block(const int32_t *blk_prefix, const int3
     return true;
 }
 
-template <typename T>
+template <typename T, int NP>
 __global__ void __launch_bounds__(kRouteBlock)
 route_count_kernel(const T *__restrict__ logits, const int32_t *__restrict__ cu, int32_t nseq,
-                   const int32_t *__restrict__ blk_prefix, int32_t H, int32_t N, int32_t k,
+                   const int32_t *__restrict__ blk_prefix, int32_t H, int32_t N, int32_t k, int32_t vec,
                    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                    int32_t *__restrict__ cnt, int32_t max_blocks) {
     __shared__ int hist[kMaxPartitions];
@@ -109,7 +109,7 @@ route_count_kernel(const T *__restrict__ logits, const int32_t *__restrict__ cu,
         if (t < s_t1) {
             int idx[kMaxTopK];
             float w[kMaxTopK];
-            route_token<T>(logits + ((int64_t)t * H + h) * N, N, k, idx, w);
+            route_token<T, NP>(logits + ((int64_t)t * H + h) * N, N, k, vec != 0, idx, w);
             const int64_t o = ((int64_t)t * H + h) * k;
             for (int jj = 0; jj < k; ++jj) {
                 topk_idx[o + jj] = idx[jj];
@@ -209,6 +209,23 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
     }
 }
 
+// Router launch with the unroll bound NP >= N; rows go through 16-byte
+// vector loads when every row starts on a 16-byte boundary.
+template <typename T>
+void launch_count(dim3 grid, cudaStream_t stream, const T *logits, const int32_t *cu, int32_t nseq,
+                  const int32_t *blk_prefix, int32_t H, int32_t N, int32_t k, int32_t *topk_idx,
+                  float *topk_w, int32_t *cnt, int32_t MB) {
+    const int vec = (N * sizeof(T)) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+#define SSE_COUNT(NP)                                                                                   \
+    route_count_kernel<T, NP><<<grid, kRouteBlock, 0, stream>>>(logits, cu, nseq, blk_prefix, H, N, k, \
+                                                               vec, topk_idx, topk_w, cnt, MB)
+    if (N <= 8) SSE_COUNT(8);
+    else if (N <= 16) SSE_COUNT(16);
+    else if (N <= 32) SSE_COUNT(32);
+    else SSE_COUNT(64);
+#undef SSE_COUNT
+}
+
 }  // namespace
 
 cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int32_t *cu_seqlens,
@@ -219,13 +236,11 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
     plan_blocks_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, rb.blk_prefix);
     dim3 grid(MB, H);
     if (cfg.dtype == SSE_BF16)
-        route_count_kernel<__nv_bfloat16><<<grid, kRouteBlock, 0, stream>>>(
-            static_cast<const __nv_bfloat16 *>(logits), cu_seqlens, num_seqs, rb.blk_prefix, H, N, k,
-            rb.topk_idx, rb.topk_w, rb.cnt, MB);
+        launch_count<__nv_bfloat16>(grid, stream, static_cast<const __nv_bfloat16 *>(logits), cu_seqlens,
+                                    num_seqs, rb.blk_prefix, H, N, k, rb.topk_idx, rb.topk_w, rb.cnt, MB);
     else
-        route_count_kernel<float><<<grid, kRouteBlock, 0, stream>>>(
-            static_cast<const float *>(logits), cu_seqlens, num_seqs, rb.blk_prefix, H, N, k,
-            rb.topk_idx, rb.topk_w, rb.cnt, MB);
+        launch_count<float>(grid, stream, static_cast<const float *>(logits), cu_seqlens, num_seqs,
+                            rb.blk_prefix, H, N, k, rb.topk_idx, rb.topk_w, rb.cnt, MB);
     if (!group) return cudaGetLastError();
     scan_blocks_kernel<<<H * N, 1024, 0, stream>>>(rb.cnt, MB);
     seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, num_seqs, H, N, rb.seg_off);

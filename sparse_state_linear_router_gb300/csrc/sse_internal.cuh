@@ -61,22 +61,41 @@ template <> struct Elem<__nv_bfloat16> {
 // Router for one (token, head): softmax over N logits in fp32 and the top-k
 // by logit, equal logits ordered by ascending index (strict comparison while
 // scanning upward keeps the lower index).  idx/w receive k entries in
-// descending-logit order.
+// descending-logit order.  NP >= N bounds the unrolled loops (8, 16, 32 or
+// 64); `vec` says that the N logits of the row are 16-byte aligned and fill
+// whole 16-byte words, so they are read with vector loads.
 // ---------------------------------------------------------------------------
-template <typename T>
-__device__ __forceinline__ void route_token(const T *logit, int N, int k, int *idx, float *w) {
-    float l[kMaxPartitions];
+template <typename T, int NP>
+__device__ __forceinline__ void route_token(const T *logit, int N, int k, bool vec, int *idx, float *w) {
+    float l[NP];
+    constexpr int EPV = 16 / sizeof(T);  // elements per 16-byte word
+    if (vec) {
+#pragma unroll
+        for (int i0 = 0; i0 < NP; i0 += EPV) {
+            if (i0 < N) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(logit + i0));
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    if (sizeof(T) == 2)
+                        l[i0 + e] = __uint_as_float(e & 1 ? (wv[e / 2] & 0xffff0000u) : (wv[e / 2] << 16));
+                    else
+                        l[i0 + e] = __uint_as_float(wv[e]);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NP; ++i)
+            if (i < N) l[i] = Elem<T>::load(logit + i);
+    }
     float m = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kMaxPartitions; ++i) {
-        if (i < N) {
-            l[i] = Elem<T>::load(logit + i);
-            m = fmaxf(m, l[i]);
-        }
-    }
+    for (int i = 0; i < NP; ++i)
+        if (i < N) m = fmaxf(m, l[i]);
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxPartitions; ++i)
+    for (int i = 0; i < NP; ++i)
         if (i < N) s += expf(l[i] - m);
     const float inv = 1.f / s;
     uint64_t taken = 0;
@@ -85,13 +104,50 @@ __device__ __forceinline__ void route_token(const T *logit, int N, int k, int *i
         int bi = -1;
         float bv = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kMaxPartitions; ++i) {
+        for (int i = 0; i < NP; ++i) {
             if (i < N && !((taken >> i) & 1ull) && (bi < 0 || l[i] > bv)) {
                 bv = l[i];
                 bi = i;
             }
         }
         taken |= 1ull << bi;
+        idx[j] = bi;
+        w[j] = expf(bv - m) * inv;
+    }
+}
+
+// The same router evaluated by one warp (lane i holds logits i and i + 32):
+// max, sum of exponentials and k rounds of argmax (ties -> lower index) by
+// shuffles.  Every lane returns the full result.
+template <typename T>
+__device__ __forceinline__ void route_token_warp(const T *logit, int N, int k, int lane, int *idx, float *w) {
+    const float l0 = lane < N ? Elem<T>::load(logit + lane) : -INFINITY;
+    const float l1 = lane + 32 < N ? Elem<T>::load(logit + lane + 32) : -INFINITY;
+    float m = fmaxf(l0, l1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = (lane < N ? expf(l0 - m) : 0.f) + (lane + 32 < N ? expf(l1 - m) : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float inv = 1.f / s;
+    bool t0 = lane >= N, t1 = lane + 32 >= N;  // taken (or absent)
+    for (int j = 0; j < k; ++j) {
+        // this lane's best remaining candidate; the lower index wins ties
+        float bv = -INFINITY;
+        int bi = 1 << 30;
+        if (!t0) { bv = l0; bi = lane; }
+        if (!t1 && (bi == (1 << 30) || l1 > bv)) { bv = l1; bi = lane + 32; }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != (1 << 30) && (bi == (1 << 30) || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi == lane) t0 = true;
+        if (bi == lane + 32) t1 = true;
         idx[j] = bi;
         w[j] = expf(bv - m) * inv;
     }
