@@ -40,6 +40,9 @@
 // and the CTA stops after releasing its TMEM.
 #include <algorithm>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "sse_internal.cuh"
 #include "umma.cuh"
 
@@ -48,7 +51,7 @@ namespace {
 
 using namespace umma;
 
-constexpr int kC = 128;          // chunk rows
+constexpr int kC = kChunkRows;   // chunk rows (128)
 constexpr int kMid = kC / 2 - 1; // midpoint row of the decay split
 constexpr int kEpiWarps = 4, kTrfWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarps + kTrfWarps);  // 384: 3 warps per SM sub-partition
@@ -72,14 +75,12 @@ struct Smem {
     static constexpr uint32_t V0 = K + kTile;
     static constexpr uint32_t V1 = V0 + kTile;
     static constexpr uint32_t P = V1 + kTile;
+    // the S' tile doubles as the output staging tile (see write_out)
     static constexpr uint32_t S = P + kTile;
-    // output staging reuses the S' tile with a padded row pitch; it spills
-    // into this extension (128 rows x 272 bytes > 32 KB)
-    static constexpr uint32_t SEXT = S + kTile;
-    static constexpr uint32_t TOT = SEXT + 2048;           // [33][128] f32 block prefixes; row 32: G_m
+    static constexpr uint32_t TOT = S + kTile;             // [33][128] f32 block prefixes; row 32: G_m
     static constexpr uint32_t SCALE = TOT + 33 * 128 * 4;  // [2 stages][2][128] f32: exp(G_m), exp(G_last-G_m)
-    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [kMetaStages] x {tok, e, partial slot}[128]
-    static constexpr uint32_t META_STAGE = 128 * (4 + 4 + 4);
+    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [kMetaStages] x {tok, e}[128]
+    static constexpr uint32_t META_STAGE = 128 * (4 + 4);
     static constexpr uint32_t BAR = META + kMetaStages * META_STAGE;
     static constexpr uint32_t MISC = BAR + 8 * kNumBars;   // TMEM slot, work item
     static constexpr uint32_t END = MISC + 16;
@@ -147,6 +148,12 @@ __device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t b
                  :: "l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Tensor (TMA) store of one box of a 2-D tensor map from shared memory; the
+// box's inner coordinate x and row coordinate y.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t ssrc, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(ssrc), "r"(x), "r"(y) : "memory");
+}
 // Waits until this thread's bulk copies have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -182,8 +189,9 @@ __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item
 
 template <int KC, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared,
-                       float scale, int32_t num_items, int32_t *work_counter) {
+chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_map, int32_t H, int32_t N,
+                       int32_t topk, int32_t use_shared, float scale, int32_t num_items,
+                       int32_t *work_counter) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *s_tot = reinterpret_cast<float *>(sm + Smem::TOT);
@@ -201,18 +209,11 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
     const __nv_bfloat16 *gg = static_cast<const __nv_bfloat16 *>(a.g);
     const __nv_bfloat16 *gqs = static_cast<const __nv_bfloat16 *>(a.qs ? a.qs : a.q);
     const __nv_bfloat16 *gks = static_cast<const __nv_bfloat16 *>(a.ks ? a.ks : a.k);
-    // Partial read-outs [T*H][ncon][DV] (bf16), summed by the slot-combine kernel.
-    __nv_bfloat16 *part = static_cast<__nv_bfloat16 *>(a.part_routed);
-    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.out);
-    const int ncon = topk + use_shared;  // contributions per (token, head) row
     const int P = N + use_shared;
 
     auto meta_tok = [&](int stage) { return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE); };
     auto meta_e = [&](int stage) {
         return reinterpret_cast<float *>(sm + Smem::META + stage * Smem::META_STAGE + 512);
-    };
-    auto meta_slot = [&](int stage) {
-        return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE + 1024);
     };
 
     // ---- set-up ------------------------------------------------------------
@@ -251,6 +252,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
         __syncthreads();
         if (stop) break;
         const Segment seg = decode_segment(a, item, H, N, use_shared);
+        const int pad_base = a.pad_off[item];  // first partial-output row of this work item
         const int nch = (seg.len + kC - 1) / kC;
         const int64_t state_off = (((int64_t)seg.b * H + seg.h) * P + seg.slot) * (int64_t)KC * DV;
         bool failed = false;
@@ -263,23 +265,20 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             const __nv_bfloat16 *qsrc = seg.shared ? gqs : gq;
             const __nv_bfloat16 *ksrc = seg.shared ? gks : gk;
 
-            // Row metadata of chunk n: token index, router weight and partial slot.
-            // Loaded into registers two chunks ahead, stored into its ring stage
-            // one chunk ahead.
-            struct RowMeta { int t; float e; int slot; };
+            // Row metadata of chunk n: token index and router weight.  Loaded
+            // into registers two chunks ahead, stored into its ring stage one
+            // chunk ahead.
+            struct RowMeta { int t; float e; };
             auto load_meta = [&](int n) {
-                RowMeta m{-1, 0.f, 0};
+                RowMeta m{-1, 0.f};
                 const int idx = n * kC + tt;
                 if (tt < kC && idx < seg.len) {
                     if (seg.shared) {
                         m.t = seg.base + idx;
                         m.e = 1.f;
-                        m.slot = topk;
                     } else {
-                        const int rec = a.perm_rec[seg.base + idx];
+                        m.t = a.perm_rec[seg.base + idx] / topk;
                         m.e = a.perm_e[seg.base + idx];
-                        m.t = rec / topk;
-                        m.slot = rec - m.t * topk;
                     }
                 }
                 return m;
@@ -289,7 +288,6 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                     const int st = n % kMetaStages;
                     meta_tok(st)[tt] = m.t;
                     meta_e(st)[tt] = m.e;
-                    meta_slot(st)[tt] = m.slot;
                 }
             };
             uint4 rq[RPT], rk[RPT], rg[RPT], rg_next[RPT];
@@ -316,7 +314,7 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                     }
                 }
             };
-            RowMeta meta_ahead{-1, 0.f, 0};  // metadata of chunk n + 1 while processing chunk n
+            RowMeta meta_ahead{-1, 0.f};  // metadata of chunk n + 1 while processing chunk n
             if (nch > 0) {
                 store_meta(0, load_meta(0));
                 if (nch > 1) meta_ahead = load_meta(1);
@@ -465,60 +463,63 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             constexpr uint32_t idO = idesc_bf16(128, DV, 0, 1);
             // Output of chunk n_o (O buffer of its parity), written one chunk late so
             // that it overlaps the transform's compute: each thread scales its TMEM
-            // row of O by the read weight e * scale, stages it as a contiguous bf16
-            // row in the S' tile (free once the O = Qt S' product of the following
-            // chunk has completed; row pitch DV*2 + 16 bytes keeps the 16-byte
-            // stores of a warp at the minimum 4-way bank conflict) and hands the
-            // row to the bulk copy engine: one asynchronous shared->global copy per
-            // row into its partial slot (straight to out when a row has a single
-            // contribution).  The staging rows are reused only after
+            // row of O by the read weight e * scale and stores it as bf16 into the
+            // S' tile (free once the O = Qt S' product of the following chunk has
+            // completed), laid out as the tensor map's 64-column boxes with the
+            // 128-byte swizzle (conflict-free 16-byte stores).  One thread then
+            // hands the whole chunk to the TMA engine: the work item's rows of the
+            // partial buffer are contiguous and padded to whole chunks, so the chunk
+            // is DV/64 box stores.  The staging tile is reused only after
             // bulk_wait_read().
-            constexpr int CPR = DV / 8;             // 16-byte chunks per row
-            constexpr uint32_t kPitch = DV * 2 + 16;
-            static_assert(128 * kPitch <= kTile + 2048, "staging exceeds S' + extension");
-            auto write_out = [&](int n_o) {
+            auto write_out = [&](int n_o, bool pend) -> bool {
                 const int st = n_o % kMetaStages;
                 const float w = meta_e(st)[row] * scale;
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
-                unsigned char *srow = sm + Smem::S + row * kPitch;
+                unsigned char *stg = sm + Smem::S;
 #pragma unroll
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        *reinterpret_cast<uint4 *>(srow + (c0 / 8 + i) * 16) = make_uint4(
-                            pack_bf16x2(w * __uint_as_float(r[8 * i]), w * __uint_as_float(r[8 * i + 1])),
-                            pack_bf16x2(w * __uint_as_float(r[8 * i + 2]), w * __uint_as_float(r[8 * i + 3])),
-                            pack_bf16x2(w * __uint_as_float(r[8 * i + 4]), w * __uint_as_float(r[8 * i + 5])),
-                            pack_bf16x2(w * __uint_as_float(r[8 * i + 6]), w * __uint_as_float(r[8 * i + 7])));
+                    for (int i = 0; i < 4; ++i) {
+                        const int col = c0 + 8 * i;
+                        const int ch = (col % 64) / 8;
+                        *reinterpret_cast<uint4 *>(stg + (col / 64) * (kC * 128) + row * 128 + ((ch ^ (row & 7)) << 4)) =
+                            make_uint4(
+                                pack_bf16x2(w * __uint_as_float(r[8 * i]), w * __uint_as_float(r[8 * i + 1])),
+                                pack_bf16x2(w * __uint_as_float(r[8 * i + 2]), w * __uint_as_float(r[8 * i + 3])),
+                                pack_bf16x2(w * __uint_as_float(r[8 * i + 4]), w * __uint_as_float(r[8 * i + 5])),
+                                pack_bf16x2(w * __uint_as_float(r[8 * i + 6]), w * __uint_as_float(r[8 * i + 7])));
+                    }
                 }
                 fence_before();
                 mbar_arrive(bar(kBarOf));  // O may be overwritten now
                 fence_proxy_async();
-                const int t = meta_tok(st)[row];
-                if (t >= 0) {
-                    const int64_t th = (int64_t)t * H + seg.h;
-                    __nv_bfloat16 *dst = ncon == 1 ? gout + th * DV : part + (th * ncon + meta_slot(st)[row]) * DV;
-                    bulk_store(dst, smem_u32(srow), DV * 2);
+                if (named_sync_or(3, 32 * kEpiWarps, pend)) return true;
+                if (tid == 0) {
+#pragma unroll
+                    for (int atom = 0; atom < DV / 64; ++atom)
+                        tma_store_2d(&part_map, smem_u32(stg + atom * (kC * 128)), atom * 64, pad_base + n_o * kC);
+                    bulk_commit();
                 }
-                bulk_commit();
+                return false;
             };
+            // A wait that runs out of time sets `pend` in the threads that saw it;
+            // the epilogue warps take every decision to stop together, at one of
+            // their named barriers (bar.red.or), so none is left waiting there.
+            bool pend = false;
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
-                if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarT), g_n & 1, kWaitNs))) { failed = true; break; }
+                pend |= !mbar_wait_bounded(bar(kBarT), g_n & 1, kWaitNs);
                 if (n >= 1) {
-                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarO), (g_n - 1) & 1, kWaitNs))) {
-                        failed = true;
-                        break;
-                    }
+                    pend |= !mbar_wait_bounded(bar(kBarO), (g_n - 1) & 1, kWaitNs);
                     fence_after();
                 }
                 // state rows: S_stored *= exp(G_m) * p; bf16 copy -> S' tile, once the
-                // bulk copies of every epilogue thread have read their staged rows
+                // TMA engine has read the previous chunk's staged output from it
                 bulk_wait_read();
-                named_sync(2, 32 * kEpiWarps);
+                if (named_sync_or(2, 32 * kEpiWarps, pend)) { failed = true; break; }
                 const float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (row < KC) {
                     const float f = s_fmid[row] * p_pending;
@@ -576,11 +577,10 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                         }
                         commit(bar(kBarQK));
                     }
-                    failed = !ok;
+                    pend |= !ok;
                 }
-                if (__any_sync(0xffffffffu, failed)) { failed = true; break; }
                 // P = causal mask of A, bf16
-                if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarA), g_n & 1, kWaitNs))) { failed = true; break; }
+                pend |= !mbar_wait_bounded(bar(kBarA), g_n & 1, kWaitNs);
                 fence_after();
                 // warp w holds rows 32w..32w+31: column blocks left of the diagonal
                 // block are copied, the diagonal block is masked, the rest is 0
@@ -624,25 +624,22 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
                         commit(bar(kBarO));
                         commit(bar((g_n & 1) ? kBarV1 : kBarV0));
                     }
-                    failed = !ok;
+                    pend |= !ok;
                 }
-                if (__any_sync(0xffffffffu, failed)) { failed = true; break; }
                 if (n >= 1) {  // output of the previous chunk, staged in S' once O = Qt S' of this one is done
-                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarQK), g_n & 1, kWaitNs))) {
-                        failed = true;
-                        break;
-                    }
+                    pend |= !mbar_wait_bounded(bar(kBarQK), g_n & 1, kWaitNs);
                     fence_after();
-                    write_out(n - 1);
+                    if (write_out(n - 1, pend)) { failed = true; break; }
+                    pend = false;
                 }
             }
             if (!failed && nch > 0) {
                 const uint32_t g_l = gch + nch - 1;
-                if (__any_sync(0xffffffffu, !mbar_wait_bounded(bar(kBarO), g_l & 1, kWaitNs))) failed = true;
-                else {
-                    fence_after();
-                    write_out(nch - 1);
-                }
+                pend |= !mbar_wait_bounded(bar(kBarO), g_l & 1, kWaitNs);
+                fence_after();
+                // the staging tile is free once the previous chunk's store has read it
+                bulk_wait_read();
+                if (named_sync_or(2, 32 * kEpiWarps, pend) || write_out(nch - 1, false)) failed = true;
             }
             bulk_wait_all();
             // final state = p * S_stored
@@ -679,21 +676,22 @@ chunked_forward_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
     }
 }
 
-// out[row, :] = sum over the row's ncon bf16 partial slots (routed slots
-// 0..k-1, then the shared slot), 8 columns per thread, fp32 accumulation.
+// out[row, :] = sum over the row's ncon bf16 partial rows rec_pos[row * ncon + j]
+// (routed contributions j < k, then the shared one), 8 columns per thread,
+// fp32 accumulation in a fixed order.
 __global__ void __launch_bounds__(256)
-slot_combine_kernel(const __nv_bfloat16 *__restrict__ part, int64_t rows, int32_t d, int32_t ncon,
-                    __nv_bfloat16 *__restrict__ out) {
+gather_combine_kernel(const __nv_bfloat16 *__restrict__ part, const int32_t *__restrict__ rec_pos, int64_t rows,
+                      int32_t d, int32_t ncon, __nv_bfloat16 *__restrict__ out) {
     const int cpr = d / 8;
     const int64_t total = rows * cpr;
     for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
          x += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = x / cpr;
         const int ch = (int)(x - row * cpr);
-        const __nv_bfloat16 *src = part + row * ncon * d + ch * 8;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int j = 0; j < ncon; ++j) {
-            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)j * d));
+            const int64_t pr = __ldg(rec_pos + row * ncon + j);
+            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(part + pr * d + ch * 8));
             const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -707,6 +705,21 @@ slot_combine_kernel(const __nv_bfloat16 *__restrict__ part, int64_t rows, int32_
             make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null when unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
 }
 
 template <int KC, int DV>
@@ -727,9 +740,23 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
 
+    // The partial buffer as a 2-D tensor [part_rows, DV] of bf16, stored in
+    // boxes of 64 columns x one chunk of rows with the 128-byte swizzle.
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)DV, (cuuint64_t)a.part_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)DV * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kC};
+    cuuint32_t elem_strides[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.part_routed, dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
     const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
     chunked_forward_kernel<KC, DV><<<grid, kThreads, kSmemBytes, stream>>>(
-        a, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
+        a, map, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
     return cudaGetLastError();
 }
 
@@ -755,14 +782,19 @@ cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a
     return e;
 }
 
-cudaError_t launch_slot_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {
+int64_t chunked_part_rows(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs) {
+    const int64_t nitems = (int64_t)num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
+    return total_tokens * cfg.num_heads * (cfg.top_k + cfg.use_shared) + nitems * (kChunkRows - 1);
+}
+
+cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {
     const int ncon = cfg.top_k + cfg.use_shared;
     const int64_t rows = a.total_tokens * cfg.num_heads;
-    if (ncon == 1 || rows == 0) return cudaSuccess;  // the main kernel wrote out directly
+    if (rows == 0) return cudaSuccess;
     const int64_t work = rows * (cfg.value_dim / 8);
     const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 152 * 16);
-    slot_combine_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(a.part_routed), rows,
-                                                    cfg.value_dim, ncon, static_cast<__nv_bfloat16 *>(a.out));
+    gather_combine_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(a.part_routed), a.rec_pos,
+                                                      rows, cfg.value_dim, ncon, static_cast<__nv_bfloat16 *>(a.out));
     return cudaGetLastError();
 }
 

@@ -10,9 +10,11 @@
 //                      per-block histogram over partitions -> cnt
 //   scan     (H*N)   : exclusive scan of cnt over blocks, per (h, i)
 //   seg_off  1 CTA   : segment sizes from the scanned counts; exclusive scan
-//                      over s -> seg_off
+//                      over s -> seg_off (and, for the chunked forward, the
+//                      chunk-padded output regions of the work items)
 //   scatter  (blk,H) : rank of each record inside its block (per-warp bit
-//                      masks + popc) + block base -> perm / perm_rec
+//                      masks + popc) + block base -> perm / perm_rec, and the
+//                      partial-output row of every contribution (rec_pos)
 #include "sse_internal.cuh"
 
 namespace sse {
@@ -138,36 +140,64 @@ scan_blocks_kernel(int32_t *__restrict__ cnt, int32_t max_blocks) {
     if (threadIdx.x == 0) row[max_blocks] = carry;
 }
 
+// Length of routed segment s = (b*H + h)*N + i from the scanned block counts.
+__device__ __forceinline__ int routed_len(const int32_t *cnt, int32_t max_blocks, const int32_t *blk_prefix,
+                                          int32_t H, int32_t N, int64_t s) {
+    const int i = (int)(s % N);
+    const int64_t bh = s / N;
+    const int h = (int)(bh % H), b = (int)(bh / H);
+    const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
+    return row[blk_prefix[b + 1]] - row[blk_prefix[b]];
+}
+
+// seg_off: exclusive scan of the routed segment lengths.  pad_off (optional):
+// exclusive scan over the work items (shared segments, then routed ones) of
+// their lengths rounded up to whole chunks.
 __global__ void __launch_bounds__(1024)
 seg_off_kernel(const int32_t *__restrict__ cnt, int32_t max_blocks,
-               const int32_t *__restrict__ blk_prefix, int32_t nseq, int32_t H, int32_t N,
-               int32_t *__restrict__ seg_off) {
+               const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cu, int32_t nseq,
+               int32_t H, int32_t N, int32_t use_shared, int32_t *__restrict__ seg_off,
+               int32_t *__restrict__ pad_off) {
     const int64_t nseg = (int64_t)nseq * H * N;
     int carry = 0;
     for (int64_t base = 0; base < nseg; base += blockDim.x) {
         const int64_t s = base + threadIdx.x;
-        int x = 0;
-        if (s < nseg) {
-            const int i = (int)(s % N);
-            const int64_t bh = s / N;
-            const int h = (int)(bh % H), b = (int)(bh / H);
-            const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
-            x = row[blk_prefix[b + 1]] - row[blk_prefix[b]];
-        }
+        const int x = s < nseg ? routed_len(cnt, max_blocks, blk_prefix, H, N, s) : 0;
         int tot;
         const int ex = block_exclusive_scan(x, &tot);
         if (s < nseg) seg_off[s] = carry + ex;
         carry += tot;
     }
     if (threadIdx.x == 0) seg_off[nseg] = carry;
+    if (!pad_off) return;
+    const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
+    const int64_t nitems = nshared + nseg;
+    carry = 0;
+    for (int64_t base = 0; base < nitems; base += blockDim.x) {
+        const int64_t u = base + threadIdx.x;
+        int x = 0;
+        if (u < nshared) {
+            const int b = (int)(u / H);
+            x = cu[b + 1] - cu[b];
+        } else if (u < nitems) {
+            x = routed_len(cnt, max_blocks, blk_prefix, H, N, u - nshared);
+        }
+        x = (x + kChunkRows - 1) / kChunkRows * kChunkRows;
+        int tot;
+        const int ex = block_exclusive_scan(x, &tot);
+        if (u < nitems) pad_off[u] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) pad_off[nitems] = carry;
 }
 
 __global__ void __launch_bounds__(kRouteBlock)
 scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ cu, int32_t nseq,
                const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cnt,
                int32_t max_blocks, const int32_t *__restrict__ seg_off, int32_t H, int32_t N,
-               int32_t k, const float *__restrict__ topk_w, int32_t *__restrict__ perm,
-               int32_t *__restrict__ perm_rec, float *__restrict__ perm_e) {
+               int32_t k, int32_t use_shared, const float *__restrict__ topk_w, int32_t *__restrict__ perm,
+               int32_t *__restrict__ perm_rec, float *__restrict__ perm_e,
+               const int32_t *__restrict__ pad_off, int32_t *__restrict__ rec_pos) {
     constexpr int kWarps = kRouteBlock / 32;
     __shared__ uint32_t wmask[kWarps][kMaxPartitions];
     __shared__ int s_b, s_t0, s_t1, s_ok;
@@ -196,16 +226,22 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
     __syncthreads();
     if (!valid) return;
     const uint32_t lt = (1u << lane) - 1u;
+    const int ncon = k + use_shared;
+    const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
+    const int64_t th = (int64_t)t * H + h;
+    if (rec_pos && use_shared) rec_pos[th * ncon + k] = pad_off[(int64_t)b * H + h] + (t - cu[b]);
     for (int jj = 0; jj < k; ++jj) {
         const int i = idx[jj];
         int rank = __popc(wmask[warp][i] & lt);
         for (int w2 = 0; w2 < warp; ++w2) rank += __popc(wmask[w2][i]);
         const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
         const int seg_rank = row[j] - row[blk_prefix[b]] + rank;
-        const int64_t pos = (int64_t)seg_off[((int64_t)b * H + h) * N + i] + seg_rank;
+        const int64_t seg = ((int64_t)b * H + h) * N + i;
+        const int64_t pos = (int64_t)seg_off[seg] + seg_rank;
         if (perm) perm[pos] = t;
         if (perm_rec) perm_rec[pos] = t * k + jj;
-        if (perm_e) perm_e[pos] = topk_w[((int64_t)t * H + h) * k + jj];
+        if (perm_e) perm_e[pos] = topk_w[th * k + jj];
+        if (rec_pos) rec_pos[th * ncon + jj] = pad_off[nshared + seg] + seg_rank;
     }
 }
 
@@ -243,10 +279,12 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
                             rb.blk_prefix, H, N, k, rb.topk_idx, rb.topk_w, rb.cnt, MB);
     if (!group) return cudaGetLastError();
     scan_blocks_kernel<<<H * N, 1024, 0, stream>>>(rb.cnt, MB);
-    seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, num_seqs, H, N, rb.seg_off);
+    seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, cu_seqlens, num_seqs, H, N,
+                                           cfg.use_shared, rb.seg_off, rb.pad_off);
     scatter_kernel<<<grid, kRouteBlock, 0, stream>>>(rb.topk_idx, cu_seqlens, num_seqs, rb.blk_prefix,
-                                                     rb.cnt, MB, rb.seg_off, H, N, k, rb.topk_w,
-                                                     rb.perm, rb.perm_rec, rb.perm_e);
+                                                     rb.cnt, MB, rb.seg_off, H, N, k, cfg.use_shared,
+                                                     rb.topk_w, rb.perm, rb.perm_rec, rb.perm_e,
+                                                     rb.pad_off, rb.rec_pos);
     return cudaGetLastError();
 }
 

@@ -40,13 +40,15 @@ sse_status_t check_sizes(const sse_config_t &c, int64_t total_tokens, int32_t nu
     const int64_t recs = total_tokens * c.num_heads * c.top_k;
     if (recs >= (int64_t(1) << 31) || total_tokens * c.top_k >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * c.num_heads * c.num_partitions >= (int64_t(1) << 30)) return SSE_ERR_UNSUPPORTED;
+    if (sse::chunked_part_rows(c, total_tokens, num_seqs) >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
     return SSE_OK;
 }
 
 // Route-stage buffers carved from the workspace.  User-provided outputs are
 // used in place; missing ones live in the workspace.
 RouteBuffers carve_route(Carver &cv, const sse_config_t &c, int64_t T, int32_t S, int32_t *topk_idx,
-                         float *topk_w, int32_t *seg_off, int32_t *perm, bool need_w, bool need_rec) {
+                         float *topk_w, int32_t *seg_off, int32_t *perm, bool need_w, bool need_rec,
+                         bool need_pos = false) {
     RouteBuffers rb{};
     rb.max_blocks = (int32_t)sse::route_max_blocks(T, S);
     rb.blk_prefix = cv.take<int32_t>(S + 1);
@@ -62,6 +64,9 @@ RouteBuffers carve_route(Carver &cv, const sse_config_t &c, int64_t T, int32_t S
     rb.perm = perm;
     rb.perm_rec = ws_rec;
     rb.perm_e = ws_pe;
+    const int64_t nitems = (int64_t)S * c.num_heads * (c.num_partitions + c.use_shared);
+    rb.pad_off = need_pos ? cv.take<int32_t>(nitems + 1) : nullptr;
+    rb.rec_pos = need_pos ? cv.take<int32_t>((size_t)T * c.num_heads * (c.top_k + c.use_shared)) : nullptr;
     return rb;
 }
 
@@ -74,6 +79,7 @@ bool use_chunked(const sse_config_t &c) {
 struct ForwardLayout {
     RouteBuffers rb;
     void *part_routed, *part_shared;
+    int64_t part_rows;
     int32_t *flags;
     void *chunk_ws;
     size_t bytes;
@@ -84,10 +90,12 @@ ForwardLayout carve_forward(void *ws, const sse_config_t &c, int64_t T, int32_t 
     Carver cv(ws);
     ForwardLayout L{};
     L.flags = cv.take<int32_t>(64);
-    L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
-    if (use_chunked(c)) {
-        // bf16 partial read-outs, one slot per contribution of each output row
-        L.part_routed = cv.take<unsigned char>((size_t)T * c.num_heads * (c.top_k + c.use_shared) * c.value_dim * 2);
+    const bool chunked = use_chunked(c);
+    L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true, chunked);
+    if (chunked) {
+        // bf16 partial read-outs, one row per contribution, in work-item order
+        L.part_rows = sse::chunked_part_rows(c, T, S);
+        L.part_routed = cv.take<unsigned char>((size_t)L.part_rows * c.value_dim * 2);
         L.part_shared = nullptr;
         L.chunk_ws = cv.take<unsigned char>(sse::chunked_extra_workspace(c, T, S));
     } else {
@@ -204,6 +212,9 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     a.perm_rec = L.rb.perm_rec;
     a.perm_e = L.rb.perm_e;
     a.topk_w = L.rb.topk_w;
+    a.pad_off = L.rb.pad_off;
+    a.rec_pos = L.rb.rec_pos;
+    a.part_rows = L.part_rows;
     a.part_routed = L.part_routed;
     a.part_shared = L.part_shared;
     a.part_bf16 = use_chunked(c) ? 1 : 0;
@@ -212,8 +223,8 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     if (use_chunked(c)) {
         e = sse::launch_forward_chunked(c, a, s, &launches);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return SSE_ERR_CUDA;
-        e = sse::launch_slot_combine(c, a, s);
-        if (c.top_k + c.use_shared > 1) launches += 1;
+        e = sse::launch_gather_combine(c, a, s);
+        launches += 1;
         if (e != cudaSuccess) return SSE_ERR_CUDA;
     } else {
         e = sse::launch_forward_recurrent(c, a, s);

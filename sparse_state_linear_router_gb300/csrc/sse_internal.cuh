@@ -14,6 +14,7 @@ constexpr int kMaxPartitions = 64;
 constexpr int kMaxTopK = 8;
 constexpr int kRouteBlock = 256;  // tokens per routing block (one thread per token)
 constexpr int kRouteLaunches = 5; // kernels launch_route issues when grouping
+constexpr int kChunkRows = 128;   // rows of a tensor-core chunk; output regions are padded to it
 
 // ---------------------------------------------------------------------------
 // Element access for the two storage dtypes.
@@ -178,6 +179,12 @@ struct RouteBuffers {
     int32_t *perm;        // [H * k * T] token ids (may be null)
     int32_t *perm_rec;    // [H * k * T] record ids t * k + j (may be null)
     float *perm_e;        // [H * k * T] router weight of each record (may be null)
+    // Output placement of the chunked forward (both may be null).  Work items
+    // are the shared segments (b, h) first, then the routed segments s; item
+    // u owns the partial-output rows pad_off[u] .. pad_off[u] + len_u, its
+    // length rounded up to whole chunks (kChunkRows).
+    int32_t *pad_off;     // [num_items + 1]
+    int32_t *rec_pos;     // [T * H * (k + shared)] partial row of each contribution of (t, h)
     int32_t max_blocks;
 };
 
@@ -202,7 +209,10 @@ struct ForwardArgs {
     const int32_t *perm_rec;
     const float *perm_e;
     const float *topk_w;
-    void *part_routed;   // recurrent: [T, H, k, d] fp32; chunked: [T, H, k + shared, d] bf16
+    const int32_t *pad_off;  // chunked path: first partial row of each work item
+    const int32_t *rec_pos;  // chunked path: partial rows of each (t, h)
+    int64_t part_rows;       // chunked path: rows of the partial buffer
+    void *part_routed;   // recurrent: [T, H, k, d] fp32; chunked: [part_rows, d] bf16 in work-item order
     void *part_shared;   // recurrent: [T, H, d] fp32; chunked: unused
     int32_t part_bf16;
     int32_t *flags;
@@ -220,8 +230,10 @@ cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a
 
 // out[t,h,:] = sum_j part_routed[t,h,j,:] + part_shared[t,h,:]   (recurrent path)
 cudaError_t launch_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
-// out[t,h,:] = sum of the bf16 slots part_routed[t,h,0..k+shared-1,:]   (chunked path)
-cudaError_t launch_slot_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+// out[t,h,:] = sum over j of the bf16 partial row rec_pos[(t*H+h)*(k+shared)+j]   (chunked path)
+cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream);
+// Rows of the chunked path's partial buffer: every work item padded to whole chunks.
+int64_t chunked_part_rows(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs);
 
 bool decode_supported(const sse_config_t &cfg);
 cudaError_t launch_decode(const sse_config_t &cfg, const void *q, const void *k, const void *v,
