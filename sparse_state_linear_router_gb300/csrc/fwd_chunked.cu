@@ -56,6 +56,11 @@ constexpr int kMid = kC / 2 - 1; // midpoint row of the decay split
 constexpr int kEpiWarps = 4, kTrfWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarps + kTrfWarps);  // 384: 3 warps per SM sub-partition
 constexpr int kTrfThreads = 32 * kTrfWarps;
+// Registers per thread: at launch (65536 / 384, rounded down to a multiple of
+// 8) and after the split between the roles (setmaxnreg).
+constexpr int kRegsLaunch = 168, kRegsEpi = 120, kRegsTrf = 192;
+static_assert(32 * kEpiWarps * kRegsEpi + kTrfThreads * kRegsTrf == kThreads * kRegsLaunch,
+              "register split must use exactly the launch allocation");
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGateRangeLog2 = 80.f * kLog2e;  // |G_r - G_m| limit (~80 natural-log units)
@@ -66,7 +71,17 @@ constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
 // may have stored the metadata of chunks up to n+3: five live stages.
 constexpr int kMetaStages = 6;
 
-enum Bar { kBarT = 0, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1, kNumBars };
+// Segment hand-off ring: the transform warps post each work item's
+// description (or the end of the work) for the epilogue warps, so that the two
+// roles move between segments independently.
+constexpr int kSegSlots = 4;
+
+enum Bar {
+    kBarT = 0, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1,
+    kBarSegF,                          // kSegSlots "descriptor posted" barriers
+    kBarSegE = kBarSegF + kSegSlots,   // kSegSlots "descriptor consumed" barriers
+    kNumBars = kBarSegE + kSegSlots
+};
 
 // Shared-memory layout (offsets from a 1024-aligned base).
 struct Smem {
@@ -81,7 +96,8 @@ struct Smem {
     static constexpr uint32_t SCALE = TOT + 33 * 128 * 4;  // [2 stages][2][128] f32: exp(G_m), exp(G_last-G_m)
     static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [kMetaStages] x {tok, e}[128]
     static constexpr uint32_t META_STAGE = 128 * (4 + 4);
-    static constexpr uint32_t BAR = META + kMetaStages * META_STAGE;
+    static constexpr uint32_t SEGQ = META + kMetaStages * META_STAGE;  // [kSegSlots][8] int
+    static constexpr uint32_t BAR = SEGQ + kSegSlots * 32;
     static constexpr uint32_t MISC = BAR + 8 * kNumBars;   // TMEM slot, work item
     static constexpr uint32_t END = MISC + 16;
 };
@@ -118,6 +134,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+template <int R> __device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(R));
+}
+template <int R> __device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(R));
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(mbar) : "memory");
 }
@@ -135,6 +157,14 @@ __device__ __forceinline__ bool named_sync_or(int id, int count, bool pred) {
         "selp.u32 %0, 1, 0, q;\n\t}\n"
         : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
     return r != 0;
+}
+// 16-byte read-only global load that does not keep its line in L1 (each row
+// piece is read once per CTA).
+__device__ __forceinline__ uint4 ldg_stream(const void *gptr) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(gptr));
+    return r;
 }
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(gptr) : "memory");
@@ -201,6 +231,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     uint32_t *s_slot = reinterpret_cast<uint32_t *>(sm + Smem::MISC);
     int *s_item = reinterpret_cast<int *>(sm + Smem::MISC + 4);
     int *s_abort = reinterpret_cast<int *>(sm + Smem::MISC + 8);
+    int *s_segq = reinterpret_cast<int *>(sm + Smem::SEGQ);
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.q);
@@ -228,6 +259,10 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
         mbar_init(bar(kBarOf), 32 * kEpiWarps);
         mbar_init(bar(kBarV0), 1);
         mbar_init(bar(kBarV1), 1);
+        for (int i = 0; i < kSegSlots; ++i) {
+            mbar_init(bar(kBarSegF + i), 1);
+            mbar_init(bar(kBarSegE + i), 32 * kEpiWarps);
+        }
         mbar_fence_init();
         *s_abort = 0;
     }
@@ -243,23 +278,52 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     fence_after();
     const uint32_t tmem = *s_slot;
 
-    uint32_t gch = 0;  // chunks processed by this CTA so far: barrier phase parity
-    for (;;) {
-        if (tid == 0) *s_item = atomicAdd(work_counter, 1);
-        __syncthreads();
-        const int item = *s_item;
-        const bool stop = item >= num_items || *s_abort;
-        __syncthreads();
-        if (stop) break;
-        const Segment seg = decode_segment(a, item, H, N, use_shared);
-        const int pad_base = a.pad_off[item];  // first partial-output row of this work item
-        const int nch = (seg.len + kC - 1) / kC;
-        const int64_t state_off = (((int64_t)seg.b * H + seg.h) * P + seg.slot) * (int64_t)KC * DV;
-        bool failed = false;
-
-        if (warp >= kEpiWarps) {
+    // The two roles walk the same sequence of work items, each at its own pace:
+    // the transform warps claim items (one ahead) and post them through the
+    // segment ring; every per-chunk barrier counts chunks globally (g), so a
+    // role can be in the next segment while the other finishes the previous one.
+    uint32_t gch = 0;  // chunks of earlier segments: barrier phase parity base
+    bool failed = false;
+    if (warp >= kEpiWarps) {
+        // Register split: the launch gives every thread kRegsLaunch registers;
+        // the two transform warpgroups take kRegsTrf each, the epilogue
+        // warpgroup keeps kRegsEpi: 128 kRegsEpi + 256 kRegsTrf = 384 kRegsLaunch.
+        reg_alloc<kRegsTrf>();
+        const int tt = tid - 32 * kEpiWarps;  // 0..255
+        if (tt == 0) *s_item = atomicAdd(work_counter, 1);
+        for (int sidx = 0;; ++sidx) {
+            named_sync(1, kTrfThreads);
+            const int item = *s_item;
+            const bool stop = named_sync_or(1, kTrfThreads, item >= num_items || *s_abort != 0);
+            Segment seg{};
+            int pad_base = 0;  // first partial-output row of this work item
+            if (!stop) {
+                seg = decode_segment(a, item, H, N, use_shared);
+                pad_base = a.pad_off[item];
+            }
+            const int nch = stop ? 0 : (seg.len + kC - 1) / kC;
+            bool bad = false;
+            if (tt == 0) {  // hand the segment (or the end of the work) to the epilogue warps
+                const int slot = sidx % kSegSlots;
+                if (sidx >= kSegSlots)
+                    bad = !mbar_wait_bounded(bar(kBarSegE + slot), ((sidx / kSegSlots) - 1) & 1, kWaitNs);
+                if (!bad) {
+                    int *d = s_segq + slot * 8;
+                    d[0] = stop ? -1 : item;
+                    d[1] = seg.b;
+                    d[2] = seg.h;
+                    d[3] = seg.slot;
+                    d[4] = seg.base;
+                    d[5] = seg.len;
+                    d[6] = pad_base;
+                    d[7] = seg.shared ? 1 : 0;
+                    mbar_arrive(bar(kBarSegF + slot));
+                }
+            }
+            if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
+            if (stop) break;
+            if (tt == 0) *s_item = atomicAdd(work_counter, 1);  // the next item, read at the top
             // =================== transform warps ===================
-            const int tt = tid - 32 * kEpiWarps;              // 0..255
             constexpr int CG = KC / 8, NRB = kTrfThreads / CG, RPT = kC / NRB;
             const int cg = tt % CG, rb = tt / CG, col0 = cg * 8;
             const __nv_bfloat16 *qsrc = seg.shared ? gqs : gq;
@@ -285,30 +349,30 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             };
             auto store_meta = [&](int n, const RowMeta &m) {
                 if (tt < kC) {
-                    const int st = n % kMetaStages;
+                    const int st = (gch + n) % kMetaStages;
                     meta_tok(st)[tt] = m.t;
                     meta_e(st)[tt] = m.e;
                 }
             };
             uint4 rq[RPT], rk[RPT], rg[RPT], rg_next[RPT];
             auto load_g = [&](int n, uint4 (&dst)[RPT]) {
-                const int *tok = meta_tok(n % kMetaStages);
+                const int *tok = meta_tok((gch + n) % kMetaStages);
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) {
                     const int t = tok[rb * RPT + i];
-                    dst[i] = t >= 0 ? __ldg(reinterpret_cast<const uint4 *>(gg + ((int64_t)t * H + seg.h) * KC + col0))
+                    dst[i] = t >= 0 ? ldg_stream(gg + ((int64_t)t * H + seg.h) * KC + col0)
                                     : make_uint4(0, 0, 0, 0);
                 }
             };
             auto load_qk = [&](int n) {
-                const int *tok = meta_tok(n % kMetaStages);
+                const int *tok = meta_tok((gch + n) % kMetaStages);
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) {
                     const int t = tok[rb * RPT + i];
                     if (t >= 0) {
                         const int64_t ro = ((int64_t)t * H + seg.h) * KC + col0;
-                        rq[i] = __ldg(reinterpret_cast<const uint4 *>(qsrc + ro));
-                        rk[i] = __ldg(reinterpret_cast<const uint4 *>(ksrc + ro));
+                        rq[i] = ldg_stream(qsrc + ro);
+                        rk[i] = ldg_stream(ksrc + ro);
                     } else {
                         rq[i] = rk[i] = make_uint4(0, 0, 0, 0);
                     }
@@ -323,7 +387,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             }
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
-                const int mst = n % kMetaStages;
+                const int mst = g_n % kMetaStages;
                 const int vb = g_n & 1;
                 unsigned char *sV = sm + (vb ? Smem::V1 : Smem::V0);
                 bool bad = false;
@@ -332,8 +396,8 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 if (n + 1 < nch) store_meta(n + 1, meta_ahead);
                 if (n + 2 < nch) meta_ahead = load_meta(n + 2);
                 load_qk(n);
-                // V buffer vb was last read by chunk g_n - 2
-                if (n >= 2) bad = !mbar_wait_bounded(bar(vb ? kBarV1 : kBarV0), ((g_n - 2) >> 1) & 1, kWaitNs);
+                // V buffer vb was last read by chunk g_n - 2 (perhaps of an earlier segment)
+                if (g_n >= 2) bad = !mbar_wait_bounded(bar(vb ? kBarV1 : kBarV0), ((g_n - 2) >> 1) & 1, kWaitNs);
                 {   // gather V rows of chunk n with cp.async
                     constexpr int VCG = DV / 8, VNRB = kTrfThreads / VCG, VRPT = kC / VNRB;
                     const int vcg = tt % VCG, vrb = tt / VCG;
@@ -383,7 +447,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 }
                 named_sync(1, kTrfThreads);
                 // Qt / Kt buffers are free once the first three MMAs of chunk n-1 completed
-                if (n >= 1) bad = !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
+                if (g_n >= 1) bad = !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
                 // pass 2: Qt, Kt rows (bf16) straight into their tiles.  The read
                 // weight e * scale is applied to the output rows by the epilogue.
                 // The decay factors are rounded to bf16 and multiplied into the bf16
@@ -431,7 +495,30 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) rg[i] = rg_next[i];
             }
-        } else {
+            if (failed) break;
+            gch += nch;
+        }
+        cp_async_wait_all();
+    } else {
+        reg_dealloc<kRegsEpi>();
+        for (int sidx = 0;; ++sidx) {
+            const int slot = sidx % kSegSlots;
+            const bool ok = mbar_wait_bounded(bar(kBarSegF + slot), (sidx / kSegSlots) & 1, kWaitNs);
+            if (named_sync_or(2, 32 * kEpiWarps, !ok)) { failed = true; break; }
+            const int *d = s_segq + slot * 8;
+            const int item = d[0];
+            Segment seg;
+            seg.b = d[1];
+            seg.h = d[2];
+            seg.slot = d[3];
+            seg.base = d[4];
+            seg.len = d[5];
+            const int pad_base = d[6];
+            seg.shared = d[7] != 0;
+            mbar_arrive(bar(kBarSegE + slot));
+            if (item < 0) break;
+            const int nch = (seg.len + kC - 1) / kC;
+            const int64_t state_off = (((int64_t)seg.b * H + seg.h) * P + seg.slot) * (int64_t)KC * DV;
             // =================== epilogue warps ===================
             const int row = tid;  // TMEM lane
             const uint32_t lb = (uint32_t)(32 * warp) << 16;
@@ -472,7 +559,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             // is DV/64 box stores.  The staging tile is reused only after
             // bulk_wait_read().
             auto write_out = [&](int n_o, bool pend) -> bool {
-                const int st = n_o % kMetaStages;
+                const int st = (gch + n_o) % kMetaStages;
                 const float w = meta_e(st)[row] * scale;
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
                 unsigned char *stg = sm + Smem::S;
@@ -659,15 +746,13 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 }
             }
             fence_before();
+                if (failed) break;
+            gch += nch;
         }
-        if (failed) {
-            atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
-            *s_abort = 1;
-        }
-        __syncthreads();
-        fence_after();
-        gch += nch;
-        if (*s_abort) break;
+    }
+    if (failed) {
+        atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
+        *s_abort = 1;
     }
     __syncthreads();
     if (warp == 0) {
