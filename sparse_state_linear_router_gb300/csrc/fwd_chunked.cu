@@ -166,6 +166,10 @@ __device__ __forceinline__ uint4 ldg_stream(const void *gptr) {
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(gptr));
     return r;
 }
+// Hint that the 128-byte line holding gptr be fetched into L2.
+__device__ __forceinline__ void prefetch_l2(const void *gptr) {
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(gptr));
+}
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(gptr) : "memory");
 }
@@ -393,7 +397,23 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 bool bad = false;
                 // the stage of chunk n+1 last held chunk n-5, whose output rows are
                 // long written (see kMetaStages)
-                if (n + 1 < nch) store_meta(n + 1, meta_ahead);
+                if (n + 1 < nch) {
+                    store_meta(n + 1, meta_ahead);
+                    // start the rows of chunk n+1 on their way from HBM into L2 (the
+                    // loads of the next step then hit L2)
+                    if (tt < kC && meta_ahead.t >= 0) {
+                        const int64_t th = (int64_t)meta_ahead.t * H + seg.h;
+#pragma unroll
+                        for (int o = 0; o < KC * 2; o += 128) {
+                            prefetch_l2(reinterpret_cast<const unsigned char *>(qsrc + th * KC) + o);
+                            prefetch_l2(reinterpret_cast<const unsigned char *>(ksrc + th * KC) + o);
+                            prefetch_l2(reinterpret_cast<const unsigned char *>(gg + th * KC) + o);
+                        }
+#pragma unroll
+                        for (int o = 0; o < DV * 2; o += 128)
+                            prefetch_l2(reinterpret_cast<const unsigned char *>(gv + th * DV) + o);
+                    }
+                }
                 if (n + 2 < nch) meta_ahead = load_meta(n + 2);
                 load_qk(n);
                 // V buffer vb was last read by chunk g_n - 2 (perhaps of an earlier segment)
