@@ -382,12 +382,29 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     }
                 }
             };
+            // the q, k, g and v rows of a chunk start on their way from HBM into L2
+            // two steps before the loads that read them (which then hit L2)
+            auto prefetch_rows = [&](const RowMeta &m) {
+                if (tt < kC && m.t >= 0) {
+                    const int64_t th = (int64_t)m.t * H + seg.h;
+#pragma unroll
+                    for (int o = 0; o < KC * 2; o += 128) {
+                        prefetch_l2(reinterpret_cast<const unsigned char *>(qsrc + th * KC) + o);
+                        prefetch_l2(reinterpret_cast<const unsigned char *>(ksrc + th * KC) + o);
+                        prefetch_l2(reinterpret_cast<const unsigned char *>(gg + th * KC) + o);
+                    }
+#pragma unroll
+                    for (int o = 0; o < DV * 2; o += 128)
+                        prefetch_l2(reinterpret_cast<const unsigned char *>(gv + th * DV) + o);
+                }
+            };
             RowMeta meta_ahead{-1, 0.f};  // metadata of chunk n + 1 while processing chunk n
             if (nch > 0) {
                 store_meta(0, load_meta(0));
                 if (nch > 1) meta_ahead = load_meta(1);
                 named_sync(1, kTrfThreads);
                 load_g(0, rg);
+                if (nch > 1) prefetch_rows(meta_ahead);
             }
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
@@ -397,23 +414,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 bool bad = false;
                 // the stage of chunk n+1 last held chunk n-5, whose output rows are
                 // long written (see kMetaStages)
-                if (n + 1 < nch) {
-                    store_meta(n + 1, meta_ahead);
-                    // start the rows of chunk n+1 on their way from HBM into L2 (the
-                    // loads of the next step then hit L2)
-                    if (tt < kC && meta_ahead.t >= 0) {
-                        const int64_t th = (int64_t)meta_ahead.t * H + seg.h;
-#pragma unroll
-                        for (int o = 0; o < KC * 2; o += 128) {
-                            prefetch_l2(reinterpret_cast<const unsigned char *>(qsrc + th * KC) + o);
-                            prefetch_l2(reinterpret_cast<const unsigned char *>(ksrc + th * KC) + o);
-                            prefetch_l2(reinterpret_cast<const unsigned char *>(gg + th * KC) + o);
-                        }
-#pragma unroll
-                        for (int o = 0; o < DV * 2; o += 128)
-                            prefetch_l2(reinterpret_cast<const unsigned char *>(gv + th * DV) + o);
-                    }
-                }
+                if (n + 1 < nch) store_meta(n + 1, meta_ahead);
                 if (n + 2 < nch) meta_ahead = load_meta(n + 2);
                 load_qk(n);
                 // V buffer vb was last read by chunk g_n - 2 (perhaps of an earlier segment)
@@ -452,6 +453,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 }
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
                 if (n + 1 < nch) load_g(n + 1, rg_next);  // a whole chunk of latency hiding
+                if (n + 2 < nch) prefetch_rows(meta_ahead);
                 float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (tt < KC) {  // per-column exclusive scan over row blocks
                     float acc = 0.f, gmid = 0.f;
