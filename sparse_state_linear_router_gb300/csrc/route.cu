@@ -98,7 +98,9 @@ route_count_kernel(const T *__restrict__ logits, const int32_t *__restrict__ cu,
                    int32_t *__restrict__ cnt, int32_t max_blocks) {
     __shared__ int hist[kMaxPartitions];
     __shared__ int s_b, s_t0, s_t1, s_ok;
-    const int j = blockIdx.x, h = blockIdx.y;
+    // consecutive CTAs take the heads of one routing block, so the partial
+    // sectors they write into [T, H, ...] rows meet in L2
+    const int h = (int)(blockIdx.x % (unsigned)H), j = (int)(blockIdx.x / (unsigned)H);
     if (threadIdx.x < kMaxPartitions) hist[threadIdx.x] = 0;
     if (threadIdx.x == 0) {
         int b = 0, t0 = 0, t1 = 0;
@@ -201,7 +203,9 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
     constexpr int kWarps = kRouteBlock / 32;
     __shared__ uint32_t wmask[kWarps][kMaxPartitions];
     __shared__ int s_b, s_t0, s_t1, s_ok;
-    const int j = blockIdx.x, h = blockIdx.y;
+    // consecutive CTAs take the heads of one routing block, so the partial
+    // sectors they write into [T, H, ...] rows meet in L2
+    const int h = (int)(blockIdx.x % (unsigned)H), j = (int)(blockIdx.x / (unsigned)H);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int x = threadIdx.x; x < kWarps * kMaxPartitions; x += blockDim.x)
         (&wmask[0][0])[x] = 0u;
@@ -270,7 +274,7 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
     const int H = cfg.num_heads, N = cfg.num_partitions, k = cfg.top_k;
     const int MB = rb.max_blocks;
     plan_blocks_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, rb.blk_prefix);
-    dim3 grid(MB, H);
+    const dim3 grid((unsigned)((int64_t)MB * H));
     if (cfg.dtype == SSE_BF16)
         launch_count<__nv_bfloat16>(grid, stream, static_cast<const __nv_bfloat16 *>(logits), cu_seqlens,
                                     num_seqs, rb.blk_prefix, H, N, k, rb.topk_idx, rb.topk_w, rb.cnt, MB);
