@@ -152,3 +152,38 @@ def test_full_size_sampled_pairs(wname):
         b = p // H
         assert H_.max_abs_rel(gpu["out"][rows, h], ref["out"][rows, h]) < H_.TOL_BF16
         assert H_.max_abs_rel(gpu["final_state"][b, h], ref["final_state"][b, h]) < H_.TOL_BF16
+
+
+@pytest.mark.parametrize("algo", ["recurrent", "chunked"])
+@pytest.mark.parametrize("strength", [1.5, 8.0])
+def test_skewed_routing(algo, strength):
+    """Per-partition bias on the router logits (beta_i rising from -s to +s
+    across partitions): partition loads range from nearly all tokens to none,
+    so segments of every length, empty ones included, meet in one launch."""
+    w = H_.workload_variant("small_bf16", num_heads=3, num_partitions=8, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=11, lengths=[700, 129, 1, 0, 385], with_init=True)
+    N = w.num_partitions
+    beta = strength * (np.arange(N) / (N - 1) - 0.5) * 2.0
+    lg = synth.bf16_bits_to_f32(inp.logits) + beta.astype(np.float32)
+    inp.logits = synth.f32_to_bf16_bits(lg.astype(np.float32))
+    gpu = H_.run_gpu_forward(w, inp, algo=algo)
+    ref = H_.run_oracle_forward(w, inp)
+    assert np.array_equal(gpu["topk_idx"], ref["topk_idx"])
+    assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
+    assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
+    assert gpu["device_flags"] == 0
+
+
+@pytest.mark.parametrize("algo", ["recurrent", "chunked"])
+def test_chunk_boundary_lengths(algo):
+    """With one routed partition every segment is a whole sequence, so the
+    sequence lengths put segment ends just before, on and after chunk
+    boundaries (127, 128, 129, 256, 257) for both the routed and the shared
+    partition."""
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=1, top_k=1)
+    inp = synth.make_forward_inputs(w, seed=4, lengths=[127, 128, 129, 256, 257, 1], with_init=True)
+    gpu = H_.run_gpu_forward(w, inp, algo=algo)
+    ref = H_.run_oracle_forward(w, inp)
+    assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
+    assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
+    assert gpu["device_flags"] == 0
