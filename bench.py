@@ -13,7 +13,8 @@ of decode states), so no L2 flush is needed between steps.
 Also reported: per-kernel CUDA-event timing of the dominant kernel against
 the measured HBM peak (roofline), the end-to-end number through the C ABI
 with host buffers (pinned host -> device copies of every step's inputs and
-device -> host copies of its outputs inside the timed region), SM clocks
+device -> host copies of its outputs inside the timed region, on copy streams
+that overlap one step's transfers with the neighbouring steps' compute), SM clocks
 sampled during the timed region, and the fp64 CPU oracle timed on a bounded
 sample of the same workload (cpu_baseline).
 
@@ -353,17 +354,18 @@ def run_native(args):
             e.record(stream)   # materialise the handles
         return evs
 
-    def forward_call(src, stage_events=None):
+    def forward_call(src, stage_events=None, out_t=None):
         st, n = binding.sse_forward_timed(cfg_f, P_(src["q"]), P_(src["k"]), P_(src["v"]), P_(src["g"]),
                                           P_(src["logits"]), None, None, P_(cu), S, T, P_(init), P_(fin),
-                                          P_(out), None, None, P_(wsp), wsp.numel(), sh,
+                                          P_(out if out_t is None else out_t), None, None, P_(wsp), wsp.numel(), sh,
                                           None if stage_events is None else [e.cuda_event for e in stage_events])
         binding._check(st, "sse_forward_timed")
         launches["n"] += n
 
-    def decode_call(x):
+    def decode_call(x, out_t=None):
         st = binding.sse_decode_step(cfg_d, P_(x["q"]), P_(x["k"]), P_(x["v"]), P_(x["g"]),
-                                     P_(x["logits"]), None, None, B, P_(state), P_(dout), None, None, sh)
+                                     P_(x["logits"]), None, None, B, P_(state),
+                                     P_(dout if out_t is None else out_t), None, None, sh)
         binding._check(st, "sse_decode_step")
         launches["n"] += 1
 
@@ -437,51 +439,75 @@ def run_native(args):
     t_bind = max(step_flops / (peaks["bf16_tflops"] * 1e12), step_bytes / (hbm * 1e9))
 
     # ---- end to end through the C ABI with host buffers ---------------------
+    # Every step copies its inputs from pinned host memory and its outputs back.
+    # The copies run on their own streams into double-buffered device tensors,
+    # so step i's inputs travel while step i-1 computes (a serving pipeline).
     e2e = None
     if not args.no_e2e:
         h2d = d2h = 0
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        ev_in, ev_done, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         if do_fwd:
             hf = {n: f[n].cpu().pin_memory() for n in names}
-            df = {n: torch.empty_like(f[n]) for n in names}
+            dfs = [{n: torch.empty_like(f[n]) for n in names} for _ in range(2)]
+            outs = [out, torch.empty_like(out)]
             hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
             h2d += sum(hf[n].numel() * hf[n].element_size() for n in names)
             d2h += hout.numel() * hout.element_size()
         if do_dec:
             hd = [{n: dq[i][n].cpu().pin_memory() for n in names} for i in range(min(pool, 8))]
-            dd = {n: torch.empty_like(dq[0][n]) for n in names}
+            dds = [{n: torch.empty_like(dq[0][n]) for n in names} for _ in range(2)]
+            douts = [dout, torch.empty_like(dout)]
             hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
             h2d += sum(hd[0][n].numel() * hd[0][n].element_size() for n in names)
             d2h += hdout.numel() * hdout.element_size()
 
         def e2e_step(i):
+            b = i % 2
+            with torch.cuda.stream(s_in):  # inputs of step i (buffers last read by step i-2)
+                if i >= 2:
+                    s_in.wait_event(ev_done[b])
+                if do_fwd:
+                    for n in names:
+                        dfs[b][n].copy_(hf[n], non_blocking=True)
+                if do_dec:
+                    x = hd[i % len(hd)]
+                    for n in names:
+                        dds[b][n].copy_(x[n], non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])  # outputs of step i-2 copied out
             if do_fwd:
-                for n in names:
-                    df[n].copy_(hf[n], non_blocking=True)
-                forward_call(df)
+                forward_call(dfs[b], out_t=outs[b])
             if do_dec:
-                x = hd[i % len(hd)]
-                for n in names:
-                    dd[n].copy_(x[n], non_blocking=True)
-                decode_call(dd)
-            if do_fwd:
-                hout.copy_(out, non_blocking=True)
-            if do_dec:
-                hdout.copy_(dout, non_blocking=True)
+                decode_call(dds[b], out_t=douts[b])
+            ev_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                if do_fwd:
+                    hout.copy_(outs[b], non_blocking=True)
+                if do_dec:
+                    hdout.copy_(douts[b], non_blocking=True)
+                ev_out[b].record(s_out)
 
         for i in range(args.warmup):
             e2e_step(i)
         torch.cuda.synchronize()
         barrier()
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
+        ea.record(s_in)
         for i in range(args.steps):
             e2e_step(i)
-        eb.record(stream)
+        s_out.synchronize()
+        eb.record(s_out)
         torch.cuda.synchronize()
         barrier()
         e2e_ms = max_over_ranks(ea.elapsed_time(eb) / args.steps)
         e2e = {"value": whole_job_tokens_per_s(ws, tokens_step, e2e_ms), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "overlap": "inputs of step i copied on a second stream while step i-1 computes"}
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------
     cpu = None
