@@ -71,7 +71,13 @@ typedef enum { SSE_F32 = 0, SSE_BF16 = 1 } sse_dtype_t;
 typedef enum {
     SSE_ALGO_AUTO = 0,      /* tensor-core chunked path where supported, else recurrent */
     SSE_ALGO_CHUNKED = 1,   /* tcgen05 chunked path: bf16, c in {64,128}, d in {64,128} */
-    SSE_ALGO_RECURRENT = 2  /* CUDA-core per-token recurrence: any supported dtype/shape */
+    SSE_ALGO_RECURRENT = 2, /* CUDA-core per-token recurrence: any supported dtype/shape */
+    SSE_ALGO_MASKED = 3     /* tcgen05 chunked path on the masking schedule ("Scaling Linear
+                               Attention with Sparse State Expansion", section 2.6, short
+                               sequences): every routed partition runs over the whole
+                               sequence; tokens it did not select add nothing and leave its
+                               state undecayed.  Same results as the grouped (varlen)
+                               schedule, no token->partition sort; same shapes as CHUNKED. */
 } sse_algo_t;
 
 typedef struct {

@@ -20,8 +20,9 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsse.so")
 
 SSE_OK, SSE_ERR_INVALID_ARG, SSE_ERR_UNSUPPORTED, SSE_ERR_WORKSPACE, SSE_ERR_CUDA, SSE_ERR_DEVICE = range(6)
 SSE_F32, SSE_BF16 = 0, 1
-SSE_ALGO_AUTO, SSE_ALGO_CHUNKED, SSE_ALGO_RECURRENT = 0, 1, 2
-_ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_ALGO_RECURRENT}
+SSE_ALGO_AUTO, SSE_ALGO_CHUNKED, SSE_ALGO_RECURRENT, SSE_ALGO_MASKED = 0, 1, 2, 3
+_ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_ALGO_RECURRENT,
+          "masked": SSE_ALGO_MASKED}
 
 # Every extern "C" symbol that include/sse.h declares.
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",

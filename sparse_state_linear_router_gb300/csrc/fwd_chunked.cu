@@ -198,7 +198,9 @@ struct Segment {
 };
 
 // Work items: the shared segments first (the longest, so the persistent CTAs
-// start them early), then the routed segments s = (b * H + h) * N + i.
+// start them early), then the routed segments s = (b * H + h) * N + i: the
+// grouped records of partition i, or (masking schedule) the whole sequence b.
+template <bool MASKED>
 __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item, int H, int N,
                                                   int use_shared) {
     Segment s;
@@ -215,13 +217,18 @@ __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item
         s.slot = r % N;
         s.h = (r / N) % H;
         s.b = r / (N * H);
-        s.base = a.seg_off[r];
-        s.len = a.seg_off[r + 1] - s.base;
+        if (MASKED) {
+            s.base = a.cu_seqlens[s.b];
+            s.len = a.cu_seqlens[s.b + 1] - s.base;
+        } else {
+            s.base = a.seg_off[r];
+            s.len = a.seg_off[r + 1] - s.base;
+        }
     }
     return s;
 }
 
-template <int KC, int DV>
+template <int KC, int DV, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
 chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_map, int32_t H, int32_t N,
                        int32_t topk, int32_t use_shared, float scale, int32_t num_items,
@@ -302,7 +309,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             Segment seg{};
             int pad_base = 0;  // first partial-output row of this work item
             if (!stop) {
-                seg = decode_segment(a, item, H, N, use_shared);
+                seg = decode_segment<MASKED>(a, item, H, N, use_shared);
                 pad_base = a.pad_off[item];
             }
             const int nch = stop ? 0 : (seg.len + kC - 1) / kC;
@@ -344,6 +351,14 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     if (seg.shared) {
                         m.t = seg.base + idx;
                         m.e = 1.f;
+                    } else if (MASKED) {
+                        // every token of the sequence; -1 marks the ones that did not
+                        // select this partition (no write, no decay, no read)
+                        m.t = seg.base + idx;
+                        m.e = -1.f;
+                        const int64_t o = ((int64_t)m.t * H + seg.h) * topk;
+                        for (int j = 0; j < topk; ++j)
+                            if (a.topk_idx[o + j] == seg.slot) m.e = a.topk_w[o + j];
                     } else {
                         m.t = a.perm_rec[seg.base + idx] / topk;
                         m.e = a.perm_e[seg.base + idx];
@@ -435,7 +450,15 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     }
                 }
                 // pass 1: per-thread running sums of g over its rows -> block totals
+                // (masking schedule: the rows of tokens that did not select this
+                // partition get gate 0, i.e. no decay)
                 {
+                    if (MASKED) {
+                        const float *me = meta_e(mst);
+#pragma unroll
+                        for (int i = 0; i < RPT; ++i)
+                            if (me[rb * RPT + i] < 0.f) rg[i] = make_uint4(0, 0, 0, 0);
+                    }
                     float run[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
@@ -486,7 +509,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
                         const int r = rb * RPT + i;
-                        const float e = me[r];
+                        const float e = MASKED ? fmaxf(me[r], 0.f) : me[r];
                         const uint32_t wg4[4] = {rg[i].x, rg[i].y, rg[i].z, rg[i].w};
                         const uint32_t wq4[4] = {rq[i].x, rq[i].y, rq[i].z, rq[i].w};
                         const uint32_t wk4[4] = {rk[i].x, rk[i].y, rk[i].z, rk[i].w};
@@ -582,7 +605,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             // bulk_wait_read().
             auto write_out = [&](int n_o, bool pend) -> bool {
                 const int st = (gch + n_o) % kMetaStages;
-                const float w = meta_e(st)[row] * scale;
+                const float w = (MASKED ? fmaxf(meta_e(st)[row], 0.f) : meta_e(st)[row]) * scale;
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
                 unsigned char *stg = sm + Smem::S;
 #pragma unroll
@@ -829,11 +852,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-template <int KC, int DV>
+template <int KC, int DV, bool MASKED>
 cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {
     static bool attr_set = false;  // benign race: every caller sets the same value
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunked_forward_kernel<KC, DV>,
+        cudaError_t e = cudaFuncSetAttribute(chunked_forward_kernel<KC, DV, MASKED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -862,7 +885,7 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
         return cudaErrorInvalidValue;
 
     const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
-    chunked_forward_kernel<KC, DV><<<grid, kThreads, kSmemBytes, stream>>>(
+    chunked_forward_kernel<KC, DV, MASKED><<<grid, kThreads, kSmemBytes, stream>>>(
         a, map, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
     return cudaGetLastError();
 }
@@ -880,10 +903,15 @@ size_t chunked_extra_workspace(const sse_config_t &, int64_t, int32_t) { return 
 cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream,
                                    int *launches) {
     cudaError_t e;
-    if (cfg.key_dim == 128 && cfg.value_dim == 128) e = launch_t<128, 128>(cfg, a, stream);
-    else if (cfg.key_dim == 128 && cfg.value_dim == 64) e = launch_t<128, 64>(cfg, a, stream);
-    else if (cfg.key_dim == 64 && cfg.value_dim == 128) e = launch_t<64, 128>(cfg, a, stream);
-    else if (cfg.key_dim == 64 && cfg.value_dim == 64) e = launch_t<64, 64>(cfg, a, stream);
+    const bool m = cfg.algo == SSE_ALGO_MASKED;
+    if (cfg.key_dim == 128 && cfg.value_dim == 128)
+        e = m ? launch_t<128, 128, true>(cfg, a, stream) : launch_t<128, 128, false>(cfg, a, stream);
+    else if (cfg.key_dim == 128 && cfg.value_dim == 64)
+        e = m ? launch_t<128, 64, true>(cfg, a, stream) : launch_t<128, 64, false>(cfg, a, stream);
+    else if (cfg.key_dim == 64 && cfg.value_dim == 128)
+        e = m ? launch_t<64, 128, true>(cfg, a, stream) : launch_t<64, 128, false>(cfg, a, stream);
+    else if (cfg.key_dim == 64 && cfg.value_dim == 64)
+        e = m ? launch_t<64, 64, true>(cfg, a, stream) : launch_t<64, 64, false>(cfg, a, stream);
     else return cudaErrorInvalidValue;
     *launches += 1;
     return e;
@@ -891,7 +919,10 @@ cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a
 
 int64_t chunked_part_rows(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs) {
     const int64_t nitems = (int64_t)num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
-    return total_tokens * cfg.num_heads * (cfg.top_k + cfg.use_shared) + nitems * (kChunkRows - 1);
+    // masking schedule: every item is a whole sequence
+    const int64_t per_token = cfg.algo == SSE_ALGO_MASKED ? cfg.num_partitions + cfg.use_shared
+                                                          : cfg.top_k + cfg.use_shared;
+    return total_tokens * cfg.num_heads * per_token + nitems * (kChunkRows - 1);
 }
 
 cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream) {

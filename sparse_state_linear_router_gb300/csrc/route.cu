@@ -15,6 +15,8 @@
 //   scatter  (blk,H) : rank of each record inside its block (per-warp bit
 //                      masks + popc) + block base -> perm / perm_rec, and the
 //                      partial-output row of every contribution (rec_pos)
+#include <algorithm>
+
 #include "sse_internal.cuh"
 
 namespace sse {
@@ -266,6 +268,71 @@ void launch_count(dim3 grid, cudaStream_t stream, const T *logits, const int32_t
 #undef SSE_COUNT
 }
 
+// Masking schedule: item u's output rows start at pad_off[u].  With pl_b the
+// length of sequence b rounded up to whole chunks and P_b their exclusive
+// prefix: shared item (b, h) -> H P_b + h pl_b; item (b, h, i) -> (shared
+// total) + H N P_b + (h N + i) pl_b.  One CTA.
+__global__ void __launch_bounds__(1024)
+masked_pad_kernel(const int32_t *__restrict__ cu, int32_t nseq, int32_t H, int32_t N, int32_t use_shared,
+                  int32_t *__restrict__ pad_off) {
+    extern __shared__ int s_pref[];  // [nseq + 1]
+    int carry = 0;
+    for (int base = 0; base < nseq; base += blockDim.x) {
+        const int b = base + threadIdx.x;
+        const int pl = b < nseq ? (cu[b + 1] - cu[b] + kChunkRows - 1) / kChunkRows * kChunkRows : 0;
+        int tot;
+        const int ex = block_exclusive_scan(pl, &tot);
+        if (b < nseq) s_pref[b] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) s_pref[nseq] = carry;
+    __syncthreads();
+    const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
+    const int64_t shared_rows = use_shared ? (int64_t)H * s_pref[nseq] : 0;
+    const int64_t nitems = nshared + (int64_t)nseq * H * N;
+    for (int64_t u = threadIdx.x; u < nitems; u += blockDim.x) {
+        int64_t v;
+        if (u < nshared) {
+            const int b = (int)(u / H), h = (int)(u % H);
+            const int pl = s_pref[b + 1] - s_pref[b];
+            v = (int64_t)H * s_pref[b] + (int64_t)h * pl;
+        } else {
+            const int64_t r = u - nshared;
+            const int b = (int)(r / ((int64_t)H * N));
+            const int hi = (int)(r % ((int64_t)H * N));  // h * N + i
+            const int pl = s_pref[b + 1] - s_pref[b];
+            v = shared_rows + (int64_t)H * N * s_pref[b] + (int64_t)hi * pl;
+        }
+        pad_off[u] = (int32_t)v;
+    }
+    if (threadIdx.x == 0) pad_off[nitems] = (int32_t)(shared_rows + (int64_t)H * N * s_pref[nseq]);
+}
+
+// Partial row of each contribution of (t, h): selected partition j of the
+// token, then the shared one.
+__global__ void __launch_bounds__(256)
+masked_recpos_kernel(const int32_t *__restrict__ cu, int32_t nseq, const int32_t *__restrict__ topk_idx,
+                     int64_t total_tokens, int32_t H, int32_t N, int32_t k, int32_t use_shared,
+                     const int32_t *__restrict__ pad_off, int32_t *__restrict__ rec_pos) {
+    const int64_t rows = total_tokens * H;
+    const int ncon = k + use_shared;
+    const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
+    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < rows; x += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(x / H), h = (int)(x % H);
+        int lo = 0, hi = nseq - 1;  // the sequence holding t: largest b with cu[b] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo, dt = t - cu[b];
+        for (int j = 0; j < k; ++j) {
+            const int i = topk_idx[x * k + j];
+            rec_pos[x * ncon + j] = pad_off[nshared + ((int64_t)b * H + h) * N + i] + dt;
+        }
+        if (use_shared) rec_pos[x * ncon + k] = pad_off[(int64_t)b * H + h] + dt;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int32_t *cu_seqlens,
@@ -289,6 +356,25 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
                                                      rb.cnt, MB, rb.seg_off, H, N, k, cfg.use_shared,
                                                      rb.topk_w, rb.perm, rb.perm_rec, rb.perm_e,
                                                      rb.pad_off, rb.rec_pos);
+    return cudaGetLastError();
+}
+
+}  // namespace sse
+
+namespace sse {
+
+cudaError_t launch_masked_plan(const sse_config_t &cfg, const int32_t *cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, const RouteBuffers &rb, cudaStream_t stream) {
+    masked_pad_kernel<<<1, 1024, sizeof(int) * (num_seqs + 1), stream>>>(cu_seqlens, num_seqs, cfg.num_heads,
+                                                                         cfg.num_partitions, cfg.use_shared,
+                                                                         rb.pad_off);
+    const int64_t rows = total_tokens * cfg.num_heads;
+    if (rows > 0) {
+        const unsigned blocks = (unsigned)std::min<int64_t>((rows + 255) / 256, 152 * 8);
+        masked_recpos_kernel<<<blocks, 256, 0, stream>>>(cu_seqlens, num_seqs, rb.topk_idx, total_tokens,
+                                                        cfg.num_heads, cfg.num_partitions, cfg.top_k,
+                                                        cfg.use_shared, rb.pad_off, rb.rec_pos);
+    }
     return cudaGetLastError();
 }
 

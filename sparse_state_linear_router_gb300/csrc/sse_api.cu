@@ -27,7 +27,7 @@ sse_status_t check_config(const sse_config_t *cfg) {
     if (c.num_partitions < 1 || c.top_k < 1 || c.top_k > c.num_partitions) return SSE_ERR_INVALID_ARG;
     if (c.use_shared != 0 && c.use_shared != 1) return SSE_ERR_INVALID_ARG;
     if (c.dtype != SSE_F32 && c.dtype != SSE_BF16) return SSE_ERR_INVALID_ARG;
-    if (c.algo < SSE_ALGO_AUTO || c.algo > SSE_ALGO_RECURRENT) return SSE_ERR_INVALID_ARG;
+    if (c.algo < SSE_ALGO_AUTO || c.algo > SSE_ALGO_MASKED) return SSE_ERR_INVALID_ARG;
     if (!std::isfinite(c.scale)) return SSE_ERR_INVALID_ARG;
     if (c.num_partitions > sse::kMaxPartitions || c.top_k > sse::kMaxTopK) return SSE_ERR_UNSUPPORTED;
     if ((c.key_dim * elem_bytes(c)) % 16 || (c.value_dim * elem_bytes(c)) % 16) return SSE_ERR_UNSUPPORTED;
@@ -72,7 +72,7 @@ RouteBuffers carve_route(Carver &cv, const sse_config_t &c, int64_t T, int32_t S
 
 bool use_chunked(const sse_config_t &c) {
     if (c.algo == SSE_ALGO_RECURRENT) return false;
-    if (c.algo == SSE_ALGO_CHUNKED) return true;
+    if (c.algo == SSE_ALGO_CHUNKED || c.algo == SSE_ALGO_MASKED) return true;
     return sse::chunked_supported(c);
 }
 
@@ -91,7 +91,8 @@ ForwardLayout carve_forward(void *ws, const sse_config_t &c, int64_t T, int32_t 
     ForwardLayout L{};
     L.flags = cv.take<int32_t>(64);
     const bool chunked = use_chunked(c);
-    L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true, chunked);
+    const bool masked = c.algo == SSE_ALGO_MASKED;  // no grouping: no per-record arrays
+    L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, !masked, chunked);
     if (chunked) {
         // bf16 partial read-outs, one row per contribution, in work-item order
         L.part_rows = sse::chunked_part_rows(c, T, S);
@@ -182,6 +183,7 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
         if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
     if (use_chunked(c)) {
         if (!sse::chunked_supported(c)) return SSE_ERR_UNSUPPORTED;
+        if (c.algo == SSE_ALGO_MASKED && num_seqs > 12000) return SSE_ERR_UNSUPPORTED;
     } else if (!sse::recurrent_supported(c)) {
         return SSE_ERR_UNSUPPORTED;
     }
@@ -196,9 +198,15 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     ForwardLayout L = carve_forward(workspace, c, total_tokens, num_seqs, topk_idx, topk_w);
     if (mark(0) != cudaSuccess) return SSE_ERR_CUDA;
     if (cudaMemsetAsync(L.flags, 0, 64 * sizeof(int32_t), s) != cudaSuccess) return SSE_ERR_CUDA;
-    cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, true, s);
+    const bool masked = c.algo == SSE_ALGO_MASKED;
+    cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, !masked, s);
     if (e != cudaSuccess) return SSE_ERR_CUDA;
-    int launches = sse::kRouteLaunches;
+    int launches = masked ? 2 : sse::kRouteLaunches;
+    if (masked) {  // output placement of the masking schedule
+        e = sse::launch_masked_plan(c, cu_seqlens, num_seqs, total_tokens, L.rb, s);
+        if (e != cudaSuccess) return SSE_ERR_CUDA;
+        launches += total_tokens > 0 ? 2 : 1;
+    }
     if (mark(1) != cudaSuccess) return SSE_ERR_CUDA;
     sse::ForwardArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = log_gate; a.qs = q_shared; a.ks = k_shared;
@@ -212,6 +220,7 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     a.perm_rec = L.rb.perm_rec;
     a.perm_e = L.rb.perm_e;
     a.topk_w = L.rb.topk_w;
+    a.topk_idx = L.rb.topk_idx;
     a.pad_off = L.rb.pad_off;
     a.rec_pos = L.rb.rec_pos;
     a.part_rows = L.part_rows;

@@ -190,6 +190,12 @@ struct RouteBuffers {
 
 int64_t route_max_blocks(int64_t total_tokens, int32_t num_seqs);
 
+// Masking schedule (no grouping): the chunk-padded output region of every work
+// item (shared (b, h), then (b, h, i) over whole sequences) and the partial row
+// of each contribution of (t, h); needs topk_idx.  Two launches.
+cudaError_t launch_masked_plan(const sse_config_t &cfg, const int32_t *cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, const RouteBuffers &rb, cudaStream_t stream);
+
 // Launches the routing + grouping kernels; returns cudaGetLastError().
 cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int32_t *cu_seqlens,
                          int32_t num_seqs, int64_t total_tokens, const RouteBuffers &rb,
@@ -209,6 +215,7 @@ struct ForwardArgs {
     const int32_t *perm_rec;
     const float *perm_e;
     const float *topk_w;
+    const int32_t *topk_idx; // masking schedule: the selected partitions of each (t, h)
     const int32_t *pad_off;  // chunked path: first partial row of each work item
     const int32_t *rec_pos;  // chunked path: partial rows of each (t, h)
     int64_t part_rows;       // chunked path: rows of the partial buffer

@@ -54,10 +54,10 @@ def _chunked_ok(w):
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
-@pytest.mark.parametrize("algo", ["auto", "recurrent", "chunked"])
+@pytest.mark.parametrize("algo", ["auto", "recurrent", "chunked", "masked"])
 def test_forward_matches_oracle(name, algo):
     w, inp = _case(name)
-    if algo == "chunked" and not _chunked_ok(w):
+    if algo in ("chunked", "masked") and not _chunked_ok(w):
         pytest.skip("shape/dtype outside the tensor-core path")
     gpu = H_.run_gpu_forward(w, inp, algo=algo)
     ref = H_.run_oracle_forward(w, inp)
@@ -86,7 +86,7 @@ def test_unselected_partitions_final_state_bitwise():
     lg = inp.logits.copy()
     lg[..., 4:] = synth.f32_to_bf16_bits(np.full(lg[..., 4:].shape, -60.0, np.float32))
     inp.logits = lg
-    for algo in ("recurrent", "chunked"):
+    for algo in ("recurrent", "chunked", "masked"):
         gpu = H_.run_gpu_forward(w, inp, algo=algo)
         assert np.array_equal(gpu["final_state"][:, :, 4:6], inp.init_state[:, :, 4:6])
 
@@ -154,7 +154,7 @@ def test_full_size_sampled_pairs(wname):
         assert H_.max_abs_rel(gpu["final_state"][b, h], ref["final_state"][b, h]) < H_.TOL_BF16
 
 
-@pytest.mark.parametrize("algo", ["recurrent", "chunked"])
+@pytest.mark.parametrize("algo", ["recurrent", "chunked", "masked"])
 @pytest.mark.parametrize("strength", [1.5, 8.0])
 def test_skewed_routing(algo, strength):
     """Per-partition bias on the router logits (beta_i rising from -s to +s
@@ -174,7 +174,7 @@ def test_skewed_routing(algo, strength):
     assert gpu["device_flags"] == 0
 
 
-@pytest.mark.parametrize("algo", ["recurrent", "chunked"])
+@pytest.mark.parametrize("algo", ["recurrent", "chunked", "masked"])
 def test_chunk_boundary_lengths(algo):
     """With one routed partition every segment is a whole sequence, so the
     sequence lengths put segment ends just before, on and after chunk
