@@ -21,24 +21,28 @@
 // accumulate Kt^T V into it, and sets p = exp(G_last - G_m).
 //
 // Persistent CTAs (one per SM) take segments from an atomic queue (shared
-// segments first: they are the longest).  Inside a CTA two warp roles run a
+// segments first: they are the longest).  Inside a CTA three warp roles run a
 // pipeline synchronised by mbarriers:
-//   transform (8 warps): load the raw g rows of the next chunk into registers
-//       while the current one finishes, then its q and k rows and row
-//       metadata one step ahead; gather V rows with cp.async into a double
-//       buffer; build Qt and Kt (128B-swizzled, see umma.cuh) and the
-//       per-row scales;
+//   loader (4 warps): warp 0 claims the work items, hands each segment to the
+//       other roles and writes every chunk's row metadata (token, router
+//       weight) into a ring a few chunks ahead; warp 1 has the TMA engine
+//       gather each chunk's V rows into a double buffer (tile::gather4, four
+//       token rows per copy, 128B swizzle, straight into the operand layout);
+//   transform (8 warps): load the raw g rows of the next chunk into
+//       registers while the current one finishes, and the chunk's q and k
+//       rows; scan g (which releases the epilogue's state-row pass); build Qt
+//       and Kt (128B-swizzled, see umma.cuh);
 //   epilogue (4 warps, one TMEM lane each): rescale the state rows and
 //       write S'; turn A into the masked bf16 P; write O (already e-weighted)
 //       as bf16 partial rows; final state at the end of the segment.  Lane 0
 //       of warp 0 also issues the tensor-core work of each chunk at the
 //       points of its loop where the operands become ready:
 //       A = Qt Kt^T; S += Kt^T V; O = Qt S' (after the state rows), then
-//       O += P V (after P).  Twelve warps keep three warps per SM
-//       sub-partition, which leaves 168 registers per thread.
+//       O += P V (after P).
 // All waits are bounded: a timeout sets SSE_DEVICE_TIMEOUT in the flags word
 // and the CTA stops after releasing its TMEM.
 #include <algorithm>
+#include <cstring>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -53,32 +57,36 @@ using namespace umma;
 
 constexpr int kC = kChunkRows;   // chunk rows (128)
 constexpr int kMid = kC / 2 - 1; // midpoint row of the decay split
-constexpr int kEpiWarps = 4, kTrfWarps = 8;
-constexpr int kThreads = 32 * (kEpiWarps + kTrfWarps);  // 384: 3 warps per SM sub-partition
+constexpr int kEpiWarps = 4, kTrfWarps = 8, kLdrWarps = 4;
+constexpr int kThreads = 32 * (kEpiWarps + kTrfWarps + kLdrWarps);  // 512: 4 warps per SM sub-partition
 constexpr int kTrfThreads = 32 * kTrfWarps;
-// Registers per thread: at launch (65536 / 384, rounded down to a multiple of
-// 8) and after the split between the roles (setmaxnreg).
-constexpr int kRegsLaunch = 168, kRegsEpi = 120, kRegsTrf = 192;
-static_assert(32 * kEpiWarps * kRegsEpi + kTrfThreads * kRegsTrf == kThreads * kRegsLaunch,
+// Registers per thread: at launch (65536 / 512) and after the split between
+// the warpgroups (setmaxnreg).
+constexpr int kRegsLaunch = 128, kRegsEpi = 120, kRegsTrf = 176, kRegsLdr = 40;
+static_assert(32 * (kEpiWarps * kRegsEpi + kTrfWarps * kRegsTrf + kLdrWarps * kRegsLdr) == kThreads * kRegsLaunch,
               "register split must use exactly the launch allocation");
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kGateRangeLog2 = 80.f * kLog2e;  // |G_r - G_m| limit (~80 natural-log units)
 
 constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
-// Row metadata ring (chunk n in stage n % 6).  The epilogue reads chunk
-// n-1's rows at the end of its chunk-n step, by which time the transform warps
-// may have stored the metadata of chunks up to n+3: five live stages.
-constexpr int kMetaStages = 6;
+// Row metadata ring (global chunk g in stage g % kMetaStages): written by the
+// loader, read by the gather warps, the transform and, last, by the epilogue
+// when it writes the chunk's output; the loader reuses a stage after that
+// (kBarMF), so it runs up to about three chunks ahead of the transform.
+constexpr int kMetaStages = 5;
 
-// Segment hand-off ring: the transform warps post each work item's
-// description (or the end of the work) for the epilogue warps, so that the two
-// roles move between segments independently.
+// Segment hand-off ring: the loader posts each work item's description (or
+// the end of the work) for the transform and epilogue warps, so that the roles
+// move between segments independently.
 constexpr int kSegSlots = 4;
 
 enum Bar {
-    kBarT = 0, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1,
-    kBarSegF,                          // kSegSlots "descriptor posted" barriers
+    kBarT = 0, kBarSc0, kBarSc1, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1,
+    kBarVL0, kBarVL1,                  // V rows of a chunk landed in V0 / V1 (TMA)
+    kBarMR,                            // kMetaStages "row metadata written" barriers
+    kBarMF = kBarMR + kMetaStages,     // kMetaStages "row metadata no longer needed" barriers
+    kBarSegF = kBarMF + kMetaStages,   // kSegSlots "descriptor posted" barriers
     kBarSegE = kBarSegF + kSegSlots,   // kSegSlots "descriptor consumed" barriers
     kNumBars = kBarSegE + kSegSlots
 };
@@ -94,8 +102,9 @@ struct Smem {
     static constexpr uint32_t S = P + kTile;
     static constexpr uint32_t TOT = S + kTile;             // [33][128] f32 block prefixes; row 32: G_m
     static constexpr uint32_t SCALE = TOT + 33 * 128 * 4;  // [2 stages][2][128] f32: exp(G_m), exp(G_last-G_m)
-    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;  // [kMetaStages] x {tok, e}[128]
-    static constexpr uint32_t META_STAGE = 128 * (4 + 4);
+    // [kMetaStages] x {tok[128], e[128], header {stop, h, shared, -}}
+    static constexpr uint32_t META = SCALE + 2 * 2 * 128 * 4;
+    static constexpr uint32_t META_STAGE = 128 * (4 + 4) + 16;
     static constexpr uint32_t SEGQ = META + kMetaStages * META_STAGE;  // [kSegSlots][8] int
     static constexpr uint32_t BAR = SEGQ + kSegSlots * 32;
     static constexpr uint32_t MISC = BAR + 8 * kNumBars;   // TMEM slot, work item
@@ -166,21 +175,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void *gptr) {
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(gptr));
     return r;
 }
-// Hint that the 128-byte line holding gptr be fetched into L2.
-__device__ __forceinline__ void prefetch_l2(const void *gptr) {
-    asm volatile("prefetch.global.L2 [%0];" :: "l"(gptr));
-}
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(saddr), "l"(gptr) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-// Bulk (TMA engine) copy of `bytes` contiguous bytes, shared -> global.
-__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Tensor (TMA) store of one box of a 2-D tensor map from shared memory; the
 // box's inner coordinate x and row coordinate y.
@@ -191,6 +185,22 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t ss
 // Waits until this thread's bulk copies have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Arrive on an mbarrier and raise the bytes its phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(mbar), "r"(bytes) : "memory");
+}
+// TMA gather of four rows (r0..r3) x one box of columns starting at x of a 2-D
+// tensor map whose box is one row high; the rows land one after another at
+// sdst (the map's swizzle applied), completion counted on mbar in bytes.
+__device__ __forceinline__ void tma_gather4(const CUtensorMap *map, uint32_t sdst, uint32_t mbar, int x, int r0,
+                                            int r1, int r2, int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        :: "r"(sdst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
+        : "memory");
+}
+
 
 struct Segment {
     int b, h, slot, base, len;
@@ -228,11 +238,42 @@ __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item
     return s;
 }
 
+// Row metadata of row idx of a work item: token index and router weight.
+struct RowMeta { int t; float e; };
+template <bool MASKED>
+__device__ __forceinline__ RowMeta row_meta(const ForwardArgs &a, const Segment &seg, int idx, int H, int topk) {
+    RowMeta m{-1, 0.f};
+    if (idx < seg.len) {
+        if (seg.shared) {
+            m.t = seg.base + idx;
+            m.e = 1.f;
+        } else if (MASKED) {
+            // every token of the sequence; -1 marks the ones that did not select
+            // this partition (no write, no decay, no read)
+            m.t = seg.base + idx;
+            m.e = -1.f;
+            const int64_t o = ((int64_t)m.t * H + seg.h) * topk;
+            for (int j = 0; j < topk; ++j)
+                if (a.topk_idx[o + j] == seg.slot) m.e = a.topk_w[o + j];
+        } else {
+            m.t = a.perm_rec[seg.base + idx] / topk;
+            m.e = a.perm_e[seg.base + idx];
+        }
+    }
+    return m;
+}
+
+// Tensor map of v as a 2-D [T * H, d] bf16 array, boxes of 64 columns x 1 row,
+// 128-byte swizzle (the TMA gathers of the loader).
+struct RowMaps {
+    CUtensorMap v;
+};
+
 template <int KC, int DV, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
-chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_map, int32_t H, int32_t N,
-                       int32_t topk, int32_t use_shared, float scale, int32_t num_items,
-                       int32_t *work_counter) {
+chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_map,
+                       const __grid_constant__ RowMaps maps, int32_t H, int32_t N, int32_t topk,
+                       int32_t use_shared, float scale, int32_t num_items, int32_t *work_counter) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *s_tot = reinterpret_cast<float *>(sm + Smem::TOT);
@@ -240,28 +281,27 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     const uint32_t bar0 = smem_u32(sm + Smem::BAR);
     auto bar = [&](int i) { return bar0 + 8u * i; };
     uint32_t *s_slot = reinterpret_cast<uint32_t *>(sm + Smem::MISC);
-    int *s_item = reinterpret_cast<int *>(sm + Smem::MISC + 4);
     int *s_abort = reinterpret_cast<int *>(sm + Smem::MISC + 8);
     int *s_segq = reinterpret_cast<int *>(sm + Smem::SEGQ);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.q);
-    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.v);
     const __nv_bfloat16 *gg = static_cast<const __nv_bfloat16 *>(a.g);
-    const __nv_bfloat16 *gqs = static_cast<const __nv_bfloat16 *>(a.qs ? a.qs : a.q);
-    const __nv_bfloat16 *gks = static_cast<const __nv_bfloat16 *>(a.ks ? a.ks : a.k);
     const int P = N + use_shared;
 
     auto meta_tok = [&](int stage) { return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE); };
     auto meta_e = [&](int stage) {
         return reinterpret_cast<float *>(sm + Smem::META + stage * Smem::META_STAGE + 512);
     };
+    auto meta_hdr = [&](int stage) {
+        return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE + 1024);
+    };
 
     // ---- set-up ------------------------------------------------------------
     if (warp == 0) tmem_alloc(smem_u32(s_slot), kTmemCols);
     if (tid == 0) {
         mbar_init(bar(kBarT), kTrfThreads);
+        mbar_init(bar(kBarSc0), KC);
+        mbar_init(bar(kBarSc1), KC);
         mbar_init(bar(kBarS), 32 * kEpiWarps);
         mbar_init(bar(kBarA), 1);
         mbar_init(bar(kBarQK), 1);
@@ -270,9 +310,15 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
         mbar_init(bar(kBarOf), 32 * kEpiWarps);
         mbar_init(bar(kBarV0), 1);
         mbar_init(bar(kBarV1), 1);
+        mbar_init(bar(kBarVL0), 1);
+        mbar_init(bar(kBarVL1), 1);
+        for (int i = 0; i < kMetaStages; ++i) {
+            mbar_init(bar(kBarMR + i), 32);
+            mbar_init(bar(kBarMF + i), 32 * kEpiWarps);
+        }
         for (int i = 0; i < kSegSlots; ++i) {
             mbar_init(bar(kBarSegF + i), 1);
-            mbar_init(bar(kBarSegE + i), 32 * kEpiWarps);
+            mbar_init(bar(kBarSegE + i), 32 * kEpiWarps + kTrfThreads);
         }
         mbar_fence_init();
         *s_abort = 0;
@@ -285,40 +331,42 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
         }
     }
     fence_before();
+    fence_proxy_async();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_slot;
 
-    // The two roles walk the same sequence of work items, each at its own pace:
-    // the transform warps claim items (one ahead) and post them through the
-    // segment ring; every per-chunk barrier counts chunks globally (g), so a
-    // role can be in the next segment while the other finishes the previous one.
+    // The roles walk the same sequence of work items, each at its own pace: the
+    // loader claims the items and posts them through the segment ring; every
+    // per-chunk barrier counts chunks globally (g), so a role can be in the
+    // next segment while another finishes the previous one.
     uint32_t gch = 0;  // chunks of earlier segments: barrier phase parity base
     bool failed = false;
-    if (warp >= kEpiWarps) {
-        // Register split: the launch gives every thread kRegsLaunch registers;
-        // the two transform warpgroups take kRegsTrf each, the epilogue
-        // warpgroup keeps kRegsEpi: 128 kRegsEpi + 256 kRegsTrf = 384 kRegsLaunch.
-        reg_alloc<kRegsTrf>();
-        const int tt = tid - 32 * kEpiWarps;  // 0..255
-        if (tt == 0) *s_item = atomicAdd(work_counter, 1);
-        for (int sidx = 0;; ++sidx) {
-            named_sync(1, kTrfThreads);
-            const int item = *s_item;
-            const bool stop = named_sync_or(1, kTrfThreads, item >= num_items || *s_abort != 0);
-            Segment seg{};
-            int pad_base = 0;  // first partial-output row of this work item
-            if (!stop) {
-                seg = decode_segment<MASKED>(a, item, H, N, use_shared);
-                pad_base = a.pad_off[item];
-            }
-            const int nch = stop ? 0 : (seg.len + kC - 1) / kC;
-            bool bad = false;
-            if (tt == 0) {  // hand the segment (or the end of the work) to the epilogue warps
+    if (warp >= kEpiWarps + kTrfWarps) {
+        // =================== loader warps ===================
+        reg_dealloc<kRegsLdr>();
+        const int lw = warp - kEpiWarps - kTrfWarps, lane = tid & 31;
+        if (lw == 0) {
+            // Work items -> segment ring; row metadata of every chunk -> meta
+            // ring (lane l: rows 4l..4l+3); L2 prefetch of those rows.  After the
+            // last item, one more stage whose header tells the gather warps to stop.
+            uint32_t g = 0;
+            for (int sidx = 0;; ++sidx) {
+                int item = 0;
+                if (lane == 0) item = *(volatile int *)s_abort ? num_items : atomicAdd(work_counter, 1);
+                item = __shfl_sync(0xffffffffu, item, 0);
+                const bool stop = item >= num_items;
+                Segment seg{};
+                int pad_base = 0;
+                if (!stop) {
+                    seg = decode_segment<MASKED>(a, item, H, N, use_shared);
+                    pad_base = a.pad_off[item];
+                }
                 const int slot = sidx % kSegSlots;
-                if (sidx >= kSegSlots)
-                    bad = !mbar_wait_bounded(bar(kBarSegE + slot), ((sidx / kSegSlots) - 1) & 1, kWaitNs);
-                if (!bad) {
+                bool ok = sidx < kSegSlots ||
+                          mbar_wait_bounded(bar(kBarSegE + slot), ((sidx / kSegSlots) - 1) & 1, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+                if (lane == 0) {
                     int *d = s_segq + slot * 8;
                     d[0] = stop ? -1 : item;
                     d[1] = seg.b;
@@ -330,66 +378,94 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     d[7] = seg.shared ? 1 : 0;
                     mbar_arrive(bar(kBarSegF + slot));
                 }
-            }
-            if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
-            if (stop) break;
-            if (tt == 0) *s_item = atomicAdd(work_counter, 1);  // the next item, read at the top
-            // =================== transform warps ===================
-            constexpr int CG = KC / 8, NRB = kTrfThreads / CG, RPT = kC / NRB;
-            const int cg = tt % CG, rb = tt / CG, col0 = cg * 8;
-            const __nv_bfloat16 *qsrc = seg.shared ? gqs : gq;
-            const __nv_bfloat16 *ksrc = seg.shared ? gks : gk;
-
-            // Row metadata of chunk n: token index and router weight.  Loaded
-            // into registers two chunks ahead, stored into its ring stage one
-            // chunk ahead.
-            struct RowMeta { int t; float e; };
-            auto load_meta = [&](int n) {
-                RowMeta m{-1, 0.f};
-                const int idx = n * kC + tt;
-                if (tt < kC && idx < seg.len) {
-                    if (seg.shared) {
-                        m.t = seg.base + idx;
-                        m.e = 1.f;
-                    } else if (MASKED) {
-                        // every token of the sequence; -1 marks the ones that did not
-                        // select this partition (no write, no decay, no read)
-                        m.t = seg.base + idx;
-                        m.e = -1.f;
-                        const int64_t o = ((int64_t)m.t * H + seg.h) * topk;
-                        for (int j = 0; j < topk; ++j)
-                            if (a.topk_idx[o + j] == seg.slot) m.e = a.topk_w[o + j];
-                    } else {
-                        m.t = a.perm_rec[seg.base + idx] / topk;
-                        m.e = a.perm_e[seg.base + idx];
-                    }
-                }
-                return m;
-            };
-            auto store_meta = [&](int n, const RowMeta &m) {
-                if (tt < kC) {
-                    const int st = (gch + n) % kMetaStages;
-                    meta_tok(st)[tt] = m.t;
-                    meta_e(st)[tt] = m.e;
-                }
-            };
-            uint4 rq[RPT], rk[RPT], rg[RPT], rg_next[RPT];
-            auto load_g = [&](int n, uint4 (&dst)[RPT]) {
-                const int *tok = meta_tok((gch + n) % kMetaStages);
+                const int nst = stop ? 1 : (seg.len + kC - 1) / kC;
+                for (int n = 0; n < nst; ++n, ++g) {
+                    const int st = g % kMetaStages;
+                    ok = g < kMetaStages ||
+                         mbar_wait_bounded(bar(kBarMF + st), ((g / kMetaStages) - 1) & 1, kWaitNs);
+                    if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
 #pragma unroll
-                for (int i = 0; i < RPT; ++i) {
-                    const int t = tok[rb * RPT + i];
-                    dst[i] = t >= 0 ? ldg_stream(gg + ((int64_t)t * H + seg.h) * KC + col0)
-                                    : make_uint4(0, 0, 0, 0);
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = 4 * lane + j;
+                        const RowMeta m = stop ? RowMeta{-1, 0.f} : row_meta<MASKED>(a, seg, n * kC + r, H, topk);
+                        meta_tok(st)[r] = m.t;
+                        meta_e(st)[r] = m.e;
+                    }
+                    if (lane == 0) {
+                        int *hd = meta_hdr(st);
+                        hd[0] = stop ? 1 : 0;
+                        hd[1] = seg.h;
+                        hd[2] = seg.shared ? 1 : 0;
+                    }
+                    mbar_arrive(bar(kBarMR + st));
                 }
-            };
+                if (failed || stop) break;
+            }
+        } else if (lw == 1) {
+            // The V rows of every chunk into V0 / V1 once the chunk two back has
+            // been consumed.  Lane l gathers rows 4l..4l+3 (rows past the
+            // segment's end copy token row 0: their Kt rows are zero, so they add
+            // nothing).
+            int64_t last = -1;  // last chunk whose copies this warp issued
+            const uint32_t off = (uint32_t)(lane >> 1) * 2048 + (uint32_t)(lane & 1) * 512;
+            for (uint32_t g = 0;; ++g) {
+                const int st = g % kMetaStages;
+                bool ok = mbar_wait_bounded(bar(kBarMR + st), (g / kMetaStages) & 1, kWaitNs);
+                if (ok && g >= 2)
+                    ok = mbar_wait_bounded(bar((g & 1) ? kBarV1 : kBarV0), ((g - 2) >> 1) & 1, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+                const int *hd = meta_hdr(st);
+                if (hd[0]) break;
+                const int h = hd[1];
+                const int *tok = meta_tok(st);
+                int rr[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = tok[4 * lane + j];
+                    rr[j] = t >= 0 ? t * H + h : 0;
+                }
+                const uint32_t mb = bar((g & 1) ? kBarVL1 : kBarVL0);
+                if (lane == 0) mbar_arrive_expect_tx(mb, kC * DV * 2);
+                __syncwarp();
+                const uint32_t dst = smem_u32(sm + ((g & 1) ? Smem::V1 : Smem::V0)) + off;
+#pragma unroll
+                for (int at = 0; at < DV / 64; ++at)
+                    tma_gather4(&maps.v, dst + at * 1024, mb, at * 64, rr[0], rr[1], rr[2], rr[3]);
+                last = g;
+            }
+            // no copy of this warp may still be writing shared memory when the CTA exits
+            if (last >= 0 &&
+                !mbar_wait_bounded(bar((last & 1) ? kBarVL1 : kBarVL0), (uint32_t)((last >> 1) & 1), kWaitNs))
+                failed = true;
+        }
+    } else if (warp >= kEpiWarps) {
+        // =================== transform warps ===================
+        reg_alloc<kRegsTrf>();
+        const int tt = tid - 32 * kEpiWarps;  // 0..255
+        constexpr int CG = KC / 8, NRB = kTrfThreads / CG, RPT = kC / NRB;
+        const int cg = tt % CG, rb = tt / CG, col0 = cg * 8;
+        for (int sidx = 0;; ++sidx) {
+            const int slot = sidx % kSegSlots;
+            const bool ok = mbar_wait_bounded(bar(kBarSegF + slot), (sidx / kSegSlots) & 1, kWaitNs);
+            if (named_sync_or(1, kTrfThreads, !ok)) { failed = true; break; }
+            const int *d = s_segq + slot * 8;
+            const int item = d[0], seg_h = d[2], seg_len = d[5];
+            const bool seg_shared = d[7] != 0;
+            mbar_arrive(bar(kBarSegE + slot));
+            if (item < 0) break;
+            const int nch = (seg_len + kC - 1) / kC;
+            const __nv_bfloat16 *qsrc = static_cast<const __nv_bfloat16 *>(seg_shared && a.qs ? a.qs : a.q);
+            const __nv_bfloat16 *ksrc = static_cast<const __nv_bfloat16 *>(seg_shared && a.ks ? a.ks : a.k);
+            uint4 rq[RPT], rk[RPT], rg[RPT], rg_next[RPT];
+            // raw q, k rows of chunk n (16-byte L1-bypassing loads); its
+            // metadata stage was waited for by load_g
             auto load_qk = [&](int n) {
                 const int *tok = meta_tok((gch + n) % kMetaStages);
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) {
                     const int t = tok[rb * RPT + i];
                     if (t >= 0) {
-                        const int64_t ro = ((int64_t)t * H + seg.h) * KC + col0;
+                        const int64_t ro = ((int64_t)t * H + seg_h) * KC + col0;
                         rq[i] = ldg_stream(qsrc + ro);
                         rk[i] = ldg_stream(ksrc + ro);
                     } else {
@@ -397,58 +473,25 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     }
                 }
             };
-            // the q, k, g and v rows of a chunk start on their way from HBM into L2
-            // two steps before the loads that read them (which then hit L2)
-            auto prefetch_rows = [&](const RowMeta &m) {
-                if (tt < kC && m.t >= 0) {
-                    const int64_t th = (int64_t)m.t * H + seg.h;
+            // raw g rows of chunk n (its metadata stage must have been written)
+            auto load_g = [&](int n, uint4 (&dst)[RPT]) -> bool {
+                const uint32_t g = gch + n;
+                const bool ok = mbar_wait_bounded(bar(kBarMR + g % kMetaStages), (g / kMetaStages) & 1, kWaitNs);
+                const int *tok = meta_tok(g % kMetaStages);
 #pragma unroll
-                    for (int o = 0; o < KC * 2; o += 128) {
-                        prefetch_l2(reinterpret_cast<const unsigned char *>(qsrc + th * KC) + o);
-                        prefetch_l2(reinterpret_cast<const unsigned char *>(ksrc + th * KC) + o);
-                        prefetch_l2(reinterpret_cast<const unsigned char *>(gg + th * KC) + o);
-                    }
-#pragma unroll
-                    for (int o = 0; o < DV * 2; o += 128)
-                        prefetch_l2(reinterpret_cast<const unsigned char *>(gv + th * DV) + o);
+                for (int i = 0; i < RPT; ++i) {
+                    const int t = ok ? tok[rb * RPT + i] : -1;
+                    dst[i] = t >= 0 ? ldg_stream(gg + ((int64_t)t * H + seg_h) * KC + col0)
+                                    : make_uint4(0, 0, 0, 0);
                 }
+                return ok;
             };
-            RowMeta meta_ahead{-1, 0.f};  // metadata of chunk n + 1 while processing chunk n
-            if (nch > 0) {
-                store_meta(0, load_meta(0));
-                if (nch > 1) meta_ahead = load_meta(1);
-                named_sync(1, kTrfThreads);
-                load_g(0, rg);
-                if (nch > 1) prefetch_rows(meta_ahead);
-            }
+            bool bad = false;
+            if (nch > 0) bad = !load_g(0, rg);
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
                 const int mst = g_n % kMetaStages;
-                const int vb = g_n & 1;
-                unsigned char *sV = sm + (vb ? Smem::V1 : Smem::V0);
-                bool bad = false;
-                // the stage of chunk n+1 last held chunk n-5, whose output rows are
-                // long written (see kMetaStages)
-                if (n + 1 < nch) store_meta(n + 1, meta_ahead);
-                if (n + 2 < nch) meta_ahead = load_meta(n + 2);
                 load_qk(n);
-                // V buffer vb was last read by chunk g_n - 2 (perhaps of an earlier segment)
-                if (g_n >= 2) bad = !mbar_wait_bounded(bar(vb ? kBarV1 : kBarV0), ((g_n - 2) >> 1) & 1, kWaitNs);
-                {   // gather V rows of chunk n with cp.async
-                    constexpr int VCG = DV / 8, VNRB = kTrfThreads / VCG, VRPT = kC / VNRB;
-                    const int vcg = tt % VCG, vrb = tt / VCG;
-                    const int *tok = meta_tok(mst);
-#pragma unroll
-                    for (int i = 0; i < VRPT; ++i) {
-                        const int r = vrb * VRPT + i;
-                        const int t = tok[r];
-                        unsigned char *dst = sV + tile_off(r, vcg * 8);
-                        if (t >= 0)
-                            cp_async16(smem_u32(dst), gv + ((int64_t)t * H + seg.h) * DV + vcg * 8);
-                        else
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-                    }
-                }
                 // pass 1: per-thread running sums of g over its rows -> block totals
                 // (masking schedule: the rows of tokens that did not select this
                 // partition get gate 0, i.e. no decay)
@@ -475,8 +518,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     for (int j = 0; j < 8; ++j) s_tot[rb * 128 + col0 + j] = run[j];
                 }
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
-                if (n + 1 < nch) load_g(n + 1, rg_next);  // a whole chunk of latency hiding
-                if (n + 2 < nch) prefetch_rows(meta_ahead);
+                if (n + 1 < nch) bad = !load_g(n + 1, rg_next);  // a whole chunk of latency hiding
                 float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (tt < KC) {  // per-column exclusive scan over row blocks
                     float acc = 0.f, gmid = 0.f;
@@ -489,14 +531,18 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     s_fmid[tt] = expf(gmid);
                     s_beta[tt] = expf(acc - gmid);
                     s_tot[32 * 128 + tt] = gmid * kLog2e;
+                    // the state rows can be rescaled now (two barriers by chunk parity:
+                    // this role may reach the next chunk's scan before the epilogue
+                    // has waited for this one)
+                    mbar_arrive(bar((g_n & 1) ? kBarSc1 : kBarSc0));
                 }
                 named_sync(1, kTrfThreads);
-                // Qt / Kt buffers are free once the first three MMAs of chunk n-1 completed
-                if (g_n >= 1) bad = !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
-                // pass 2: Qt, Kt rows (bf16) straight into their tiles.  The read
-                // weight e * scale is applied to the output rows by the epilogue.
-                // The decay factors are rounded to bf16 and multiplied into the bf16
-                // q / k pairs with packed bf16 products.
+                // Qt / Kt tiles are free once the products of chunk g_n - 1 read them
+                if (g_n >= 1) bad |= !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
+                // pass 2: Qt, Kt rows (bf16) into their tiles.  The read weight
+                // e * scale is applied to the output rows by the epilogue.  The decay
+                // factors are rounded to bf16 and multiplied into the bf16 q / k pairs
+                // with packed bf16 products.
                 {
                     float run[8], gm2[8];
 #pragma unroll
@@ -533,7 +579,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     }
                     if (maxdev > kGateRangeLog2) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
                 }
-                cp_async_wait_all();
                 fence_proxy_async();
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
                 mbar_arrive(bar(kBarT));
@@ -543,7 +588,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             if (failed) break;
             gch += nch;
         }
-        cp_async_wait_all();
     } else {
         reg_dealloc<kRegsEpi>();
         for (int sidx = 0;; ++sidx) {
@@ -606,6 +650,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             auto write_out = [&](int n_o, bool pend) -> bool {
                 const int st = (gch + n_o) % kMetaStages;
                 const float w = (MASKED ? fmaxf(meta_e(st)[row], 0.f) : meta_e(st)[row]) * scale;
+                mbar_arrive(bar(kBarMF + st));  // the chunk's metadata stage is free again
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
                 unsigned char *stg = sm + Smem::S;
 #pragma unroll
@@ -643,7 +688,9 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             bool pend = false;
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
-                pend |= !mbar_wait_bounded(bar(kBarT), g_n & 1, kWaitNs);
+                // the state-row pass needs only the chunk's gate scan; it overlaps
+                // the transform's Qt / Kt pass
+                pend |= !mbar_wait_bounded(bar((g_n & 1) ? kBarSc1 : kBarSc0), (g_n >> 1) & 1, kWaitNs);
                 if (n >= 1) {
                     pend |= !mbar_wait_bounded(bar(kBarO), (g_n - 1) & 1, kWaitNs);
                     fence_after();
@@ -679,8 +726,9 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 mbar_arrive(bar(kBarS));
                 const uint32_t v0 = smem_u32(sm + ((g_n & 1) ? Smem::V1 : Smem::V0));
                 if (issuer) {
-                    // A = Qt Kt^T; S += Kt^T V; O = Qt S'
-                    bool ok = mbar_wait_bounded(bar(kBarS), g_n & 1, kWaitNs);
+                    // A = Qt Kt^T once Qt, Kt are written; S += Kt^T V and O = Qt S'
+                    // once the state rows are rescaled and the V rows have landed
+                    bool ok = mbar_wait_bounded(bar(kBarT), g_n & 1, kWaitNs);
                     if (ok) {
                         fence_after();
 #pragma unroll
@@ -690,6 +738,11 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                                      desc_sw128(k0 + ko, 16, 2048), idA, k16 > 0);
                         }
                         commit(bar(kBarA));
+                        ok = mbar_wait_bounded(bar(kBarS), g_n & 1, kWaitNs) &&
+                             mbar_wait_bounded(bar((g_n & 1) ? kBarVL1 : kBarVL0), (g_n >> 1) & 1, kWaitNs);
+                    }
+                    if (ok) {
+                        fence_after();
 #pragma unroll
                         for (int k16 = 0; k16 < kC; k16 += 16) {
                             const uint32_t ro = (k16 / 8) * 2048;
@@ -873,6 +926,22 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     // The partial buffer as a 2-D tensor [part_rows, DV] of bf16, stored in
     // boxes of 64 columns x one chunk of rows with the 128-byte swizzle.
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    // v as [T * H, d] bf16, gathered in boxes of 64 columns x 1 row with the
+    // 128-byte swizzle (no rows: never read, left zero).
+    const int64_t th_rows = a.total_tokens * cfg.num_heads;
+    auto row_map = [&](CUtensorMap *m, const void *base, int width) -> bool {
+        memset(m, 0, sizeof *m);
+        if (th_rows == 0) return true;
+        cuuint64_t d[2] = {(cuuint64_t)width, (cuuint64_t)th_rows};
+        cuuint64_t st[1] = {(cuuint64_t)width * 2};
+        cuuint32_t bx[2] = {64, 1};
+        cuuint32_t es[2] = {1, 1};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), d, st, bx, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    RowMaps maps;
+    if (!row_map(&maps.v, a.v, DV)) return cudaErrorInvalidValue;
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap map;
     cuuint64_t dims[2] = {(cuuint64_t)DV, (cuuint64_t)a.part_rows};
@@ -886,7 +955,8 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
 
     const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
     chunked_forward_kernel<KC, DV, MASKED><<<grid, kThreads, kSmemBytes, stream>>>(
-        a, map, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
+        a, map, maps, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg,
+        counter);
     return cudaGetLastError();
 }
 
