@@ -82,7 +82,7 @@ constexpr int kMetaStages = 5;
 constexpr int kSegSlots = 4;
 
 enum Bar {
-    kBarT = 0, kBarSc0, kBarSc1, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf, kBarV0, kBarV1,
+    kBarT = 0, kBarSc0, kBarSc1, kBarS, kBarA, kBarQK, kBarP, kBarO, kBarOf0, kBarOf1, kBarV0, kBarV1,
     kBarVL0, kBarVL1,                  // V rows of a chunk landed in V0 / V1 (TMA)
     kBarMR,                            // kMetaStages "row metadata written" barriers
     kBarMF = kBarMR + kMetaStages,     // kMetaStages "row metadata no longer needed" barriers
@@ -307,7 +307,8 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
         mbar_init(bar(kBarQK), 1);
         mbar_init(bar(kBarP), 32 * kEpiWarps);
         mbar_init(bar(kBarO), 1);
-        mbar_init(bar(kBarOf), 32 * kEpiWarps);
+        mbar_init(bar(kBarOf0), 32 * kEpiWarps);
+        mbar_init(bar(kBarOf1), 32 * kEpiWarps);
         mbar_init(bar(kBarV0), 1);
         mbar_init(bar(kBarV1), 1);
         mbar_init(bar(kBarVL0), 1);
@@ -413,6 +414,11 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 bool ok = mbar_wait_bounded(bar(kBarMR + st), (g / kMetaStages) & 1, kWaitNs);
                 if (ok && g >= 2)
                     ok = mbar_wait_bounded(bar((g & 1) ? kBarV1 : kBarV0), ((g - 2) >> 1) & 1, kWaitNs);
+                // Queue behind the output store of chunk g - 3 (the TMA engine works
+                // in order: the epilogue's next state-row pass waits for that store
+                // to have read its staging tile, not for these gathers).
+                if (ok && g >= 3)
+                    ok = mbar_wait_bounded(bar(kBarMF + (g - 3) % kMetaStages), ((g - 3) / kMetaStages) & 1, kWaitNs);
                 if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
                 const int *hd = meta_hdr(st);
                 if (hd[0]) break;
@@ -437,6 +443,77 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             if (last >= 0 &&
                 !mbar_wait_bounded(bar((last & 1) ? kBarVL1 : kBarVL0), (uint32_t)((last >> 1) & 1), kWaitNs))
                 failed = true;
+        } else if (lw == 2) {
+            // The tensor-core products of every chunk, issued by lane 0 as their
+            // operands become ready: A = Qt Kt^T once Qt, Kt are written (P of
+            // the previous chunk was read out of A before its P V was issued);
+            // S += Kt^T V once the state rows are rescaled and V has landed;
+            // O = Qt S' once that O buffer has been read out for chunk g - 2;
+            // O += P V once P is written.
+            const uint32_t q0 = smem_u32(sm + Smem::Q), k0 = smem_u32(sm + Smem::K);
+            const uint32_t p0 = smem_u32(sm + Smem::P), s0 = smem_u32(sm + Smem::S);
+            constexpr uint32_t idA = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t idS = idesc_bf16(128, DV, 1, 1);
+            constexpr uint32_t idO = idesc_bf16(128, DV, 0, 1);
+            for (uint32_t g = 0;; ++g) {
+                const int st = g % kMetaStages;
+                bool ok = mbar_wait_bounded(bar(kBarMR + st), (g / kMetaStages) & 1, kWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+                if (meta_hdr(st)[0]) break;
+                const uint32_t v0 = smem_u32(sm + ((g & 1) ? Smem::V1 : Smem::V0));
+                const uint32_t tO = tmem + ((g & 1) ? kTmemO1 : kTmemO0);
+                ok = mbar_wait_bounded(bar(kBarT), g & 1, kWaitNs);
+                if (ok && lane == 0) {
+                    fence_after();
+#pragma unroll 1
+                    for (int k16 = 0; k16 < KC; k16 += 16) {
+                        const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                        mma_bf16(tmem + kTmemA, desc_sw128(q0 + ko, 16, 2048), desc_sw128(k0 + ko, 16, 2048), idA,
+                                 k16 > 0);
+                    }
+                    commit(bar(kBarA));
+                }
+                __syncwarp();
+                ok = ok && mbar_wait_bounded(bar(kBarS), g & 1, kWaitNs) &&
+                     mbar_wait_bounded(bar((g & 1) ? kBarVL1 : kBarVL0), (g >> 1) & 1, kWaitNs);
+                if (ok && lane == 0) {
+                    fence_after();
+#pragma unroll 1
+                    for (int k16 = 0; k16 < kC; k16 += 16) {
+                        const uint32_t ro = (k16 / 8) * 2048;
+                        mma_bf16(tmem + kTmemS, desc_sw128(k0 + ro, 1024, 2048), desc_sw128(v0 + ro, 1024, 2048), idS,
+                                 1);
+                    }
+                }
+                __syncwarp();
+                // two read-out barriers by chunk parity: at a segment's end the
+                // epilogue reads out the last O without waiting for this warp
+                if (ok && g >= 2) ok = mbar_wait_bounded(bar((g & 1) ? kBarOf1 : kBarOf0), ((g - 2) >> 1) & 1, kWaitNs);
+                if (ok && lane == 0) {
+                    fence_after();
+#pragma unroll 1
+                    for (int k16 = 0; k16 < KC; k16 += 16) {
+                        const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                        mma_bf16(tO, desc_sw128(q0 + ko, 16, 2048), desc_sw128(s0 + (k16 / 8) * 2048, 1024, 2048), idO,
+                                 k16 > 0);
+                    }
+                    commit(bar(kBarQK));
+                }
+                __syncwarp();
+                ok = ok && mbar_wait_bounded(bar(kBarP), g & 1, kWaitNs);
+                if (ok && lane == 0) {
+                    fence_after();
+#pragma unroll 1
+                    for (int k16 = 0; k16 < kC; k16 += 16) {
+                        const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                        mma_bf16(tO, desc_sw128(p0 + ko, 16, 2048), desc_sw128(v0 + (k16 / 8) * 2048, 1024, 2048), idO,
+                                 1);
+                    }
+                    commit(bar(kBarO));
+                    commit(bar((g & 1) ? kBarV1 : kBarV0));
+                }
+                if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+            }
         }
     } else if (warp >= kEpiWarps) {
         // =================== transform warps ===================
@@ -631,12 +708,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 tmem_wait_st();
             }
             float p_pending = 1.f;
-            const bool issuer = tid == 0;
-            const uint32_t q0 = smem_u32(sm + Smem::Q), k0 = smem_u32(sm + Smem::K);
-            const uint32_t p0 = smem_u32(sm + Smem::P), s0 = smem_u32(sm + Smem::S);
-            constexpr uint32_t idA = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t idS = idesc_bf16(128, DV, 1, 1);
-            constexpr uint32_t idO = idesc_bf16(128, DV, 0, 1);
             // Output of chunk n_o (O buffer of its parity), written one chunk late so
             // that it overlaps the transform's compute: each thread scales its TMEM
             // row of O by the read weight e * scale and stores it as bf16 into the
@@ -650,7 +721,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             auto write_out = [&](int n_o, bool pend) -> bool {
                 const int st = (gch + n_o) % kMetaStages;
                 const float w = (MASKED ? fmaxf(meta_e(st)[row], 0.f) : meta_e(st)[row]) * scale;
-                mbar_arrive(bar(kBarMF + st));  // the chunk's metadata stage is free again
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
                 unsigned char *stg = sm + Smem::S;
 #pragma unroll
@@ -671,7 +741,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     }
                 }
                 fence_before();
-                mbar_arrive(bar(kBarOf));  // O may be overwritten now
+                mbar_arrive(bar(((gch + n_o) & 1) ? kBarOf1 : kBarOf0));  // O may be overwritten now
                 fence_proxy_async();
                 if (named_sync_or(3, 32 * kEpiWarps, pend)) return true;
                 if (tid == 0) {
@@ -680,6 +750,9 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                         tma_store_2d(&part_map, smem_u32(stg + atom * (kC * 128)), atom * 64, pad_base + n_o * kC);
                     bulk_commit();
                 }
+                // the chunk's metadata stage is free again, and its output store is
+                // queued on the TMA engine (the V gathers of chunk n_o + 3 wait for this)
+                mbar_arrive(bar(kBarMF + st));
                 return false;
             };
             // A wait that runs out of time sets `pend` in the threads that saw it;
@@ -724,46 +797,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 fence_proxy_async();
                 fence_before();
                 mbar_arrive(bar(kBarS));
-                const uint32_t v0 = smem_u32(sm + ((g_n & 1) ? Smem::V1 : Smem::V0));
-                if (issuer) {
-                    // A = Qt Kt^T once Qt, Kt are written; S += Kt^T V and O = Qt S'
-                    // once the state rows are rescaled and the V rows have landed
-                    bool ok = mbar_wait_bounded(bar(kBarT), g_n & 1, kWaitNs);
-                    if (ok) {
-                        fence_after();
-#pragma unroll
-                        for (int k16 = 0; k16 < KC; k16 += 16) {
-                            const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                            mma_bf16(tmem + kTmemA, desc_sw128(q0 + ko, 16, 2048),
-                                     desc_sw128(k0 + ko, 16, 2048), idA, k16 > 0);
-                        }
-                        commit(bar(kBarA));
-                        ok = mbar_wait_bounded(bar(kBarS), g_n & 1, kWaitNs) &&
-                             mbar_wait_bounded(bar((g_n & 1) ? kBarVL1 : kBarVL0), (g_n >> 1) & 1, kWaitNs);
-                    }
-                    if (ok) {
-                        fence_after();
-#pragma unroll
-                        for (int k16 = 0; k16 < kC; k16 += 16) {
-                            const uint32_t ro = (k16 / 8) * 2048;
-                            mma_bf16(tmem + kTmemS, desc_sw128(k0 + ro, 1024, 2048),
-                                     desc_sw128(v0 + ro, 1024, 2048), idS, 1);
-                        }
-                        // O buffer g_n & 1 was last read out for chunk g_n - 2
-                        if (n >= 2) ok = mbar_wait_bounded(bar(kBarOf), g_n & 1, kWaitNs);
-                    }
-                    if (ok) {
-                        fence_after();
-#pragma unroll
-                        for (int k16 = 0; k16 < KC; k16 += 16) {
-                            const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                            mma_bf16(tmem + ((g_n & 1) ? kTmemO1 : kTmemO0), desc_sw128(q0 + ko, 16, 2048),
-                                     desc_sw128(s0 + (k16 / 8) * 2048, 1024, 2048), idO, k16 > 0);
-                        }
-                        commit(bar(kBarQK));
-                    }
-                    pend |= !ok;
-                }
                 // P = causal mask of A, bf16
                 pend |= !mbar_wait_bounded(bar(kBarA), g_n & 1, kWaitNs);
                 fence_after();
@@ -795,22 +828,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 fence_proxy_async();
                 fence_before();
                 mbar_arrive(bar(kBarP));
-                if (issuer) {
-                    // O += P V once every epilogue thread has written its row of P
-                    const bool ok = mbar_wait_bounded(bar(kBarP), g_n & 1, kWaitNs);
-                    if (ok) {
-                        fence_after();
-#pragma unroll
-                        for (int k16 = 0; k16 < kC; k16 += 16) {
-                            const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
-                            mma_bf16(tmem + ((g_n & 1) ? kTmemO1 : kTmemO0), desc_sw128(p0 + ko, 16, 2048),
-                                     desc_sw128(v0 + (k16 / 8) * 2048, 1024, 2048), idO, 1);
-                        }
-                        commit(bar(kBarO));
-                        commit(bar((g_n & 1) ? kBarV1 : kBarV0));
-                    }
-                    pend |= !ok;
-                }
                 if (n >= 1) {  // output of the previous chunk, staged in S' once O = Qt S' of this one is done
                     pend |= !mbar_wait_bounded(bar(kBarQK), g_n & 1, kWaitNs);
                     fence_after();
