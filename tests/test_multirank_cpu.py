@@ -72,3 +72,20 @@ def test_single_process_helpers():
     assert bench.max_over_ranks_of(4.5, 1, None) == 4.5
     assert bench.whole_job_tokens_per_s(1, 32768 + 256, 1.0) == pytest.approx(33024e3)
     bench.rank_barrier(1)
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary only while the
+    kernel source still has the hash recorded in it."""
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_bytes(b"kernel v1\n")
+    import hashlib
+    h = hashlib.sha256(b"kernel v1\n").hexdigest()
+    md = tmp_path / "p.md"
+    md.write_text(f"# summary\n\n    source_sha256: {h}\n    dram_bytes_per_launch: 12345\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("k.cu", "p.md") == 12345
+    src.write_bytes(b"kernel v2\n")
+    assert bench.profiled_traffic("k.cu", "p.md") is None
+    assert bench.profiled_traffic("missing.cu", "p.md") is None
