@@ -156,10 +156,12 @@ sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *router_logit
  *                       every token (same contents as sse_route).
  * Workspace: sse_forward_workspace_size bytes (256-byte aligned).
  * Numerics: float32 states and accumulation.  The chunked path rounds its
- * tensor-core operands to bfloat16 and needs the summed log-gate of any 128
- * consecutive tokens of a segment to stay above -80 per key row (the decay
- * factors are split around the chunk midpoint); a chunk outside this range
- * sets the SSE_DEVICE_GATE_RANGE flag read by sse_read_device_status.
+ * tensor-core operands to bfloat16 and splits the decay factors of each
+ * 128-row chunk of a segment around its midpoint: it needs the summed
+ * log-gate of each half chunk to stay above -80 per key row.  A chunk outside
+ * this range sets the SSE_DEVICE_GATE_RANGE flag read by
+ * sse_read_device_status.  The check takes the log-gates to be <= 0 (decays in
+ * (0, 1], as in the method); positive log-gates are not range-checked.
  * ------------------------------------------------------------------------- */
 size_t sse_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
 

@@ -67,7 +67,6 @@ static_assert(32 * (kEpiWarps * kRegsEpi + kTrfWarps * kRegsTrf + kLdrWarps * kR
               "register split must use exactly the launch allocation");
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kGateRangeLog2 = 80.f * kLog2e;  // |G_r - G_m| limit (~80 natural-log units)
 
 constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
 // Row metadata ring (global chunk g in stage g % kMetaStages): written by the
@@ -608,6 +607,10 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     s_fmid[tt] = expf(gmid);
                     s_beta[tt] = expf(acc - gmid);
                     s_tot[32 * 128 + tt] = gmid * kLog2e;
+                    // |G_r - G_m| over the chunk: with log-gates <= 0 (decays in
+                    // (0, 1]) G_r falls monotonically from 0, so it is at most
+                    // max(|G_m|, |G_last - G_m|)
+                    if (fmaxf(fabsf(gmid), fabsf(acc - gmid)) > 80.f) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
                     // the state rows can be rescaled now (two barriers by chunk parity:
                     // this role may reach the next chunk's scan before the epilogue
                     // has waited for this one)
@@ -621,14 +624,12 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 // factors are rounded to bf16 and multiplied into the bf16 q / k pairs
                 // with packed bf16 products.
                 {
-                    float run[8], gm2[8];
+                    // run = (G_r - G_m) log2(e), advanced row by row
+                    float run[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        run[j] = s_tot[rb * 128 + col0 + j] * kLog2e;
-                        gm2[j] = s_tot[32 * 128 + col0 + j];
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        run[j] = fmaf(s_tot[rb * 128 + col0 + j], kLog2e, -s_tot[32 * 128 + col0 + j]);
                     const float *me = meta_e(mst);
-                    float maxdev = 0.f;
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
                         const int r = rb * RPT + i;
@@ -643,9 +644,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                             unpack2(wg4[j], g0, g1);
                             run[2 * j] = fmaf(g0, kLog2e, run[2 * j]);
                             run[2 * j + 1] = fmaf(g1, kLog2e, run[2 * j + 1]);
-                            const float d0 = run[2 * j] - gm2[2 * j];
-                            const float d1 = run[2 * j + 1] - gm2[2 * j + 1];
-                            maxdev = fmaxf(maxdev, fmaxf(fabsf(d0), fabsf(d1)));
+                            const float d0 = run[2 * j], d1 = run[2 * j + 1];
                             pq[j] = bf16x2_mul(wq4[j], pack_bf16x2(ex2(d0), ex2(d1)));
                             pk[j] = bf16x2_mul(wk4[j], pack_bf16x2(e * ex2(-d0), e * ex2(-d1)));
                         }
@@ -654,7 +653,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                         *reinterpret_cast<uint4 *>(sm + Smem::K + tile_off(r, col0)) =
                             make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
-                    if (maxdev > kGateRangeLog2) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
                 }
                 fence_proxy_async();
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
@@ -774,14 +772,18 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 if (named_sync_or(2, 32 * kEpiWarps, pend)) { failed = true; break; }
                 const float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (row < KC) {
-                    const float f = s_fmid[row] * p_pending;
+                    // S_stored * p is the state itself, then * exp(G_m): the two
+                    // factors are applied one after the other because their product
+                    // (down to e^-160 within the gate range) would underflow
+                    const float fm = s_fmid[row];
 #pragma unroll
                     for (int c0 = 0; c0 < DV; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tS + c0, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint((__uint_as_float(r[i]) * p_pending) * fm);
                         tmem_st32(tS + c0, r);
 #pragma unroll
                         for (int i = 0; i < 32; i += 8)

@@ -187,3 +187,23 @@ def test_chunk_boundary_lengths(algo):
     assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
     assert gpu["device_flags"] == 0
+
+
+@pytest.mark.parametrize("algo", ["chunked", "masked"])
+@pytest.mark.parametrize("base", ["small_bf16", "layer_bf16"])
+def test_gate_range_flag(algo, base):
+    """The tensor-core schedules split each chunk's decay factors at its
+    midpoint and need every half chunk's summed log-gate above -80 per key
+    row: a constant log-gate of -2 (half-chunk sum -128) sets
+    SSE_DEVICE_GATE_RANGE; -1 (sum -64) stays in range and matches the oracle."""
+    w = H_.workload_variant(base, num_heads=2, num_partitions=4, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=5, lengths=[300, 64])
+    for gate, flagged in ((-1.0, False), (-2.0, True)):
+        inp.g = synth.f32_to_bf16_bits(np.full(inp.q.shape, gate, dtype=np.float32))
+        gpu = H_.run_gpu_forward(w, inp, algo=algo)
+        assert (gpu["device_flags"] & 1) == (1 if flagged else 0), (gate, gpu["device_flags"])
+        assert (gpu["device_flags"] & 2) == 0
+        if not flagged:
+            ref = H_.run_oracle_forward(w, inp)
+            assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
+            assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
