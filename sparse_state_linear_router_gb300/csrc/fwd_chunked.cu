@@ -28,10 +28,11 @@
 //       weight) into a ring a few chunks ahead; warp 1 has the TMA engine
 //       gather each chunk's V rows into a double buffer (tile::gather4, four
 //       token rows per copy, 128B swizzle, straight into the operand layout);
-//   transform (8 warps): load the raw g rows of the next chunk into
-//       registers while the current one finishes, and the chunk's q and k
-//       rows; scan g (which releases the epilogue's state-row pass); build Qt
-//       and Kt (128B-swizzled, see umma.cuh);
+//   transform (8 warps): load the chunk's raw q and k rows between the row
+//       sums of its first pass over g, and the next chunk's g rows inside the
+//       decay pass (into the registers each row has just released); scan g
+//       (which releases the epilogue's state-row pass); build Qt and Kt
+//       (128B-swizzled, see umma.cuh);
 //   epilogue (4 warps, one TMEM lane each): rescale the state rows and
 //       write S'; turn A into the masked bf16 P; write O (already e-weighted)
 //       as bf16 partial rows; final state at the end of the segment.  Lane 0
@@ -532,23 +533,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             const int nch = (seg_len + kC - 1) / kC;
             const __nv_bfloat16 *qsrc = static_cast<const __nv_bfloat16 *>(seg_shared && a.qs ? a.qs : a.q);
             const __nv_bfloat16 *ksrc = static_cast<const __nv_bfloat16 *>(seg_shared && a.ks ? a.ks : a.k);
-            uint4 rq[RPT], rk[RPT], rg[RPT], rg_next[RPT];
-            // raw q, k rows of chunk n (16-byte L1-bypassing loads); its
-            // metadata stage was waited for by load_g
-            auto load_qk = [&](int n) {
-                const int *tok = meta_tok((gch + n) % kMetaStages);
-#pragma unroll
-                for (int i = 0; i < RPT; ++i) {
-                    const int t = tok[rb * RPT + i];
-                    if (t >= 0) {
-                        const int64_t ro = ((int64_t)t * H + seg_h) * KC + col0;
-                        rq[i] = ldg_stream(qsrc + ro);
-                        rk[i] = ldg_stream(ksrc + ro);
-                    } else {
-                        rq[i] = rk[i] = make_uint4(0, 0, 0, 0);
-                    }
-                }
-            };
+            uint4 rq[RPT], rk[RPT], rg[RPT];
             // raw g rows of chunk n (its metadata stage must have been written)
             auto load_g = [&](int n, uint4 (&dst)[RPT]) -> bool {
                 const uint32_t g = gch + n;
@@ -567,7 +552,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
                 const int mst = g_n % kMetaStages;
-                load_qk(n);
+                const int *tok_n = meta_tok(mst);
                 // pass 1: per-thread running sums of g over its rows -> block totals
                 // (masking schedule: the rows of tokens that did not select this
                 // partition get gate 0, i.e. no decay)
@@ -581,6 +566,15 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     float run[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
+                        // this row's raw q, k (used by pass 2), issued between the sums
+                        const int t = tok_n[rb * RPT + i];
+                        if (t >= 0) {
+                            const int64_t ro = ((int64_t)t * H + seg_h) * KC + col0;
+                            rq[i] = ldg_stream(qsrc + ro);
+                            rk[i] = ldg_stream(ksrc + ro);
+                        } else {
+                            rq[i] = rk[i] = make_uint4(0, 0, 0, 0);
+                        }
                         const uint32_t w[4] = {rg[i].x, rg[i].y, rg[i].z, rg[i].w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -594,7 +588,13 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     for (int j = 0; j < 8; ++j) s_tot[rb * 128 + col0 + j] = run[j];
                 }
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
-                if (n + 1 < nch) bad = !load_g(n + 1, rg_next);  // a whole chunk of latency hiding
+                // the next chunk's metadata, for its g rows loaded inside pass 2
+                const int *tok_next = nullptr;
+                if (n + 1 < nch) {
+                    const uint32_t g1 = g_n + 1;
+                    bad = !mbar_wait_bounded(bar(kBarMR + g1 % kMetaStages), (g1 / kMetaStages) & 1, kWaitNs);
+                    if (!bad) tok_next = meta_tok(g1 % kMetaStages);
+                }
                 float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
                 if (tt < KC) {  // per-column exclusive scan over row blocks
                     float acc = 0.f, gmid = 0.f;
@@ -648,6 +648,12 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                             pq[j] = bf16x2_mul(wq4[j], pack_bf16x2(ex2(d0), ex2(d1)));
                             pk[j] = bf16x2_mul(wk4[j], pack_bf16x2(e * ex2(-d0), e * ex2(-d1)));
                         }
+                        // row i of the next chunk's g, into the registers just consumed
+                        {
+                            const int t1 = tok_next ? tok_next[r] : -1;
+                            rg[i] = t1 >= 0 ? ldg_stream(gg + ((int64_t)t1 * H + seg_h) * KC + col0)
+                                            : make_uint4(0, 0, 0, 0);
+                        }
                         *reinterpret_cast<uint4 *>(sm + Smem::Q + tile_off(r, col0)) =
                             make_uint4(pq[0], pq[1], pq[2], pq[3]);
                         *reinterpret_cast<uint4 *>(sm + Smem::K + tile_off(r, col0)) =
@@ -657,8 +663,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 fence_proxy_async();
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
                 mbar_arrive(bar(kBarT));
-#pragma unroll
-                for (int i = 0; i < RPT; ++i) rg[i] = rg_next[i];
             }
             if (failed) break;
             gch += nch;
