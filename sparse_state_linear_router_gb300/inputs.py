@@ -36,6 +36,10 @@ __all__ = [
     "DecodeInputs",
     "make_forward_inputs",
     "make_decode_inputs",
+    "FrontEndWorkload",
+    "FRONT_END_WORKLOADS",
+    "FrontEndInputs",
+    "make_front_end_inputs",
     "f32_to_bf16_bits",
     "bf16_bits_to_f32",
 ]
@@ -206,3 +210,69 @@ def make_decode_inputs(w: Workload, step: int, batch: Optional[int] = None) -> D
     sig = w.sigma_router
     logits = _draw(rng, (B, H, N), w.dtype, lambda x: x * sig)
     return DecodeInputs(w, q, k, v, g, logits)
+
+
+# ----------------------------------------------------------------------------
+# Front end (projections from the hidden states)
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class FrontEndWorkload:
+    name: str
+    tokens: int                # T
+    hidden: int                # D
+    num_heads: int
+    key_dim: int               # c
+    value_dim: int             # d
+    num_partitions: int        # N
+    lora_rank: int             # r of the shared partition's Q/K LoRA (0: none)
+
+
+FRONT_END_WORKLOADS = {
+    # ragged token count (not a multiple of 128), c = d = 64, H x N = 32 router columns
+    "front_end_small": FrontEndWorkload("front_end_small", 300, 256, 4, 64, 64, 8, 64),
+    # the 2B-scale layer's tokens (8 x 4096) from hidden size 2048: H16, c=d=128, N8, rank-64 LoRA
+    "front_end_bf16": FrontEndWorkload("front_end_bf16", 32768, 2048, 16, 128, 128, 8, 64),
+}
+
+
+@dataclasses.dataclass
+class FrontEndInputs:
+    """Hidden states and projection weights ([out_features, in_features]
+    layout), bfloat16 bit patterns."""
+    workload: FrontEndWorkload
+    x: np.ndarray              # [T, D]
+    w_q: np.ndarray            # [H*c, D]
+    w_k: np.ndarray            # [H*c, D]
+    w_v: np.ndarray            # [H*d, D]
+    w_g: np.ndarray            # [H*c, D]
+    w_e: np.ndarray            # [H*N, D]
+    a_q: Optional[np.ndarray]  # [r, D]
+    b_q: Optional[np.ndarray]  # [H*c, r]
+    a_k: Optional[np.ndarray]
+    b_k: Optional[np.ndarray]
+
+
+def make_front_end_inputs(w: FrontEndWorkload, seed: int = 0, tokens: Optional[int] = None) -> FrontEndInputs:
+    """Recipe (``default_rng(seed)``, this draw order, bf16 storage):
+    x = normal(0, 1, [T, D]); w_q, w_k, w_v, w_g = normal(0, 1/sqrt(D));
+    w_e = normal(0, 1.5/sqrt(D)) (router logits of std about 1.5);
+    LoRA: a_q, a_k = normal(0, 1/sqrt(D), [r, D]), b_q, b_k =
+    normal(0, 0.5/sqrt(r), [H*c, r])."""
+    rng = np.random.default_rng(seed)
+    T = w.tokens if tokens is None else tokens
+    D, H, c, d, N, r = w.hidden, w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.lora_rank
+    s = 1.0 / np.sqrt(D)
+    x = _draw(rng, (T, D), "bf16", lambda z: z)
+    wq = _draw(rng, (H * c, D), "bf16", lambda z: z * s)
+    wk = _draw(rng, (H * c, D), "bf16", lambda z: z * s)
+    wv = _draw(rng, (H * d, D), "bf16", lambda z: z * s)
+    wg = _draw(rng, (H * c, D), "bf16", lambda z: z * s)
+    we = _draw(rng, (H * N, D), "bf16", lambda z: z * 1.5 * s)
+    aq = bq = ak = bk = None
+    if r:
+        sb = 0.5 / np.sqrt(r)
+        aq = _draw(rng, (r, D), "bf16", lambda z: z * s)
+        bq = _draw(rng, (H * c, r), "bf16", lambda z: z * sb)
+        ak = _draw(rng, (r, D), "bf16", lambda z: z * s)
+        bk = _draw(rng, (H * c, r), "bf16", lambda z: z * sb)
+    return FrontEndInputs(w, x, wq, wk, wv, wg, we, aq, bq, ak, bk)
