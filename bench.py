@@ -585,6 +585,78 @@ def run_native(args):
     return 0
 
 
+def front_end_flops(w) -> int:
+    """Tensor-core flops of one sse_front_end call: the projection GEMMs
+    (q, k, v, g and the router logits) plus the shared LoRA's two factors."""
+    T, D, H, c, d, N, r = w.tokens, w.hidden, w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.lora_rank
+    main = 2 * T * D * H * (3 * c + d + N)
+    lora = (2 * T * D * 2 * r + 2 * T * r * 2 * H * c) if r else 0
+    return main + lora
+
+
+def run_front_end(args):
+    """One JSON line for the front end alone (sse_front_end on the
+    32768-token, D = 2048 workload): tokens/s and its tensor-core roofline."""
+    import torch
+    from sparse_state_linear_router_gb300 import binding
+    ws, rank, local = _dist()
+    if ws > 1:
+        raise SystemExit("--part front_end runs on one GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.FRONT_END_WORKLOADS["front_end_bf16"]
+    inp = synth.make_front_end_inputs(w, seed=0)
+    cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, 2, 1, 1.0, "bf16")
+    dv = {n: (None if getattr(inp, n) is None else binding.to_device(getattr(inp, n), dev))
+          for n in ("x", "w_q", "w_k", "w_v", "w_g", "w_e", "a_q", "b_q", "a_k", "b_k")}
+
+    def call():
+        return binding.front_end(cfg, dv["x"], dv["w_q"], dv["w_k"], dv["w_v"], dv["w_g"], dv["w_e"],
+                                 a_q=dv["a_q"], b_q=dv["b_q"], a_k=dv["a_k"], b_k=dv["b_k"], outs=outs,
+                                 workspace=wsp)
+    outs, wsp = None, None
+    first = call()
+    outs = {n: first[n] for n in ("q", "k", "v", "log_gate", "logits", "q_shared", "k_shared")}
+    wsp = first["workspace"]
+    for _ in range(args.warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.15)
+        ev[0].record(stream)
+        for _ in range(args.steps):
+            call()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.15)
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    st, flags = binding.sse_read_device_status(wsp.data_ptr(), binding._stream())
+    peaks = _peaks()
+    flops = front_end_flops(w)
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": "SSE front end tokens/s (projections, key softmax, log-gate, shared LoRA) on 1 GB300",
+        "value": w.tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} (T={w.tokens}, D={w.hidden}, H{w.num_heads}, c={w.key_dim}, "
+                               f"d={w.value_dim}, N{w.num_partitions}, LoRA rank {w.lora_rank})",
+                   "l2": "weights (33 MB) stay in L2, x (134 MB) and outputs (0.81 GB) exceed it; no flush"},
+        "roofline": {"kernel": "front_end_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16_tflops (MEASURED_PEAKS.json)",
+                     "algorithmic_flops_per_call": flops},
+        "gpu_launches": 2 * args.steps,
+        "device_flags": flags,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,8 +667,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--part", choices=["both", "forward", "decode"], default="both",
-                    help="time the whole step (default) or only one of its two calls")
+    ap.add_argument("--part", choices=["both", "forward", "decode", "front_end"], default="both",
+                    help="time the whole step (default), one of its two calls, or the front end alone")
     ap.add_argument("--fwd-workload", choices=["layer_bf16", "varlen_bf16", "small_bf16"],
                     default=FWD_WORKLOAD, help="forward batch of the step")
     args = ap.parse_args(argv)
@@ -604,6 +676,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.part == "front_end":
+        return run_front_end(args)
     return run_native(args)
 
 

@@ -207,14 +207,50 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
                              float *state, void *out, int32_t *topk_idx, float *topk_w,
                              sse_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * sse_front_end -- the layer's projections from the hidden states
+ * ("Scaling Linear Attention with Sparse State Expansion", eqs. 9-10; the
+ * shared partition's rank-64 Q/K LoRA of section 2.5; GLA's diagonal gate).
+ * Per token t and head h, with y = x W^T for each weight W:
+ *   q = y_q;  k = softmax(y_k) over the c keys;  v = y_v;
+ *   log_gate = logsigmoid(y_g) * gate_inv_tau   (GLA: alpha = sigmoid^(1/tau));
+ *   router_logits = y_e  (the router softmax and top-k stay in sse_route /
+ *   sse_forward);
+ *   with the LoRA factors: q_shared = y_q + (x A_q^T) B_q^T and
+ *   k_shared = softmax(y_k + (x A_k^T) B_k^T).
+ * The outputs are exactly the token tensors sse_forward and sse_decode_step
+ * take.  bf16 only (cfg->dtype == SSE_BF16); fp32 accumulation on the tensor
+ * cores; one rounding of x A to bf16 before the LoRA's second factor.
+ *
+ *   x                  [T, D] bf16 (D = hidden, a multiple of 64, >= 64)
+ *   w_q, w_k, w_g      [H*c, D]      w_v [H*d, D]      w_e [H*N, D]
+ *   a_q, a_k           [64, D]       b_q, b_k [H*c, 64]   (all four NULL: no LoRA)
+ *   q, k, log_gate, q_shared, k_shared [T, H, c]   v [T, H, d]
+ *   router_logits      [T, H, N]
+ * Weights use the [out_features, in_features] layout (row n holds the D
+ * weights of output n).  All pointers are device pointers, 16-byte aligned;
+ * q_shared / k_shared are required with the LoRA factors and ignored without.
+ * Supported: c, d in {64, 128}; H*N a multiple of 16 and at most 256; T >= 128.
+ * Workspace: sse_front_end_workspace_size bytes (256-byte aligned); its first
+ * word holds the device-check flags (sse_read_device_status reads them).
+ * ------------------------------------------------------------------------- */
+size_t sse_front_end_workspace_size(const sse_config_t *cfg, int32_t hidden, int64_t total_tokens);
+
+sse_status_t sse_front_end(const sse_config_t *cfg, int32_t hidden, int64_t total_tokens, const void *x,
+                           const void *w_q, const void *w_k, const void *w_v, const void *w_g,
+                           const void *w_e, const void *a_q, const void *b_q, const void *a_k,
+                           const void *b_k, float gate_inv_tau, void *q, void *k, void *v,
+                           void *log_gate, void *router_logits, void *q_shared, void *k_shared,
+                           void *workspace, size_t workspace_bytes, sse_stream_t stream);
+
 /* Device-side check flags (bit mask).
  *   SSE_DEVICE_GATE_RANGE: a chunk's log-gate sum left the chunked path's range
  *   SSE_DEVICE_TIMEOUT:    a bounded wait on the tensor core expired; the
  *                          affected segments stopped early (results invalid) */
 enum { SSE_DEVICE_GATE_RANGE = 1, SSE_DEVICE_TIMEOUT = 2 };
 
-/* Reads the device-check flags recorded by the last sse_forward that used
- * `workspace` (each sse_forward clears them first).  Synchronizes `stream`.
+/* Reads the device-check flags recorded by the last sse_forward or
+ * sse_front_end that used `workspace` (each call clears them first).  Synchronizes `stream`.
  * *flags receives the bit mask; returns SSE_ERR_DEVICE if any flag is set,
  * SSE_ERR_CUDA if the copy fails. */
 sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_t stream);

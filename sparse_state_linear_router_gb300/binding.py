@@ -27,7 +27,7 @@ _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_A
 # Every extern "C" symbol that include/sse.h declares.
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
             "sse_route_noalloc", "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
-            "sse_read_device_status")
+            "sse_front_end_workspace_size", "sse_front_end", "sse_read_device_status")
 
 
 class sse_config_t(ctypes.Structure):
@@ -76,6 +76,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                       P, ctypes.POINTER(i32)]
     lib.sse_decode_step.restype = ctypes.c_int
     lib.sse_decode_step.argtypes = [cfgp, P, P, P, P, P, P, P, i32, P, P, P, P, P]
+    lib.sse_front_end_workspace_size.restype = sz
+    lib.sse_front_end_workspace_size.argtypes = [cfgp, i32, i64]
+    lib.sse_front_end.restype = ctypes.c_int
+    lib.sse_front_end.argtypes = [cfgp, i32, i64, P, P, P, P, P, P, P, P, P, P, ctypes.c_float,
+                                  P, P, P, P, P, P, P, P, sz, P]
     lib.sse_read_device_status.restype = ctypes.c_int
     lib.sse_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
     _lib = lib
@@ -134,6 +139,18 @@ def sse_decode_step(cfg, q, k, v, log_gate, logits, q_shared, k_shared, batch, s
                     topk_idx, topk_w, stream) -> int:
     return load().sse_decode_step(ctypes.byref(cfg), q, k, v, log_gate, logits, q_shared, k_shared,
                                   batch, state, out, topk_idx, topk_w, stream)
+
+
+def sse_front_end_workspace_size(cfg: sse_config_t, hidden: int, total_tokens: int) -> int:
+    return int(load().sse_front_end_workspace_size(ctypes.byref(cfg), hidden, total_tokens))
+
+
+def sse_front_end(cfg, hidden, total_tokens, x, w_q, w_k, w_v, w_g, w_e, a_q, b_q, a_k, b_k,
+                  gate_inv_tau, q, k, v, log_gate, logits, q_shared, k_shared, workspace,
+                  workspace_bytes, stream) -> int:
+    return load().sse_front_end(ctypes.byref(cfg), hidden, total_tokens, x, w_q, w_k, w_v, w_g, w_e,
+                                a_q, b_q, a_k, b_k, float(gate_inv_tau), q, k, v, log_gate, logits,
+                                q_shared, k_shared, workspace, workspace_bytes, stream)
 
 
 def sse_read_device_status(workspace, stream):
@@ -242,6 +259,30 @@ def decode_step(cfg, state, q, k, v, log_gate, logits, *, q_shared=None, k_share
                            _ptr(q_shared), _ptr(k_shared), B, _ptr(state), _ptr(out), _ptr(idx),
                            _ptr(w), _stream()), "sse_decode_step")
     return {"out": out, "topk_idx": idx, "topk_w": w}
+
+
+def front_end(cfg, x, w_q, w_k, w_v, w_g, w_e, *, a_q=None, b_q=None, a_k=None, b_k=None,
+              gate_inv_tau=1.0 / 16.0, outs=None, workspace=None):
+    """Projections from the hidden states x [T, D] (bf16 device tensors);
+    returns dict(q, k, v, log_gate, logits, q_shared, k_shared, workspace)."""
+    import torch
+    T, D = x.shape
+    H, c, d, N = cfg.num_heads, cfg.key_dim, cfg.value_dim, cfg.num_partitions
+    dev = x.device
+    lora = a_q is not None
+    if outs is None:
+        e = lambda w: torch.empty((T, H, w), dtype=torch.bfloat16, device=dev)  # noqa: E731
+        outs = {"q": e(c), "k": e(c), "v": e(d), "log_gate": e(c), "logits": e(N),
+                "q_shared": e(c) if lora else None, "k_shared": e(c) if lora else None}
+    if workspace is None:
+        workspace = torch.empty(max(sse_front_end_workspace_size(cfg, D, T), 256), dtype=torch.uint8,
+                                device=dev)
+    _check(sse_front_end(cfg, D, T, _ptr(x), _ptr(w_q), _ptr(w_k), _ptr(w_v), _ptr(w_g), _ptr(w_e),
+                         _ptr(a_q), _ptr(b_q), _ptr(a_k), _ptr(b_k), gate_inv_tau, _ptr(outs["q"]),
+                         _ptr(outs["k"]), _ptr(outs["v"]), _ptr(outs["log_gate"]), _ptr(outs["logits"]),
+                         _ptr(outs["q_shared"]), _ptr(outs["k_shared"]), _ptr(workspace), workspace.numel(),
+                         _stream()), "sse_front_end")
+    return dict(outs, workspace=workspace)
 
 
 def to_device(arr, device="cuda"):

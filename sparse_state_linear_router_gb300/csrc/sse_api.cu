@@ -278,6 +278,68 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
     return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
 }
 
+size_t sse_front_end_workspace_size(const sse_config_t *cfg, int32_t hidden, int64_t total_tokens) {
+    if (!cfg || hidden < 0 || total_tokens < 0) return 0;
+    Carver cv(nullptr);
+    cv.take<int32_t>(64);                                          // device-check flags
+    cv.take<uint16_t>((size_t)total_tokens * 2 * sse::kLoraRank);  // x A_q | x A_k, bf16
+    return (cv.off + 255) & ~size_t(255);
+}
+
+sse_status_t sse_front_end(const sse_config_t *cfg, int32_t hidden, int64_t total_tokens, const void *x,
+                           const void *w_q, const void *w_k, const void *w_v, const void *w_g,
+                           const void *w_e, const void *a_q, const void *b_q, const void *a_k,
+                           const void *b_k, float gate_inv_tau, void *q, void *k, void *v,
+                           void *log_gate, void *router_logits, void *q_shared, void *k_shared,
+                           void *workspace, size_t workspace_bytes, sse_stream_t stream) {
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if (hidden < 0 || total_tokens < 0 || !std::isfinite(gate_inv_tau)) return SSE_ERR_INVALID_ARG;
+    if (!sse::front_end_supported(*cfg, hidden)) return SSE_ERR_UNSUPPORTED;
+    // row tiles of 128 tokens; every tile index fits in 32 bits
+    if (total_tokens > 0 && total_tokens < 128) return SSE_ERR_UNSUPPORTED;
+    if (total_tokens / 128 * (4 * (int64_t)cfg->num_heads + 1) >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    const bool lora = a_q || b_q || a_k || b_k;
+    if (lora && !(a_q && b_q && a_k && b_k && q_shared && k_shared)) return SSE_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!x || !w_q || !w_k || !w_v || !w_g || !w_e || !q || !k || !v || !log_gate ||
+                             !router_logits))
+        return SSE_ERR_INVALID_ARG;
+    for (const void *p : std::initializer_list<const void *>{x, w_q, w_k, w_v, w_g, w_e, a_q, b_q, a_k, b_k, q, k,
+                                                             v, log_gate, router_logits, q_shared, k_shared})
+        if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
+    const size_t need = sse_front_end_workspace_size(cfg, hidden, total_tokens);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return SSE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Carver cv(workspace);
+    sse::FrontEndArgs f{};
+    f.flags = cv.take<int32_t>(64);
+    f.xa = cv.take<uint16_t>((size_t)total_tokens * 2 * sse::kLoraRank);
+    if (cudaMemsetAsync(f.flags, 0, 64 * sizeof(int32_t), s) != cudaSuccess) return SSE_ERR_CUDA;
+    f.T = total_tokens;
+    f.hidden = hidden;
+    f.gate_inv_tau = gate_inv_tau;
+    f.x = x;
+    f.w_q = w_q;
+    f.w_k = w_k;
+    f.w_v = w_v;
+    f.w_g = w_g;
+    f.w_e = w_e;
+    f.a_q = lora ? a_q : nullptr;
+    f.b_q = lora ? b_q : nullptr;
+    f.a_k = lora ? a_k : nullptr;
+    f.b_k = lora ? b_k : nullptr;
+    f.q = q;
+    f.k = k;
+    f.v = v;
+    f.g = log_gate;
+    f.logits = router_logits;
+    f.q_shared = lora ? q_shared : nullptr;
+    f.k_shared = lora ? k_shared : nullptr;
+    int launches = 0;
+    return sse::launch_front_end(*cfg, f, s, &launches) == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
+
 sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_t stream) {
     if (!workspace || !flags || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SSE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -248,4 +248,19 @@ cudaError_t launch_decode(const sse_config_t &cfg, const void *q, const void *k,
                           int32_t batch, float *state, void *out, int32_t *topk_idx,
                           float *topk_w, cudaStream_t stream);
 
+// Front end (projections from the hidden states); pointers as in sse_front_end.
+struct FrontEndArgs {
+    int64_t T;
+    int32_t hidden;
+    float gate_inv_tau;
+    const void *x, *w_q, *w_k, *w_v, *w_g, *w_e, *a_q, *b_q, *a_k, *b_k;
+    void *q, *k, *v, *g, *logits, *q_shared, *k_shared;
+    void *xa;        // [T, 128] bf16 scratch: x A_q | x A_k
+    int32_t *flags;
+};
+constexpr int kLoraRank = 64;
+bool front_end_supported(const sse_config_t &cfg, int32_t hidden);
+// Adds the number of kernels it launched to *launches.
+cudaError_t launch_front_end(const sse_config_t &cfg, const FrontEndArgs &f, cudaStream_t stream, int *launches);
+
 }  // namespace sse

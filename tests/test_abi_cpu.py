@@ -109,3 +109,33 @@ def test_workspace_sizes(lib):
     assert b.sse_forward_workspace_size(_cfg(top_k=0), 100, 2) == 0
     assert b.sse_route_workspace_size(cfg, 100, 2) > 0
     assert b.sse_route_workspace_size(cfg, 0, 1) > 0
+
+
+def _fe(cfg, D=256, T=300, x=FAKE, a_q=None, qs=None, ws=FAKE, ws_bytes=1 << 40, tau=1.0 / 16):
+    from sparse_state_linear_router_gb300 import binding
+    lora = a_q is not None
+    return binding.sse_front_end(cfg, D, T, x, FAKE, FAKE, FAKE, FAKE, FAKE, a_q, FAKE if lora else None,
+                                 FAKE if lora else None, FAKE if lora else None, tau, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, qs, qs, ws, ws_bytes, None)
+
+
+def test_front_end_rejects_bad_arguments(lib):
+    from sparse_state_linear_router_gb300 import binding as b
+    cfg = _cfg()
+    assert _fe(_cfg(dtype="f32")) == b.SSE_ERR_UNSUPPORTED
+    assert _fe(cfg, D=100) == b.SSE_ERR_UNSUPPORTED            # hidden not a multiple of 64
+    assert _fe(_cfg(key_dim=96)) == b.SSE_ERR_UNSUPPORTED
+    assert _fe(_cfg(num_heads=1, num_partitions=8)) == b.SSE_ERR_UNSUPPORTED  # H*N = 8 columns
+    assert _fe(_cfg(num_heads=64, num_partitions=8)) == b.SSE_ERR_UNSUPPORTED  # H*N = 512 columns
+    assert _fe(cfg, T=100) == b.SSE_ERR_UNSUPPORTED             # fewer than one 128-token tile
+    assert _fe(cfg, T=-1) == b.SSE_ERR_INVALID_ARG
+    assert _fe(cfg, tau=float("inf")) == b.SSE_ERR_INVALID_ARG
+    assert _fe(cfg, x=None) == b.SSE_ERR_INVALID_ARG
+    assert _fe(cfg, x=FAKE + 8) == b.SSE_ERR_INVALID_ARG        # misaligned
+    assert _fe(cfg, a_q=FAKE, qs=None) == b.SSE_ERR_INVALID_ARG  # LoRA without shared outputs
+    assert _fe(cfg, ws=None) == b.SSE_ERR_WORKSPACE
+    assert _fe(cfg, ws=FAKE + 128) == b.SSE_ERR_WORKSPACE
+    assert _fe(cfg, ws_bytes=64) == b.SSE_ERR_WORKSPACE
+    small = b.sse_front_end_workspace_size(cfg, 256, 300)
+    assert small % 256 == 0 and small >= 256 + 300 * 128 * 2
+    assert b.sse_front_end_workspace_size(cfg, 256, 3000) > small
