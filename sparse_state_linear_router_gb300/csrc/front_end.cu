@@ -10,8 +10,12 @@
 // operand is K-major.
 //
 // One persistent kernel computes output tiles of 128 tokens x one projection
-// block (one head's q, k, v or g, or all heads' router logits), K = D in
-// steps of 64 (one 128-byte swizzle atom):
+// block, K = D in steps of 64 (one 128-byte swizzle atom).  Blocks: one
+// head's [v | g] (N = d + c), its q and k (N = c each, with the LoRA) or
+// [q | k] (N = 2c, without it), and all heads' router logits.  The wide blocks
+// halve the x tiles read per output and the shared-memory operand traffic per
+// flop (an N = 128 MMA reads as many operand bytes per flop as the shared
+// memory delivers).
 //   warp 0 (lane 0): TMA loads of each step's x tile and weight tile into a
 //       four-stage ring;
 //   warp 1 (lane 0): the tcgen05 MMAs (M = 128, N = block width, K = 16) into
@@ -53,9 +57,10 @@ enum { kBarFull = 0, kBarEmpty = kStages, kBarAccF = 2 * kStages, kBarAccE = 2 *
 constexpr uint32_t kSmemBar = kStages * kStageBytes;
 constexpr size_t kSmemBytes = kSmemBar + 8 * kNumBars + 16 + 1024;
 
-// Block kinds.  Phase 1: one head's q, k, v, g, or all heads' logits;
-// phase 0: the two LoRA first factors x A_q, x A_k.
-enum Kind { kQ = 0, kK, kV, kG, kE, kXAq, kXAk };
+// Block kinds.  Phase 1: one head's q and k (with the LoRA) or [q | k]
+// (without), its [v | g], or all heads' logits; phase 0: the two LoRA first
+// factors x A_q, x A_k.
+enum Kind { kQ = 0, kK, kQK, kVG, kE, kXAq, kXAk };
 
 struct FeArgs {
     int32_t T, D, H, c, d, Np, has_lora, phase;
@@ -68,32 +73,44 @@ struct FeMaps {
     CUtensorMap x, xa, wq, wk, wv, wg, we, aq, ak, bq, bk;
 };
 
+// n = n1 + n2: a pair block's B tile stacks n1 rows of its first weight and
+// n2 rows of its second.
 struct Tile {
-    int row0, kind, h, n, wrow0;
+    int row0, kind, h, n, n1;
 };
 
-__device__ __forceinline__ int num_col_blocks(const FeArgs &a) { return a.phase == 0 ? 2 : 4 * a.H + 1; }
+// phase 1: with the LoRA q_0..q_{H-1}, k_0.., [v|g]_0.., logits (3H + 1
+// blocks); without it [q|k]_0.., [v|g]_0.., logits (2H + 1)
+__device__ __forceinline__ int num_col_blocks(const FeArgs &a) {
+    return a.phase == 0 ? 2 : (a.has_lora ? 3 : 2) * a.H + 1;
+}
 
 __device__ __forceinline__ Tile decode_tile(const FeArgs &a, int tile) {
     const int ncol = num_col_blocks(a);
     Tile t;
     t.row0 = (tile / ncol) * kRows;
     const int cb = tile % ncol;
+    t.h = 0;
     if (a.phase == 0) {
         t.kind = kXAq + cb;
-        t.h = 0;
-        t.n = 64;
-        t.wrow0 = 0;
-    } else if (cb == 4 * a.H) {
+        t.n = t.n1 = 64;
+    } else if (cb == ncol - 1) {
         t.kind = kE;
-        t.h = 0;
-        t.n = a.H * a.Np;
-        t.wrow0 = 0;
+        t.n = t.n1 = a.H * a.Np;
     } else {
-        t.kind = cb / a.H;
+        const int grp = cb / a.H;
         t.h = cb % a.H;
-        t.n = t.kind == kV ? a.d : a.c;
-        t.wrow0 = t.h * t.n;
+        if (a.has_lora) t.kind = grp == 0 ? kQ : grp == 1 ? kK : kVG;
+        else t.kind = grp == 0 ? kQK : kVG;
+        if (t.kind == kVG) {
+            t.n1 = a.d;
+            t.n = a.d + a.c;
+        } else if (t.kind == kQK) {
+            t.n1 = a.c;
+            t.n = 2 * a.c;
+        } else {
+            t.n = t.n1 = a.c;
+        }
     }
     return t;
 }
@@ -233,9 +250,13 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
         if (lane == 0) {
             for (int tile = blockIdx.x; tile < num_tiles && !failed; tile += gridDim.x) {
                 const Tile t = decode_tile(a, tile);
-                const CUtensorMap *wmap = t.kind == kQ ? &maps.wq : t.kind == kK ? &maps.wk
-                                        : t.kind == kV ? &maps.wv : t.kind == kG ? &maps.wg
-                                        : t.kind == kE ? &maps.we : t.kind == kXAq ? &maps.aq : &maps.ak;
+                // first (and, for pair blocks, second) weight of the block, with the
+                // row of its first output
+                const CUtensorMap *w1 = t.kind == kQ || t.kind == kQK ? &maps.wq : t.kind == kK ? &maps.wk
+                                      : t.kind == kVG ? &maps.wv : t.kind == kE ? &maps.we
+                                      : t.kind == kXAq ? &maps.aq : &maps.ak;
+                const CUtensorMap *w2 = t.kind == kQK ? &maps.wk : t.kind == kVG ? &maps.wg : nullptr;
+                const int r1 = t.kind == kVG ? t.h * a.d : t.h * a.c, r2 = t.h * a.c;
                 const int nk = nk_main + (has_lora_step(a, t) ? 1 : 0);
                 for (int ks = 0; ks < nk; ++ks, ++it) {
                     const int s = it % kStages;
@@ -248,10 +269,11 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
                     mbar_arrive_expect_tx(bar(kBarFull + s), kATile + (uint32_t)t.n * 128u);
                     if (ks < nk_main) {
                         tma_load_2d(&maps.x, sa, bar(kBarFull + s), ks * kKStep, t.row0);
-                        tma_load_2d(wmap, sb, bar(kBarFull + s), ks * kKStep, t.wrow0);
+                        tma_load_2d(w1, sb, bar(kBarFull + s), ks * kKStep, r1);
+                        if (w2) tma_load_2d(w2, sb + (uint32_t)t.n1 * 128u, bar(kBarFull + s), ks * kKStep, r2);
                     } else {  // the LoRA step: (x A) [128 x 64] times B rows of this head
                         tma_load_2d(&maps.xa, sa, bar(kBarFull + s), t.kind == kQ ? 0 : 64, t.row0);
-                        tma_load_2d(t.kind == kQ ? &maps.bq : &maps.bk, sb, bar(kBarFull + s), 0, t.wrow0);
+                        tma_load_2d(t.kind == kQ ? &maps.bq : &maps.bk, sb, bar(kBarFull + s), 0, r1);
                     }
                 }
             }
@@ -323,12 +345,13 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
                 epi_softmax(tacc, t.n, false, live ? a.k + tok * hc + t.h * a.c : nullptr);
                 if (lora) epi_softmax(tacc, t.n, true, live ? a.ks + tok * hc + t.h * a.c : nullptr);
                 break;
-            case kV:
-                epi_plain(tacc, t.n, false, false, 0.f,
-                          live ? a.v + tok * (int64_t)a.H * a.d + t.h * a.d : nullptr);
+            case kQK:  // columns [0, c): q; [c, 2c): the key logits
+                epi_plain(tacc, a.c, false, false, 0.f, live ? a.q + tok * hc + t.h * a.c : nullptr);
+                epi_softmax(tacc + a.c, a.c, false, live ? a.k + tok * hc + t.h * a.c : nullptr);
                 break;
-            case kG:
-                epi_plain(tacc, t.n, false, true, a.gate_inv_tau, live ? a.g + tok * hc + t.h * a.c : nullptr);
+            case kVG:  // columns [0, d): v; [d, d + c): the gate
+                epi_plain(tacc, a.d, false, false, 0.f, live ? a.v + tok * (int64_t)a.H * a.d + t.h * a.d : nullptr);
+                epi_plain(tacc + a.d, a.c, false, true, a.gate_inv_tau, live ? a.g + tok * hc + t.h * a.c : nullptr);
                 break;
             case kE:
                 epi_plain(tacc, t.n, false, false, 0.f, live ? a.logits + tok * (int64_t)t.n : nullptr);
@@ -435,7 +458,7 @@ cudaError_t launch_front_end(const sse_config_t &cfg, const FrontEndArgs &f, cud
     const int64_t row_tiles = (T + kRows - 1) / kRows;
     for (int phase = lora ? 0 : 1; phase <= 1; ++phase) {
         a.phase = phase;
-        const int64_t tiles = row_tiles * (phase == 0 ? 2 : 4 * H + 1);
+        const int64_t tiles = row_tiles * (phase == 0 ? 2 : (lora ? 3 : 2) * H + 1);
         const int grid = (int)std::min<int64_t>(tiles, sms);
         front_end_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, m, (int32_t)tiles);
         cudaError_t e = cudaGetLastError();
