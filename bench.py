@@ -19,7 +19,7 @@ sampled during the timed region, and the fp64 CPU oracle timed on a bounded
 sample of the same workload (cpu_baseline).
 
 ``--impl reference`` times the CPU oracle alone on bounded samples of the same
-workload (the reference arm of this build: the pages publish no code).
+workload (the reference arm: the pages publish no code to run).
 Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
 collective on the data path); rank 0 prints the line.
 """
