@@ -11,16 +11,17 @@
 //
 // One persistent kernel computes output tiles of 128 tokens x one projection
 // block, K = D in steps of 64 (one 128-byte swizzle atom).  Blocks: one
-// head's [v | g] (N = d + c), its q and k (N = c each, with the LoRA) or
-// [q | k] (N = 2c, without it), and all heads' router logits.  The wide blocks
-// halve the x tiles read per output and the shared-memory operand traffic per
-// flop (an N = 128 MMA reads as many operand bytes per flop as the shared
-// memory delivers).
+// head's [q | k] (N = 2c) or [v | g] (N = d + c), and all heads' router
+// logits.  The wide blocks halve the x tiles read per output and the
+// shared-memory operand traffic per flop (an N = 128 MMA reads as many
+// operand bytes per flop as the shared memory delivers).
 //   warp 0 (lane 0): TMA loads of each step's x tile and weight tile into a
 //       four-stage ring;
 //   warp 1 (lane 0): the tcgen05 MMAs (M = 128, N = block width, K = 16) into
-//       one of two TMEM accumulators; q and k tiles take one more step, (x A)
-//       times B, into a second accumulator region (the LoRA term);
+//       one of two TMEM accumulators; once the epilogue has read q and k of a
+//       [q | k] tile, two more K steps add the LoRA terms (x A_q) B_q and
+//       (x A_k) B_k onto the same columns (issued half way through the next
+//       tile's mainloop), and the epilogue reads q^s and k^s;
 //   warps 2-5 (one TMEM lane = one token each): the block's epilogue
 //       (identity, key softmax, log-sigmoid gate) from TMEM to bf16 outputs,
 //       while the MMAs of the next tile fill the other accumulator.
@@ -53,14 +54,14 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum { kBarFull = 0, kBarEmpty = kStages, kBarAccF = 2 * kStages, kBarAccE = 2 * kStages + 2,
-       kNumBars = 2 * kStages + 4 };
+       kBarAccM = 2 * kStages + 4,  // first read-out of a [q | k] tile done (before its LoRA steps)
+       kNumBars = 2 * kStages + 6 };
 constexpr uint32_t kSmemBar = kStages * kStageBytes;
 constexpr size_t kSmemBytes = kSmemBar + 8 * kNumBars + 16 + 1024;
 
-// Block kinds.  Phase 1: one head's q and k (with the LoRA) or [q | k]
-// (without), its [v | g], or all heads' logits; phase 0: the two LoRA first
-// factors x A_q, x A_k.
-enum Kind { kQ = 0, kK, kQK, kVG, kE, kXAq, kXAk };
+// Block kinds.  Phase 1: one head's [q | k] or [v | g], or all heads' logits;
+// phase 0: the two LoRA first factors x A_q, x A_k.
+enum Kind { kQK = 0, kVG, kE, kXAq, kXAk };
 
 struct FeArgs {
     int32_t T, D, H, c, d, Np, has_lora, phase;
@@ -79,11 +80,8 @@ struct Tile {
     int row0, kind, h, n, n1;
 };
 
-// phase 1: with the LoRA q_0..q_{H-1}, k_0.., [v|g]_0.., logits (3H + 1
-// blocks); without it [q|k]_0.., [v|g]_0.., logits (2H + 1)
-__device__ __forceinline__ int num_col_blocks(const FeArgs &a) {
-    return a.phase == 0 ? 2 : (a.has_lora ? 3 : 2) * a.H + 1;
-}
+// phase 1: [q|k]_0..[q|k]_{H-1}, [v|g]_0.., logits (2H + 1 blocks)
+__device__ __forceinline__ int num_col_blocks(const FeArgs &a) { return a.phase == 0 ? 2 : 2 * a.H + 1; }
 
 __device__ __forceinline__ Tile decode_tile(const FeArgs &a, int tile) {
     const int ncol = num_col_blocks(a);
@@ -98,25 +96,16 @@ __device__ __forceinline__ Tile decode_tile(const FeArgs &a, int tile) {
         t.kind = kE;
         t.n = t.n1 = a.H * a.Np;
     } else {
-        const int grp = cb / a.H;
+        t.kind = cb < a.H ? kQK : kVG;
         t.h = cb % a.H;
-        if (a.has_lora) t.kind = grp == 0 ? kQ : grp == 1 ? kK : kVG;
-        else t.kind = grp == 0 ? kQK : kVG;
-        if (t.kind == kVG) {
-            t.n1 = a.d;
-            t.n = a.d + a.c;
-        } else if (t.kind == kQK) {
-            t.n1 = a.c;
-            t.n = 2 * a.c;
-        } else {
-            t.n = t.n1 = a.c;
-        }
+        t.n1 = t.kind == kVG ? a.d : a.c;
+        t.n = t.n1 + a.c;
     }
     return t;
 }
 
 __device__ __forceinline__ bool has_lora_step(const FeArgs &a, const Tile &t) {
-    return a.has_lora && (t.kind == kQ || t.kind == kK);
+    return a.has_lora && t.kind == kQK;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
@@ -158,29 +147,21 @@ __device__ __forceinline__ void store32(__nv_bfloat16 *dst, const float (&f)[32]
                        pack_bf16x2(f[i + 4], f[i + 5]), pack_bf16x2(f[i + 6], f[i + 7]));
 }
 
-// 32 accumulator columns of this lane, plus (lora) the same columns of the
-// LoRA region.
-__device__ __forceinline__ void load_acc(uint32_t tacc, int c0, bool lora, float (&f)[32]) {
+// 32 accumulator columns of this lane.
+__device__ __forceinline__ void load_acc(uint32_t tacc, int c0, float (&f)[32]) {
     uint32_t r[32];
     tmem_ld32(tacc + c0, r);
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
-    if (lora) {
-        tmem_ld32(tacc + 128 + c0, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] += __uint_as_float(r[i]);
-    }
 }
 
 // Plain block: y -> bf16 (optionally the gate transform).  n is a multiple of
 // 16 (the router block can end half way through a 32-column load).
-__device__ __forceinline__ void epi_plain(uint32_t tacc, int n, bool lora, bool gate, float inv_tau,
-                                          __nv_bfloat16 *dst) {
+__device__ __forceinline__ void epi_plain(uint32_t tacc, int n, bool gate, float inv_tau, __nv_bfloat16 *dst) {
     for (int c0 = 0; c0 < n; c0 += 32) {
         float f[32];
-        load_acc(tacc, c0, lora, f);
+        load_acc(tacc, c0, f);
         if (gate) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = log_sigmoid(f[i]) * inv_tau;
@@ -190,11 +171,11 @@ __device__ __forceinline__ void epi_plain(uint32_t tacc, int n, bool lora, bool 
 }
 
 // Key block: softmax over the row's n columns -> bf16.
-__device__ __forceinline__ void epi_softmax(uint32_t tacc, int n, bool lora, __nv_bfloat16 *dst) {
+__device__ __forceinline__ void epi_softmax(uint32_t tacc, int n, __nv_bfloat16 *dst) {
     float m = -INFINITY;
     for (int c0 = 0; c0 < n; c0 += 32) {
         float f[32];
-        load_acc(tacc, c0, lora, f);
+        load_acc(tacc, c0, f);
 #pragma unroll
         for (int i = 0; i < 32; ++i) m = fmaxf(m, f[i]);
     }
@@ -202,14 +183,14 @@ __device__ __forceinline__ void epi_softmax(uint32_t tacc, int n, bool lora, __n
     float s = 0.f;
     for (int c0 = 0; c0 < n; c0 += 32) {
         float f[32];
-        load_acc(tacc, c0, lora, f);
+        load_acc(tacc, c0, f);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s += ex2(fmaf(f[i], kLog2e, -mb));
     }
     const float inv = 1.f / s;
     for (int c0 = 0; c0 < n; c0 += 32) {
         float f[32];
-        load_acc(tacc, c0, lora, f);
+        load_acc(tacc, c0, f);
 #pragma unroll
         for (int i = 0; i < 32; ++i) f[i] = ex2(fmaf(f[i], kLog2e, -mb)) * inv;
         if (dst) store32(dst + c0, f);
@@ -234,6 +215,7 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarAccF + b), 1);
             mbar_init(bar(kBarAccE + b), 128);
+            mbar_init(bar(kBarAccM + b), 128);
         }
         mbar_fence_init();
     }
@@ -244,39 +226,63 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
     const int nk_main = a.D / kKStep;
     bool failed = false;
 
+    // The LoRA steps of a [q | k] tile (two K steps of 64: (x A_q) B_q onto the
+    // q columns, (x A_k) B_k onto the k columns) run after the epilogue has
+    // read q and k, half way through the next tile's mainloop (or right after
+    // the tile when it is this CTA's last).  Producer and MMA warp walk the same
+    // stage sequence.
+    const int lora_at = nk_main / 2;
+
     if (warp == 0) {
         // ---- TMA producer ----------------------------------------------------
         uint32_t it = 0;
         if (lane == 0) {
+            auto next_stage = [&](uint32_t bytes) -> int {  // -1 on timeout
+                const int s = it % kStages;
+                if (it >= kStages && !mbar_wait_bounded(bar(kBarEmpty + s), ((it / kStages) - 1) & 1, kWaitNs))
+                    return -1;
+                mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
+                ++it;
+                return s;
+            };
+            auto emit_lora = [&](const Tile &t) -> bool {
+                for (int half = 0; half < 2; ++half) {
+                    const int s = next_stage(kATile + (uint32_t)a.c * 128u);
+                    if (s < 0) return false;
+                    const uint32_t sa = smem_u32(sm + s * kStageBytes), sb = sa + kATile;
+                    tma_load_2d(&maps.xa, sa, bar(kBarFull + s), half * 64, t.row0);
+                    tma_load_2d(half ? &maps.bk : &maps.bq, sb, bar(kBarFull + s), 0, t.h * a.c);
+                }
+                return true;
+            };
+            bool pend = false;
+            Tile tp{};
             for (int tile = blockIdx.x; tile < num_tiles && !failed; tile += gridDim.x) {
                 const Tile t = decode_tile(a, tile);
                 // first (and, for pair blocks, second) weight of the block, with the
                 // row of its first output
-                const CUtensorMap *w1 = t.kind == kQ || t.kind == kQK ? &maps.wq : t.kind == kK ? &maps.wk
-                                      : t.kind == kVG ? &maps.wv : t.kind == kE ? &maps.we
-                                      : t.kind == kXAq ? &maps.aq : &maps.ak;
+                const CUtensorMap *w1 = t.kind == kQK ? &maps.wq : t.kind == kVG ? &maps.wv
+                                      : t.kind == kE ? &maps.we : t.kind == kXAq ? &maps.aq : &maps.ak;
                 const CUtensorMap *w2 = t.kind == kQK ? &maps.wk : t.kind == kVG ? &maps.wg : nullptr;
                 const int r1 = t.kind == kVG ? t.h * a.d : t.h * a.c, r2 = t.h * a.c;
-                const int nk = nk_main + (has_lora_step(a, t) ? 1 : 0);
-                for (int ks = 0; ks < nk; ++ks, ++it) {
-                    const int s = it % kStages;
-                    if (it >= kStages &&
-                        !mbar_wait_bounded(bar(kBarEmpty + s), ((it / kStages) - 1) & 1, kWaitNs)) {
-                        failed = true;
-                        break;
+                for (int ks = 0; ks < nk_main; ++ks) {
+                    if (pend && ks == lora_at) {
+                        if (!emit_lora(tp)) { failed = true; break; }
+                        pend = false;
                     }
+                    const int s = next_stage(kATile + (uint32_t)t.n * 128u);
+                    if (s < 0) { failed = true; break; }
                     const uint32_t sa = smem_u32(sm + s * kStageBytes), sb = sa + kATile;
-                    mbar_arrive_expect_tx(bar(kBarFull + s), kATile + (uint32_t)t.n * 128u);
-                    if (ks < nk_main) {
-                        tma_load_2d(&maps.x, sa, bar(kBarFull + s), ks * kKStep, t.row0);
-                        tma_load_2d(w1, sb, bar(kBarFull + s), ks * kKStep, r1);
-                        if (w2) tma_load_2d(w2, sb + (uint32_t)t.n1 * 128u, bar(kBarFull + s), ks * kKStep, r2);
-                    } else {  // the LoRA step: (x A) [128 x 64] times B rows of this head
-                        tma_load_2d(&maps.xa, sa, bar(kBarFull + s), t.kind == kQ ? 0 : 64, t.row0);
-                        tma_load_2d(t.kind == kQ ? &maps.bq : &maps.bk, sb, bar(kBarFull + s), 0, r1);
-                    }
+                    tma_load_2d(&maps.x, sa, bar(kBarFull + s), ks * kKStep, t.row0);
+                    tma_load_2d(w1, sb, bar(kBarFull + s), ks * kKStep, r1);
+                    if (w2) tma_load_2d(w2, sb + (uint32_t)t.n1 * 128u, bar(kBarFull + s), ks * kKStep, r2);
+                }
+                if (has_lora_step(a, t)) {
+                    pend = true;
+                    tp = t;
                 }
             }
+            if (!failed && pend && !emit_lora(tp)) failed = true;
             // no copy may still be writing shared memory when the CTA exits
             for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
                 if (!mbar_wait_bounded(bar(kBarFull + j % kStages), (j / kStages) & 1, kWaitNs)) failed = true;
@@ -286,6 +292,36 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
         // ---- MMA issue ----------------------------------------------------------
         if (lane == 0) {
             uint32_t it = 0, tc = 0;
+            uint32_t mpar = 0;  // bit b: parity of the next first-read-out phase of accumulator b
+            auto take_stage = [&](uint32_t &sa, uint32_t &sb) -> bool {
+                const int s = it % kStages;
+                if (!mbar_wait_bounded(bar(kBarFull + s), (it / kStages) & 1, kWaitNs)) return false;
+                fence_after();
+                sa = smem_u32(sm + s * kStageBytes);
+                sb = sa + kATile;
+                return true;
+            };
+            auto release_stage = [&]() { commit(bar(kBarEmpty + (it % kStages))); ++it; };
+            // (x A) B onto the q and k columns of accumulator b, once its first
+            // read-out is done; then the second "accumulator full".
+            auto do_lora = [&](int b) -> bool {
+                if (!mbar_wait_bounded(bar(kBarAccM + b), (mpar >> b) & 1, kWaitNs)) return false;
+                mpar ^= 1u << b;
+                fence_after();
+                const uint32_t idl = idesc_bf16(kRows, a.c, 0, 0);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sa, sb;
+                    if (!take_stage(sa, sb)) return false;
+#pragma unroll
+                    for (int k16 = 0; k16 < kKStep; k16 += 16)
+                        mma_bf16(tmem + (uint32_t)b * 256u + (uint32_t)(half * a.c), desc_sw128(sa + k16 * 2, 16, 1024),
+                                 desc_sw128(sb + k16 * 2, 16, 1024), idl, 1);
+                    release_stage();
+                }
+                commit(bar(kBarAccF + b));
+                return true;
+            };
+            int pend_b = -1;
             for (int tile = blockIdx.x; tile < num_tiles && !failed; tile += gridDim.x, ++tc) {
                 const Tile t = decode_tile(a, tile);
                 const int b = tc & 1;
@@ -296,25 +332,24 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
                 fence_after();
                 const uint32_t acc = tmem + (uint32_t)b * 256u;
                 const uint32_t idesc = idesc_bf16(kRows, t.n, 0, 0);
-                const int nk = nk_main + (has_lora_step(a, t) ? 1 : 0);
-                for (int ks = 0; ks < nk; ++ks, ++it) {
-                    const int s = it % kStages;
-                    if (!mbar_wait_bounded(bar(kBarFull + s), (it / kStages) & 1, kWaitNs)) {
-                        failed = true;
-                        break;
+                for (int ks = 0; ks < nk_main; ++ks) {
+                    if (pend_b >= 0 && ks == lora_at) {
+                        if (!do_lora(pend_b)) { failed = true; break; }
+                        pend_b = -1;
                     }
-                    fence_after();
-                    const uint32_t sa = smem_u32(sm + s * kStageBytes), sb = sa + kATile;
-                    const bool lora = ks == nk_main;
+                    uint32_t sa, sb;
+                    if (!take_stage(sa, sb)) { failed = true; break; }
 #pragma unroll
                     for (int k16 = 0; k16 < kKStep; k16 += 16)
-                        mma_bf16(lora ? acc + 128 : acc, desc_sw128(sa + k16 * 2, 16, 1024),
-                                 desc_sw128(sb + k16 * 2, 16, 1024), idesc, (lora ? k16 : ks + k16) > 0);
-                    commit(bar(kBarEmpty + s));
+                        mma_bf16(acc, desc_sw128(sa + k16 * 2, 16, 1024), desc_sw128(sb + k16 * 2, 16, 1024), idesc,
+                                 (ks + k16) > 0);
+                    release_stage();
                 }
                 if (failed) break;
                 commit(bar(kBarAccF + b));
+                if (has_lora_step(a, t)) pend_b = b;
             }
+            if (!failed && pend_b >= 0 && !do_lora(pend_b)) failed = true;
         }
         __syncwarp();
     } else {
@@ -322,45 +357,53 @@ front_end_kernel(FeArgs a, const __grid_constant__ FeMaps maps, int32_t num_tile
         const int row = 32 * (warp & 3) + lane;
         const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t tc = 0;
+        uint32_t fpar = 0;  // bit b: parity of the next "accumulator full" phase of accumulator b
+        auto wait_full = [&](int b) -> bool {
+            const bool ok = mbar_wait_bounded(bar(kBarAccF + b), (fpar >> b) & 1, kWaitNs);
+            fpar ^= 1u << b;
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            fence_after();
+            return true;
+        };
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
             const Tile t = decode_tile(a, tile);
             const int b = tc & 1;
-            const bool ok = mbar_wait_bounded(bar(kBarAccF + b), (tc >> 1) & 1, kWaitNs);
-            if (!__all_sync(0xffffffffu, ok)) {
+            if (!wait_full(b)) {
                 failed = true;
                 break;
             }
-            fence_after();
             const uint32_t tacc = tmem + lb + (uint32_t)b * 256u;
             const int tok = t.row0 + row;
             const bool live = tok < a.T;
             const int64_t hc = (int64_t)a.H * a.c;
-            const bool lora = has_lora_step(a, t);
             switch (t.kind) {
-            case kQ:
-                epi_plain(tacc, t.n, false, false, 0.f, live ? a.q + tok * hc + t.h * a.c : nullptr);
-                if (lora) epi_plain(tacc, t.n, true, false, 0.f, live ? a.qs + tok * hc + t.h * a.c : nullptr);
-                break;
-            case kK:
-                epi_softmax(tacc, t.n, false, live ? a.k + tok * hc + t.h * a.c : nullptr);
-                if (lora) epi_softmax(tacc, t.n, true, live ? a.ks + tok * hc + t.h * a.c : nullptr);
-                break;
             case kQK:  // columns [0, c): q; [c, 2c): the key logits
-                epi_plain(tacc, a.c, false, false, 0.f, live ? a.q + tok * hc + t.h * a.c : nullptr);
-                epi_softmax(tacc + a.c, a.c, false, live ? a.k + tok * hc + t.h * a.c : nullptr);
+                epi_plain(tacc, a.c, false, 0.f, live ? a.q + tok * hc + t.h * a.c : nullptr);
+                epi_softmax(tacc + a.c, a.c, live ? a.k + tok * hc + t.h * a.c : nullptr);
+                if (has_lora_step(a, t)) {  // the same columns after the LoRA steps
+                    fence_before();
+                    mbar_arrive(bar(kBarAccM + b));
+                    if (!wait_full(b)) {
+                        failed = true;
+                        break;
+                    }
+                    epi_plain(tacc, a.c, false, 0.f, live ? a.qs + tok * hc + t.h * a.c : nullptr);
+                    epi_softmax(tacc + a.c, a.c, live ? a.ks + tok * hc + t.h * a.c : nullptr);
+                }
                 break;
             case kVG:  // columns [0, d): v; [d, d + c): the gate
-                epi_plain(tacc, a.d, false, false, 0.f, live ? a.v + tok * (int64_t)a.H * a.d + t.h * a.d : nullptr);
-                epi_plain(tacc + a.d, a.c, false, true, a.gate_inv_tau, live ? a.g + tok * hc + t.h * a.c : nullptr);
+                epi_plain(tacc, a.d, false, 0.f, live ? a.v + tok * (int64_t)a.H * a.d + t.h * a.d : nullptr);
+                epi_plain(tacc + a.d, a.c, true, a.gate_inv_tau, live ? a.g + tok * hc + t.h * a.c : nullptr);
                 break;
             case kE:
-                epi_plain(tacc, t.n, false, false, 0.f, live ? a.logits + tok * (int64_t)t.n : nullptr);
+                epi_plain(tacc, t.n, false, 0.f, live ? a.logits + tok * (int64_t)t.n : nullptr);
                 break;
             default:  // x A_q -> columns 0..63, x A_k -> 64..127
-                epi_plain(tacc, t.n, false, false, 0.f,
+                epi_plain(tacc, t.n, false, 0.f,
                           live ? a.xa + tok * (int64_t)128 + (t.kind == kXAq ? 0 : 64) : nullptr);
                 break;
             }
+            if (failed) break;
             fence_before();
             mbar_arrive(bar(kBarAccE + b));
         }
@@ -458,7 +501,7 @@ cudaError_t launch_front_end(const sse_config_t &cfg, const FrontEndArgs &f, cud
     const int64_t row_tiles = (T + kRows - 1) / kRows;
     for (int phase = lora ? 0 : 1; phase <= 1; ++phase) {
         a.phase = phase;
-        const int64_t tiles = row_tiles * (phase == 0 ? 2 : (lora ? 3 : 2) * H + 1);
+        const int64_t tiles = row_tiles * (phase == 0 ? 2 : 2 * H + 1);
         const int grid = (int)std::min<int64_t>(tiles, sms);
         front_end_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a, m, (int32_t)tiles);
         cudaError_t e = cudaGetLastError();
