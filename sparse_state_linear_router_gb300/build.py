@@ -18,6 +18,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE]
+if os.environ.get("SSE_NVTX") == "1":   # NVTX ranges around every entry point
+    FLAGS.append("-DSSE_NVTX")
 
 
 def _nvcc() -> str:

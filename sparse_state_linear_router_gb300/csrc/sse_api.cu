@@ -8,6 +8,19 @@
 
 #include "sse_internal.cuh"
 
+#ifdef SSE_NVTX
+#include <nvtx3/nvToolsExt.h>
+// One NVTX range per entry-point call, for profiler timelines; compiled in
+// only with -DSSE_NVTX (build.py: SSE_NVTX=1 in the environment).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+#define SSE_RANGE(name) NvtxRange sse_nvtx_range_(name)
+#else
+#define SSE_RANGE(name) ((void)0)
+#endif
+
 namespace {
 
 using sse::Carver;
@@ -138,6 +151,7 @@ sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits, const
                        int32_t num_seqs, int64_t total_tokens, int32_t *topk_idx, float *topk_w,
                        int32_t *seg_off, int32_t *perm, void *workspace, size_t workspace_bytes,
                        sse_stream_t stream) {
+    SSE_RANGE("sse_route");
     sse_status_t st = check_config(cfg);
     if (st != SSE_OK) return st;
     if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
@@ -169,6 +183,7 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
                                void *out, int32_t *topk_idx, float *topk_w, void *workspace,
                                size_t workspace_bytes, sse_stream_t stream, void *const *stage_events,
                                int32_t *num_launches) {
+    SSE_RANGE("sse_forward_timed");
     if (num_launches) *num_launches = 0;
     sse_status_t st = check_config(cfg);
     if (st != SSE_OK) return st;
@@ -254,6 +269,7 @@ sse_status_t sse_forward(const sse_config_t *cfg, const void *q, const void *k, 
                          int64_t total_tokens, const float *initial_state, float *final_state,
                          void *out, int32_t *topk_idx, float *topk_w, void *workspace,
                          size_t workspace_bytes, sse_stream_t stream) {
+    SSE_RANGE("sse_forward");
     return sse_forward_timed(cfg, q, k, v, log_gate, router_logits, q_shared, k_shared, cu_seqlens,
                              num_seqs, total_tokens, initial_state, final_state, out, topk_idx, topk_w,
                              workspace, workspace_bytes, stream, nullptr, nullptr);
@@ -263,6 +279,7 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
                              const void *log_gate, const void *router_logits, const void *q_shared,
                              const void *k_shared, int32_t batch, float *state, void *out,
                              int32_t *topk_idx, float *topk_w, sse_stream_t stream) {
+    SSE_RANGE("sse_decode_step");
     sse_status_t st = check_config(cfg);
     if (st != SSE_OK) return st;
     if (batch < 0) return SSE_ERR_INVALID_ARG;
@@ -292,6 +309,7 @@ sse_status_t sse_front_end(const sse_config_t *cfg, int32_t hidden, int64_t tota
                            const void *b_k, float gate_inv_tau, void *q, void *k, void *v,
                            void *log_gate, void *router_logits, void *q_shared, void *k_shared,
                            void *workspace, size_t workspace_bytes, sse_stream_t stream) {
+    SSE_RANGE("sse_front_end");
     sse_status_t st = check_config(cfg);
     if (st != SSE_OK) return st;
     if (hidden < 0 || total_tokens < 0 || !std::isfinite(gate_inv_tau)) return SSE_ERR_INVALID_ARG;

@@ -139,3 +139,13 @@ def test_front_end_rejects_bad_arguments(lib):
     small = b.sse_front_end_workspace_size(cfg, 256, 300)
     assert small % 256 == 0 and small >= 256 + 300 * 128 * 2
     assert b.sse_front_end_workspace_size(cfg, 256, 3000) > small
+
+
+def test_nvtx_build_compiles(tmp_path):
+    """The optional NVTX ranges (-DSSE_NVTX, SSE_NVTX=1 for build.py) compile."""
+    import subprocess
+    from sparse_state_linear_router_gb300 import build
+    src = os.path.join(build.CSRC, "sse_api.cu")
+    r = subprocess.run([build._nvcc(), *build.ARCH, *build.FLAGS, "-DSSE_NVTX", "-c", src, "-o",
+                        str(tmp_path / "api.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
