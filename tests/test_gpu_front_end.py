@@ -76,6 +76,11 @@ VARIANTS = {
     # mixed widths: c = 128, d = 64, H*N = 256 router columns (the widest block)
     "c128_d64_wide_router": ("front_end_small", {"tokens": 384, "hidden": 128, "num_heads": 16, "key_dim": 128,
                                                  "value_dim": 64, "num_partitions": 16}, True),
+    # one K step (the LoRA steps then precede the next tile's only step) and
+    # about seven tiles per CTA, so every [q | k] tile but the last of a CTA
+    # takes the deferred path
+    "d64_many_tiles": ("front_end_small", {"tokens": 4096, "hidden": 64, "num_heads": 16, "key_dim": 128,
+                                           "value_dim": 128, "num_partitions": 8}, True),
 }
 
 
