@@ -149,3 +149,18 @@ def test_nvtx_build_compiles(tmp_path):
     r = subprocess.run([build._nvcc(), *build.ARCH, *build.FLAGS, "-DSSE_NVTX", "-c", src, "-o",
                         str(tmp_path / "api.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_size_limits_rejected_before_launch(lib):
+    """Sizes past the kernels' 32-bit row and record indices, and the masking
+    schedule's sequence-count limit, are refused on the host."""
+    from sparse_state_linear_router_gb300 import binding as b
+    cfg = _cfg(num_heads=16, num_partitions=8, top_k=2)
+    # T * H * k records must fit in 31 bits
+    assert _fwd(cfg, T=(1 << 31) // 32 + 1, S=1) == b.SSE_ERR_UNSUPPORTED
+    assert b.sse_forward_workspace_size(cfg, (1 << 31) // 32 + 1, 1) == 0
+    # the masking schedule's placement kernel holds one entry per sequence in shared memory
+    assert _fwd(_cfg(algo="masked"), T=12001, S=12001) == b.SSE_ERR_UNSUPPORTED
+    # decode: batch * H must fit in 31 bits
+    assert b.sse_decode_step(_cfg(num_heads=64), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, (1 << 31) // 64,
+                             FAKE, FAKE, None, None, None) == b.SSE_ERR_UNSUPPORTED
