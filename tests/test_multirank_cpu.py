@@ -89,3 +89,24 @@ def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     src.write_bytes(b"kernel v2\n")
     assert bench.profiled_traffic("k.cu", "p.md") is None
     assert bench.profiled_traffic("missing.cu", "p.md") is None
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the CPU oracle on bounded samples) prints one
+    JSON line with the native arm's metric, unit and config plus its own
+    cpu_baseline and a zero-copy e2e entry."""
+    import bench
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-seconds", "0.5"])
+    assert rc == 0
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 3
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["config"]["workload"]
