@@ -17,8 +17,6 @@
 // Two calls whose kernels overlap on the same GPU (different streams, or
 // different host threads) race on the array and corrupt each other's
 // results; serialise them.
-#include <mutex>
-
 #include "sse_internal.cuh"
 
 namespace {
@@ -30,26 +28,17 @@ constexpr size_t kScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mutex;
-
-// Device address of g_route_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up
-// (once per device, with that device current) through the runtime.
+// Device address of g_route_scratch in the current device's context.  In
+// host code the array's name is only a host-side stand-in, so the address is
+// looked up through the runtime, with the device current, on every call: the
+// lookup is a cheap host-side query, and a cached address could outlive its
+// context (after cudaDeviceReset, or for a caller on another context of the
+// same device).
 cudaError_t scratch_address(void **addr) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_route_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *addr = g_scratch_addr[dev];
+    *addr = p;
     return cudaSuccess;
 }
 
@@ -61,16 +50,12 @@ extern "C" sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *r
                                           const int32_t *cu_seqlens, int32_t num_seqs,
                                           int64_t total_tokens, int32_t *topk_idx, float *topk_w,
                                           int32_t *seg_off, int32_t *perm, sse_stream_t stream) {
-    // Argument checks: the same rules as sse_route, minus the workspace.
-    if (!cfg) return SSE_ERR_INVALID_ARG;
+    // Argument checks: the same rules (and the same code) as sse_route, minus
+    // the workspace.
+    sse_status_t st = sse::check_config(cfg);
+    if (st != SSE_OK) return st;
     const sse_config_t &c = *cfg;
-    if (c.num_heads < 1 || c.key_dim < 1 || c.value_dim < 1) return SSE_ERR_INVALID_ARG;
-    if (c.num_partitions < 1 || c.top_k < 1 || c.top_k > c.num_partitions) return SSE_ERR_INVALID_ARG;
-    if (c.use_shared != 0 && c.use_shared != 1) return SSE_ERR_INVALID_ARG;
-    if (c.dtype != SSE_F32 && c.dtype != SSE_BF16) return SSE_ERR_INVALID_ARG;
-    if (c.num_partitions > sse::kMaxPartitions || c.top_k > sse::kMaxTopK) return SSE_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || total_tokens < 0 || (num_seqs == 0 && total_tokens != 0)) return SSE_ERR_INVALID_ARG;
-    if (total_tokens * c.num_heads * c.top_k >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    if ((st = sse::check_sizes(c, total_tokens, num_seqs)) != SSE_OK) return st;
     if (!cu_seqlens || !topk_idx || (total_tokens > 0 && !router_logits)) return SSE_ERR_INVALID_ARG;
     if (!aligned16(router_logits)) return SSE_ERR_INVALID_ARG;
     const bool group = seg_off || perm;

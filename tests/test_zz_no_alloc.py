@@ -27,17 +27,18 @@ def lib():
     return binding.load()
 
 
-def _noalloc(lib, cfg, logits, cu, S, T):
+def _noalloc(lib, cfg, logits, cu, S, T, with_w=True, group=True):
     from sparse_state_linear_router_gb300 import binding
     H, k, N = cfg.num_heads, cfg.top_k, cfg.num_partitions
     idx = torch.full((T, H, k), -7, dtype=torch.int32, device="cuda")
-    w = torch.full((T, H, k), -7.0, dtype=torch.float32, device="cuda")
-    seg_off = torch.full((S * H * N + 1,), -7, dtype=torch.int32, device="cuda")
-    perm = torch.full((H * k * T,), -7, dtype=torch.int32, device="cuda")
-    st = lib.sse_route_noalloc(ctypes.byref(cfg), logits.data_ptr(), cu.data_ptr(), S, T, idx.data_ptr(),
-                               w.data_ptr(), seg_off.data_ptr(), perm.data_ptr(), binding._stream())
+    w = torch.full((T, H, k), -7.0, dtype=torch.float32, device="cuda") if with_w else None
+    seg_off = torch.full((S * H * N + 1,), -7, dtype=torch.int32, device="cuda") if group else None
+    perm = torch.full((max(1, H * k * T),), -7, dtype=torch.int32, device="cuda") if group else None
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    st = lib.sse_route_noalloc(ctypes.byref(cfg), ptr(logits), cu.data_ptr(), S, T, idx.data_ptr(),
+                               ptr(w), ptr(seg_off), ptr(perm), binding._stream())
     assert st == binding.SSE_OK, binding.sse_status_string(st)
-    return idx, w, seg_off, perm
+    return idx, w, seg_off, None if perm is None else perm[:H * k * T]
 
 
 def test_noalloc_route_matches_route_on_two_calls(lib):
@@ -59,6 +60,36 @@ def test_noalloc_route_matches_route_on_two_calls(lib):
         assert torch.equal(seg_off, ref["seg_off"])
         assert torch.equal(perm, ref["perm"])
         np.testing.assert_allclose(wts.cpu().numpy(), ref["topk_w"].cpu().numpy(), rtol=2e-6, atol=1e-7)
+
+
+def test_noalloc_route_optional_outputs(lib):
+    """The documented variants through the no-allocation entry point: no
+    router weights (topk_w NULL), routing only without the grouping
+    (seg_off = perm = NULL), and an empty batch (num_seqs = 0) -- each
+    compared with sse_route the same way."""
+    from sparse_state_linear_router_gb300 import binding
+    w = H_.workload_variant("small_bf16", num_heads=3, num_partitions=8, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=23, lengths=[411, 0, 97])
+    cfg = H_.config_of(w)
+    logits = binding.to_device(inp.logits)
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    S, T = inp.num_seqs, inp.total_tokens
+    ref = binding.route(cfg, logits, cu)
+    idx, wts, seg_off, perm = _noalloc(lib, cfg, logits, cu, S, T, with_w=False)
+    idx2, wts2, seg2, perm2 = _noalloc(lib, cfg, logits, cu, S, T, group=False)
+    torch.cuda.synchronize()
+    assert wts is None and seg2 is None and perm2 is None
+    assert torch.equal(idx, ref["topk_idx"]) and torch.equal(idx2, ref["topk_idx"])
+    assert torch.equal(seg_off, ref["seg_off"]) and torch.equal(perm, ref["perm"])
+    np.testing.assert_allclose(wts2.cpu().numpy(), ref["topk_w"].cpu().numpy(), rtol=2e-6, atol=1e-7)
+    # empty batch: nothing launched, outputs untouched
+    empty_cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sentinel = torch.full((1, 3, 2), -7, dtype=torch.int32, device="cuda")
+    st = lib.sse_route_noalloc(ctypes.byref(cfg), None, empty_cu.data_ptr(), 0, 0, sentinel.data_ptr(),
+                               None, None, None, binding._stream())
+    assert st == binding.SSE_OK
+    torch.cuda.synchronize()
+    assert bool((sentinel == -7).all())
 
 
 def test_noalloc_route_rejects_sizes_beyond_its_scratch(lib):
