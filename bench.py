@@ -322,6 +322,91 @@ def describe_decode(w):
             f"N{w.num_partitions}, top-{w.top_k}{', shared' if w.use_shared else ''}, fp32 states resident)")
 
 
+def time_forward_variants(args, dev, peaks):
+    """Forward-only timings of the other forward workloads, reported beside
+    the step (not part of `value`): the long-context varlen batch (16
+    sequences, lengths U[1024, 32768] with the seed-0 draw, H16, N16, random
+    initial state, initial and final state I/O), the small batch (B2 T2048 H4
+    c=d=64 N8) under both schedules, and the layer batch with a per-partition
+    router bias that skews the partition loads (stress variant) under both
+    schedules.  Inputs are drawn on the device (same distributions as the
+    parity tests' numpy generator, another stream of numbers); each is larger
+    than L2 except the small batch (4 MB), whose time is launch-bound."""
+    import torch
+    from sparse_state_linear_router_gb300 import binding
+    stream = torch.cuda.current_stream(dev)
+    hbm, tflops = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    P_ = binding._ptr
+    res = {}
+    N8 = synth.WORKLOADS["layer_bf16"].num_partitions
+    skew = 1.5 * (np.arange(N8) / (N8 - 1) - 0.5) * 2.0
+    import dataclasses
+    k_eq_n = dataclasses.replace(synth.WORKLOADS["small_bf16"], name="small_bf16_k4_of_4", num_partitions=4,
+                                 top_k=4)
+    cases = [("varlen_bf16", "varlen_bf16", None, "auto"),
+             ("small_bf16", "small_bf16", None, "auto"),
+             ("small_bf16_masked", "small_bf16", None, "masked"),
+             ("small_bf16_k4_of_4", k_eq_n, None, "auto"),
+             ("small_bf16_k4_of_4_grouped", k_eq_n, None, "chunked"),
+             ("layer_bf16_skewed", "layer_bf16", skew, "auto"),
+             ("layer_bf16_skewed_masked", "layer_bf16", skew, "masked")]
+    for key, wname, bias, algo in cases:
+        w = synth.WORKLOADS[wname] if isinstance(wname, str) else wname
+        x = synth.make_forward_inputs_device(w, seed=0, device=dev, router_bias=bias)
+        T, S = x["total_tokens"], x["num_seqs"]
+        cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k,
+                                  w.use_shared, 1.0, w.dtype, algo)
+        out = torch.empty((T, w.num_heads, w.value_dim), dtype=torch.bfloat16, device=dev)
+        fin = torch.empty((S, w.num_heads, w.num_slots, w.key_dim, w.value_dim), dtype=torch.float32, device=dev)
+        wsp = binding.forward_workspace(cfg, T, S, dev)
+        nl = {"n": 0}
+
+        def call(evs=None):
+            st, n = binding.sse_forward_timed(cfg, P_(x["q"]), P_(x["k"]), P_(x["v"]), P_(x["g"]),
+                                              P_(x["logits"]), None, None, P_(x["cu_seqlens"]), S, T,
+                                              P_(x["init"]), P_(fin), P_(out), None, None, P_(wsp), wsp.numel(),
+                                              stream.cuda_stream,
+                                              None if evs is None else [e.cuda_event for e in evs])
+            binding._check(st, "sse_forward_timed")
+            nl["n"] = n
+        for _ in range(max(3, args.warmup)):
+            call()
+        reps = 10
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        for e4 in evs:
+            for e in e4:
+                e.record(stream)
+        torch.cuda.synchronize()
+        for i in range(reps):
+            call(evs[i])
+        torch.cuda.synchronize()
+        st, flags = binding.sse_read_device_status(wsp.data_ptr(), stream.cuda_stream)
+        ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
+        main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        has_init = x["init"] is not None
+        fb = forward_step_bytes(w, T, S, init=has_init)
+        ff = forward_flops(w, T)
+        t_bind = max(ff / (tflops * 1e12), fb / (hbm * 1e9))
+        mb = forward_main_bytes(w, T, S, init=has_init)
+        res[key] = {
+            "workload": describe_forward(w, synth.LayerInputs(w, None, None, None, None, None,
+                                                              x["cu_seqlens"].cpu().numpy(),
+                                                              np.zeros(1) if has_init else None)),
+            "algo": algo, "router_bias": None if bias is None else [round(float(b), 4) for b in bias],
+            "ms": ms, "route_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+            "main_ms": main_ms, "tail_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+            "tokens_per_s": T / (ms * 1e-3), "launches": nl["n"],
+            "roofline": {"bound": "hbm" if fb / (hbm * 1e9) >= ff / (tflops * 1e12) else "tensor",
+                         "binding_ms": t_bind * 1e3, "frac": t_bind / (ms * 1e-3),
+                         "main_kernel_gbs": mb / (main_ms * 1e6), "main_kernel_frac_of_hbm": mb / (main_ms * 1e6) / hbm,
+                         "algorithmic_bytes": fb, "algorithmic_flops": ff},
+            "device_status": st, "device_flags": flags,
+        }
+        del x, out, fin, wsp
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_native(args):
     import torch
     ws, rank, local = _dist()
@@ -529,6 +614,13 @@ def run_native(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "overlap": "inputs of step i copied on a second stream while step i-1 computes"}
 
+    # ---- the other forward workloads (rank 0, N = 1, default run only) -------
+    variants, variant_clocks = None, None
+    if do_fwd and do_dec and rank == 0 and ws == 1 and not args.no_variants:
+        with ClockSampler(local) as vclk:
+            variants = time_forward_variants(args, dev, peaks)
+        variant_clocks = vclk.summary()
+
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -578,6 +670,9 @@ def run_native(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
     }
+    if variants is not None:
+        line["forward_variants"] = variants
+        line["forward_variants_clocks"] = variant_clocks
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -666,6 +761,8 @@ def main(argv=None):
     ap.add_argument("--algo", choices=["auto", "chunked", "recurrent", "masked"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the forward-only timings of the other workloads (varlen, small, skewed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--part", choices=["both", "forward", "decode", "front_end"], default="both",
                     help="time the whole step (default), one of its two calls, or the front end alone")

@@ -23,7 +23,8 @@
  * ---------------------------------
  * - All array pointers are DEVICE pointers owned by the caller.  The library
  *   allocates no device or host memory, keeps no state between calls and
- *   never synchronizes the stream (except sse_read_device_status).  Calls are
+ *   never synchronizes the stream (except sse_read_device_status and
+ *   sse_get_last_device_error).  Calls are
  *   asynchronous on `stream` (NULL = legacy default stream) and thread-safe.
  * - Token tensors are packed over all sequences, head-interleaved, row-major:
  *   q, k, log_gate, q_shared, k_shared : [total_tokens, H, c]
@@ -62,7 +63,9 @@ typedef enum {
     SSE_ERR_UNSUPPORTED = 2, /* well-formed but not supported (c, d, N, dtype, algo) */
     SSE_ERR_WORKSPACE = 3,   /* workspace null, misaligned (256 B) or too small */
     SSE_ERR_CUDA = 4,        /* a kernel launch failed */
-    SSE_ERR_DEVICE = 5       /* a device-side check failed (sse_read_device_status) */
+    SSE_ERR_DEVICE = 5,      /* a device-side check failed (sse_read_device_status) */
+    SSE_ERR_DEVICE_TIMEOUT = 6 /* a bounded wait inside a kernel expired: the affected work
+                                  stopped early and its results are invalid */
 } sse_status_t;
 
 typedef enum { SSE_F32 = 0, SSE_BF16 = 1 } sse_dtype_t;
@@ -132,11 +135,15 @@ sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits,
  * process exits.  Limit: (num_seqs + 1) + H * N * (ceil(total_tokens / 256)
  * + num_seqs + 1) int32 entries (plus 256-byte alignment padding) must fit in
  * 4 MiB -- about one million tokens at H = 16, N = 16; larger calls return
- * SSE_ERR_WORKSPACE before any launch.  The first call on each device looks
- * up the array's device address (make that first call before any stream
- * capture).  Nothing is allocated or freed.  All calls on a device share the
- * array and it keeps the previous call's contents (no entry needs to start
- * at zero); calls that overlap on the GPU race on it and must be serialised. */
+ * SSE_ERR_WORKSPACE before any launch.  The configuration and size checks are
+ * those of sse_route (same status for the same bad argument).  Every call
+ * looks up the array's device address in the current device's context (a
+ * host-side query, never cached, so a device reset or another context on the
+ * same device is safe); the first call on a device also loads the array, so
+ * make that first call before any stream capture.  Nothing is allocated or
+ * freed.  All calls on a device share the array and it keeps the previous
+ * call's contents (no entry needs to start at zero); calls that overlap on
+ * the GPU race on it and must be serialised. */
 sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *router_logits,
                                const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                                int32_t *topk_idx, float *topk_w, int32_t *seg_off, int32_t *perm,
@@ -157,11 +164,14 @@ sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *router_logit
  * Workspace: sse_forward_workspace_size bytes (256-byte aligned).
  * Numerics: float32 states and accumulation.  The chunked path rounds its
  * tensor-core operands to bfloat16 and splits the decay factors of each
- * 128-row chunk of a segment around its midpoint: it needs the summed
- * log-gate of each half chunk to stay above -80 per key row.  A chunk outside
- * this range sets the SSE_DEVICE_GATE_RANGE flag read by
- * sse_read_device_status.  The check takes the log-gates to be <= 0 (decays in
- * (0, 1], as in the method); positive log-gates are not range-checked.
+ * 128-row chunk of a segment around its midpoint, which takes the summed
+ * log-gate of each half chunk to stay above -64 per key row.  A segment with a
+ * chunk past that (strong decays: e.g. log-gates of -2 on every row) is
+ * recomputed in the same call, token by token in float32 on the CUDA cores,
+ * so every decay in (0, 1] gives a valid result; sse_read_device_status then
+ * reports the informational SSE_DEVICE_RECOMPUTED bit.  The range check takes
+ * the log-gates to be <= 0 (decays in (0, 1], as in the method); positive
+ * log-gates are outside the method and not checked.
  * ------------------------------------------------------------------------- */
 size_t sse_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
 
@@ -243,17 +253,29 @@ sse_status_t sse_front_end(const sse_config_t *cfg, int32_t hidden, int64_t tota
                            void *log_gate, void *router_logits, void *q_shared, void *k_shared,
                            void *workspace, size_t workspace_bytes, sse_stream_t stream);
 
-/* Device-side check flags (bit mask).
- *   SSE_DEVICE_GATE_RANGE: a chunk's log-gate sum left the chunked path's range
- *   SSE_DEVICE_TIMEOUT:    a bounded wait on the tensor core expired; the
- *                          affected segments stopped early (results invalid) */
-enum { SSE_DEVICE_GATE_RANGE = 1, SSE_DEVICE_TIMEOUT = 2 };
+/* Device-side status bits (bit mask), written by the kernels into the first
+ * word of the workspace of sse_forward and sse_front_end (each call clears
+ * them first).
+ *   SSE_DEVICE_TIMEOUT      error: a bounded wait on the tensor-core pipeline
+ *                           expired; the affected segments stopped early and
+ *                           the call's results are invalid
+ *   SSE_DEVICE_RECOMPUTED   information only: at least one segment had a chunk
+ *                           whose summed log-gate left the chunked path's
+ *                           factorised range and was recomputed token by token
+ *                           (results valid) */
+enum { SSE_DEVICE_TIMEOUT = 2, SSE_DEVICE_RECOMPUTED = 4 };
 
-/* Reads the device-check flags recorded by the last sse_forward or
- * sse_front_end that used `workspace` (each call clears them first).  Synchronizes `stream`.
- * *flags receives the bit mask; returns SSE_ERR_DEVICE if any flag is set,
+/* Reads the device-status bits of the last sse_forward or sse_front_end that
+ * used `workspace`.  Synchronizes `stream`.  *flags receives the bit mask.
+ * Returns SSE_ERR_DEVICE_TIMEOUT if the timeout bit is set, SSE_ERR_DEVICE for
+ * any other error bit, SSE_OK otherwise (informational bits included), and
  * SSE_ERR_CUDA if the copy fails. */
 sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_t stream);
+
+/* The status alone: sse_read_device_status without the bit mask
+ * ("Scaling Linear Attention with Sparse State Expansion" has no counterpart;
+ * this is the failure-detection hook of the library). */
+sse_status_t sse_get_last_device_error(void *workspace, sse_stream_t stream);
 
 #ifdef __cplusplus
 }

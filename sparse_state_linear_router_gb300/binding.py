@@ -18,7 +18,10 @@ from typing import Optional
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libsse.so")
 
-SSE_OK, SSE_ERR_INVALID_ARG, SSE_ERR_UNSUPPORTED, SSE_ERR_WORKSPACE, SSE_ERR_CUDA, SSE_ERR_DEVICE = range(6)
+(SSE_OK, SSE_ERR_INVALID_ARG, SSE_ERR_UNSUPPORTED, SSE_ERR_WORKSPACE, SSE_ERR_CUDA, SSE_ERR_DEVICE,
+ SSE_ERR_DEVICE_TIMEOUT) = range(7)
+# device-status bits (sse_read_device_status)
+SSE_DEVICE_TIMEOUT, SSE_DEVICE_RECOMPUTED = 2, 4
 SSE_F32, SSE_BF16 = 0, 1
 SSE_ALGO_AUTO, SSE_ALGO_CHUNKED, SSE_ALGO_RECURRENT, SSE_ALGO_MASKED = 0, 1, 2, 3
 _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_ALGO_RECURRENT,
@@ -27,7 +30,8 @@ _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_A
 # Every extern "C" symbol that include/sse.h declares.
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
             "sse_route_noalloc", "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
-            "sse_front_end_workspace_size", "sse_front_end", "sse_read_device_status")
+            "sse_front_end_workspace_size", "sse_front_end", "sse_read_device_status",
+            "sse_get_last_device_error")
 
 
 class sse_config_t(ctypes.Structure):
@@ -83,6 +87,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                   P, P, P, P, P, P, P, P, sz, P]
     lib.sse_read_device_status.restype = ctypes.c_int
     lib.sse_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
+    lib.sse_get_last_device_error.restype = ctypes.c_int
+    lib.sse_get_last_device_error.argtypes = [P, P]
     _lib = lib
     return lib
 
@@ -157,6 +163,10 @@ def sse_read_device_status(workspace, stream):
     flags = ctypes.c_int32(0)
     st = load().sse_read_device_status(workspace, ctypes.byref(flags), stream)
     return st, flags.value
+
+
+def sse_get_last_device_error(workspace, stream) -> int:
+    return load().sse_get_last_device_error(workspace, stream)
 
 
 # ---------------------------------------------------------------------------

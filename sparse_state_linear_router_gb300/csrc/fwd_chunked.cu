@@ -68,6 +68,14 @@ static_assert(32 * (kEpiWarps * kRegsEpi + kTrfWarps * kRegsTrf + kLdrWarps * kR
               "register split must use exactly the launch allocation");
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
+// Largest |G_r - G_m| (summed log-gate over a half chunk, per key row) the
+// factorised form takes.  Every factor exp(+-(G_r - G_m)) then stays within
+// e^64: a bf16 operand that underflows (below ~1e-38) is multiplied by at most
+// e^64 (~6e27) in any product, so what rounding loses there stays below
+// ~1e-10 of |q| |k| |v| -- far under bf16's own rounding.  A chunk past it is
+// not evaluated in factorised form: its whole segment goes to the redo list
+// and is recomputed token by token (segment_redo_kernel).
+constexpr float kGateRange = 64.f;
 
 constexpr uint32_t kTile = 128 * 256;   // one 128 x 128 bf16 tile: 32 KB
 // Row metadata ring (global chunk g in stage g % kMetaStages): written by the
@@ -547,7 +555,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 }
                 return ok;
             };
-            bool bad = false;
+            bool bad = false, seg_redo = false;
             if (nch > 0) bad = !load_g(0, rg);
             for (int n = 0; n < nch; ++n) {
                 const uint32_t g_n = gch + n;
@@ -596,6 +604,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     if (!bad) tok_next = meta_tok(g1 % kMetaStages);
                 }
                 float *s_fmid = s_scale + (g_n & 1) * 256, *s_beta = s_fmid + 128;
+                bool out_of_range = false;
                 if (tt < KC) {  // per-column exclusive scan over row blocks
                     float acc = 0.f, gmid = 0.f;
                     for (int r2 = 0; r2 < NRB; ++r2) {
@@ -610,13 +619,22 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     // |G_r - G_m| over the chunk: with log-gates <= 0 (decays in
                     // (0, 1]) G_r falls monotonically from 0, so it is at most
                     // max(|G_m|, |G_last - G_m|)
-                    if (fmaxf(fabsf(gmid), fabsf(acc - gmid)) > 80.f) atomicOr(a.flags, SSE_DEVICE_GATE_RANGE);
+                    out_of_range = fmaxf(fabsf(gmid), fabsf(acc - gmid)) > kGateRange;
                     // the state rows can be rescaled now (two barriers by chunk parity:
                     // this role may reach the next chunk's scan before the epilogue
                     // has waited for this one)
                     mbar_arrive(bar((g_n & 1) ? kBarSc1 : kBarSc0));
                 }
-                named_sync(1, kTrfThreads);
+                // A chunk past the gate range: the segment is finished as usual
+                // (its results are overwritten) and queued once for the exact
+                // per-token recomputation.
+                if (named_sync_or(1, kTrfThreads, out_of_range) && !seg_redo) {
+                    seg_redo = true;
+                    if (tt == 0) {
+                        atomicOr(a.flags, SSE_DEVICE_RECOMPUTED);
+                        a.redo_list[atomicAdd(a.flags + 1, 1)] = item;
+                    }
+                }
                 // Qt / Kt tiles are free once the products of chunk g_n - 1 read them
                 if (g_n >= 1) bad |= !mbar_wait_bounded(bar(kBarQK), (g_n - 1) & 1, kWaitNs);
                 // pass 2: Qt, Kt rows (bf16) into their tiles.  The read weight
@@ -882,6 +900,102 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     }
 }
 
+// Exact per-token recomputation of the work items the tensor-core kernel put
+// on the redo list (a chunk whose summed log-gate left the factorised form's
+// range, kGateRange).  The recurrence of eqs. 13-14 is evaluated one row at a
+// time in float32 -- decay of the state rows, write of e k^T v, read of
+// w q S -- with exp(g) taken per row, so any decay in (0, 1] is exact to
+// float32 rounding.  Each item's partial rows (pad_off[item] + row) and its
+// final state overwrite what the tensor-core kernel wrote.  CTAs stride over
+// the list; an empty list costs one launch that reads one word.
+// Thread layout: DV/4 column quads x R row groups, KC/R state rows each.
+template <int KC, int DV, bool MASKED>
+__global__ void __launch_bounds__(256)
+segment_redo_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared, float scale) {
+    constexpr int D4 = DV / 4, R = 256 / D4, RPT = KC / R, kBatch = 32;
+    __shared__ float s_q[KC], s_k[KC], s_a[KC], s_v[DV];
+    __shared__ float s_red[R][DV];
+    __shared__ int s_tok[kBatch];
+    __shared__ float s_e[kBatch];
+    const int tid = threadIdx.x, cq = tid % D4, rg = tid / D4, col = 4 * cq;
+    const int count = *(volatile const int32_t *)(a.flags + 1);
+    const int P = N + use_shared;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *kk = static_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
+    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.g);
+    __nv_bfloat16 *part = static_cast<__nv_bfloat16 *>(a.part_routed);
+    for (int li = blockIdx.x; li < count; li += gridDim.x) {
+        const int item = a.redo_list[li];
+        const Segment seg = decode_segment<MASKED>(a, item, H, N, use_shared);
+        const int64_t state_off = (((int64_t)seg.b * H + seg.h) * P + seg.slot) * (int64_t)KC * DV;
+        const int64_t row0 = a.pad_off[item];
+        const __nv_bfloat16 *qsrc = seg.shared && a.qs ? static_cast<const __nv_bfloat16 *>(a.qs) : q;
+        const __nv_bfloat16 *ksrc = seg.shared && a.ks ? static_cast<const __nv_bfloat16 *>(a.ks) : kk;
+        float4 st[RPT];
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int r = rg + m * R;
+            st[m] = a.init ? *reinterpret_cast<const float4 *>(a.init + state_off + (int64_t)r * DV + col)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int i0 = 0; i0 < seg.len; i0 += kBatch) {
+            __syncthreads();  // the previous batch's metadata has been read
+            if (tid < kBatch) {
+                const RowMeta mt = row_meta<MASKED>(a, seg, i0 + tid, H, topk);
+                s_tok[tid] = mt.t;
+                s_e[tid] = mt.e;
+            }
+            __syncthreads();
+            const int nb = min(kBatch, seg.len - i0);
+            for (int j = 0; j < nb; ++j) {
+                const int t = s_tok[j];
+                const float e = s_e[j];
+                if (MASKED && e < 0.f) continue;  // not selected: no decay, no write, no read
+                const int64_t th = (int64_t)t * H + seg.h;
+                for (int r = tid; r < KC; r += 256) {
+                    s_q[r] = e * scale * __bfloat162float(qsrc[th * KC + r]);
+                    s_k[r] = e * __bfloat162float(ksrc[th * KC + r]);
+                    s_a[r] = expf(__bfloat162float(g[th * KC + r]));
+                }
+                for (int c2 = tid; c2 < DV; c2 += 256) s_v[c2] = __bfloat162float(v[th * DV + c2]);
+                __syncthreads();
+                const float4 v4 = *reinterpret_cast<const float4 *>(s_v + col);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < RPT; ++m) {
+                    const int r = rg + m * R;
+                    const float ar = s_a[r], kr = s_k[r], qr = s_q[r];
+                    st[m].x = fmaf(ar, st[m].x, kr * v4.x);
+                    st[m].y = fmaf(ar, st[m].y, kr * v4.y);
+                    st[m].z = fmaf(ar, st[m].z, kr * v4.z);
+                    st[m].w = fmaf(ar, st[m].w, kr * v4.w);
+                    acc.x = fmaf(qr, st[m].x, acc.x);
+                    acc.y = fmaf(qr, st[m].y, acc.y);
+                    acc.z = fmaf(qr, st[m].z, acc.z);
+                    acc.w = fmaf(qr, st[m].w, acc.w);
+                }
+                *reinterpret_cast<float4 *>(&s_red[rg][col]) = acc;
+                __syncthreads();
+                for (int c2 = tid; c2 < DV; c2 += 256) {
+                    float o = 0.f;
+#pragma unroll
+                    for (int r2 = 0; r2 < R; ++r2) o += s_red[r2][c2];
+                    part[(row0 + i0 + j) * DV + c2] = __float2bfloat16_rn(o);
+                }
+                __syncthreads();  // s_q .. s_red are rewritten by the next row
+            }
+        }
+        if (a.final_state) {
+#pragma unroll
+            for (int m = 0; m < RPT; ++m) {
+                const int r = rg + m * R;
+                *reinterpret_cast<float4 *>(a.final_state + state_off + (int64_t)r * DV + col) = st[m];
+            }
+        }
+    }
+}
+
 // out[row, :] = sum over the row's ncon bf16 partial rows rec_pos[row * ncon + j]
 // (routed contributions j < k, then the shared one), 8 columns per thread,
 // fp32 accumulation in a fixed order.
@@ -945,6 +1059,7 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     int32_t *counter = static_cast<int32_t *>(a.chunk_ws);
     cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
+    // the redo list's length, a.flags[1], starts at zero with the flags word
 
     // The partial buffer as a 2-D tensor [part_rows, DV] of bf16, stored in
     // boxes of 64 columns x one chunk of rows with the 128-byte swizzle.
@@ -980,6 +1095,11 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     chunked_forward_kernel<KC, DV, MASKED><<<grid, kThreads, kSmemBytes, stream>>>(
         a, map, maps, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg,
         counter);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int redo_grid = (int)std::min<int64_t>(nseg, 2 * (sms > 0 ? sms : 148));
+    segment_redo_kernel<KC, DV, MASKED><<<redo_grid, 256, 0, stream>>>(a, cfg.num_heads, cfg.num_partitions,
+                                                                       cfg.top_k, cfg.use_shared, cfg.scale);
     return cudaGetLastError();
 }
 
@@ -991,7 +1111,11 @@ bool chunked_supported(const sse_config_t &cfg) {
     return cfg.dtype == SSE_BF16 && c_ok && d_ok;
 }
 
-size_t chunked_extra_workspace(const sse_config_t &, int64_t, int32_t) { return 256; }
+// work counter (256 bytes), then the redo list (one entry per work item)
+size_t chunked_extra_workspace(const sse_config_t &cfg, int64_t, int32_t num_seqs) {
+    const int64_t nitems = (int64_t)num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
+    return 256 + (size_t)nitems * sizeof(int32_t);
+}
 
 cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t stream,
                                    int *launches) {
@@ -1006,7 +1130,7 @@ cudaError_t launch_forward_chunked(const sse_config_t &cfg, const ForwardArgs &a
     else if (cfg.key_dim == 64 && cfg.value_dim == 64)
         e = m ? launch_t<64, 64, true>(cfg, a, stream) : launch_t<64, 64, false>(cfg, a, stream);
     else return cudaErrorInvalidValue;
-    *launches += 1;
+    *launches += 2;  // the tensor-core kernel and the (usually empty) redo pass
     return e;
 }
 

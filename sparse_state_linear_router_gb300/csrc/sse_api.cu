@@ -21,18 +21,12 @@ struct NvtxRange {
 #define SSE_RANGE(name) ((void)0)
 #endif
 
+namespace sse {
+
 namespace {
-
-using sse::Carver;
-using sse::RouteBuffers;
-
-constexpr int32_t kAbiVersion = 1;
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 int elem_bytes(const sse_config_t &c) { return c.dtype == SSE_BF16 ? 2 : 4; }
+}  // namespace
 
-// Checks shared by every entry point.
 sse_status_t check_config(const sse_config_t *cfg) {
     if (!cfg) return SSE_ERR_INVALID_ARG;
     const sse_config_t &c = *cfg;
@@ -42,7 +36,8 @@ sse_status_t check_config(const sse_config_t *cfg) {
     if (c.dtype != SSE_F32 && c.dtype != SSE_BF16) return SSE_ERR_INVALID_ARG;
     if (c.algo < SSE_ALGO_AUTO || c.algo > SSE_ALGO_MASKED) return SSE_ERR_INVALID_ARG;
     if (!std::isfinite(c.scale)) return SSE_ERR_INVALID_ARG;
-    if (c.num_partitions > sse::kMaxPartitions || c.top_k > sse::kMaxTopK) return SSE_ERR_UNSUPPORTED;
+    if (c.num_partitions > kMaxPartitions || c.top_k > kMaxTopK) return SSE_ERR_UNSUPPORTED;
+    if (c.num_heads > kMaxHeads || c.key_dim > kMaxDim || c.value_dim > kMaxDim) return SSE_ERR_UNSUPPORTED;
     if ((c.key_dim * elem_bytes(c)) % 16 || (c.value_dim * elem_bytes(c)) % 16) return SSE_ERR_UNSUPPORTED;
     return SSE_OK;
 }
@@ -50,12 +45,29 @@ sse_status_t check_config(const sse_config_t *cfg) {
 sse_status_t check_sizes(const sse_config_t &c, int64_t total_tokens, int32_t num_seqs) {
     if (num_seqs < 0 || total_tokens < 0) return SSE_ERR_INVALID_ARG;
     if (num_seqs == 0 && total_tokens != 0) return SSE_ERR_INVALID_ARG;
+    // Bound each factor before forming a product: with total_tokens < 2^31,
+    // heads <= kMaxHeads and top_k <= kMaxTopK every product below fits in
+    // 64 bits.
+    if (total_tokens >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
     const int64_t recs = total_tokens * c.num_heads * c.top_k;
     if (recs >= (int64_t(1) << 31) || total_tokens * c.top_k >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * c.num_heads * c.num_partitions >= (int64_t(1) << 30)) return SSE_ERR_UNSUPPORTED;
-    if (sse::chunked_part_rows(c, total_tokens, num_seqs) >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    if (chunked_part_rows(c, total_tokens, num_seqs) >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
     return SSE_OK;
 }
+
+}  // namespace sse
+
+namespace {
+
+using sse::Carver;
+using sse::RouteBuffers;
+using sse::check_config;
+using sse::check_sizes;
+
+constexpr int32_t kAbiVersion = 2;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Route-stage buffers carved from the workspace.  User-provided outputs are
 // used in place; missing ones live in the workspace.
@@ -87,6 +99,26 @@ bool use_chunked(const sse_config_t &c) {
     if (c.algo == SSE_ALGO_RECURRENT) return false;
     if (c.algo == SSE_ALGO_CHUNKED || c.algo == SSE_ALGO_MASKED) return true;
     return sse::chunked_supported(c);
+}
+
+// The concrete algorithm AUTO stands for (a pure function of the
+// configuration, so the workspace size and the call agree).  The pages'
+// two schedules ("Scaling Linear Attention with Sparse State Expansion",
+// section 2.6): masking (every routed partition over the whole sequence) and
+// varlen grouping.  With top_k == N every token selects every partition: the
+// grouping is the identity, the two schedules do the same chunk work, and the
+// masking schedule skips the token->partition sort, so AUTO takes it.  For
+// top_k < N masking does (N + shared) / (k + shared) times the chunk work;
+// measured on GB300 it was slower on every such workload, short ones included
+// (B2 T2048 H4 c=d=64 N8 k2: 0.108 ms masked vs 0.090 ms grouped), so AUTO
+// takes the grouped schedule -- and the recurrent path for shapes outside the
+// tensor-core path.
+sse_config_t resolve_algo(const sse_config_t &c, int64_t /*total_tokens*/, int32_t /*num_seqs*/) {
+    sse_config_t r = c;
+    if (c.algo != SSE_ALGO_AUTO) return r;
+    if (!sse::chunked_supported(c)) r.algo = SSE_ALGO_RECURRENT;
+    else r.algo = c.top_k == c.num_partitions ? SSE_ALGO_MASKED : SSE_ALGO_CHUNKED;
+    return r;
 }
 
 struct ForwardLayout {
@@ -136,6 +168,7 @@ const char *sse_status_string(sse_status_t s) {
     case SSE_ERR_WORKSPACE: return "SSE_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case SSE_ERR_CUDA: return "SSE_ERR_CUDA: kernel launch failed";
     case SSE_ERR_DEVICE: return "SSE_ERR_DEVICE: a device-side check failed";
+    case SSE_ERR_DEVICE_TIMEOUT: return "SSE_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel expired";
     default: return "unknown sse_status_t";
     }
 }
@@ -172,8 +205,10 @@ sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits, const
 }
 
 size_t sse_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs) {
-    if (check_config(cfg) != SSE_OK || check_sizes(*cfg, total_tokens, num_seqs) != SSE_OK) return 0;
-    return carve_forward(nullptr, *cfg, total_tokens, num_seqs, nullptr, nullptr).bytes;
+    if (check_config(cfg) != SSE_OK) return 0;
+    const sse_config_t c = resolve_algo(*cfg, total_tokens, num_seqs);
+    if (check_sizes(c, total_tokens, num_seqs) != SSE_OK) return 0;
+    return carve_forward(nullptr, c, total_tokens, num_seqs, nullptr, nullptr).bytes;
 }
 
 sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const void *k, const void *v,
@@ -187,8 +222,8 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     if (num_launches) *num_launches = 0;
     sse_status_t st = check_config(cfg);
     if (st != SSE_OK) return st;
-    if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
-    const sse_config_t &c = *cfg;
+    const sse_config_t c = resolve_algo(*cfg, total_tokens, num_seqs);
+    if ((st = check_sizes(c, total_tokens, num_seqs)) != SSE_OK) return st;
     if (!cu_seqlens) return SSE_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!q || !k || !v || !log_gate || !router_logits || !out))
         return SSE_ERR_INVALID_ARG;
@@ -244,6 +279,7 @@ sse_status_t sse_forward_timed(const sse_config_t *cfg, const void *q, const voi
     a.part_bf16 = use_chunked(c) ? 1 : 0;
     a.flags = L.flags;
     a.chunk_ws = L.chunk_ws;
+    a.redo_list = L.chunk_ws ? reinterpret_cast<int32_t *>(static_cast<unsigned char *>(L.chunk_ws) + 256) : nullptr;
     if (use_chunked(c)) {
         e = sse::launch_forward_chunked(c, a, s, &launches);
         if (e != cudaSuccess || mark(2) != cudaSuccess) return SSE_ERR_CUDA;
@@ -366,7 +402,14 @@ sse_status_t sse_read_device_status(void *workspace, int32_t *flags, sse_stream_
         return SSE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SSE_ERR_CUDA;
     *flags = host;
-    return host ? SSE_ERR_DEVICE : SSE_OK;
+    if (host & SSE_DEVICE_TIMEOUT) return SSE_ERR_DEVICE_TIMEOUT;
+    if (host & ~SSE_DEVICE_RECOMPUTED) return SSE_ERR_DEVICE;
+    return SSE_OK;
+}
+
+sse_status_t sse_get_last_device_error(void *workspace, sse_stream_t stream) {
+    int32_t flags = 0;
+    return sse_read_device_status(workspace, &flags, stream);
 }
 
 }  // extern "C"

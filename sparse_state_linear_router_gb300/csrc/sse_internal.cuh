@@ -12,6 +12,8 @@ namespace sse {
 
 constexpr int kMaxPartitions = 64;
 constexpr int kMaxTopK = 8;
+constexpr int kMaxHeads = 1 << 16;  // bounds the size products of the host checks
+constexpr int kMaxDim = 1 << 12;    // key_dim, value_dim
 constexpr int kRouteBlock = 256;  // tokens per routing block (one thread per token)
 constexpr int kRouteLaunches = 5; // kernels launch_route issues when grouping
 constexpr int kChunkRows = 128;   // rows of a tensor-core chunk; output regions are padded to it
@@ -155,6 +157,14 @@ __device__ __forceinline__ void route_token_warp(const T *logit, int N, int k, i
 }
 
 // ---------------------------------------------------------------------------
+// Host-side argument checks shared by every entry point (sse_api.cu):
+// check_config validates the configuration, check_sizes the token and
+// sequence counts against the kernels' 32-bit row and record indices.
+// ---------------------------------------------------------------------------
+sse_status_t check_config(const sse_config_t *cfg);
+sse_status_t check_sizes(const sse_config_t &c, int64_t total_tokens, int32_t num_seqs);
+
+// ---------------------------------------------------------------------------
 // Workspace carving (256-byte aligned regions).
 // ---------------------------------------------------------------------------
 struct Carver {
@@ -222,8 +232,9 @@ struct ForwardArgs {
     void *part_routed;   // recurrent: [T, H, k, d] fp32; chunked: [part_rows, d] bf16 in work-item order
     void *part_shared;   // recurrent: [T, H, d] fp32; chunked: unused
     int32_t part_bf16;
-    int32_t *flags;
+    int32_t *flags;      // [0]: device-check flags; [1]: entries of redo_list
     void *chunk_ws;      // chunked path scratch
+    int32_t *redo_list;  // chunked path: work items to recompute token by token
 };
 
 bool recurrent_supported(const sse_config_t &cfg);

@@ -40,6 +40,8 @@ __all__ = [
     "FRONT_END_WORKLOADS",
     "FrontEndInputs",
     "make_front_end_inputs",
+    "make_forward_inputs_device",
+    "workload_lengths",
     "f32_to_bf16_bits",
     "bf16_bits_to_f32",
 ]
@@ -161,6 +163,54 @@ class DecodeInputs:
     v: np.ndarray            # [B, H, d]
     g: np.ndarray
     logits: np.ndarray       # [B, H, N]
+
+
+def workload_lengths(w: Workload, seed: int = 0) -> np.ndarray:
+    """The sequence lengths make_forward_inputs(w, seed) uses (the first draw
+    of a varlen workload's generator)."""
+    if w.varlen is not None:
+        ns, lo, hi = w.varlen
+        return np.random.default_rng(seed).integers(lo, hi + 1, ns)
+    return np.asarray(w.lengths, dtype=np.int64)
+
+
+def make_forward_inputs_device(w: Workload, seed: int = 0, device="cuda", router_bias=None):
+    """One forward batch of workload ``w`` drawn on the GPU with torch's
+    generator (benchmark inputs at full size in well under a second): the same
+    shapes, sequence lengths (workload_lengths) and distributions as
+    make_forward_inputs -- q = N(0,1)/sqrt(c), k = softmax over c of N(0,1),
+    v = N(0,1), g = logsigmoid(N(0,1))/16, logits = N(0, sigma_r) (+ an
+    optional per-partition bias, for load-skew stress runs), initial state
+    N(0, init_std) -- but another stream of numbers, so parity tests keep the
+    numpy generator.  Returns dict of device tensors (bf16 token tensors, int32
+    cu_seqlens, float32 init or None)."""
+    import torch
+    assert w.dtype == "bf16"
+    lengths = workload_lengths(w, seed)
+    cu = np.zeros(len(lengths) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lengths)
+    T, S = int(cu[-1]), len(lengths)
+    H, c, d, N = w.num_heads, w.key_dim, w.value_dim, w.num_partitions
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normal(*shape):
+        return torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+
+    out = {
+        "q": (normal(T, H, c) / np.sqrt(c)).to(torch.bfloat16),
+        "k": torch.softmax(normal(T, H, c), dim=-1).to(torch.bfloat16),
+        "v": normal(T, H, d).to(torch.bfloat16),
+        "g": (torch.nn.functional.logsigmoid(normal(T, H, c)) / 16.0).to(torch.bfloat16),
+    }
+    lg = normal(T, H, N) * w.sigma_router
+    if router_bias is not None:
+        lg = lg + torch.as_tensor(np.asarray(router_bias, dtype=np.float32), device=device)
+    out["logits"] = lg.to(torch.bfloat16)
+    out["cu_seqlens"] = torch.from_numpy(cu.astype(np.int32)).to(device)
+    out["init"] = (normal(S, H, w.num_slots, c, d) * w.init_std) if w.init_std is not None else None
+    out["total_tokens"], out["num_seqs"] = T, S
+    return out
 
 
 def make_forward_inputs(w: Workload, seed: int = 0, lengths=None, with_init=None) -> LayerInputs:

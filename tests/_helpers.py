@@ -62,7 +62,7 @@ def run_gpu_forward(w: synth.Workload, inp: synth.LayerInputs, algo="auto", scal
     st, flags = binding.sse_read_device_status(res["workspace"].data_ptr(), binding._stream())
     return {"out": to_numpy(res["out"]), "final_state": to_numpy(res["final_state"]),
             "topk_idx": to_numpy(res["topk_idx"]), "topk_w": to_numpy(res["topk_w"]),
-            "device_flags": flags}
+            "device_flags": flags, "device_status": st}
 
 
 def run_oracle_forward(w: synth.Workload, inp: synth.LayerInputs, scale=1.0, pairs=None,

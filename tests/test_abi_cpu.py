@@ -34,9 +34,10 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     from sparse_state_linear_router_gb300 import binding
-    assert binding.sse_abi_version() == 1
-    for s in range(6):
+    assert binding.sse_abi_version() == 2
+    for s in range(7):
         assert binding.sse_status_string(s).startswith("SSE_")
+    assert binding.sse_status_string(binding.SSE_ERR_DEVICE_TIMEOUT).startswith("SSE_ERR_DEVICE_TIMEOUT")
 
 
 def _cfg(**kw):
@@ -164,3 +165,54 @@ def test_size_limits_rejected_before_launch(lib):
     # decode: batch * H must fit in 31 bits
     assert b.sse_decode_step(_cfg(num_heads=64), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, (1 << 31) // 64,
                              FAKE, FAKE, None, None, None) == b.SSE_ERR_UNSUPPORTED
+
+
+def test_noalloc_route_checks_match_route(lib):
+    """sse_route_noalloc runs the same configuration and size checks as
+    sse_route: a bad argument gets the same status from both, before any
+    launch (the size limit of the no-allocation scratch aside)."""
+    from sparse_state_linear_router_gb300 import binding as b
+    bad = [
+        (_cfg(top_k=0), 1, 16),
+        (_cfg(top_k=9, num_partitions=8), 1, 16),
+        (_cfg(num_partitions=65, top_k=2), 1, 16),
+        (_cfg(top_k=9, num_partitions=16), 1, 16),
+        (_cfg(use_shared=2), 1, 16),
+        (_cfg(dtype=7), 1, 16),
+        (_cfg(algo=9), 1, 16),
+        (_cfg(scale=float("inf")), 1, 16),
+        (_cfg(key_dim=12), 1, 16),
+        (_cfg(num_heads=1 << 17), 1, 16),
+        (_cfg(), -1, 16),
+        (_cfg(), 1, -1),
+        (_cfg(), 0, 5),
+        (_cfg(num_heads=16), 1, (1 << 31) // 32 + 1),
+        (_cfg(), 1, 1 << 40),    # total_tokens past 2^31: refused before any product is formed
+        (_cfg(), 1, (1 << 63) - 1),
+    ]
+    for cfg, S, T in bad:
+        st_route = b.sse_route(cfg, FAKE, FAKE, S, T, FAKE, None, None, None, FAKE, 1 << 40, None)
+        st_noalloc = lib.sse_route_noalloc(ctypes.byref(cfg), FAKE, FAKE, S, T, FAKE, None, None, None, None)
+        assert st_route != b.SSE_OK
+        assert st_noalloc == st_route, (cfg.num_heads, cfg.top_k, S, T, st_noalloc, st_route)
+    # argument pointers: same rules
+    cfg = _cfg()
+    assert lib.sse_route_noalloc(ctypes.byref(cfg), FAKE, FAKE, 1, 16, None, None, None, None,
+                                 None) == b.SSE_ERR_INVALID_ARG
+    assert lib.sse_route_noalloc(ctypes.byref(cfg), FAKE, FAKE, 1, 16, FAKE, None, FAKE, None,
+                                 None) == b.SSE_ERR_INVALID_ARG
+    assert lib.sse_route_noalloc(ctypes.byref(cfg), FAKE + 8, FAKE, 1, 16, FAKE, None, None, None,
+                                 None) == b.SSE_ERR_INVALID_ARG
+    assert lib.sse_route_noalloc(None, FAKE, FAKE, 1, 16, FAKE, None, None, None, None) == b.SSE_ERR_INVALID_ARG
+    # an empty batch is valid and launches nothing
+    assert lib.sse_route_noalloc(ctypes.byref(cfg), None, FAKE, 0, 0, FAKE, None, None, None, None) == b.SSE_OK
+
+
+def test_device_status_readers_reject_bad_workspace(lib):
+    """sse_read_device_status / sse_get_last_device_error validate the
+    workspace pointer on the host (null or not 256-byte aligned) before any
+    copy."""
+    from sparse_state_linear_router_gb300 import binding as b
+    assert b.sse_get_last_device_error(None, None) == b.SSE_ERR_INVALID_ARG
+    assert b.sse_get_last_device_error(FAKE + 64, None) == b.SSE_ERR_INVALID_ARG
+    assert b.sse_read_device_status(None, None)[0] == b.SSE_ERR_INVALID_ARG

@@ -95,3 +95,59 @@ def test_decode_matches_forward_continuation():
         torch.cuda.synchronize()
         assert H_.max_abs_rel(H_.to_numpy(r["out"])[0], full["out"][t]) < H_.TOL_BF16
     assert H_.max_abs_rel(H_.to_numpy(st), full["final_state"]) < H_.TOL_BF16
+
+
+def test_decode_1000_steps_full_size():
+    """The full decode workload run for 1000 consecutive steps on states
+    resident in device memory: 256 sequences x 16 heads, N = 16 routed
+    partitions of 128 x 128 plus the shared one (4.6 GB of float32 states),
+    fresh seeded inputs every step (seed 1000 + s).  The fp64 oracle follows a
+    sample of sequences (first, middle, last and two others) through every
+    step; routing is compared bit for bit every step, outputs and states at
+    steps 0, 1, 499 and 999 (float32 drift of the in-place updates would show
+    there); every step, every state the step did not select must be
+    bit-identical to before the step ("Scaling Linear Attention with Sparse
+    State Expansion", section 2.6: decoding recurs only on the selected
+    states)."""
+    import concurrent.futures as cf
+
+    import oracle
+    from sparse_state_linear_router_gb300 import binding
+    w = synth.WORKLOADS["decode_bf16"]
+    B, H, N, P = w.decode_batch, w.num_heads, w.num_partitions, w.num_slots
+    steps, checkpoints = 1000, {0, 1, 499, 999}
+    sample = np.array([0, 61, 128, 200, B - 1])
+    cfg = H_.config_of(w)
+    dstate = torch.zeros((B, H, P, w.key_dim, w.value_dim), dtype=torch.float32, device="cuda")
+    before = torch.empty_like(dstate)
+    ref_state = np.zeros((len(sample), H, P, w.key_dim, w.value_dim), dtype=np.float64)
+    checked = []
+    # the inputs of later steps are drawn on host threads while the GPU and the
+    # oracle work on the current one (numpy's generators and ufuncs release the GIL)
+    with cf.ThreadPoolExecutor(max_workers=8) as pool:
+        futs = {s: pool.submit(synth.make_decode_inputs, w, s, B) for s in range(min(steps, 16))}
+        for s in range(steps):
+            tok = futs.pop(s).result()
+            if s + 16 < steps:
+                futs[s + 16] = pool.submit(synth.make_decode_inputs, w, s + 16, B)
+            before.copy_(dstate)
+            dv = {n: binding.to_device(getattr(tok, n)) for n in ("q", "k", "v", "g", "logits")}
+            r = binding.decode_step(cfg, dstate, dv["q"], dv["k"], dv["v"], dv["g"], dv["logits"],
+                                    want_routing=True)
+            ref = oracle.decode_step(ref_state, *(getattr(tok, n)[sample] for n in ("q", "k", "v", "g", "logits")),
+                                     top_k=w.top_k, use_shared=w.use_shared)
+            all_idx = H_.to_numpy(r["topk_idx"])
+            assert np.array_equal(all_idx[sample], ref["topk_idx"]), s
+            # states the step did not select: bit-identical
+            changed = (dstate != before).flatten(3).any(-1).cpu().numpy()  # [B, H, P]
+            sel = np.zeros(changed.shape, dtype=bool)
+            np.put_along_axis(sel, all_idx.astype(np.int64), True, axis=-1)
+            sel[..., N] = True
+            assert not np.any(changed & ~sel), s
+            if s in checkpoints:
+                e_out = H_.max_abs_rel(H_.to_numpy(r["out"])[sample], ref["out"])
+                e_st = H_.max_abs_rel(H_.to_numpy(dstate[torch.from_numpy(sample).cuda()]), ref_state)
+                checked.append((s, e_out, e_st))
+                assert e_out < H_.TOL_BF16 and e_st < H_.TOL_BF16, (s, e_out, e_st)
+    assert [c[0] for c in checked] == sorted(checkpoints)
+    print("decode 1000 steps: (step, out err, state err)", checked)

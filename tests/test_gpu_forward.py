@@ -66,7 +66,7 @@ def test_forward_matches_oracle(name, algo):
     np.testing.assert_allclose(gpu["topk_w"], ref["topk_w"], rtol=2e-6, atol=1e-7)
     assert H_.max_abs_rel(gpu["out"], ref["out"]) < tol
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < tol
-    assert gpu["device_flags"] == 0
+    assert gpu["device_flags"] == 0 and gpu["device_status"] == 0
 
 
 def test_forward_scale_and_separate_shared_qk():
@@ -142,7 +142,7 @@ def test_full_size_sampled_pairs(wname):
     w = synth.WORKLOADS[wname]
     inp = synth.make_forward_inputs(w, seed=0)
     gpu = H_.run_gpu_forward(w, inp)
-    assert gpu["device_flags"] == 0
+    assert gpu["device_flags"] == 0 and gpu["device_status"] == 0
     assert np.array_equal(gpu["topk_idx"], _stable_topk(inp.logits, w.top_k))
     S, H = inp.num_seqs, w.num_heads
     rng = np.random.default_rng(123)
@@ -171,7 +171,7 @@ def test_skewed_routing(algo, strength):
     assert np.array_equal(gpu["topk_idx"], ref["topk_idx"])
     assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
-    assert gpu["device_flags"] == 0
+    assert gpu["device_flags"] == 0 and gpu["device_status"] == 0
 
 
 @pytest.mark.parametrize("algo", ["recurrent", "chunked", "masked"])
@@ -186,24 +186,76 @@ def test_chunk_boundary_lengths(algo):
     ref = H_.run_oracle_forward(w, inp)
     assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
-    assert gpu["device_flags"] == 0
+    assert gpu["device_flags"] == 0 and gpu["device_status"] == 0
 
 
-@pytest.mark.parametrize("algo", ["chunked", "masked"])
+@pytest.mark.parametrize("algo", ["auto", "chunked", "masked"])
 @pytest.mark.parametrize("base", ["small_bf16", "layer_bf16"])
-def test_gate_range_flag(algo, base):
-    """The tensor-core schedules split each chunk's decay factors at its
-    midpoint and need every half chunk's summed log-gate above -80 per key
-    row: a constant log-gate of -2 (half-chunk sum -128) sets
-    SSE_DEVICE_GATE_RANGE; -1 (sum -64) stays in range and matches the oracle."""
+def test_strong_gates(algo, base):
+    """Every decay in (0, 1] gives a valid result (eq. 13 takes any diagonal
+    gate).  The tensor-core schedules evaluate a chunk in factorised form only
+    while each half chunk's summed log-gate stays above -64 per key row: a
+    constant log-gate of -1 (half-chunk sum -64) stays on that path; -2 (sum
+    -128), a mix with a fifth of the rows at -5, and a single row at -200
+    (decay e^-200, zero in float32) are recomputed token by token in the same
+    call -- all match the oracle, with no error status."""
+    from sparse_state_linear_router_gb300 import binding
     w = H_.workload_variant(base, num_heads=2, num_partitions=4, top_k=2)
-    inp = synth.make_forward_inputs(w, seed=5, lengths=[300, 64])
-    for gate, flagged in ((-1.0, False), (-2.0, True)):
-        inp.g = synth.f32_to_bf16_bits(np.full(inp.q.shape, gate, dtype=np.float32))
+    inp = synth.make_forward_inputs(w, seed=5, lengths=[300, 64, 0, 517], with_init=True)
+    rng = np.random.default_rng(8)
+    base_g = synth.bf16_bits_to_f32(inp.g)
+    mixed = np.where(rng.random(size=inp.q.shape[:2] + (1,)) < 0.2, -5.0, base_g).astype(np.float32)
+    spike = base_g.copy()
+    spike[150, :, :] = -200.0
+    cases = (("const -1", np.full(inp.q.shape, -1.0, np.float32), False),
+             ("const -2", np.full(inp.q.shape, -2.0, np.float32), True),
+             ("mixed -5", mixed, True),
+             ("one row -200", spike, True))
+    for name, gate, redo in cases:
+        inp.g = synth.f32_to_bf16_bits(gate)
         gpu = H_.run_gpu_forward(w, inp, algo=algo)
-        assert (gpu["device_flags"] & 1) == (1 if flagged else 0), (gate, gpu["device_flags"])
-        assert (gpu["device_flags"] & 2) == 0
-        if not flagged:
-            ref = H_.run_oracle_forward(w, inp)
-            assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
-            assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
+        assert gpu["device_status"] == binding.SSE_OK, name
+        assert bool(gpu["device_flags"] & binding.SSE_DEVICE_RECOMPUTED) == redo, (name, gpu["device_flags"])
+        assert (gpu["device_flags"] & ~binding.SSE_DEVICE_RECOMPUTED) == 0, name
+        ref = H_.run_oracle_forward(w, inp)
+        assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16, name
+        assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16, name
+
+
+def _launches(w, inp, algo):
+    from sparse_state_linear_router_gb300 import binding
+    cfg = H_.config_of(w, algo)
+    t = {n: binding.to_device(getattr(inp, n)) for n in ("q", "k", "v", "g", "logits")}
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    T, S = inp.total_tokens, inp.num_seqs
+    P = w.num_partitions + w.use_shared
+    out = torch.empty((T, w.num_heads, w.value_dim), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((S, w.num_heads, P, w.key_dim, w.value_dim), dtype=torch.float32, device="cuda")
+    ws = binding.forward_workspace(cfg, T, S)
+    st, n = binding.sse_forward_timed(cfg, t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(),
+                                      t["g"].data_ptr(), t["logits"].data_ptr(), None, None, cu.data_ptr(), S, T,
+                                      None, fin.data_ptr(), out.data_ptr(), None, None, ws.data_ptr(),
+                                      ws.numel(), binding._stream())
+    assert st == binding.SSE_OK
+    torch.cuda.synchronize()
+    return n, H_.to_numpy(out), H_.to_numpy(fin)
+
+
+def test_auto_picks_the_schedule():
+    """AUTO takes the masking schedule ("Scaling Linear Attention with Sparse
+    State Expansion", section 2.6) when top_k == N -- every token selects
+    every partition, so the grouping is the identity and the sort is pure
+    overhead -- and the grouped varlen schedule otherwise; the launch count
+    tells them apart (masking: no token->partition sort) and the results are
+    the same bits."""
+    k_eq_n = H_.workload_variant("small_bf16", num_partitions=4, top_k=4)
+    for w, lengths, expect in ((k_eq_n, [300, 129], "masked"),
+                               (H_.workload_variant("small_bf16"), None, "chunked"),
+                               (H_.workload_variant("layer_bf16", num_heads=4), [200] * 8, "chunked"),
+                               (H_.workload_variant("small_bf16", use_shared=0), None, "chunked")):
+        inp = synth.make_forward_inputs(w, seed=6, lengths=lengths)
+        n_auto, out_auto, fin_auto = _launches(w, inp, "auto")
+        n_exp, out_exp, fin_exp = _launches(w, inp, expect)
+        n_other, _, _ = _launches(w, inp, "chunked" if expect == "masked" else "masked")
+        assert n_auto == n_exp != n_other, (expect, n_auto, n_exp, n_other)
+        assert np.array_equal(out_auto, out_exp) and np.array_equal(fin_auto, fin_exp)
