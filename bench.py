@@ -407,6 +407,58 @@ def time_forward_variants(args, dev, peaks):
     return res
 
 
+def time_fwd_bwd_fig6(args, dev, L=8192):
+    """Forward and backward times at the operator shape of the pages' Fig. 6
+    ("Scaling Linear Attention with Sparse State Expansion", section 2.6:
+    8 heads, head dim 128, top-1, N = 4 / 8 / 16, cu_seqlens = [0, L/2, L]),
+    bf16 token tensors, fp32 states, d_out ~ N(0, 1); the pages give no
+    numbers for it (a figure only)."""
+    import dataclasses
+
+    import torch
+    from sparse_state_linear_router_gb300 import binding
+    stream = torch.cuda.current_stream(dev)
+    P_ = binding._ptr
+    res = {}
+    for N in (4, 8, 16):
+        w = dataclasses.replace(synth.WORKLOADS["layer_bf16"], name=f"fig6_N{N}", num_heads=8, num_partitions=N,
+                                top_k=1, lengths=(L // 2, L // 2), sigma_router=1.0)
+        x = synth.make_forward_inputs_device(w, seed=0, device=dev)
+        T, S = x["total_tokens"], x["num_seqs"]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        d_out = torch.randn((T, w.num_heads, w.value_dim), generator=gen, device=dev).to(torch.bfloat16)
+        cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, N, 1, 1, 1.0, "bf16")
+        fws = binding.forward_workspace(cfg, T, S, dev)
+        bws = torch.empty(binding.sse_backward_workspace_size(cfg, T, S), dtype=torch.uint8, device=dev)
+        out = torch.empty((T, w.num_heads, w.value_dim), dtype=torch.bfloat16, device=dev)
+
+        def fwd():
+            binding.forward(cfg, x["q"], x["k"], x["v"], x["g"], x["logits"], x["cu_seqlens"], out=out,
+                            want_final_state=False, workspace=fws)
+
+        def bwd():
+            binding.backward(cfg, x["q"], x["k"], x["v"], x["g"], x["logits"], x["cu_seqlens"], d_out,
+                             want_d_initial_state=False, workspace=bws)
+
+        times = {}
+        for name, fn, reps in (("forward", fwd, 10), ("backward", bwd, 3)):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[name + "_ms"] = e0.elapsed_time(e1) / reps
+        res[f"N{N}"] = dict(times, fwd_bwd_ms=times["forward_ms"] + times["backward_ms"],
+                            workload=f"H8, c=d=128, top-1 of N={N}, shared, cu_seqlens=[0, {L // 2}, {L}], bf16")
+        del x, fws, bws, out, d_out
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_native(args):
     import torch
     ws, rank, local = _dist()
@@ -615,10 +667,11 @@ def run_native(args):
                "overlap": "inputs of step i copied on a second stream while step i-1 computes"}
 
     # ---- the other forward workloads (rank 0, N = 1, default run only) -------
-    variants, variant_clocks = None, None
+    variants, variant_clocks, fig6 = None, None, None
     if do_fwd and do_dec and rank == 0 and ws == 1 and not args.no_variants:
         with ClockSampler(local) as vclk:
             variants = time_forward_variants(args, dev, peaks)
+            fig6 = time_fwd_bwd_fig6(args, dev)
         variant_clocks = vclk.summary()
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------
@@ -672,6 +725,7 @@ def run_native(args):
     }
     if variants is not None:
         line["forward_variants"] = variants
+        line["fwd_bwd_fig6_shape"] = fig6
         line["forward_variants_clocks"] = variant_clocks
     print(json.dumps(line), flush=True)
     if ws > 1:

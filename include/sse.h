@@ -218,6 +218,40 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
                              sse_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * sse_backward -- gradients of the SSE layer (eqs. 9-14 and the shared
+ * partition of section 2.5) for L = <d_out, out> + <d_final_state,
+ * final_state>, the forward of sse_forward with the same arguments.  The
+ * router weight e_t[i] receives gradient from both the write and the read
+ * (section 2.3: the same e_t[i] appears in eq. 13 and eq. 14) and flows to the
+ * logits through the softmax over all N partitions; the top-k selection is
+ * piecewise constant and carries none.
+ *
+ *   d_out          [total_tokens, H, d] in cfg->dtype
+ *   d_final_state  float32 [num_seqs, H, P, c, d], may be NULL (zero)
+ *   dq, dk, d_log_gate [total_tokens, H, c]; dv [total_tokens, H, d];
+ *   d_router_logits [total_tokens, H, N]: all in cfg->dtype, fully written
+ *   dq_shared, dk_shared  [total_tokens, H, c]: given exactly when q_shared /
+ *                  k_shared are; with NULL q_shared the shared partition's
+ *                  query gradient is added into dq (likewise dk)
+ *   d_initial_state float32 [num_seqs, H, P, c, d], may be NULL (not written)
+ * The routing is recomputed from router_logits.  Every (token, head) gets
+ * one float32 contribution per selected partition and one from the shared
+ * partition, summed in a fixed order (deterministic).  Computed token by token
+ * in float32 on the CUDA cores (any shape the recurrent forward takes).
+ * Workspace: sse_backward_workspace_size bytes (256-byte aligned).
+ * ------------------------------------------------------------------------- */
+size_t sse_backward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
+
+sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                          const void *log_gate, const void *router_logits,
+                          const void *q_shared, const void *k_shared,
+                          const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                          const float *initial_state, const void *d_out, const float *d_final_state,
+                          void *dq, void *dk, void *dv, void *d_log_gate, void *d_router_logits,
+                          void *dq_shared, void *dk_shared, float *d_initial_state,
+                          void *workspace, size_t workspace_bytes, sse_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * sse_front_end -- the layer's projections from the hidden states
  * ("Scaling Linear Attention with Sparse State Expansion", eqs. 9-10; the
  * shared partition's rank-64 Q/K LoRA of section 2.5; GLA's diagonal gate).

@@ -31,7 +31,7 @@ _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_A
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
             "sse_route_noalloc", "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
             "sse_front_end_workspace_size", "sse_front_end", "sse_read_device_status",
-            "sse_get_last_device_error")
+            "sse_get_last_device_error", "sse_backward_workspace_size", "sse_backward")
 
 
 class sse_config_t(ctypes.Structure):
@@ -89,6 +89,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sse_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
     lib.sse_get_last_device_error.restype = ctypes.c_int
     lib.sse_get_last_device_error.argtypes = [P, P]
+    lib.sse_backward_workspace_size.restype = sz
+    lib.sse_backward_workspace_size.argtypes = [cfgp, i64, i32]
+    lib.sse_backward.restype = ctypes.c_int
+    lib.sse_backward.argtypes = [cfgp, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
     _lib = lib
     return lib
 
@@ -167,6 +171,18 @@ def sse_read_device_status(workspace, stream):
 
 def sse_get_last_device_error(workspace, stream) -> int:
     return load().sse_get_last_device_error(workspace, stream)
+
+
+def sse_backward_workspace_size(cfg: sse_config_t, total_tokens: int, num_seqs: int) -> int:
+    return load().sse_backward_workspace_size(ctypes.byref(cfg), total_tokens, num_seqs)
+
+
+def sse_backward(cfg, q, k, v, log_gate, logits, q_shared, k_shared, cu_seqlens, num_seqs, total_tokens,
+                 initial_state, d_out, d_final_state, dq, dk, dv, d_log_gate, d_logits, dq_shared, dk_shared,
+                 d_initial_state, workspace, workspace_bytes, stream) -> int:
+    return load().sse_backward(ctypes.byref(cfg), q, k, v, log_gate, logits, q_shared, k_shared, cu_seqlens,
+                               num_seqs, total_tokens, initial_state, d_out, d_final_state, dq, dk, dv, d_log_gate,
+                               d_logits, dq_shared, dk_shared, d_initial_state, workspace, workspace_bytes, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -269,6 +285,35 @@ def decode_step(cfg, state, q, k, v, log_gate, logits, *, q_shared=None, k_share
                            _ptr(q_shared), _ptr(k_shared), B, _ptr(state), _ptr(out), _ptr(idx),
                            _ptr(w), _stream()), "sse_decode_step")
     return {"out": out, "topk_idx": idx, "topk_w": w}
+
+
+def backward(cfg, q, k, v, log_gate, logits, cu_seqlens, d_out, *, q_shared=None, k_shared=None,
+             initial_state=None, d_final_state=None, want_d_initial_state=True, workspace=None):
+    """Gradients of <d_out, out> + <d_final_state, final_state> on device
+    tensors; returns dict(dq, dk, dv, dg, dlogits, dq_shared, dk_shared,
+    d_initial_state, workspace)."""
+    import torch
+    T = q.shape[0]
+    S = cu_seqlens.numel() - 1
+    H, c, d, N = cfg.num_heads, cfg.key_dim, cfg.value_dim, cfg.num_partitions
+    P = N + cfg.use_shared
+    dev = q.device
+    dt = _token_dtype(cfg)
+    e = lambda w: torch.empty((T, H, w), dtype=dt, device=dev)  # noqa: E731
+    out = {"dq": e(c), "dk": e(c), "dv": e(d), "dg": e(c), "dlogits": e(N),
+           "dq_shared": e(c) if q_shared is not None else None,
+           "dk_shared": e(c) if k_shared is not None else None,
+           "d_initial_state": (torch.empty((S, H, P, c, d), dtype=torch.float32, device=dev)
+                               if want_d_initial_state else None)}
+    if workspace is None:
+        workspace = torch.empty(max(sse_backward_workspace_size(cfg, T, S), 256), dtype=torch.uint8, device=dev)
+    _check(sse_backward(cfg, _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(logits), _ptr(q_shared),
+                        _ptr(k_shared), _ptr(cu_seqlens), S, T, _ptr(initial_state), _ptr(d_out),
+                        _ptr(d_final_state), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                        _ptr(out["dlogits"]), _ptr(out["dq_shared"]), _ptr(out["dk_shared"]),
+                        _ptr(out["d_initial_state"]), _ptr(workspace), workspace.numel(), _stream()),
+           "sse_backward")
+    return dict(out, workspace=workspace)
 
 
 def front_end(cfg, x, w_q, w_k, w_v, w_g, w_e, *, a_q=None, b_q=None, a_k=None, b_k=None,

@@ -711,7 +711,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             const uint32_t tA = tmem + lb + kTmemA, tS = tmem + lb + kTmemS;
             // initial state -> TMEM
             if (row < KC) {
-#pragma unroll
+#pragma unroll 1  // once per segment: rolled, small code
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     uint32_t r[32];
                     const float *src = a.init ? a.init + state_off + (int64_t)row * DV + c0 : nullptr;
@@ -743,7 +743,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 const float w = (MASKED ? fmaxf(meta_e(st)[row], 0.f) : meta_e(st)[row]) * scale;
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
                 unsigned char *stg = sm + Smem::S;
-#pragma unroll
+#pragma unroll 1  // one 32-column block per iteration: keeps the hot code small
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tO + c0, r);
@@ -798,7 +798,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     // factors are applied one after the other because their product
                     // (down to e^-160 within the gate range) would underflow
                     const float fm = s_fmid[row];
-#pragma unroll
+#pragma unroll 1  // one 32-column block per iteration: keeps the hot code small
                     for (int c0 = 0; c0 < DV; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tS + c0, r);
@@ -826,7 +826,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 fence_after();
                 // warp w holds rows 32w..32w+31: column blocks left of the diagonal
                 // block are copied, the diagonal block is masked, the rest is 0
-#pragma unroll
+#pragma unroll 1  // one 32-column block per iteration: keeps the hot code small
                 for (int c0 = 0; c0 < kC; c0 += 32) {
                     if (c0 > 32 * warp) {
 #pragma unroll
@@ -870,7 +870,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             bulk_wait_all();
             // final state = p * S_stored
             if (!failed && a.final_state && row < KC) {
-#pragma unroll
+#pragma unroll 1  // once per segment: rolled, small code
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tS + c0, r);

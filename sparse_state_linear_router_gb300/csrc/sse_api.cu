@@ -102,22 +102,17 @@ bool use_chunked(const sse_config_t &c) {
 }
 
 // The concrete algorithm AUTO stands for (a pure function of the
-// configuration, so the workspace size and the call agree).  The pages'
-// two schedules ("Scaling Linear Attention with Sparse State Expansion",
-// section 2.6): masking (every routed partition over the whole sequence) and
-// varlen grouping.  With top_k == N every token selects every partition: the
-// grouping is the identity, the two schedules do the same chunk work, and the
-// masking schedule skips the token->partition sort, so AUTO takes it.  For
-// top_k < N masking does (N + shared) / (k + shared) times the chunk work;
-// measured on GB300 it was slower on every such workload, short ones included
-// (B2 T2048 H4 c=d=64 N8 k2: 0.108 ms masked vs 0.090 ms grouped), so AUTO
-// takes the grouped schedule -- and the recurrent path for shapes outside the
-// tensor-core path.
+// configuration, so the workspace size and the call agree): the grouped
+// varlen schedule wherever the tensor-core path applies, else the recurrent
+// path.  The pages ("Scaling Linear Attention with Sparse State Expansion",
+// section 2.6) name masking for short inputs; on GB300 it was slower in every
+// measured case, short ones and top_k == N (identity grouping) included --
+// B2 T2048 H4 c=d=64 N8 k2: 0.109 ms masked vs 0.092 ms grouped; the same
+// with N = k = 4: 0.131 vs 0.093 ms; B8 T4096 H16 c=d=128 N8 k2 with skewed
+// loads: 1.53 vs 0.63 ms -- so AUTO never picks it.
 sse_config_t resolve_algo(const sse_config_t &c, int64_t /*total_tokens*/, int32_t /*num_seqs*/) {
     sse_config_t r = c;
-    if (c.algo != SSE_ALGO_AUTO) return r;
-    if (!sse::chunked_supported(c)) r.algo = SSE_ALGO_RECURRENT;
-    else r.algo = c.top_k == c.num_partitions ? SSE_ALGO_MASKED : SSE_ALGO_CHUNKED;
+    if (c.algo == SSE_ALGO_AUTO) r.algo = sse::chunked_supported(c) ? SSE_ALGO_CHUNKED : SSE_ALGO_RECURRENT;
     return r;
 }
 
@@ -328,6 +323,90 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
     cudaError_t e = sse::launch_decode(*cfg, q, k, v, log_gate, router_logits, q_shared, k_shared,
                                        batch, state, out, topk_idx, topk_w,
                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
+
+namespace {
+struct BackwardLayout {
+    RouteBuffers rb;
+    float *dq_c, *dk_c, *dg_c, *dv_c, *de_c;
+    size_t bytes;
+};
+
+BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_t S) {
+    Carver cv(ws);
+    BackwardLayout L{};
+    L.rb = carve_route(cv, c, T, S, nullptr, nullptr, nullptr, nullptr, true, true);
+    const size_t slots = (size_t)T * c.num_heads * (c.top_k + c.use_shared);
+    L.dq_c = cv.take<float>(slots * c.key_dim);
+    L.dk_c = cv.take<float>(slots * c.key_dim);
+    L.dg_c = cv.take<float>(slots * c.key_dim);
+    L.dv_c = cv.take<float>(slots * c.value_dim);
+    L.de_c = cv.take<float>((size_t)T * c.num_heads * c.top_k * 2);
+    L.bytes = (cv.off + 255) & ~size_t(255);
+    return L;
+}
+}  // namespace
+
+size_t sse_backward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs) {
+    if (check_config(cfg) != SSE_OK || check_sizes(*cfg, total_tokens, num_seqs) != SSE_OK) return 0;
+    return carve_backward(nullptr, *cfg, total_tokens, num_seqs).bytes;
+}
+
+sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                          const void *log_gate, const void *router_logits, const void *q_shared,
+                          const void *k_shared, const int32_t *cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, const float *initial_state, const void *d_out,
+                          const float *d_final_state, void *dq, void *dk, void *dv, void *d_log_gate,
+                          void *d_router_logits, void *dq_shared, void *dk_shared, float *d_initial_state,
+                          void *workspace, size_t workspace_bytes, sse_stream_t stream) {
+    SSE_RANGE("sse_backward");
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
+    const sse_config_t &c = *cfg;
+    if (!cu_seqlens) return SSE_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !log_gate || !router_logits || !d_out || !dq || !dk || !dv ||
+                             !d_log_gate || !d_router_logits))
+        return SSE_ERR_INVALID_ARG;
+    // separate shared q / k get their own gradient buffers (and only then)
+    if ((q_shared != nullptr) != (dq_shared != nullptr) || (k_shared != nullptr) != (dk_shared != nullptr))
+        return SSE_ERR_INVALID_ARG;
+    for (const void *p : std::initializer_list<const void *>{q, k, v, log_gate, router_logits, q_shared, k_shared,
+                                                             (const void *)initial_state, d_out,
+                                                             (const void *)d_final_state, dq, dk, dv, d_log_gate,
+                                                             d_router_logits, dq_shared, dk_shared,
+                                                             (const void *)d_initial_state})
+        if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
+    if (!sse::backward_supported(c)) return SSE_ERR_UNSUPPORTED;
+    const size_t need = sse_backward_workspace_size(cfg, total_tokens, num_seqs);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return SSE_ERR_WORKSPACE;
+    if (num_seqs == 0) return SSE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    BackwardLayout L = carve_backward(workspace, c, total_tokens, num_seqs);
+    cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, true, s);
+    if (e != cudaSuccess) return SSE_ERR_CUDA;
+    sse::BackwardArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = log_gate; a.logits = router_logits;
+    a.qs = c.use_shared ? q_shared : nullptr;
+    a.ks = c.use_shared ? k_shared : nullptr;
+    a.d_out = d_out;
+    a.cu_seqlens = cu_seqlens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.init = initial_state;
+    a.d_final = d_final_state;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = d_log_gate; a.d_logits = d_router_logits;
+    a.dq_shared = dq_shared; a.dk_shared = dk_shared;
+    a.d_init = d_initial_state;
+    a.seg_off = L.rb.seg_off;
+    a.perm_rec = L.rb.perm_rec;
+    a.perm_e = L.rb.perm_e;
+    a.topk_idx = L.rb.topk_idx;
+    a.dq_c = L.dq_c; a.dk_c = L.dk_c; a.dg_c = L.dg_c; a.dv_c = L.dv_c; a.de_c = L.de_c;
+    int launches = sse::kRouteLaunches;
+    e = sse::launch_backward(c, a, s, &launches);
     return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
 }
 

@@ -253,6 +253,26 @@ cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a,
 // Rows of the chunked path's partial buffer: every work item padded to whole chunks.
 int64_t chunked_part_rows(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs);
 
+// Backward (backward.cu): pointers as in sse_backward, plus the routing of
+// the forward (recomputed) and the float32 contribution slots
+// [T, H, k + shared, width] of every (token, head) that the per-token pass sums.
+struct BackwardArgs {
+    const void *q, *k, *v, *g, *logits, *qs, *ks, *d_out;
+    const int32_t *cu_seqlens;
+    int32_t num_seqs;
+    int64_t total_tokens;
+    const float *init, *d_final;
+    void *dq, *dk, *dv, *dg, *d_logits, *dq_shared, *dk_shared;
+    float *d_init;
+    const int32_t *seg_off, *perm_rec, *topk_idx;
+    const float *perm_e;
+    float *dq_c, *dk_c, *dg_c, *dv_c;  // contribution slots
+    float *de_c;                       // [T, H, k, 2] router-weight gradient of each selected partition (read, write)
+};
+bool backward_supported(const sse_config_t &cfg);
+// Adds the number of kernels it launched to *launches.
+cudaError_t launch_backward(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream, int *launches);
+
 bool decode_supported(const sse_config_t &cfg);
 cudaError_t launch_decode(const sse_config_t &cfg, const void *q, const void *k, const void *v,
                           const void *g, const void *logits, const void *qs, const void *ks,

@@ -216,3 +216,31 @@ def test_device_status_readers_reject_bad_workspace(lib):
     assert b.sse_get_last_device_error(None, None) == b.SSE_ERR_INVALID_ARG
     assert b.sse_get_last_device_error(FAKE + 64, None) == b.SSE_ERR_INVALID_ARG
     assert b.sse_read_device_status(None, None)[0] == b.SSE_ERR_INVALID_ARG
+
+
+def _bwd(cfg, T=16, S=1, q=FAKE, qs=None, dqs=None, ks=None, dks=None, ws=FAKE, ws_bytes=1 << 40, dq=FAKE):
+    from sparse_state_linear_router_gb300 import binding
+    return binding.sse_backward(cfg, q, FAKE, FAKE, FAKE, FAKE, qs, ks, FAKE, S, T, None, FAKE, None, dq, FAKE, FAKE,
+                                FAKE, FAKE, dqs, dks, None, ws, ws_bytes, None)
+
+
+def test_backward_rejects_bad_arguments(lib):
+    """sse_backward validates on the host before any launch: the shared
+    configuration and size checks, required pointers, alignment, the pairing
+    of separate shared q / k with their gradient buffers, the workspace."""
+    from sparse_state_linear_router_gb300 import binding as b
+    assert _bwd(_cfg(top_k=0)) == b.SSE_ERR_INVALID_ARG
+    assert _bwd(_cfg(num_partitions=65, top_k=2)) == b.SSE_ERR_UNSUPPORTED
+    assert _bwd(_cfg(key_dim=12)) == b.SSE_ERR_UNSUPPORTED
+    assert _bwd(_cfg(value_dim=48, dtype="f32")) == b.SSE_ERR_UNSUPPORTED   # no kernel for d = 48
+    assert _bwd(_cfg(), q=None) == b.SSE_ERR_INVALID_ARG
+    assert _bwd(_cfg(), dq=None) == b.SSE_ERR_INVALID_ARG
+    assert _bwd(_cfg(), q=FAKE + 8) == b.SSE_ERR_INVALID_ARG
+    assert _bwd(_cfg(), qs=FAKE) == b.SSE_ERR_INVALID_ARG           # q_shared without dq_shared
+    assert _bwd(_cfg(), dks=FAKE) == b.SSE_ERR_INVALID_ARG          # dk_shared without k_shared
+    assert _bwd(_cfg(), T=-1) == b.SSE_ERR_INVALID_ARG
+    assert _bwd(_cfg(), ws=None) == b.SSE_ERR_WORKSPACE
+    assert _bwd(_cfg(), ws_bytes=64) == b.SSE_ERR_WORKSPACE
+    assert _bwd(_cfg(), S=0, T=0) == b.SSE_OK
+    assert b.sse_backward_workspace_size(_cfg(), 100, 2) > b.sse_forward_workspace_size(_cfg(algo="recurrent"), 0, 1)
+    assert b.sse_backward_workspace_size(_cfg(top_k=0), 100, 2) == 0

@@ -1,0 +1,137 @@
+"""GPU parity of sse_backward against the float64 backward oracle
+(``oracle/backward.py``, itself pinned by finite differences of the forward
+oracle), on the same seeded inputs, through the C ABI (marked gpu).
+
+The GPU side takes the gate gradient through the running sum of the log-gate
+(dL/dG_t = Q_t * u_t - K_t * dK_t, reverse-summed); the oracle takes it
+through the decay of every step (rowsum(G * S_before) * a): two different
+routes to the same number."""
+import numpy as np
+import pytest
+
+from sparse_state_linear_router_gb300 import inputs as synth
+from tests import _helpers as H_
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_state_linear_router_gb300 import binding
+    binding.load()
+
+
+def _store(x, dtype):
+    x = np.asarray(x, dtype=np.float32)
+    return x if dtype == "f32" else synth.f32_to_bf16_bits(x)
+
+
+def _run(w, inp, *, seed=0, with_dfin=True, separate_shared=False, scale=1.0, pairs_only=None):
+    """GPU and oracle gradients of <d_out, out> + <d_final, final_state>."""
+    from oracle import backward as bw
+    from sparse_state_linear_router_gb300 import binding
+    rng = np.random.default_rng(100 + seed)
+    T, S, H = inp.total_tokens, inp.num_seqs, w.num_heads
+    P = w.num_slots
+    d_out = _store(rng.normal(size=(T, H, w.value_dim)), w.dtype)
+    d_fin = (rng.normal(size=(S, H, P, w.key_dim, w.value_dim)) * 0.5).astype(np.float32) if with_dfin else None
+    qs = ks = None
+    if separate_shared:
+        qs = _store(rng.normal(size=inp.q.shape) / np.sqrt(w.key_dim), w.dtype)
+        ks = _store(rng.random(size=inp.k.shape) / w.key_dim, w.dtype)
+    cfg = H_.config_of(w, scale=scale)
+    dv_ = lambda a: None if a is None else binding.to_device(a)  # noqa: E731
+    t = {n: dv_(getattr(inp, n)) for n in ("q", "k", "v", "g", "logits")}
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    init = None if inp.init_state is None else torch.from_numpy(inp.init_state).cuda()
+    dfin_t = None if d_fin is None else torch.from_numpy(d_fin).cuda()
+    r = binding.backward(cfg, t["q"], t["k"], t["v"], t["g"], t["logits"], cu, dv_(d_out), q_shared=dv_(qs),
+                         k_shared=dv_(ks), initial_state=init, d_final_state=dfin_t)
+    torch.cuda.synchronize()
+    gpu = {k_: (None if v_ is None else H_.to_numpy(v_)) for k_, v_ in r.items() if k_ != "workspace"}
+    if pairs_only is None:
+        ref = bw.backward(inp.q, inp.k, inp.v, inp.g, inp.logits, inp.cu_seqlens, d_out, top_k=w.top_k,
+                          use_shared=w.use_shared, scale=scale, q_shared=qs, k_shared=ks,
+                          initial_state=inp.init_state, d_final_state=d_fin)
+        return gpu, ref, None
+    # one (sequence, head) pair at a time: the gradients of a pair depend on its own rows only
+    refs = []
+    for p in pairs_only:
+        b, h = divmod(int(p), H)
+        t0, t1 = int(inp.cu_seqlens[b]), int(inp.cu_seqlens[b + 1])
+        sl = lambda a: None if a is None else np.ascontiguousarray(a[t0:t1, h:h + 1])  # noqa: E731
+        ref = bw.backward(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.g), sl(inp.logits),
+                          np.array([0, t1 - t0]), sl(d_out), top_k=w.top_k, use_shared=w.use_shared, scale=scale,
+                          q_shared=sl(qs), k_shared=sl(ks),
+                          initial_state=None if inp.init_state is None else inp.init_state[b:b + 1, h:h + 1],
+                          d_final_state=None if d_fin is None else d_fin[b:b + 1, h:h + 1])
+        refs.append((b, h, t0, t1, ref))
+    return gpu, None, refs
+
+
+NAMES = ("dq", "dk", "dv", "dg", "dlogits", "d_initial_state", "dq_shared", "dk_shared")
+
+
+def _compare(gpu, ref, tol):
+    for n in NAMES:
+        if ref[n] is None:
+            assert gpu[n] is None, n
+            continue
+        err = H_.max_abs_rel(gpu[n], ref[n])
+        assert err < tol, (n, err)
+
+
+CASES = {
+    # name: (workload, lengths, overrides, kwargs)
+    "tiny_f32": ("tiny_f32", [40, 0, 23], {}, {}),
+    "f32_separate_shared": ("tiny_f32", [31, 17], {"num_partitions": 4, "top_k": 2}, {"separate_shared": True}),
+    "small_bf16_varlen": ("small_bf16", [300, 1, 0, 129], {"num_heads": 2}, {}),
+    "bf16_scale_separate_shared": ("small_bf16", [200, 77], {"num_heads": 2}, {"separate_shared": True, "scale": 0.5}),
+    "noshared_k3": ("small_bf16", [180], {"num_heads": 1, "num_partitions": 6, "top_k": 3, "use_shared": 0}, {}),
+    "k_equals_N": ("small_bf16", [150, 60], {"num_heads": 1, "num_partitions": 3, "top_k": 3}, {}),
+    "c128_d128_no_dfin": ("layer_bf16", [257, 64], {"num_heads": 1, "num_partitions": 4}, {"with_dfin": False}),
+    "c128_d64": ("layer_bf16", [130, 3], {"num_heads": 2, "value_dim": 64}, {}),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_backward_matches_oracle(name):
+    wname, lengths, over, kw = CASES[name]
+    w = H_.workload_variant(wname, **over)
+    inp = synth.make_forward_inputs(w, seed=3, lengths=lengths, with_init=True)
+    gpu, ref, _ = _run(w, inp, **kw)
+    _compare(gpu, ref, H_.tol_for(w))
+
+
+def test_backward_skewed_routing_and_empty_segments():
+    """Per-partition router bias: some partitions take nearly every token,
+    others none, so empty segments (whose initial-state gradient is the final
+    state's gradient, undecayed) meet long ones."""
+    w = H_.workload_variant("small_bf16", num_heads=2, num_partitions=8, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=12, lengths=[260, 0, 41], with_init=True)
+    beta = 8.0 * (np.arange(8) / 7 - 0.5) * 2.0
+    inp.logits = synth.f32_to_bf16_bits((synth.bf16_bits_to_f32(inp.logits) + beta).astype(np.float32))
+    gpu, ref, _ = _run(w, inp)
+    _compare(gpu, ref, H_.TOL_BF16)
+
+
+def test_backward_layer_shape_sampled_pairs():
+    """The layer workload's shape (16 heads, c = d = 128, N = 8, top-2,
+    shared, 8 sequences) at 256 tokens per sequence through the GPU backward;
+    the oracle -- which keeps every state, 2.4 MB per token here -- recomputes
+    three (sequence, head) pairs on their own rows."""
+    w = synth.WORKLOADS["layer_bf16"]
+    inp = synth.make_forward_inputs(w, seed=0, lengths=[256] * 8, with_init=True)
+    S, H = inp.num_seqs, w.num_heads
+    pairs = [0, 37, S * H - 1]
+    gpu, _, refs = _run(w, inp, pairs_only=pairs)
+    for b, h, t0, t1, ref in refs:
+        for n in ("dq", "dk", "dv", "dg", "dlogits"):
+            err = H_.max_abs_rel(gpu[n][t0:t1, h:h + 1], ref[n])
+            assert err < H_.TOL_BF16, (b, h, n, err)
+        err = H_.max_abs_rel(gpu["d_initial_state"][b:b + 1, h:h + 1], ref["d_initial_state"])
+        assert err < H_.TOL_BF16, (b, h, "d_initial_state", err)

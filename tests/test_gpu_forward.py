@@ -242,20 +242,18 @@ def _launches(w, inp, algo):
 
 
 def test_auto_picks_the_schedule():
-    """AUTO takes the masking schedule ("Scaling Linear Attention with Sparse
-    State Expansion", section 2.6) when top_k == N -- every token selects
-    every partition, so the grouping is the identity and the sort is pure
-    overhead -- and the grouped varlen schedule otherwise; the launch count
-    tells them apart (masking: no token->partition sort) and the results are
-    the same bits."""
+    """AUTO takes the grouped varlen schedule wherever the tensor-core path
+    applies: the masking schedule ("Scaling Linear Attention with Sparse State
+    Expansion", section 2.6, short inputs) measured slower on GB300 in every
+    case, top_k == N included.  The launch count tells the schedules apart
+    (masking: no token->partition sort); AUTO's results are the grouped
+    schedule's bits."""
     k_eq_n = H_.workload_variant("small_bf16", num_partitions=4, top_k=4)
-    for w, lengths, expect in ((k_eq_n, [300, 129], "masked"),
-                               (H_.workload_variant("small_bf16"), None, "chunked"),
-                               (H_.workload_variant("layer_bf16", num_heads=4), [200] * 8, "chunked"),
-                               (H_.workload_variant("small_bf16", use_shared=0), None, "chunked")):
+    for w, lengths in ((k_eq_n, [300, 129]), (H_.workload_variant("small_bf16"), None),
+                       (H_.workload_variant("small_bf16", use_shared=0), None)):
         inp = synth.make_forward_inputs(w, seed=6, lengths=lengths)
         n_auto, out_auto, fin_auto = _launches(w, inp, "auto")
-        n_exp, out_exp, fin_exp = _launches(w, inp, expect)
-        n_other, _, _ = _launches(w, inp, "chunked" if expect == "masked" else "masked")
-        assert n_auto == n_exp != n_other, (expect, n_auto, n_exp, n_other)
-        assert np.array_equal(out_auto, out_exp) and np.array_equal(fin_auto, fin_exp)
+        n_grp, out_grp, fin_grp = _launches(w, inp, "chunked")
+        n_msk, _, _ = _launches(w, inp, "masked")
+        assert n_auto == n_grp != n_msk, (n_auto, n_grp, n_msk)
+        assert np.array_equal(out_auto, out_grp) and np.array_equal(fin_auto, fin_grp)
