@@ -272,6 +272,9 @@ def run_reference(args):
     if rank != 0:
         return 0
     w_fwd, w_dec = synth.WORKLOADS[args.fwd_workload], synth.WORKLOADS[DEC_WORKLOAD]
+    if args.decode_batch:  # a smaller decode batch (profiling captures)
+        import dataclasses
+        w_dec = dataclasses.replace(w_dec, decode_batch=args.decode_batch)
     fwd_inp = synth.make_forward_inputs(w_fwd, seed=0)
     dec_steps = [synth.make_decode_inputs(w_dec, s, batch=16) for s in range(4)]
     T = fwd_inp.total_tokens
@@ -481,6 +484,9 @@ def run_native(args):
     launches = {"n": 0}
 
     w_fwd, w_dec = synth.WORKLOADS[args.fwd_workload], synth.WORKLOADS[DEC_WORKLOAD]
+    if args.decode_batch:  # a smaller decode batch (profiling captures)
+        import dataclasses
+        w_dec = dataclasses.replace(w_dec, decode_batch=args.decode_batch)
     fwd_inp = synth.make_forward_inputs(w_fwd, seed=rank)   # also the CPU-baseline sample
     T, S = fwd_inp.total_tokens, fwd_inp.num_seqs
     B = w_dec.decode_batch
@@ -815,6 +821,8 @@ def main(argv=None):
     ap.add_argument("--algo", choices=["auto", "chunked", "recurrent", "masked"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="decode sequences per step (default: the workload's 256; smaller for ncu captures)")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the forward-only timings of the other workloads (varlen, small, skewed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -246,6 +246,25 @@ __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item
     return s;
 }
 
+// Queue position -> work item.  With the shared partition on, the (sequence,
+// head) pairs go in waves of kWavePairs: a wave's shared segments first (the
+// longest items, started early), then its routed segments pair by pair, so
+// that more of the k + 1 reads of a token row meet in L2.  Measured on GB300
+// (main kernel, layer workload 8 x 4096 tokens H16 N8 / varlen 16 sequences
+// H16 N16, one box): plain order 0.430 / 3.19 ms; waves of 16 pairs
+// 0.466 / 3.50; 32: 0.429 / 3.46; 48: 0.429 / 3.55; 64: 0.418 / 3.18.
+constexpr int kWavePairs = 64;
+__device__ __forceinline__ int queue_item(int qpos, int npairs, int N, int use_shared) {
+    if (!use_shared) return qpos;
+    const int per_wave = kWavePairs * (N + 1);
+    const int w = qpos / per_wave, r = qpos - w * per_wave;
+    const int p0 = w * kWavePairs;
+    const int wc = min(kWavePairs, npairs - p0);  // pairs in this wave (the last one may be short)
+    if (r < wc) return p0 + r;                     // shared segment of pair p0 + r
+    const int rr = r - wc;
+    return npairs + (p0 + rr / N) * N + rr % N;    // routed segment (pair, partition)
+}
+
 // Row metadata of row idx of a work item: token index and router weight.
 struct RowMeta { int t; float e; };
 template <bool MASKED>
@@ -362,7 +381,10 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             uint32_t g = 0;
             for (int sidx = 0;; ++sidx) {
                 int item = 0;
-                if (lane == 0) item = *(volatile int *)s_abort ? num_items : atomicAdd(work_counter, 1);
+                if (lane == 0) {
+                    item = *(volatile int *)s_abort ? num_items : atomicAdd(work_counter, 1);
+                    if (item < num_items) item = queue_item(item, a.num_seqs * H, N, use_shared);
+                }
                 item = __shfl_sync(0xffffffffu, item, 0);
                 const bool stop = item >= num_items;
                 Segment seg{};
