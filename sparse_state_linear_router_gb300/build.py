@@ -13,6 +13,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsse.so")
+# Checked build for the failure-detection test: fwd_chunked.cu compiled with
+# -DSSE_FAULT_INJECT (short bounded waits, a switch that withholds one
+# barrier arrival), linked with the same objects as libsse.so.
+LIB_CHECKED = os.path.join(BUILD, "libsse_checked.so")
+CHECKED_SRC = "fwd_chunked.cu"
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -42,10 +47,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    def compile_one(job):
+        src, checked = job
+        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ("_checked.o" if checked else ".o"))
         if force or _stale(obj, [src] + hdrs):
-            cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, *(["-DSSE_FAULT_INJECT"] if checked else []), "-c", src,
+                   "-o", obj]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -55,14 +62,21 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 print(r.stdout + r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(compile_one, srcs))
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".tmp.%d" % os.getpid()
-        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+    checked_src = os.path.join(CSRC, CHECKED_SRC)
+    jobs = [(src, False) for src in srcs] + [(checked_src, True)]
+    # the largest translation units first, so the parallel compile ends sooner
+    jobs.sort(key=lambda j: -os.path.getsize(j[0]))
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
+        done = dict(zip(jobs, ex.map(compile_one, jobs)))
+    objs = [done[(src, False)] for src in srcs]
+    checked_objs = [done[(checked_src, True)] if src == checked_src else done[(src, False)] for src in srcs]
+    for lib, lib_objs in ((LIB, objs), (LIB_CHECKED, checked_objs)):
+        if force or _stale(lib, lib_objs):
+            tmp = lib + ".tmp.%d" % os.getpid()
+            r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *lib_objs], capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+            os.replace(tmp, lib)
     return LIB
 
 

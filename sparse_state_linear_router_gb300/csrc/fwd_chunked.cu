@@ -66,7 +66,18 @@ constexpr int kTrfThreads = 32 * kTrfWarps;
 constexpr int kRegsLaunch = 128, kRegsEpi = 120, kRegsTrf = 176, kRegsLdr = 40;
 static_assert(32 * (kEpiWarps * kRegsEpi + kTrfWarps * kRegsTrf + kLdrWarps * kRegsLdr) == kThreads * kRegsLaunch,
               "register split must use exactly the launch allocation");
+#ifdef SSE_FAULT_INJECT
+// Checked build (libsse_checked.so, for the failure-detection test only):
+// every bounded wait gives up after 50 ms, and g_fault_mode = 1 makes CTA 0's
+// transform warps withhold their "Qt / Kt written" arrival for the first
+// chunk, so that the waits on it run out and the kernel takes its abort path
+// (SSE_DEVICE_TIMEOUT, roles stop together, TMEM freed).  Nothing faults or
+// hangs: every wait in the kernel is bounded.
+__device__ int g_fault_mode = 0;
+constexpr uint64_t kWaitNs = 50000000ull;
+#else
 constexpr uint64_t kWaitNs = 2000000000ull;
+#endif
 constexpr float kLog2e = 1.4426950408889634f;
 // Largest |G_r - G_m| (summed log-gate over a half chunk, per key row) the
 // factorised form takes.  Every factor exp(+-(G_r - G_m)) then stays within
@@ -702,6 +713,9 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 }
                 fence_proxy_async();
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
+#ifdef SSE_FAULT_INJECT
+                if (!(g_fault_mode == 1 && blockIdx.x == 0 && g_n == 0))
+#endif
                 mbar_arrive(bar(kBarT));
             }
             if (failed) break;
@@ -1176,3 +1190,12 @@ cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a,
 }
 
 }  // namespace sse
+
+#ifdef SSE_FAULT_INJECT
+// Checked build only: sets the fault mode read by chunked_forward_kernel (0 =
+// none, 1 = CTA 0 withholds its first transform arrival).  Returns the CUDA
+// error of the copy.
+extern "C" int sse_debug_set_fault(int mode) {
+    return (int)cudaMemcpyToSymbol(sse::g_fault_mode, &mode, sizeof(int));
+}
+#endif
