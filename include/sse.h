@@ -252,6 +252,44 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
                           void *workspace, size_t workspace_bytes, sse_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * sse_delta_forward / sse_delta_decode_step -- SSE on a gated delta-rule
+ * transition: the close-reading notes of "Scaling Linear Attention with
+ * Sparse State Expansion" name Gated DeltaNet's structured transition
+ * (section 2.1, eq. 6) as the alternative to GLA's diagonal decay and the
+ * combination as future work (section 6); DeltaNet's update is on the
+ * "动态线性注意力" page (section 2.1, eq. 4).  Same router, grouping, shared
+ * partition and read-out as sse_forward; the state update of a selected
+ * partition i becomes
+ *   S_i <- alpha_t (I - e_t[i] beta_t k_t^T k_t) S_i + e_t[i] beta_t k_t^T v_t
+ * (the router weight scales the delta write), the shared one the same with
+ * weight 1, unselected partitions untouched.  alpha_t = exp(log_alpha_t) and
+ * beta_t are one scalar each per (token, head); the caller normalises the
+ * keys (DeltaNet takes unit keys).
+ *
+ *   log_alpha, beta   [total_tokens, H] (decode: [batch, H]) in cfg->dtype
+ *   everything else   as sse_forward / sse_decode_step (cfg->algo ignored)
+ * Computed token by token in float32 on the CUDA cores; read-outs summed per
+ * (token, head) in a fixed order.  Shapes: d in {16, 32, 64, 128, 256},
+ * c <= 256 (and c <= 4 * 256 * 16 / d).  Workspace (forward only):
+ * sse_delta_forward_workspace_size bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+size_t sse_delta_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
+
+sse_status_t sse_delta_forward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                               const void *log_alpha, const void *beta, const void *router_logits,
+                               const void *q_shared, const void *k_shared,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                               const float *initial_state, float *final_state, void *out,
+                               int32_t *topk_idx, float *topk_w,
+                               void *workspace, size_t workspace_bytes, sse_stream_t stream);
+
+sse_status_t sse_delta_decode_step(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                                   const void *log_alpha, const void *beta, const void *router_logits,
+                                   const void *q_shared, const void *k_shared, int32_t batch,
+                                   float *state, void *out, int32_t *topk_idx, float *topk_w,
+                                   sse_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * sse_front_end -- the layer's projections from the hidden states
  * ("Scaling Linear Attention with Sparse State Expansion", eqs. 9-10; the
  * shared partition's rank-64 Q/K LoRA of section 2.5; GLA's diagonal gate).

@@ -31,7 +31,8 @@ _ALGOS = {"auto": SSE_ALGO_AUTO, "chunked": SSE_ALGO_CHUNKED, "recurrent": SSE_A
 EXPORTED = ("sse_abi_version", "sse_status_string", "sse_route_workspace_size", "sse_route",
             "sse_route_noalloc", "sse_forward_workspace_size", "sse_forward", "sse_forward_timed", "sse_decode_step",
             "sse_front_end_workspace_size", "sse_front_end", "sse_read_device_status",
-            "sse_get_last_device_error", "sse_backward_workspace_size", "sse_backward")
+            "sse_get_last_device_error", "sse_backward_workspace_size", "sse_backward",
+            "sse_delta_forward_workspace_size", "sse_delta_forward", "sse_delta_decode_step")
 
 
 class sse_config_t(ctypes.Structure):
@@ -93,6 +94,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sse_backward_workspace_size.argtypes = [cfgp, i64, i32]
     lib.sse_backward.restype = ctypes.c_int
     lib.sse_backward.argtypes = [cfgp, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.sse_delta_forward_workspace_size.restype = sz
+    lib.sse_delta_forward_workspace_size.argtypes = [cfgp, i64, i32]
+    lib.sse_delta_forward.restype = ctypes.c_int
+    lib.sse_delta_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, sz, P]
+    lib.sse_delta_decode_step.restype = ctypes.c_int
+    lib.sse_delta_decode_step.argtypes = [cfgp, P, P, P, P, P, P, P, P, i32, P, P, P, P, P]
     _lib = lib
     return lib
 
@@ -314,6 +321,50 @@ def backward(cfg, q, k, v, log_gate, logits, cu_seqlens, d_out, *, q_shared=None
                         _ptr(out["d_initial_state"]), _ptr(workspace), workspace.numel(), _stream()),
            "sse_backward")
     return dict(out, workspace=workspace)
+
+
+def delta_forward(cfg, q, k, v, log_alpha, beta, logits, cu_seqlens, *, q_shared=None, k_shared=None,
+                  initial_state=None, want_final_state=True, want_routing=False, workspace=None):
+    """SSE on the gated delta rule (sse_delta_forward) on device tensors;
+    returns dict(out, final_state, topk_idx, topk_w, workspace)."""
+    import torch
+    T = q.shape[0]
+    S = cu_seqlens.numel() - 1
+    H, d, c = cfg.num_heads, cfg.value_dim, cfg.key_dim
+    P = cfg.num_partitions + cfg.use_shared
+    dev = q.device
+    out = torch.empty((T, H, d), dtype=_token_dtype(cfg), device=dev)
+    fin = torch.empty((S, H, P, c, d), dtype=torch.float32, device=dev) if want_final_state else None
+    idx = w = None
+    if want_routing:
+        idx = torch.empty((T, H, cfg.top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, H, cfg.top_k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        n = load().sse_delta_forward_workspace_size(ctypes.byref(cfg), T, S)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    _check(load().sse_delta_forward(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                    _ptr(logits), _ptr(q_shared), _ptr(k_shared), _ptr(cu_seqlens), S, T,
+                                    _ptr(initial_state), _ptr(fin), _ptr(out), _ptr(idx), _ptr(w), _ptr(workspace),
+                                    workspace.numel(), _stream()), "sse_delta_forward")
+    return {"out": out, "final_state": fin, "topk_idx": idx, "topk_w": w, "workspace": workspace}
+
+
+def delta_decode_step(cfg, state, q, k, v, log_alpha, beta, logits, *, q_shared=None, k_shared=None,
+                      want_routing=False):
+    """One delta-rule decode step; ``state`` [B,H,P,c,d] float32 is updated in place."""
+    import torch
+    B = q.shape[0]
+    H, d = cfg.num_heads, cfg.value_dim
+    dev = q.device
+    out = torch.empty((B, H, d), dtype=_token_dtype(cfg), device=dev)
+    idx = w = None
+    if want_routing:
+        idx = torch.empty((B, H, cfg.top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((B, H, cfg.top_k), dtype=torch.float32, device=dev)
+    _check(load().sse_delta_decode_step(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                        _ptr(logits), _ptr(q_shared), _ptr(k_shared), B, _ptr(state), _ptr(out),
+                                        _ptr(idx), _ptr(w), _stream()), "sse_delta_decode_step")
+    return {"out": out, "topk_idx": idx, "topk_w": w}
 
 
 def front_end(cfg, x, w_q, w_k, w_v, w_g, w_e, *, a_q=None, b_q=None, a_k=None, b_k=None,

@@ -1,0 +1,339 @@
+// delta.cu -- SSE on a gated delta-rule transition (CUDA cores, float32).
+//
+// The close-reading notes of "Scaling Linear Attention with Sparse State
+// Expansion" name Gated DeltaNet's structured transition (section 2.1, eq. 6)
+// as the alternative to GLA's diagonal decay and the combination as future
+// work (section 6); DeltaNet's update is on the "动态线性注意力" page (section
+// 2.1, eq. 4).  With the SSE router (eqs. 9-10), per token t and head h:
+//
+//   for i in T_t:  S_i <- alpha_t (I - e_t[i] beta_t k_t^T k_t) S_i + e_t[i] beta_t k_t^T v_t
+//   shared:        S_N <- alpha_t (I - beta_t ks_t^T ks_t) S_N + beta_t ks_t^T v_t
+//   o_t = sum_{i in T_t} e_t[i] (scale q_t) S_i + (scale qs_t) S_N
+//
+// alpha_t = exp(log_alpha_t) and beta_t are one scalar each per (token, head).
+// Row by row: with w = k S (the state's answer to the key, before the step),
+//   S[r, :] <- alpha S[r, :] + e beta k[r] (v - alpha w).
+//
+// Forward: one CTA per (sequence, head, partition) segment of the grouping
+// (section 2.6, varlen schedule) and per shared (sequence, head), walking its
+// rows in time order with the c x d state in registers; read-outs go to the
+// float32 partial slots that launch_combine sums (the recurrent path's).
+// Decode: one CTA per (sequence, head) routes the token (warp-level softmax
+// and top-k) and updates only the k + 1 selected states in place.
+#include <algorithm>
+
+#include "sse_internal.cuh"
+
+namespace sse {
+namespace {
+
+constexpr int kDThreads = 256;
+constexpr int kDMaxRows = 16;  // state rows per thread
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Thread layout (both kernels): D4 = d/4 column quads x R = 256/D4 row groups;
+// thread (rg, cq) holds rows rg, rg + R, ... (at most kDMaxRows) x 4 columns.
+// Shared memory: s_k, s_q [c], s_v [d], s_w [d], s_cols [R][d].
+template <int D4>
+struct DeltaRow {
+    static constexpr int R = kDThreads / D4;
+    // column sums over the row groups: every thread's partial float4 in
+    // s_cols, then threads < d add the R partials of their column.
+    static __device__ __forceinline__ void col_reduce(float4 part, float *s_cols, int rg, int col, int tid, int d,
+                                                      float *dst) {
+        *reinterpret_cast<float4 *>(s_cols + rg * d + col) = part;
+        __syncthreads();
+        if (tid < d) {
+            float s = 0.f;
+#pragma unroll
+            for (int r2 = 0; r2 < R; ++r2) s += s_cols[r2 * d + tid];
+            dst[tid] = s;
+        }
+        __syncthreads();
+    }
+};
+
+// One delta-rule step on the thread's state rows; returns the thread's partial
+// of q S (after the step) for its four columns.  s_w must hold w = k S.
+template <int D4>
+__device__ __forceinline__ float4 delta_rows(float4 (&st)[kDMaxRows], const float *s_k, const float *s_q,
+                                             const float *s_v, const float *s_w, float alpha, float eb, int rg,
+                                             int col, int c) {
+    constexpr int R = kDThreads / D4;
+    const float4 v4 = *reinterpret_cast<const float4 *>(s_v + col);
+    const float4 w4 = *reinterpret_cast<const float4 *>(s_w + col);
+    const float4 u = make_float4(v4.x - alpha * w4.x, v4.y - alpha * w4.y, v4.z - alpha * w4.z, v4.w - alpha * w4.w);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < kDMaxRows; ++m) {
+        const int r = rg + m * R;
+        if (r < c) {
+            const float kr = eb * s_k[r], qr = s_q[r];
+            st[m].x = fmaf(alpha, st[m].x, kr * u.x);
+            st[m].y = fmaf(alpha, st[m].y, kr * u.y);
+            st[m].z = fmaf(alpha, st[m].z, kr * u.z);
+            st[m].w = fmaf(alpha, st[m].w, kr * u.w);
+            acc.x = fmaf(qr, st[m].x, acc.x);
+            acc.y = fmaf(qr, st[m].y, acc.y);
+            acc.z = fmaf(qr, st[m].z, acc.z);
+            acc.w = fmaf(qr, st[m].w, acc.w);
+        }
+    }
+    return acc;
+}
+
+// The thread's partial of w = k S for its four columns.
+template <int D4>
+__device__ __forceinline__ float4 key_answer(const float4 (&st)[kDMaxRows], const float *s_k, int rg, int c) {
+    constexpr int R = kDThreads / D4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < kDMaxRows; ++m) {
+        const int r = rg + m * R;
+        if (r < c) {
+            const float kr = s_k[r];
+            acc.x = fmaf(kr, st[m].x, acc.x);
+            acc.y = fmaf(kr, st[m].y, acc.y);
+            acc.z = fmaf(kr, st[m].z, acc.z);
+            acc.w = fmaf(kr, st[m].w, acc.w);
+        }
+    }
+    return acc;
+}
+
+template <typename T, int D4>
+__global__ void __launch_bounds__(kDThreads)
+delta_segment_kernel(DeltaArgs a, int32_t H, int32_t c, int32_t N, int32_t topk, int32_t use_shared, float scale) {
+    constexpr int R = kDThreads / D4;
+    constexpr int d = 4 * D4;
+    extern __shared__ float smem[];
+    float *s_k = smem, *s_q = s_k + c, *s_v = s_q + c, *s_w = s_v + d, *s_o = s_w + d, *s_cols = s_o + d;
+    const T *q = static_cast<const T *>(a.q);
+    const T *kk = static_cast<const T *>(a.k);
+    const T *v = static_cast<const T *>(a.v);
+    const T *la = static_cast<const T *>(a.log_alpha);
+    const T *bt = static_cast<const T *>(a.beta);
+    const int nshared = use_shared ? a.num_seqs * H : 0;
+    const int P = N + use_shared;
+    const bool is_shared = (int)blockIdx.x < nshared;
+    int b, h, slot, len, base;
+    if (is_shared) {
+        b = blockIdx.x / H;
+        h = blockIdx.x % H;
+        slot = N;
+        base = a.cu_seqlens[b];
+        len = a.cu_seqlens[b + 1] - base;
+    } else {
+        const int s = blockIdx.x - nshared;
+        slot = s % N;
+        h = (s / N) % H;
+        b = s / (N * H);
+        base = a.seg_off[s];
+        len = a.seg_off[s + 1] - base;
+    }
+    const T *qsrc = is_shared && a.qs ? static_cast<const T *>(a.qs) : q;
+    const T *ksrc = is_shared && a.ks ? static_cast<const T *>(a.ks) : kk;
+    const int tid = threadIdx.x, cq = tid % D4, rg = tid / D4, col = 4 * cq;
+    const int64_t state_off = (((int64_t)b * H + h) * P + slot) * (int64_t)c * d;
+    // decode-style in-place use with nothing to do: leave the state alone
+    if (len == 0 && a.init == a.final_state) return;
+
+    float4 st[kDMaxRows];
+#pragma unroll
+    for (int m = 0; m < kDMaxRows; ++m) {
+        const int r = rg + m * R;
+        st[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < c && a.init) st[m] = *reinterpret_cast<const float4 *>(a.init + state_off + (int64_t)r * d + col);
+    }
+    // row inputs travel one row ahead as raw elements
+    struct Raw { T q, k, v, la, b; };
+    auto fetch = [&](int n, int &t, int &jj, float &e) -> Raw {
+        if (is_shared) {
+            t = base + n;
+            jj = 0;
+            e = 1.f;
+        } else {
+            const int rec = a.perm_rec[base + n];
+            t = rec / topk;
+            jj = rec - t * topk;
+            e = a.topk_w[((int64_t)t * H + h) * topk + jj];
+        }
+        const int64_t th = (int64_t)t * H + h;
+        Raw x{};
+        if (tid < c) {
+            x.q = qsrc[th * c + tid];
+            x.k = ksrc[th * c + tid];
+        }
+        if (tid < d) x.v = v[th * d + tid];
+        x.la = la[th];
+        x.b = bt[th];
+        return x;
+    };
+    int t_nx = 0, j_nx = 0;
+    float e_nx = 0.f;
+    Raw x_nx{};
+    if (len > 0) x_nx = fetch(0, t_nx, j_nx, e_nx);
+    for (int n = 0; n < len; ++n) {
+        const int t = t_nx, jj = j_nx;
+        const float e = e_nx;
+        const Raw x = x_nx;
+        if (tid < c) {
+            s_q[tid] = e * scale * to_f32(x.q);
+            s_k[tid] = to_f32(x.k);
+        }
+        if (tid < d) s_v[tid] = to_f32(x.v);
+        const float alpha = expf(to_f32(x.la)), eb = e * to_f32(x.b);
+        if (n + 1 < len) x_nx = fetch(n + 1, t_nx, j_nx, e_nx);
+        __syncthreads();
+        DeltaRow<D4>::col_reduce(key_answer<D4>(st, s_k, rg, c), s_cols, rg, col, tid, d, s_w);
+        DeltaRow<D4>::col_reduce(delta_rows<D4>(st, s_k, s_q, s_v, s_w, alpha, eb, rg, col, c), s_cols, rg, col,
+                                 tid, d, s_o);
+        const int64_t th = (int64_t)t * H + h;
+        float *dst = is_shared ? a.part_shared + th * d : a.part_routed + (th * topk + jj) * d;
+        if (tid < d) dst[tid] = s_o[tid];
+    }
+    if (a.final_state) {
+#pragma unroll
+        for (int m = 0; m < kDMaxRows; ++m) {
+            const int r = rg + m * R;
+            if (r < c) *reinterpret_cast<float4 *>(a.final_state + state_off + (int64_t)r * d + col) = st[m];
+        }
+    }
+}
+
+// Decode: one CTA per (sequence, head).
+template <typename T, int D4>
+__global__ void __launch_bounds__(kDThreads)
+delta_decode_kernel(DeltaDecodeArgs a, int32_t H, int32_t c, int32_t N, int32_t topk, int32_t use_shared,
+                    float scale) {
+    constexpr int R = kDThreads / D4;
+    constexpr int d = 4 * D4;
+    extern __shared__ float smem[];
+    float *s_k = smem, *s_q = s_k + c, *s_v = s_q + c, *s_w = s_v + d, *s_o = s_w + d, *s_cols = s_o + d;
+    __shared__ int s_idx[kMaxTopK];
+    __shared__ float s_e[kMaxTopK];
+    const int bh = blockIdx.x;
+    const int tid = threadIdx.x, cq = tid % D4, rg = tid / D4, col = 4 * cq;
+    const int P = N + use_shared;
+    if (tid < 32) {
+        int idx[kMaxTopK];
+        float w[kMaxTopK];
+        route_token_warp<T>(static_cast<const T *>(a.logits) + (int64_t)bh * N, N, topk, tid, idx, w);
+        if (tid == 0) {
+            for (int j = 0; j < topk; ++j) {
+                s_idx[j] = idx[j];
+                s_e[j] = w[j];
+                if (a.topk_idx) a.topk_idx[(int64_t)bh * topk + j] = idx[j];
+                if (a.topk_w) a.topk_w[(int64_t)bh * topk + j] = w[j];
+            }
+        }
+    }
+    const float alpha = expf(to_f32(static_cast<const T *>(a.log_alpha)[bh]));
+    const float beta = to_f32(static_cast<const T *>(a.beta)[bh]);
+    float o_col = 0.f;  // thread tid < d: column tid of the output
+    for (int j = 0; j < topk + use_shared; ++j) {
+        __syncthreads();  // routing written; the previous slot's shared memory consumed
+        const bool shared_slot = j == topk;
+        const int slot = shared_slot ? N : s_idx[j];
+        const float e = shared_slot ? 1.f : s_e[j];
+        const T *qsrc = static_cast<const T *>(shared_slot && a.qs ? a.qs : a.q);
+        const T *ksrc = static_cast<const T *>(shared_slot && a.ks ? a.ks : a.k);
+        if (tid < c) {
+            s_q[tid] = e * scale * to_f32(qsrc[(int64_t)bh * c + tid]);
+            s_k[tid] = to_f32(ksrc[(int64_t)bh * c + tid]);
+        }
+        if (tid < d) s_v[tid] = to_f32(static_cast<const T *>(a.v)[(int64_t)bh * d + tid]);
+        float *S = a.state + ((int64_t)bh * P + slot) * (int64_t)c * d;
+        float4 st[kDMaxRows];
+#pragma unroll
+        for (int m = 0; m < kDMaxRows; ++m) {
+            const int r = rg + m * R;
+            st[m] = r < c ? __ldcs(reinterpret_cast<const float4 *>(S + (int64_t)r * d + col))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
+        DeltaRow<D4>::col_reduce(key_answer<D4>(st, s_k, rg, c), s_cols, rg, col, tid, d, s_w);
+        DeltaRow<D4>::col_reduce(delta_rows<D4>(st, s_k, s_q, s_v, s_w, alpha, e * beta, rg, col, c), s_cols, rg,
+                                 col, tid, d, s_o);
+        if (tid < d) o_col += s_o[tid];
+#pragma unroll
+        for (int m = 0; m < kDMaxRows; ++m) {
+            const int r = rg + m * R;
+            if (r < c) __stcs(reinterpret_cast<float4 *>(S + (int64_t)r * d + col), st[m]);
+        }
+    }
+    if (tid < d) Elem<T>::store(static_cast<T *>(a.out) + (int64_t)bh * d + tid, o_col);
+}
+
+template <typename T, int D4>
+cudaError_t launch_fwd_t(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream) {
+    constexpr int R = kDThreads / D4;
+    const int c = cfg.key_dim, d = 4 * D4;
+    const size_t smem = sizeof(float) * (2 * c + 3 * d + R * d);
+    const int64_t nseg = (int64_t)a.num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
+    if (nseg == 0) return cudaSuccess;
+    delta_segment_kernel<T, D4><<<(unsigned)nseg, kDThreads, smem, stream>>>(
+        a, cfg.num_heads, c, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
+    return cudaGetLastError();
+}
+
+template <typename T, int D4>
+cudaError_t launch_dec_t(const sse_config_t &cfg, const DeltaDecodeArgs &a, cudaStream_t stream) {
+    constexpr int R = kDThreads / D4;
+    const int c = cfg.key_dim, d = 4 * D4;
+    const size_t smem = sizeof(float) * (2 * c + 3 * d + R * d);
+    const int64_t rows = (int64_t)a.batch * cfg.num_heads;
+    if (rows == 0) return cudaSuccess;
+    delta_decode_kernel<T, D4><<<(unsigned)rows, kDThreads, smem, stream>>>(
+        a, cfg.num_heads, c, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
+    return cudaGetLastError();
+}
+
+template <typename T, typename Args, cudaError_t (*F16)(const sse_config_t &, const Args &, cudaStream_t),
+          cudaError_t (*F32)(const sse_config_t &, const Args &, cudaStream_t),
+          cudaError_t (*F64)(const sse_config_t &, const Args &, cudaStream_t),
+          cudaError_t (*F128)(const sse_config_t &, const Args &, cudaStream_t),
+          cudaError_t (*F256)(const sse_config_t &, const Args &, cudaStream_t)>
+cudaError_t by_d(const sse_config_t &cfg, const Args &a, cudaStream_t stream) {
+    switch (cfg.value_dim) {
+    case 16: return F16(cfg, a, stream);
+    case 32: return F32(cfg, a, stream);
+    case 64: return F64(cfg, a, stream);
+    case 128: return F128(cfg, a, stream);
+    case 256: return F256(cfg, a, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t fwd_dispatch(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream) {
+    return by_d<T, DeltaArgs, launch_fwd_t<T, 4>, launch_fwd_t<T, 8>, launch_fwd_t<T, 16>, launch_fwd_t<T, 32>,
+                launch_fwd_t<T, 64>>(cfg, a, stream);
+}
+
+template <typename T>
+cudaError_t dec_dispatch(const sse_config_t &cfg, const DeltaDecodeArgs &a, cudaStream_t stream) {
+    return by_d<T, DeltaDecodeArgs, launch_dec_t<T, 4>, launch_dec_t<T, 8>, launch_dec_t<T, 16>, launch_dec_t<T, 32>,
+                launch_dec_t<T, 64>>(cfg, a, stream);
+}
+
+}  // namespace
+
+bool delta_supported(const sse_config_t &cfg) {
+    const int d = cfg.value_dim, c = cfg.key_dim;
+    if (!(d == 16 || d == 32 || d == 64 || d == 128 || d == 256)) return false;
+    const int R = kDThreads / (d / 4);
+    return c >= 1 && c <= R * kDMaxRows && c <= kDThreads;
+}
+
+cudaError_t launch_delta_forward(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream) {
+    return cfg.dtype == SSE_BF16 ? fwd_dispatch<__nv_bfloat16>(cfg, a, stream) : fwd_dispatch<float>(cfg, a, stream);
+}
+
+cudaError_t launch_delta_decode(const sse_config_t &cfg, const DeltaDecodeArgs &a, cudaStream_t stream) {
+    return cfg.dtype == SSE_BF16 ? dec_dispatch<__nv_bfloat16>(cfg, a, stream) : dec_dispatch<float>(cfg, a, stream);
+}
+
+}  // namespace sse

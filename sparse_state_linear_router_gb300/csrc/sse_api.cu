@@ -410,6 +410,108 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
     return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
 }
 
+namespace {
+struct DeltaLayout {
+    RouteBuffers rb;
+    float *part_routed, *part_shared;
+    size_t bytes;
+};
+
+DeltaLayout carve_delta(void *ws, const sse_config_t &c, int64_t T, int32_t S, int32_t *topk_idx, float *topk_w) {
+    Carver cv(ws);
+    DeltaLayout L{};
+    L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
+    L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
+    L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
+    L.bytes = (cv.off + 255) & ~size_t(255);
+    return L;
+}
+}  // namespace
+
+size_t sse_delta_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs) {
+    if (check_config(cfg) != SSE_OK || check_sizes(*cfg, total_tokens, num_seqs) != SSE_OK) return 0;
+    return carve_delta(nullptr, *cfg, total_tokens, num_seqs, nullptr, nullptr).bytes;
+}
+
+sse_status_t sse_delta_forward(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                               const void *log_alpha, const void *beta, const void *router_logits,
+                               const void *q_shared, const void *k_shared, const int32_t *cu_seqlens,
+                               int32_t num_seqs, int64_t total_tokens, const float *initial_state,
+                               float *final_state, void *out, int32_t *topk_idx, float *topk_w, void *workspace,
+                               size_t workspace_bytes, sse_stream_t stream) {
+    SSE_RANGE("sse_delta_forward");
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if ((st = check_sizes(*cfg, total_tokens, num_seqs)) != SSE_OK) return st;
+    const sse_config_t &c = *cfg;
+    if (!cu_seqlens) return SSE_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !router_logits || !out))
+        return SSE_ERR_INVALID_ARG;
+    for (const void *p : std::initializer_list<const void *>{q, k, v, log_alpha, beta, router_logits, q_shared,
+                                                             k_shared, out, (const void *)initial_state,
+                                                             (const void *)final_state})
+        if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
+    if (!sse::delta_supported(c)) return SSE_ERR_UNSUPPORTED;
+    const size_t need = sse_delta_forward_workspace_size(cfg, total_tokens, num_seqs);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return SSE_ERR_WORKSPACE;
+    if (num_seqs == 0) return SSE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeltaLayout L = carve_delta(workspace, c, total_tokens, num_seqs, topk_idx, topk_w);
+    cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, true, s);
+    if (e != cudaSuccess) return SSE_ERR_CUDA;
+    sse::DeltaArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+    a.qs = c.use_shared ? q_shared : nullptr;
+    a.ks = c.use_shared ? k_shared : nullptr;
+    a.cu_seqlens = cu_seqlens;
+    a.num_seqs = num_seqs;
+    a.total_tokens = total_tokens;
+    a.init = initial_state;
+    a.final_state = final_state;
+    a.seg_off = L.rb.seg_off;
+    a.perm_rec = L.rb.perm_rec;
+    a.topk_w = L.rb.topk_w;
+    a.part_routed = L.part_routed;
+    a.part_shared = L.part_shared;
+    if (sse::launch_delta_forward(c, a, s) != cudaSuccess) return SSE_ERR_CUDA;
+    sse::ForwardArgs fa{};
+    fa.total_tokens = total_tokens;
+    fa.out = out;
+    fa.part_routed = L.part_routed;
+    fa.part_shared = L.part_shared;
+    fa.part_bf16 = 0;
+    return sse::launch_combine(c, fa, s) == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+}
+
+sse_status_t sse_delta_decode_step(const sse_config_t *cfg, const void *q, const void *k, const void *v,
+                                   const void *log_alpha, const void *beta, const void *router_logits,
+                                   const void *q_shared, const void *k_shared, int32_t batch, float *state,
+                                   void *out, int32_t *topk_idx, float *topk_w, sse_stream_t stream) {
+    SSE_RANGE("sse_delta_decode_step");
+    sse_status_t st = check_config(cfg);
+    if (st != SSE_OK) return st;
+    if (batch < 0) return SSE_ERR_INVALID_ARG;
+    if ((int64_t)batch * cfg->num_heads >= (int64_t(1) << 31)) return SSE_ERR_UNSUPPORTED;
+    if (batch > 0 && (!q || !k || !v || !log_alpha || !beta || !router_logits || !state || !out))
+        return SSE_ERR_INVALID_ARG;
+    for (const void *p : std::initializer_list<const void *>{q, k, v, log_alpha, beta, router_logits, q_shared,
+                                                             k_shared, out, (const void *)state})
+        if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
+    if (!sse::delta_supported(*cfg)) return SSE_ERR_UNSUPPORTED;
+    sse::DeltaDecodeArgs a{};
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.logits = router_logits;
+    a.qs = cfg->use_shared ? q_shared : nullptr;
+    a.ks = cfg->use_shared ? k_shared : nullptr;
+    a.batch = batch;
+    a.state = state;
+    a.out = out;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    return sse::launch_delta_decode(*cfg, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSE_OK
+                                                                                                    : SSE_ERR_CUDA;
+}
+
 size_t sse_front_end_workspace_size(const sse_config_t *cfg, int32_t hidden, int64_t total_tokens) {
     if (!cfg || hidden < 0 || total_tokens < 0) return 0;
     Carver cv(nullptr);

@@ -273,6 +273,33 @@ bool backward_supported(const sse_config_t &cfg);
 // Adds the number of kernels it launched to *launches.
 cudaError_t launch_backward(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream, int *launches);
 
+// SSE on a gated delta-rule transition (delta.cu).  log_alpha, beta:
+// [T, H] in the token dtype.  Forward read-outs go to the float32 partial
+// slots of the recurrent path (part_routed [T, H, k, d], part_shared
+// [T, H, d]) that launch_combine sums.
+struct DeltaArgs {
+    const void *q, *k, *v, *log_alpha, *beta, *qs, *ks;
+    const int32_t *cu_seqlens;
+    int32_t num_seqs;
+    int64_t total_tokens;
+    const float *init;
+    float *final_state;
+    const int32_t *seg_off, *perm_rec;
+    const float *topk_w;
+    float *part_routed, *part_shared;
+};
+struct DeltaDecodeArgs {
+    const void *q, *k, *v, *log_alpha, *beta, *logits, *qs, *ks;
+    int32_t batch;
+    float *state;
+    void *out;
+    int32_t *topk_idx;
+    float *topk_w;
+};
+bool delta_supported(const sse_config_t &cfg);
+cudaError_t launch_delta_forward(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream);
+cudaError_t launch_delta_decode(const sse_config_t &cfg, const DeltaDecodeArgs &a, cudaStream_t stream);
+
 bool decode_supported(const sse_config_t &cfg);
 cudaError_t launch_decode(const sse_config_t &cfg, const void *q, const void *k, const void *v,
                           const void *g, const void *logits, const void *qs, const void *ks,

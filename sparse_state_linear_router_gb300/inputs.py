@@ -41,6 +41,8 @@ __all__ = [
     "FrontEndInputs",
     "make_front_end_inputs",
     "make_forward_inputs_device",
+    "DeltaInputs",
+    "make_delta_inputs",
     "workload_lengths",
     "f32_to_bf16_bits",
     "bf16_bits_to_f32",
@@ -326,3 +328,64 @@ def make_front_end_inputs(w: FrontEndWorkload, seed: int = 0, tokens: Optional[i
         ak = _draw(rng, (r, D), "bf16", lambda z: z * s)
         bk = _draw(rng, (H * c, r), "bf16", lambda z: z * sb)
     return FrontEndInputs(w, x, wq, wk, wv, wg, we, aq, bq, ak, bk)
+
+
+# ----------------------------------------------------------------------------
+# SSE on a gated delta-rule transition
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class DeltaInputs:
+    """Packed varlen (or single-token decode) inputs of the delta-rule layer."""
+    workload: Workload
+    q: np.ndarray            # [T, H, c]
+    k: np.ndarray            # [T, H, c], unit rows
+    v: np.ndarray            # [T, H, d]
+    log_alpha: np.ndarray    # [T, H]
+    beta: np.ndarray         # [T, H]
+    logits: np.ndarray       # [T, H, N]
+    cu_seqlens: np.ndarray   # [S+1] int32
+    init_state: Optional[np.ndarray]
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.cu_seqlens) - 1
+
+
+def _unit_rows(x):
+    return x / np.sqrt((x * x).sum(axis=-1, keepdims=True))
+
+
+def make_delta_inputs(w: Workload, seed: int = 0, lengths=None, with_init=None) -> DeltaInputs:
+    """Inputs of the delta-rule layer, numpy ``default_rng(seed)``, in this
+    draw order: (varlen) lengths; q = N(0,1)/sqrt(c); k = unit rows of N(0,1)
+    (DeltaNet normalises its keys); v = N(0,1); log_alpha = logsigmoid(N(0,1))/16
+    and beta = sigmoid(N(0,1)), one per (token, head); logits = N(0, sigma_r);
+    initial state N(0, init_std or 0.1).  float64, cast to the workload dtype."""
+    rng = np.random.default_rng(seed)
+    if lengths is None:
+        if w.varlen is not None:
+            ns, lo, hi = w.varlen
+            lengths = rng.integers(lo, hi + 1, ns)
+        else:
+            lengths = w.lengths
+    lengths = np.asarray(lengths, dtype=np.int64)
+    cu = np.zeros(len(lengths) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lengths)
+    T = int(cu[-1])
+    H, c, d, N = w.num_heads, w.key_dim, w.value_dim, w.num_partitions
+    q = _draw(rng, (T, H, c), w.dtype, lambda x: x / np.sqrt(c))
+    k = _draw(rng, (T, H, c), w.dtype, _unit_rows)
+    v = _draw(rng, (T, H, d), w.dtype, lambda x: x)
+    la = _draw(rng, (T, H), w.dtype, lambda x: _logsigmoid(x) / 16.0)
+    beta = _draw(rng, (T, H), w.dtype, lambda x: 1.0 / (1.0 + np.exp(-x)))
+    logits = _draw(rng, (T, H, N), w.dtype, lambda x: x * w.sigma_router)
+    init = None
+    want_init = (w.init_std is not None) if with_init is None else with_init
+    if want_init:
+        std = w.init_std if w.init_std is not None else 0.1
+        init = rng.normal(0.0, std, (len(lengths), H, w.num_slots, c, d)).astype(np.float32)
+    return DeltaInputs(w, q, k, v, la, beta, logits, cu.astype(np.int32), init)
