@@ -462,6 +462,71 @@ def time_fwd_bwd_fig6(args, dev, L=8192):
     return res
 
 
+def time_delta(args, dev):
+    """SSE on the gated delta rule (CUDA cores): the forward on the layer
+    workload's shape (8 x 4096 tokens, H16, c=d=128, N8, top-2, shared) and
+    one decode step on the decode workload's shape (256 sequences x H16,
+    N16, top-2, shared, fp32 states resident), inputs drawn on the device with
+    the delta recipe (unit keys, log_alpha = logsigmoid(N(0,1))/16 and
+    beta = sigmoid(N(0,1)) per (token, head))."""
+    import torch
+    from sparse_state_linear_router_gb300 import binding
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+
+    def normal(*shape):
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+
+    def inputs(w, T):
+        H, c, d, N = w.num_heads, w.key_dim, w.value_dim, w.num_partitions
+        k = normal(T, H, c)
+        return {"q": (normal(T, H, c) / np.sqrt(c)).to(torch.bfloat16),
+                "k": (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16),
+                "v": normal(T, H, d).to(torch.bfloat16),
+                "la": (torch.nn.functional.logsigmoid(normal(T, H)) / 16).to(torch.bfloat16),
+                "b": torch.sigmoid(normal(T, H)).to(torch.bfloat16),
+                "lg": (normal(T, H, N) * w.sigma_router).to(torch.bfloat16)}
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    res = {}
+    w = synth.WORKLOADS["layer_bf16"]
+    T = sum(w.lengths)
+    x = inputs(w, T)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(w.lengths)]).astype(np.int32), device=dev)
+    cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k, 1, 1.0, "bf16")
+    ws = torch.empty(binding.load().sse_delta_forward_workspace_size(binding.ctypes.byref(cfg), T, len(w.lengths)),
+                     dtype=torch.uint8, device=dev)
+    ms = timed(lambda: binding.delta_forward(cfg, x["q"], x["k"], x["v"], x["la"], x["b"], x["lg"], cu,
+                                             workspace=ws), 3)
+    res["forward_layer_shape"] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3),
+                                  "workload": "8 x 4096 tokens, H16, c=d=128, N8, top-2, shared, bf16"}
+    del x, ws
+    w = synth.WORKLOADS["decode_bf16"]
+    B = w.decode_batch
+    x = inputs(w, B)
+    cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k, 1, 1.0, "bf16")
+    state = torch.zeros((B, w.num_heads, w.num_slots, w.key_dim, w.value_dim), dtype=torch.float32, device=dev)
+    ms = timed(lambda: binding.delta_decode_step(cfg, state, x["q"], x["k"], x["v"], x["la"], x["b"], x["lg"]), 10)
+    nbytes = decode_bytes(w, B)  # the same state traffic as the GLA decode: k + 1 states read and written
+    res["decode_step"] = {"ms": ms, "tokens_per_s": B / (ms * 1e-3), "gbs": nbytes / (ms * 1e6),
+                          "frac_of_hbm_peak": nbytes / (ms * 1e6) / _peaks()["hbm_gbs"],
+                          "workload": "256 sequences x H16, c=d=128, N16, top-2, shared, fp32 states"}
+    del x, state
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_native(args):
     import torch
     ws, rank, local = _dist()
@@ -673,11 +738,12 @@ def run_native(args):
                "overlap": "inputs of step i copied on a second stream while step i-1 computes"}
 
     # ---- the other forward workloads (rank 0, N = 1, default run only) -------
-    variants, variant_clocks, fig6 = None, None, None
+    variants, variant_clocks, fig6, delta = None, None, None, None
     if do_fwd and do_dec and rank == 0 and ws == 1 and not args.no_variants:
         with ClockSampler(local) as vclk:
             variants = time_forward_variants(args, dev, peaks)
             fig6 = time_fwd_bwd_fig6(args, dev)
+            delta = time_delta(args, dev)
         variant_clocks = vclk.summary()
 
     # ---- CPU oracle baseline (rank 0, N = 1 only) ----------------------------
@@ -732,6 +798,7 @@ def run_native(args):
     if variants is not None:
         line["forward_variants"] = variants
         line["fwd_bwd_fig6_shape"] = fig6
+        line["delta_rule"] = delta
         line["forward_variants_clocks"] = variant_clocks
     print(json.dumps(line), flush=True)
     if ws > 1:

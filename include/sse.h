@@ -132,9 +132,10 @@ sse_status_t sse_route(const sse_config_t *cfg, const void *router_logits,
  * convenience.  Same arguments, outputs and results as sse_route, without the
  * workspace: the routing scratch lives in a 4 MiB array inside the library's
  * device image, reserved on every GPU that loads the library until the
- * process exits.  Limit: (num_seqs + 1) + H * N * (ceil(total_tokens / 256)
- * + num_seqs + 1) int32 entries (plus 256-byte alignment padding) must fit in
- * 4 MiB -- about one million tokens at H = 16, N = 16; larger calls return
+ * process exits.  Limit: (num_seqs + 1) + 4 B + H * N * (B + 1) int32
+ * entries, B = ceil(total_tokens / 256) + num_seqs (plus 256-byte alignment
+ * padding), must fit in 4 MiB -- about one million tokens at H = 16, N = 16;
+ * larger calls return
  * SSE_ERR_WORKSPACE before any launch.  The configuration and size checks are
  * those of sse_route (same status for the same bad argument).  Every call
  * looks up the array's device address in the current device's context (a

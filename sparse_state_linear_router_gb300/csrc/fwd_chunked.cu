@@ -154,6 +154,59 @@ __device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
 
 __device__ __forceinline__ uint32_t tile_off(int row, int col) { return sw128_offset(row, col, 2); }
 
+// Two float32 lanes in one 64-bit register, for Blackwell's packed f32x2
+// arithmetic (each lane is the scalar IEEE operation, round to nearest: the
+// results are those of two scalar instructions, in one).
+#ifndef SSE_F32X2
+#define SSE_F32X2 1
+#endif
+struct F2 { uint64_t v; };
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ F2 f2_bits(uint32_t lo, uint32_t hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_get(F2 x) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x.v));
+    return r;
+}
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+#if SSE_F32X2
+    F2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+#else
+    const float2 x = f2_get(a), y = f2_get(b);
+    return f2(x.x + y.x, x.y + y.y);
+#endif
+}
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+#if SSE_F32X2
+    F2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+#else
+    const float2 x = f2_get(a), y = f2_get(b);
+    return f2(x.x * y.x, x.y * y.y);
+#endif
+}
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+#if SSE_F32X2
+    F2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+#else
+    const float2 x = f2_get(a), y = f2_get(b), z = f2_get(c);
+    return f2(fmaf(x.x, y.x, z.x), fmaf(x.y, y.y, z.y));
+#endif
+}
+
 // 2^x with the SFU instruction (relative error ~2^-22, flushes denormals);
 // its operands are rounded to bf16 right after.
 __device__ __forceinline__ float ex2(float x) {
@@ -604,7 +657,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                         for (int i = 0; i < RPT; ++i)
                             if (me[rb * RPT + i] < 0.f) rg[i] = make_uint4(0, 0, 0, 0);
                     }
-                    float run[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    F2 run[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
                         // this row's raw q, k (used by pass 2), issued between the sums
@@ -621,12 +674,15 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                         for (int j = 0; j < 4; ++j) {
                             float lo, hi;
                             unpack2(w[j], lo, hi);
-                            run[2 * j] += lo;
-                            run[2 * j + 1] += hi;
+                            run[j] = add2(run[j], f2(lo, hi));
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) s_tot[rb * 128 + col0 + j] = run[j];
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 x = f2_get(run[j]);
+                        s_tot[rb * 128 + col0 + 2 * j] = x.x;
+                        s_tot[rb * 128 + col0 + 2 * j + 1] = x.y;
+                    }
                 }
                 if (named_sync_or(1, kTrfThreads, bad)) { failed = true; break; }
                 // the next chunk's metadata, for its g rows loaded inside pass 2
@@ -676,15 +732,19 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 // with packed bf16 products.
                 {
                     // run = (G_r - G_m) log2(e), advanced row by row
-                    float run[8];
+                    F2 run[4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        run[j] = fmaf(s_tot[rb * 128 + col0 + j], kLog2e, -s_tot[32 * 128 + col0 + j]);
+                    for (int j = 0; j < 4; ++j)
+                        run[j] = f2(fmaf(s_tot[rb * 128 + col0 + 2 * j], kLog2e, -s_tot[32 * 128 + col0 + 2 * j]),
+                                    fmaf(s_tot[rb * 128 + col0 + 2 * j + 1], kLog2e,
+                                         -s_tot[32 * 128 + col0 + 2 * j + 1]));
+                    const F2 l2e = f2(kLog2e, kLog2e);
                     const float *me = meta_e(mst);
 #pragma unroll
                     for (int i = 0; i < RPT; ++i) {
                         const int r = rb * RPT + i;
                         const float e = MASKED ? fmaxf(me[r], 0.f) : me[r];
+                        const F2 e2 = f2(e, e);
                         const uint32_t wg4[4] = {rg[i].x, rg[i].y, rg[i].z, rg[i].w};
                         const uint32_t wq4[4] = {rq[i].x, rq[i].y, rq[i].z, rq[i].w};
                         const uint32_t wk4[4] = {rk[i].x, rk[i].y, rk[i].z, rk[i].w};
@@ -693,11 +753,11 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                         for (int j = 0; j < 4; ++j) {
                             float g0, g1;
                             unpack2(wg4[j], g0, g1);
-                            run[2 * j] = fmaf(g0, kLog2e, run[2 * j]);
-                            run[2 * j + 1] = fmaf(g1, kLog2e, run[2 * j + 1]);
-                            const float d0 = run[2 * j], d1 = run[2 * j + 1];
-                            pq[j] = bf16x2_mul(wq4[j], pack_bf16x2(ex2(d0), ex2(d1)));
-                            pk[j] = bf16x2_mul(wk4[j], pack_bf16x2(e * ex2(-d0), e * ex2(-d1)));
+                            run[j] = fma2(f2(g0, g1), l2e, run[j]);
+                            const float2 dd = f2_get(run[j]);
+                            pq[j] = bf16x2_mul(wq4[j], pack_bf16x2(ex2(dd.x), ex2(dd.y)));
+                            const float2 kf = f2_get(mul2(e2, f2(ex2(-dd.x), ex2(-dd.y))));
+                            pk[j] = bf16x2_mul(wk4[j], pack_bf16x2(kf.x, kf.y));
                         }
                         // row i of the next chunk's g, into the registers just consumed
                         {
@@ -777,6 +837,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
             auto write_out = [&](int n_o, bool pend) -> bool {
                 const int st = (gch + n_o) % kMetaStages;
                 const float w = (MASKED ? fmaxf(meta_e(st)[row], 0.f) : meta_e(st)[row]) * scale;
+                const F2 w2 = f2(w, w);
                 const uint32_t tO = tmem + lb + (((gch + n_o) & 1) ? kTmemO1 : kTmemO0);
                 unsigned char *stg = sm + Smem::S;
 #pragma unroll 1  // one 32-column block per iteration: keeps the hot code small
@@ -788,12 +849,14 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     for (int i = 0; i < 4; ++i) {
                         const int col = c0 + 8 * i;
                         const int ch = (col % 64) / 8;
+                        uint32_t o4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float2 x = f2_get(mul2(w2, f2_bits(r[8 * i + 2 * u], r[8 * i + 2 * u + 1])));
+                            o4[u] = pack_bf16x2(x.x, x.y);
+                        }
                         *reinterpret_cast<uint4 *>(stg + (col / 64) * (kC * 128) + row * 128 + ((ch ^ (row & 7)) << 4)) =
-                            make_uint4(
-                                pack_bf16x2(w * __uint_as_float(r[8 * i]), w * __uint_as_float(r[8 * i + 1])),
-                                pack_bf16x2(w * __uint_as_float(r[8 * i + 2]), w * __uint_as_float(r[8 * i + 3])),
-                                pack_bf16x2(w * __uint_as_float(r[8 * i + 4]), w * __uint_as_float(r[8 * i + 5])),
-                                pack_bf16x2(w * __uint_as_float(r[8 * i + 6]), w * __uint_as_float(r[8 * i + 7])));
+                            make_uint4(o4[0], o4[1], o4[2], o4[3]);
                     }
                 }
                 fence_before();
@@ -834,14 +897,18 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     // factors are applied one after the other because their product
                     // (down to e^-160 within the gate range) would underflow
                     const float fm = s_fmid[row];
+                    const F2 pp2 = f2(p_pending, p_pending), fm2 = f2(fm, fm);
 #pragma unroll 1  // one 32-column block per iteration: keeps the hot code small
                     for (int c0 = 0; c0 < DV; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tS + c0, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint((__uint_as_float(r[i]) * p_pending) * fm);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 x = f2_get(mul2(mul2(f2_bits(r[i], r[i + 1]), pp2), fm2));
+                            r[i] = __float_as_uint(x.x);
+                            r[i + 1] = __float_as_uint(x.y);
+                        }
                         tmem_st32(tS + c0, r);
 #pragma unroll
                         for (int i = 0; i < 32; i += 8)

@@ -5,7 +5,8 @@
 //
 // Stages (all deterministic, integer-exact):
 //   plan     1 CTA   : routing blocks per sequence (256 tokens, never
-//                      straddling a sequence) -> blk_prefix
+//                      straddling a sequence) -> blk_prefix, and the table
+//                      blk_info (sequence, token range) of every block
 //   count    (blk,H) : route every token of the block, write topk_idx/topk_w,
 //                      per-block histogram over partitions -> cnt
 //   scan     (H*N)   : exclusive scan of cnt over blocks, per (h, i)
@@ -13,8 +14,9 @@
 //                      over s -> seg_off (and, for the chunked forward, the
 //                      chunk-padded output regions of the work items)
 //   scatter  (blk,H) : rank of each record inside its block (per-warp bit
-//                      masks + popc) + block base -> perm / perm_rec, and the
-//                      partial-output row of every contribution (rec_pos)
+//                      masks + popc) + the block's base per partition (staged
+//                      once per CTA) -> perm / perm_rec, and the partial-output
+//                      row of every contribution (rec_pos)
 #include <algorithm>
 
 #include "sse_internal.cuh"
@@ -59,60 +61,49 @@ __device__ int block_exclusive_scan(int x, int *total) {
     return warp_off[warp] + incl - x;
 }
 
-__global__ void plan_blocks_kernel(const int32_t *__restrict__ cu, int32_t nseq,
-                                   int32_t *__restrict__ blk_prefix) {
+// Routing blocks: each sequence is cut into blocks of kRouteBlock tokens
+// (never straddling two sequences).  blk_prefix[b] = blocks before sequence b;
+// blk_info[j] = (sequence, first token, end token) of block j, sequence -1 for
+// the unused tail up to max_blocks.  One CTA.
+__global__ void plan_blocks_kernel(const int32_t *__restrict__ cu, int32_t nseq, int32_t *__restrict__ blk_prefix,
+                                   int4 *__restrict__ blk_info, int32_t max_blocks) {
     int carry = 0;
     for (int base = 0; base < nseq; base += blockDim.x) {
         const int b = base + threadIdx.x;
-        int nb = 0;
-        if (b < nseq) nb = (cu[b + 1] - cu[b] + kRouteBlock - 1) / kRouteBlock;
+        int nb = 0, t0 = 0, t1 = 0;
+        if (b < nseq) {
+            t0 = cu[b];
+            t1 = cu[b + 1];
+            nb = (t1 - t0 + kRouteBlock - 1) / kRouteBlock;
+        }
         int tot;
         const int ex = block_exclusive_scan(nb, &tot);
-        if (b < nseq) blk_prefix[b] = carry + ex;
+        if (b < nseq) {
+            blk_prefix[b] = carry + ex;
+            for (int jb = 0; jb < nb; ++jb)
+                blk_info[carry + ex + jb] = make_int4(b, t0 + jb * kRouteBlock, min(t0 + (jb + 1) * kRouteBlock, t1), 0);
+        }
         carry += tot;
     }
     if (threadIdx.x == 0) blk_prefix[nseq] = carry;
-}
-
-// Locates routing block j: its sequence and token range.  Returns false when
-// j is past the last block.
-__device__ __forceinline__ bool find_block(const int32_t *blk_prefix, const int32_t *cu,
-                                           int32_t nseq, int j, int &b, int &t0, int &t1) {
-    if (j >= blk_prefix[nseq]) return false;
-    int lo = 0, hi = nseq - 1;  // largest b with blk_prefix[b] <= j and a non-empty range
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (blk_prefix[mid] <= j) lo = mid; else hi = mid - 1;
-    }
-    // zero-length sequences share their prefix with the next one; the largest
-    // b with blk_prefix[b] <= j is the non-empty sequence owning block j.
-    b = lo;
-    t0 = cu[b] + (j - blk_prefix[b]) * kRouteBlock;
-    t1 = min(t0 + kRouteBlock, cu[b + 1]);
-    return true;
+    for (int j = carry + threadIdx.x; j < max_blocks; j += blockDim.x) blk_info[j] = make_int4(-1, 0, 0, 0);
 }
 
 template <typename T, int NP>
 __global__ void __launch_bounds__(kRouteBlock)
-route_count_kernel(const T *__restrict__ logits, const int32_t *__restrict__ cu, int32_t nseq,
-                   const int32_t *__restrict__ blk_prefix, int32_t H, int32_t N, int32_t k, int32_t vec,
-                   int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+route_count_kernel(const T *__restrict__ logits, const int4 *__restrict__ blk_info, int32_t H, int32_t N,
+                   int32_t k, int32_t vec, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                    int32_t *__restrict__ cnt, int32_t max_blocks) {
     __shared__ int hist[kMaxPartitions];
-    __shared__ int s_b, s_t0, s_t1, s_ok;
     // consecutive CTAs take the heads of one routing block, so the partial
     // sectors they write into [T, H, ...] rows meet in L2
     const int h = (int)(blockIdx.x % (unsigned)H), j = (int)(blockIdx.x / (unsigned)H);
+    const int4 bi = blk_info[j];  // (sequence, first token, end token); sequence -1: past the last block
     if (threadIdx.x < kMaxPartitions) hist[threadIdx.x] = 0;
-    if (threadIdx.x == 0) {
-        int b = 0, t0 = 0, t1 = 0;
-        s_ok = find_block(blk_prefix, cu, nseq, j, b, t0, t1);
-        s_b = b; s_t0 = t0; s_t1 = t1;
-    }
     __syncthreads();
-    if (s_ok) {
-        const int t = s_t0 + threadIdx.x;
-        if (t < s_t1) {
+    if (bi.x >= 0) {
+        const int t = bi.y + threadIdx.x;
+        if (t < bi.z) {
             int idx[kMaxTopK];
             float w[kMaxTopK];
             route_token<T, NP>(logits + ((int64_t)t * H + h) * N, N, k, vec != 0, idx, w);
@@ -197,30 +188,39 @@ seg_off_kernel(const int32_t *__restrict__ cnt, int32_t max_blocks,
 
 __global__ void __launch_bounds__(kRouteBlock)
 scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ cu, int32_t nseq,
-               const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cnt,
-               int32_t max_blocks, const int32_t *__restrict__ seg_off, int32_t H, int32_t N,
-               int32_t k, int32_t use_shared, const float *__restrict__ topk_w, int32_t *__restrict__ perm,
+               const int32_t *__restrict__ blk_prefix, const int4 *__restrict__ blk_info,
+               const int32_t *__restrict__ cnt, int32_t max_blocks, const int32_t *__restrict__ seg_off, int32_t H,
+               int32_t N, int32_t k, int32_t use_shared, const float *__restrict__ topk_w, int32_t *__restrict__ perm,
                int32_t *__restrict__ perm_rec, float *__restrict__ perm_e,
                const int32_t *__restrict__ pad_off, int32_t *__restrict__ rec_pos) {
     constexpr int kWarps = kRouteBlock / 32;
     __shared__ uint32_t wmask[kWarps][kMaxPartitions];
-    __shared__ int s_b, s_t0, s_t1, s_ok;
+    // per partition i: where this block's records of segment (b, h, i) start
+    // in perm, and in the partial-output rows; for the shared partition, the
+    // partial row of token t is s_shared + t
+    __shared__ int s_base[kMaxPartitions], s_pad[kMaxPartitions], s_shared;
     // consecutive CTAs take the heads of one routing block, so the partial
     // sectors they write into [T, H, ...] rows meet in L2
     const int h = (int)(blockIdx.x % (unsigned)H), j = (int)(blockIdx.x / (unsigned)H);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int4 bi = blk_info[j];  // (sequence, first token, end token); sequence -1: past the last block
+    if (bi.x < 0) return;
+    const int b = bi.x;
+    const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
     for (int x = threadIdx.x; x < kWarps * kMaxPartitions; x += blockDim.x)
         (&wmask[0][0])[x] = 0u;
-    if (threadIdx.x == 0) {
-        int b = 0, t0 = 0, t1 = 0;
-        s_ok = find_block(blk_prefix, cu, nseq, j, b, t0, t1);
-        s_b = b; s_t0 = t0; s_t1 = t1;
+    if (threadIdx.x < N) {
+        const int i = threadIdx.x;
+        const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
+        const int before = row[j] - row[blk_prefix[b]];  // records of (b, h, i) in earlier blocks
+        const int64_t seg = ((int64_t)b * H + h) * N + i;
+        s_base[i] = seg_off[seg] + before;
+        if (pad_off) s_pad[i] = pad_off[nshared + seg] + before;
     }
+    if (threadIdx.x == kRouteBlock - 1 && rec_pos && use_shared) s_shared = pad_off[(int64_t)b * H + h] - cu[b];
     __syncthreads();
-    if (!s_ok) return;
-    const int b = s_b;
-    const int t = s_t0 + threadIdx.x;
-    const bool valid = t < s_t1;
+    const int t = bi.y + threadIdx.x;
+    const bool valid = t < bi.z;
     int idx[kMaxTopK];
     if (valid) {
         const int64_t o = ((int64_t)t * H + h) * k;
@@ -233,34 +233,29 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
     if (!valid) return;
     const uint32_t lt = (1u << lane) - 1u;
     const int ncon = k + use_shared;
-    const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
     const int64_t th = (int64_t)t * H + h;
-    if (rec_pos && use_shared) rec_pos[th * ncon + k] = pad_off[(int64_t)b * H + h] + (t - cu[b]);
+    if (rec_pos && use_shared) rec_pos[th * ncon + k] = s_shared + t;
     for (int jj = 0; jj < k; ++jj) {
         const int i = idx[jj];
         int rank = __popc(wmask[warp][i] & lt);
         for (int w2 = 0; w2 < warp; ++w2) rank += __popc(wmask[w2][i]);
-        const int32_t *row = cnt + ((int64_t)h * N + i) * (max_blocks + 1);
-        const int seg_rank = row[j] - row[blk_prefix[b]] + rank;
-        const int64_t seg = ((int64_t)b * H + h) * N + i;
-        const int64_t pos = (int64_t)seg_off[seg] + seg_rank;
+        const int64_t pos = (int64_t)s_base[i] + rank;
         if (perm) perm[pos] = t;
         if (perm_rec) perm_rec[pos] = t * k + jj;
         if (perm_e) perm_e[pos] = topk_w[th * k + jj];
-        if (rec_pos) rec_pos[th * ncon + jj] = pad_off[nshared + seg] + seg_rank;
+        if (rec_pos) rec_pos[th * ncon + jj] = s_pad[i] + rank;
     }
 }
 
 // Router launch with the unroll bound NP >= N; rows go through 16-byte
 // vector loads when every row starts on a 16-byte boundary.
 template <typename T>
-void launch_count(dim3 grid, cudaStream_t stream, const T *logits, const int32_t *cu, int32_t nseq,
-                  const int32_t *blk_prefix, int32_t H, int32_t N, int32_t k, int32_t *topk_idx,
-                  float *topk_w, int32_t *cnt, int32_t MB) {
+void launch_count(dim3 grid, cudaStream_t stream, const T *logits, const int4 *blk_info, int32_t H, int32_t N,
+                  int32_t k, int32_t *topk_idx, float *topk_w, int32_t *cnt, int32_t MB) {
     const int vec = (N * sizeof(T)) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
 #define SSE_COUNT(NP)                                                                                   \
-    route_count_kernel<T, NP><<<grid, kRouteBlock, 0, stream>>>(logits, cu, nseq, blk_prefix, H, N, k, \
-                                                               vec, topk_idx, topk_w, cnt, MB)
+    route_count_kernel<T, NP><<<grid, kRouteBlock, 0, stream>>>(logits, blk_info, H, N, k, vec, topk_idx, topk_w, \
+                                                               cnt, MB)
     if (N <= 8) SSE_COUNT(8);
     else if (N <= 16) SSE_COUNT(16);
     else if (N <= 32) SSE_COUNT(32);
@@ -340,19 +335,19 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
                          bool group, cudaStream_t stream) {
     const int H = cfg.num_heads, N = cfg.num_partitions, k = cfg.top_k;
     const int MB = rb.max_blocks;
-    plan_blocks_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, rb.blk_prefix);
+    plan_blocks_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, rb.blk_prefix, rb.blk_info, MB);
     const dim3 grid((unsigned)((int64_t)MB * H));
     if (cfg.dtype == SSE_BF16)
-        launch_count<__nv_bfloat16>(grid, stream, static_cast<const __nv_bfloat16 *>(logits), cu_seqlens,
-                                    num_seqs, rb.blk_prefix, H, N, k, rb.topk_idx, rb.topk_w, rb.cnt, MB);
+        launch_count<__nv_bfloat16>(grid, stream, static_cast<const __nv_bfloat16 *>(logits), rb.blk_info, H, N, k,
+                                    rb.topk_idx, rb.topk_w, rb.cnt, MB);
     else
-        launch_count<float>(grid, stream, static_cast<const float *>(logits), cu_seqlens, num_seqs,
-                            rb.blk_prefix, H, N, k, rb.topk_idx, rb.topk_w, rb.cnt, MB);
+        launch_count<float>(grid, stream, static_cast<const float *>(logits), rb.blk_info, H, N, k, rb.topk_idx,
+                            rb.topk_w, rb.cnt, MB);
     if (!group) return cudaGetLastError();
     scan_blocks_kernel<<<H * N, 1024, 0, stream>>>(rb.cnt, MB);
     seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, cu_seqlens, num_seqs, H, N,
                                            cfg.use_shared, rb.seg_off, rb.pad_off);
-    scatter_kernel<<<grid, kRouteBlock, 0, stream>>>(rb.topk_idx, cu_seqlens, num_seqs, rb.blk_prefix,
+    scatter_kernel<<<grid, kRouteBlock, 0, stream>>>(rb.topk_idx, cu_seqlens, num_seqs, rb.blk_prefix, rb.blk_info,
                                                      rb.cnt, MB, rb.seg_off, H, N, k, cfg.use_shared,
                                                      rb.topk_w, rb.perm, rb.perm_rec, rb.perm_e,
                                                      rb.pad_off, rb.rec_pos);

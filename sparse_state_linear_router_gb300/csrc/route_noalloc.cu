@@ -21,9 +21,10 @@
 
 namespace {
 
-// 4 MiB: room for (num_seqs + 1) + H * N * (ceil(T / 256) + num_seqs + 1)
-// int32 entries plus the 256-byte alignment of the two regions; with 16 heads
-// and 16 partitions that is about one million tokens per call.
+// 4 MiB: room for (num_seqs + 1) + 4 * B + H * N * (B + 1) int32 entries,
+// B = ceil(T / 256) + num_seqs routing blocks, plus the 256-byte alignment of
+// the three regions; with 16 heads and 16 partitions that is about one
+// million tokens per call.
 constexpr size_t kScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
@@ -66,6 +67,7 @@ extern "C" sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *r
     const int64_t cnt_entries = (int64_t)c.num_heads * c.num_partitions * (max_blocks + 1);
     sse::Carver cv(nullptr);
     cv.take<int32_t>((size_t)num_seqs + 1);
+    cv.take<int4>((size_t)max_blocks);
     cv.take<int32_t>((size_t)cnt_entries);
     if (cv.off > kScratchBytes) return SSE_ERR_WORKSPACE;
     if (num_seqs == 0) return SSE_OK;
@@ -76,6 +78,7 @@ extern "C" sse_status_t sse_route_noalloc(const sse_config_t *cfg, const void *r
     sse::RouteBuffers rb{};
     rb.max_blocks = (int32_t)max_blocks;
     rb.blk_prefix = sc.take<int32_t>((size_t)num_seqs + 1);
+    rb.blk_info = sc.take<int4>((size_t)max_blocks);
     rb.cnt = sc.take<int32_t>((size_t)cnt_entries);
     rb.seg_off = seg_off;
     rb.topk_idx = topk_idx;

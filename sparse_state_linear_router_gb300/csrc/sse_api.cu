@@ -77,6 +77,7 @@ RouteBuffers carve_route(Carver &cv, const sse_config_t &c, int64_t T, int32_t S
     RouteBuffers rb{};
     rb.max_blocks = (int32_t)sse::route_max_blocks(T, S);
     rb.blk_prefix = cv.take<int32_t>(S + 1);
+    rb.blk_info = cv.take<int4>((size_t)rb.max_blocks);
     rb.cnt = cv.take<int32_t>((size_t)c.num_heads * c.num_partitions * (rb.max_blocks + 1));
     int32_t *ws_seg = cv.take<int32_t>((size_t)S * c.num_heads * c.num_partitions + 1);
     int32_t *ws_idx = cv.take<int32_t>((size_t)T * c.num_heads * c.top_k);

@@ -182,6 +182,7 @@ struct Carver {
 // Device buffers of the routing/grouping stage.
 struct RouteBuffers {
     int32_t *blk_prefix;  // [num_seqs + 1] routing blocks before each sequence
+    int4 *blk_info;       // [max_blocks] (sequence, first token, end token, 0) per block; sequence -1 past the last
     int32_t *cnt;         // [H * N * (max_blocks + 1)] per-block counts, scanned in place
     int32_t *seg_off;     // [num_seqs * H * N + 1]
     int32_t *topk_idx;    // [T * H * k]
