@@ -59,24 +59,22 @@ def _peaks():
             "source": "fallback"}
 
 
-def profiled_traffic(kernel_src: str, summary: str):
-    """DRAM bytes (read + write) per launch of a kernel from its committed ncu
-    summary, or None once the kernel's source no longer has the hash recorded
-    there (the counters then describe another build)."""
+def profiled_traffic(kernel: str):
+    """DRAM bytes (read + write) per launch of a kernel from the ncu capture
+    recorded in profiles/dram_traffic.json, or None once the kernel's source
+    no longer has the hash recorded there (the counters then describe another
+    build).  Returns (bytes, the summary that documents the capture)."""
     import hashlib
-    import re
     try:
-        with open(os.path.join(ROOT, kernel_src), "rb") as f:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            entry = json.load(f)[kernel]
+        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
             digest = hashlib.sha256(f.read()).hexdigest()
-        with open(os.path.join(ROOT, summary)) as f:
-            text = f.read()
-    except OSError:
-        return None
-    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    b = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
-    if not (h and b) or h.group(1) != digest:
-        return None
-    return int(b.group(1))
+    except (OSError, KeyError, ValueError):
+        return None, None
+    if entry.get("source_sha256") != digest:
+        return None, None
+    return int(entry["dram_bytes_per_launch"]), entry.get("summary")
 
 
 # ---------------------------------------------------------------------------
@@ -766,10 +764,9 @@ def run_native(args):
     # measured DRAM bytes of the dominant kernel (ncu, same workload and build)
     traffic, traffic_src = None, None
     if dom_name == "forward_main" and args.fwd_workload == FWD_WORKLOAD and args.algo in ("auto", "chunked"):
-        traffic = profiled_traffic("sparse_state_linear_router_gb300/csrc/fwd_chunked.cu",
-                                   "profiles/chunked_forward_kernel_layer_bf16.md")
+        traffic, summary = profiled_traffic("chunked_forward_kernel")
         if traffic is not None:
-            traffic_src = "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/chunked_forward_kernel_layer_bf16.md"
+            traffic_src = f"ncu dram__bytes_read.sum + dram__bytes_write.sum, {summary}"
     parts = ([describe_forward(w_fwd, fwd_inp)] if do_fwd else []) + ([describe_decode(w_dec)] if do_dec else [])
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
