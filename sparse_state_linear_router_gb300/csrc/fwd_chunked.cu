@@ -248,6 +248,13 @@ __device__ __forceinline__ uint4 ldg_stream(const void *gptr) {
     return r;
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Prefetch into L2 of the 128-byte lines of `bytes` of global memory starting
+// at a 128-byte boundary (plain per-thread prefetches: no completion to wait
+// for, and nothing queued on the TMA engine).
+__device__ __forceinline__ void prefetch_l2(const void *gptr, uint32_t bytes) {
+    for (uint32_t o = 0; o < bytes; o += 128)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(static_cast<const char *>(gptr) + o));
+}
 // Tensor (TMA) store of one box of a 2-D tensor map from shared memory; the
 // box's inner coordinate x and row coordinate y.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t ssrc, int x, int y) {
@@ -440,8 +447,12 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
         const int lw = warp - kEpiWarps - kTrfWarps, lane = tid & 31;
         if (lw == 0) {
             // Work items -> segment ring; row metadata of every chunk -> meta
-            // ring (lane l: rows 4l..4l+3); L2 prefetch of those rows.  After the
-            // last item, one more stage whose header tells the gather warps to stop.
+            // ring (lane l: rows 4l..4l+3), with an L2 prefetch of those rows of
+            // q, k, g and v: the ring runs two to four chunks ahead of the
+            // transform, so its row loads find them in L2 instead of waiting on
+            // DRAM.  After the last item, one more stage whose header tells the
+            // gather warps to stop.
+            const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.v);
             uint32_t g = 0;
             for (int sidx = 0;; ++sidx) {
                 int item = 0;
@@ -474,6 +485,8 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                     mbar_arrive(bar(kBarSegF + slot));
                 }
                 const int nst = stop ? 1 : (seg.len + kC - 1) / kC;
+                const __nv_bfloat16 *pq = static_cast<const __nv_bfloat16 *>(seg.shared && a.qs ? a.qs : a.q);
+                const __nv_bfloat16 *pk = static_cast<const __nv_bfloat16 *>(seg.shared && a.ks ? a.ks : a.k);
                 for (int n = 0; n < nst; ++n, ++g) {
                     const int st = g % kMetaStages;
                     ok = g < kMetaStages ||
@@ -485,6 +498,13 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                         const RowMeta m = stop ? RowMeta{-1, 0.f} : row_meta<MASKED>(a, seg, n * kC + r, H, topk);
                         meta_tok(st)[r] = m.t;
                         meta_e(st)[r] = m.e;
+                        if (m.t >= 0) {
+                            const int64_t th = (int64_t)m.t * H + seg.h;
+                            prefetch_l2(pq + th * KC, KC * 2);
+                            prefetch_l2(pk + th * KC, KC * 2);
+                            prefetch_l2(gg + th * KC, KC * 2);
+                            prefetch_l2(gv + th * DV, DV * 2);
+                        }
                     }
                     if (lane == 0) {
                         int *hd = meta_hdr(st);
