@@ -75,20 +75,23 @@ def test_single_process_helpers():
 
 
 def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
-    """roofline.traffic comes from a committed ncu summary only while the
-    kernel source still has the hash recorded in it."""
+    """roofline.traffic comes from the ncu record in profiles/dram_traffic.json
+    only while the kernel source still has the hash recorded there."""
+    import hashlib
     import bench
     src = tmp_path / "k.cu"
     src.write_bytes(b"kernel v1\n")
-    import hashlib
-    h = hashlib.sha256(b"kernel v1\n").hexdigest()
-    md = tmp_path / "p.md"
-    md.write_text(f"# summary\n\n    source_sha256: {h}\n    dram_bytes_per_launch: 12345\n")
+    (tmp_path / "profiles").mkdir()
+    rec = {"kern": {"source": "k.cu", "source_sha256": hashlib.sha256(b"kernel v1\n").hexdigest(),
+                    "dram_bytes_per_launch": 12345, "summary": "profiles/p.md"}}
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.profiled_traffic("k.cu", "p.md") == 12345
+    assert bench.profiled_traffic("kern") == (12345, "profiles/p.md")
+    assert bench.profiled_traffic("other") == (None, None)
     src.write_bytes(b"kernel v2\n")
-    assert bench.profiled_traffic("k.cu", "p.md") is None
-    assert bench.profiled_traffic("missing.cu", "p.md") is None
+    assert bench.profiled_traffic("kern") == (None, None)
+    src.unlink()
+    assert bench.profiled_traffic("kern") == (None, None)
 
 
 def test_reference_arm_json_line():
