@@ -224,9 +224,6 @@ template <int R> __device__ __forceinline__ void reg_dealloc() {
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(mbar) : "memory");
 }
-__device__ __forceinline__ void named_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
-}
 // Named barrier that also ORs a predicate over the participating threads,
 // so that every participant takes the same branch afterwards.
 __device__ __forceinline__ bool named_sync_or(int id, int count, bool pred) {
@@ -385,6 +382,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     const int tid = threadIdx.x, warp = tid >> 5;
     const __nv_bfloat16 *gg = static_cast<const __nv_bfloat16 *>(a.g);
     const int P = N + use_shared;
+    griddep_launch_dependents();
 
     auto meta_tok = [&](int stage) { return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE); };
     auto meta_e = [&](int stage) {
@@ -434,6 +432,8 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_slot;
+    // everything above is on-chip; the routing's outputs are read from here on
+    griddep_wait();
 
     // The roles walk the same sequence of work items, each at its own pace: the
     // loader claims the items and posts them through the segment ring; every
@@ -1040,6 +1040,8 @@ segment_redo_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t u
     __shared__ float s_red[R][DV];
     __shared__ int s_tok[kBatch];
     __shared__ float s_e[kBatch];
+    griddep_launch_dependents();
+    griddep_wait();
     const int tid = threadIdx.x, cq = tid % D4, rg = tid / D4, col = 4 * cq;
     const int count = *(volatile const int32_t *)(a.flags + 1);
     const int P = N + use_shared;
@@ -1119,23 +1121,35 @@ segment_redo_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t u
     }
 }
 
-// out[row, :] = sum over the row's ncon bf16 partial rows rec_pos[row * ncon + j]
+// out[row, :] = sum over the row's NC bf16 partial rows rec_pos[row * NC + j]
 // (routed contributions j < k, then the shared one), 8 columns per thread,
-// fp32 accumulation in a fixed order.
+// fp32 accumulation in a fixed order.  NC is a template constant so that a
+// thread issues all NC position loads, then all NC row loads, before it sums
+// (measured: 99 -> 87 us on the 8 x 4096-token layer, 92 % of the HBM copy
+// rate; taking two or four pieces per thread was no faster, or slower).
+template <int NC>
 __global__ void __launch_bounds__(256)
 gather_combine_kernel(const __nv_bfloat16 *__restrict__ part, const int32_t *__restrict__ rec_pos, int64_t rows,
-                      int32_t d, int32_t ncon, __nv_bfloat16 *__restrict__ out) {
+                      int32_t d, __nv_bfloat16 *__restrict__ out) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int cpr = d / 8;
     const int64_t total = rows * cpr;
     for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
          x += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = x / cpr;
         const int ch = (int)(x - row * cpr);
+        int32_t pr[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) pr[j] = __ldg(rec_pos + row * NC + j);
+        uint4 pv[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j)
+            pv[j] = __ldcs(reinterpret_cast<const uint4 *>(part + (int64_t)pr[j] * d + ch * 8));
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int j = 0; j < ncon; ++j) {
-            const int64_t pr = __ldg(rec_pos + row * ncon + j);
-            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(part + pr * d + ch * 8));
-            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            const uint32_t wv[4] = {pv[j].x, pv[j].y, pv[j].z, pv[j].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float lo, hi;
@@ -1179,10 +1193,10 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int32_t *counter = static_cast<int32_t *>(a.chunk_ws);
-    cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int32_t), stream);
-    if (e != cudaSuccess) return e;
-    // the redo list's length, a.flags[1], starts at zero with the flags word
+    // the work counter (a.flags[2]) and the redo list's length (a.flags[1])
+    // start at zero with the flags words, cleared by the caller before routing
+    int32_t *counter = a.flags + 2;
+    cudaError_t e;
 
     // The partial buffer as a 2-D tensor [part_rows, DV] of bf16, stored in
     // boxes of 64 columns x one chunk of rows with the 128-byte swizzle.
@@ -1215,15 +1229,13 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
         return cudaErrorInvalidValue;
 
     const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
-    chunked_forward_kernel<KC, DV, MASKED><<<grid, kThreads, kSmemBytes, stream>>>(
-        a, map, maps, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg,
-        counter);
-    e = cudaGetLastError();
+    e = launch_dependent(chunked_forward_kernel<KC, DV, MASKED>, dim3(grid), dim3(kThreads), kSmemBytes, stream, a,
+                         map, maps, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale,
+                         (int32_t)nseg, counter);
     if (e != cudaSuccess) return e;
     const int redo_grid = (int)std::min<int64_t>(nseg, 2 * (sms > 0 ? sms : 148));
-    segment_redo_kernel<KC, DV, MASKED><<<redo_grid, 256, 0, stream>>>(a, cfg.num_heads, cfg.num_partitions,
-                                                                       cfg.top_k, cfg.use_shared, cfg.scale);
-    return cudaGetLastError();
+    return launch_dependent(segment_redo_kernel<KC, DV, MASKED>, dim3(redo_grid), dim3(256), 0, stream, a,
+                            cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
 }
 
 }  // namespace
@@ -1234,7 +1246,8 @@ bool chunked_supported(const sse_config_t &cfg) {
     return cfg.dtype == SSE_BF16 && c_ok && d_ok;
 }
 
-// work counter (256 bytes), then the redo list (one entry per work item)
+// 256 bytes reserved (the work counter lives in the flags words), then the redo
+// list (one entry per work item)
 size_t chunked_extra_workspace(const sse_config_t &cfg, int64_t, int32_t num_seqs) {
     const int64_t nitems = (int64_t)num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
     return 256 + (size_t)nitems * sizeof(int32_t);
@@ -1271,9 +1284,18 @@ cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a,
     if (rows == 0) return cudaSuccess;
     const int64_t work = rows * (cfg.value_dim / 8);
     const unsigned blocks = (unsigned)std::min<int64_t>((work + 255) / 256, 152 * 16);
-    gather_combine_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(a.part_routed), a.rec_pos,
-                                                      rows, cfg.value_dim, ncon, static_cast<__nv_bfloat16 *>(a.out));
-    return cudaGetLastError();
+    const __nv_bfloat16 *part = static_cast<const __nv_bfloat16 *>(a.part_routed);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+    const int32_t *rp = a.rec_pos;
+    switch (ncon) {
+#define SSE_COMBINE(NC) \
+    case NC: return launch_dependent(gather_combine_kernel<NC>, dim3(blocks), dim3(256), 0, stream, part, rp, rows, \
+                                     cfg.value_dim, out)
+        SSE_COMBINE(1); SSE_COMBINE(2); SSE_COMBINE(3); SSE_COMBINE(4); SSE_COMBINE(5);
+        SSE_COMBINE(6); SSE_COMBINE(7); SSE_COMBINE(8); SSE_COMBINE(9);
+#undef SSE_COMBINE
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace sse

@@ -67,6 +67,8 @@ __device__ int block_exclusive_scan(int x, int *total) {
 // the unused tail up to max_blocks.  One CTA.
 __global__ void plan_blocks_kernel(const int32_t *__restrict__ cu, int32_t nseq, int32_t *__restrict__ blk_prefix,
                                    int4 *__restrict__ blk_info, int32_t max_blocks) {
+    griddep_launch_dependents();
+    griddep_wait();
     int carry = 0;
     for (int base = 0; base < nseq; base += blockDim.x) {
         const int b = base + threadIdx.x;
@@ -95,11 +97,13 @@ route_count_kernel(const T *__restrict__ logits, const int4 *__restrict__ blk_in
                    int32_t k, int32_t vec, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                    int32_t *__restrict__ cnt, int32_t max_blocks) {
     __shared__ int hist[kMaxPartitions];
+    griddep_launch_dependents();
+    if (threadIdx.x < kMaxPartitions) hist[threadIdx.x] = 0;
+    griddep_wait();
     // consecutive CTAs take the heads of one routing block, so the partial
     // sectors they write into [T, H, ...] rows meet in L2
     const int h = (int)(blockIdx.x % (unsigned)H), j = (int)(blockIdx.x / (unsigned)H);
     const int4 bi = blk_info[j];  // (sequence, first token, end token); sequence -1: past the last block
-    if (threadIdx.x < kMaxPartitions) hist[threadIdx.x] = 0;
     __syncthreads();
     if (bi.x >= 0) {
         const int t = bi.y + threadIdx.x;
@@ -122,6 +126,8 @@ route_count_kernel(const T *__restrict__ logits, const int4 *__restrict__ blk_in
 
 __global__ void __launch_bounds__(1024)
 scan_blocks_kernel(int32_t *__restrict__ cnt, int32_t max_blocks) {
+    griddep_launch_dependents();
+    griddep_wait();
     int32_t *row = cnt + (int64_t)blockIdx.x * (max_blocks + 1);
     int carry = 0;
     for (int base = 0; base < max_blocks; base += blockDim.x) {
@@ -153,6 +159,8 @@ seg_off_kernel(const int32_t *__restrict__ cnt, int32_t max_blocks,
                const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cu, int32_t nseq,
                int32_t H, int32_t N, int32_t use_shared, int32_t *__restrict__ seg_off,
                int32_t *__restrict__ pad_off) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t nseg = (int64_t)nseq * H * N;
     int carry = 0;
     for (int64_t base = 0; base < nseg; base += blockDim.x) {
@@ -203,6 +211,8 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
     // sectors they write into [T, H, ...] rows meet in L2
     const int h = (int)(blockIdx.x % (unsigned)H), j = (int)(blockIdx.x / (unsigned)H);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    griddep_launch_dependents();
+    griddep_wait();
     const int4 bi = blk_info[j];  // (sequence, first token, end token); sequence -1: past the last block
     if (bi.x < 0) return;
     const int b = bi.x;
@@ -250,16 +260,16 @@ scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__
 // Router launch with the unroll bound NP >= N; rows go through 16-byte
 // vector loads when every row starts on a 16-byte boundary.
 template <typename T>
-void launch_count(dim3 grid, cudaStream_t stream, const T *logits, const int4 *blk_info, int32_t H, int32_t N,
+cudaError_t launch_count(dim3 grid, cudaStream_t stream, const T *logits, const int4 *blk_info, int32_t H, int32_t N,
                   int32_t k, int32_t *topk_idx, float *topk_w, int32_t *cnt, int32_t MB) {
     const int vec = (N * sizeof(T)) % 16 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
-#define SSE_COUNT(NP)                                                                                   \
-    route_count_kernel<T, NP><<<grid, kRouteBlock, 0, stream>>>(logits, blk_info, H, N, k, vec, topk_idx, topk_w, \
-                                                               cnt, MB)
-    if (N <= 8) SSE_COUNT(8);
-    else if (N <= 16) SSE_COUNT(16);
-    else if (N <= 32) SSE_COUNT(32);
-    else SSE_COUNT(64);
+#define SSE_COUNT(NP)                                                                                         \
+    launch_dependent(route_count_kernel<T, NP>, grid, dim3(kRouteBlock), 0, stream, logits, blk_info, H, N, k, vec, \
+                     topk_idx, topk_w, cnt, MB)
+    if (N <= 8) return SSE_COUNT(8);
+    if (N <= 16) return SSE_COUNT(16);
+    if (N <= 32) return SSE_COUNT(32);
+    return SSE_COUNT(64);
 #undef SSE_COUNT
 }
 
@@ -271,6 +281,8 @@ __global__ void __launch_bounds__(1024)
 masked_pad_kernel(const int32_t *__restrict__ cu, int32_t nseq, int32_t H, int32_t N, int32_t use_shared,
                   int32_t *__restrict__ pad_off) {
     extern __shared__ int s_pref[];  // [nseq + 1]
+    griddep_launch_dependents();
+    griddep_wait();
     int carry = 0;
     for (int base = 0; base < nseq; base += blockDim.x) {
         const int b = base + threadIdx.x;
@@ -309,6 +321,8 @@ __global__ void __launch_bounds__(256)
 masked_recpos_kernel(const int32_t *__restrict__ cu, int32_t nseq, const int32_t *__restrict__ topk_idx,
                      int64_t total_tokens, int32_t H, int32_t N, int32_t k, int32_t use_shared,
                      const int32_t *__restrict__ pad_off, int32_t *__restrict__ rec_pos) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t rows = total_tokens * H;
     const int ncon = k + use_shared;
     const int64_t nshared = use_shared ? (int64_t)nseq * H : 0;
@@ -336,22 +350,26 @@ cudaError_t launch_route(const sse_config_t &cfg, const void *logits, const int3
     const int H = cfg.num_heads, N = cfg.num_partitions, k = cfg.top_k;
     const int MB = rb.max_blocks;
     plan_blocks_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, rb.blk_prefix, rb.blk_info, MB);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((int64_t)MB * H));
-    if (cfg.dtype == SSE_BF16)
-        launch_count<__nv_bfloat16>(grid, stream, static_cast<const __nv_bfloat16 *>(logits), rb.blk_info, H, N, k,
-                                    rb.topk_idx, rb.topk_w, rb.cnt, MB);
-    else
-        launch_count<float>(grid, stream, static_cast<const float *>(logits), rb.blk_info, H, N, k, rb.topk_idx,
-                            rb.topk_w, rb.cnt, MB);
-    if (!group) return cudaGetLastError();
-    scan_blocks_kernel<<<H * N, 1024, 0, stream>>>(rb.cnt, MB);
-    seg_off_kernel<<<1, 1024, 0, stream>>>(rb.cnt, MB, rb.blk_prefix, cu_seqlens, num_seqs, H, N,
-                                           cfg.use_shared, rb.seg_off, rb.pad_off);
-    scatter_kernel<<<grid, kRouteBlock, 0, stream>>>(rb.topk_idx, cu_seqlens, num_seqs, rb.blk_prefix, rb.blk_info,
-                                                     rb.cnt, MB, rb.seg_off, H, N, k, cfg.use_shared,
-                                                     rb.topk_w, rb.perm, rb.perm_rec, rb.perm_e,
-                                                     rb.pad_off, rb.rec_pos);
-    return cudaGetLastError();
+    e = cfg.dtype == SSE_BF16
+            ? launch_count<__nv_bfloat16>(grid, stream, static_cast<const __nv_bfloat16 *>(logits), rb.blk_info, H, N,
+                                          k, rb.topk_idx, rb.topk_w, rb.cnt, MB)
+            : launch_count<float>(grid, stream, static_cast<const float *>(logits), rb.blk_info, H, N, k,
+                                  rb.topk_idx, rb.topk_w, rb.cnt, MB);
+    if (e != cudaSuccess || !group) return e;
+    e = launch_dependent(scan_blocks_kernel, dim3(H * N), dim3(1024), 0, stream, rb.cnt, MB);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(seg_off_kernel, dim3(1), dim3(1024), 0, stream, (const int32_t *)rb.cnt, MB,
+                         (const int32_t *)rb.blk_prefix, cu_seqlens, num_seqs, H, N, cfg.use_shared, rb.seg_off,
+                         rb.pad_off);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(scatter_kernel, grid, dim3(kRouteBlock), 0, stream, (const int32_t *)rb.topk_idx,
+                            cu_seqlens, num_seqs, (const int32_t *)rb.blk_prefix, (const int4 *)rb.blk_info,
+                            (const int32_t *)rb.cnt, MB, (const int32_t *)rb.seg_off, H, N, k, cfg.use_shared,
+                            (const float *)rb.topk_w, rb.perm, rb.perm_rec, rb.perm_e, (const int32_t *)rb.pad_off,
+                            rb.rec_pos);
 }
 
 }  // namespace sse

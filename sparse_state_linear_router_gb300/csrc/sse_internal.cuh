@@ -19,6 +19,36 @@ constexpr int kRouteLaunches = 5; // kernels launch_route issues when grouping
 constexpr int kChunkRows = 128;   // rows of a tensor-core chunk; output regions are padded to it
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The forward's kernels are launched so that
+// each may start while the previous one in the stream is finishing (its CTAs
+// are scheduled and run their prologue early).  Every kernel of such a chain
+// calls griddep_wait() before it touches global memory -- and before any
+// early return, so that no grid of the chain completes before the one ahead
+// of it -- and calls griddep_launch_dependents() at its start, which lets the
+// next kernel be scheduled once all of this grid's CTAs are running.  Both are
+// no-ops for a kernel launched the ordinary way.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // Element access for the two storage dtypes.
 // ---------------------------------------------------------------------------
 template <typename T> struct Elem;
@@ -233,7 +263,7 @@ struct ForwardArgs {
     void *part_routed;   // recurrent: [T, H, k, d] fp32; chunked: [part_rows, d] bf16 in work-item order
     void *part_shared;   // recurrent: [T, H, d] fp32; chunked: unused
     int32_t part_bf16;
-    int32_t *flags;      // [0]: device-check flags; [1]: entries of redo_list
+    int32_t *flags;      // [0]: device-check flags; [1]: entries of redo_list; [2]: chunked work counter
     void *chunk_ws;      // chunked path scratch
     int32_t *redo_list;  // chunked path: work items to recompute token by token
 };
