@@ -67,16 +67,22 @@ backward_segment_kernel(BackwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
     const int ncon = topk + use_shared;
     const int nshared = use_shared ? a.num_seqs * H : 0;
     const int P = N + use_shared;
-    const bool is_shared = (int)blockIdx.x < nshared;
+    // the work item: this CTA's index, or the list entry it names
+    int item = (int)blockIdx.x;
+    if (a.seg_list) {
+        if (item >= *(volatile const int32_t *)a.seg_count) return;
+        item = a.seg_list[item];
+    }
+    const bool is_shared = item < nshared;
     int b, h, slot, len, base;
     if (is_shared) {
-        b = blockIdx.x / H;
-        h = blockIdx.x % H;
+        b = item / H;
+        h = item % H;
         slot = N;
         base = a.cu_seqlens[b];
         len = a.cu_seqlens[b + 1] - base;
     } else {
-        const int s = blockIdx.x - nshared;
+        const int s = item - nshared;
         slot = s % N;
         h = (s / N) % H;
         b = s / (N * H);
@@ -412,17 +418,11 @@ cudaError_t dispatch_d(const sse_config_t &cfg, const BackwardArgs &a, cudaStrea
 
 }  // namespace
 
-bool backward_supported(const sse_config_t &cfg) {
-    const int d = cfg.value_dim, c = cfg.key_dim;
-    if (!(d == 16 || d == 32 || d == 64 || d == 128 || d == 256)) return false;
-    const int R = kBwdThreads / (d / 4);
-    return c >= 4 && c % 4 == 0 && c <= R * kBwdMaxRows && c <= kBwdThreads;
+cudaError_t launch_backward_segments(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream) {
+    return cfg.dtype == SSE_BF16 ? dispatch_d<__nv_bfloat16>(cfg, a, stream) : dispatch_d<float>(cfg, a, stream);
 }
 
-cudaError_t launch_backward(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream, int *launches) {
-    cudaError_t e = cfg.dtype == SSE_BF16 ? dispatch_d<__nv_bfloat16>(cfg, a, stream) : dispatch_d<float>(cfg, a, stream);
-    if (e != cudaSuccess) return e;
-    *launches += 1;
+cudaError_t launch_backward_combine(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream) {
     const int64_t rows = a.total_tokens * cfg.num_heads;
     if (rows == 0) return cudaSuccess;
     const int per_row = 1 + 4 * (cfg.key_dim / 4) + cfg.value_dim / 4;
@@ -434,8 +434,23 @@ cudaError_t launch_backward(const sse_config_t &cfg, const BackwardArgs &a, cuda
     else
         backward_combine_kernel<float><<<blocks, 256, 0, stream>>>(a, rows, cfg.key_dim, cfg.value_dim,
                                                                   cfg.num_partitions, cfg.top_k, cfg.use_shared);
-    *launches += 1;
     return cudaGetLastError();
+}
+
+bool backward_supported(const sse_config_t &cfg) {
+    const int d = cfg.value_dim, c = cfg.key_dim;
+    if (!(d == 16 || d == 32 || d == 64 || d == 128 || d == 256)) return false;
+    const int R = kBwdThreads / (d / 4);
+    return c >= 4 && c % 4 == 0 && c <= R * kBwdMaxRows && c <= kBwdThreads;
+}
+
+cudaError_t launch_backward(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream, int *launches) {
+    cudaError_t e = launch_backward_segments(cfg, a, stream);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    e = launch_backward_combine(cfg, a, stream);
+    *launches += 1;
+    return e;
 }
 
 }  // namespace sse

@@ -331,13 +331,40 @@ namespace {
 struct BackwardLayout {
     RouteBuffers rb;
     float *dq_c, *dk_c, *dg_c, *dv_c, *de_c;
+    // chunked form
+    bool chunked;
+    int64_t num_chunks;
+    float *ustate, *wgrad, *gamma, *gscratch, *fterm, *dgtot;
+    int32_t *marks, *redo_list, *flags;
     size_t bytes;
 };
+
+// The chunked (tensor-core) backward unless the recurrent one is asked for.
+bool use_chunked_backward(const sse_config_t &c) {
+    return c.algo != SSE_ALGO_RECURRENT && sse::backward_chunked_supported(c);
+}
 
 BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_t S) {
     Carver cv(ws);
     BackwardLayout L{};
-    L.rb = carve_route(cv, c, T, S, nullptr, nullptr, nullptr, nullptr, true, true);
+    L.chunked = use_chunked_backward(c);
+    L.rb = carve_route(cv, c, T, S, nullptr, nullptr, nullptr, nullptr, true, true, L.chunked);
+    if (L.chunked) {
+        sse_config_t grouped = c;
+        grouped.algo = SSE_ALGO_AUTO;  // chunk-padded grouped records, as the chunked forward lays them out
+        L.num_chunks = sse::chunked_part_rows(grouped, T, S) / sse::kChunkRows;
+        const size_t nch = (size_t)L.num_chunks, kc = (size_t)c.key_dim, dv = (size_t)c.value_dim;
+        const size_t nitems = (size_t)S * c.num_heads * (c.num_partitions + c.use_shared);
+        L.ustate = cv.take<float>(nch * kc * dv);
+        L.wgrad = cv.take<float>(nch * kc * dv);
+        L.gamma = cv.take<float>(nch * kc);
+        L.dgtot = cv.take<float>(nch * kc);
+        L.gscratch = cv.take<float>((size_t)sse::kBwdScratchCtas * sse::kChunkRows * kc);
+        L.fterm = cv.take<float>(nitems * kc);
+        L.marks = cv.take<int32_t>(nitems);
+        L.redo_list = cv.take<int32_t>(nitems);
+        L.flags = cv.take<int32_t>(64);
+    }
     const size_t slots = (size_t)T * c.num_heads * (c.top_k + c.use_shared);
     L.dq_c = cv.take<float>(slots * c.key_dim);
     L.dk_c = cv.take<float>(slots * c.key_dim);
@@ -380,6 +407,7 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
                                                              (const void *)d_initial_state})
         if (!aligned16(p)) return SSE_ERR_INVALID_ARG;
     if (!sse::backward_supported(c)) return SSE_ERR_UNSUPPORTED;
+    if (c.algo == SSE_ALGO_CHUNKED && !sse::backward_chunked_supported(c)) return SSE_ERR_UNSUPPORTED;
     const size_t need = sse_backward_workspace_size(cfg, total_tokens, num_seqs);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
         return SSE_ERR_WORKSPACE;
@@ -407,6 +435,14 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
     a.topk_idx = L.rb.topk_idx;
     a.dq_c = L.dq_c; a.dk_c = L.dk_c; a.dg_c = L.dg_c; a.dv_c = L.dv_c; a.de_c = L.de_c;
     int launches = sse::kRouteLaunches;
+    if (L.chunked) {
+        a.pad_off = L.rb.pad_off;
+        a.num_chunks = L.num_chunks;
+        a.ustate = L.ustate; a.wgrad = L.wgrad; a.gamma = L.gamma; a.gscratch = L.gscratch;
+        a.fterm = L.fterm; a.dgtot = L.dgtot; a.marks = L.marks; a.redo_list = L.redo_list; a.flags = L.flags;
+        e = sse::launch_backward_chunked(c, a, s, &launches);
+        return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
+    }
     e = sse::launch_backward(c, a, s, &launches);
     return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
 }

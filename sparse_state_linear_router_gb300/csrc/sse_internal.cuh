@@ -299,8 +299,34 @@ struct BackwardArgs {
     const float *perm_e;
     float *dq_c, *dk_c, *dg_c, *dv_c;  // contribution slots
     float *de_c;                       // [T, H, k, 2] router-weight gradient of each selected partition (read, write)
+    // Per-token kernel restricted to a list of work items (shared (b, h) first,
+    // then routed (b, h, i)): item seg_list[x] for x < *seg_count.  Null: all.
+    const int32_t *seg_list, *seg_count;
+    // Chunked (tensor-core) form, c = 128: buffers of backward_chunked.cu.
+    const int32_t *pad_off;  // chunk-padded first row of each work item; chunk = row / 128
+    int64_t num_chunks;      // upper bound of the chunks (launch size; items past the last exit)
+    float *ustate;           // [chunks, c, d]: K_hat^T V of the chunk, then the state at its start
+    float *wgrad;            // [chunks, c, d]: Q_hat^T dO of the chunk, then dL/dS at its end
+    float *gamma;            // [chunks, c]: exp(G_last), the chunk's decay of each state row
+    float *gscratch;         // [kBwdScratchCtas, 128, c]: G_r - G_m of the chunk in flight, per CTA
+    float *fterm;            // [items, c]: rowsum(S_T * dL/dS_T) of each work item
+    float *dgtot;            // [chunks, c]: gate-gradient sums of each chunk, then of all later rows
+    int32_t *marks;          // [items]: item queued for the per-token kernel (gate range)
+    int32_t *redo_list;      // [items] and its length in flags[1]
+    int32_t *flags;          // [0]: device-check flags, [1]: entries of redo_list
 };
+constexpr int kBwdScratchCtas = 256;  // CTAs of the chunked gradient kernel (one scratch slot each)
 bool backward_supported(const sse_config_t &cfg);
+// The chunked form: bf16, c = 128, d in {64, 128}.
+bool backward_chunked_supported(const sse_config_t &cfg);
+// Launches the chunked form: every work item, then the per-token kernel over
+// the items whose gates left the factorised form's range, then the per-token
+// sums.  Adds the number of kernels it launched to *launches.
+cudaError_t launch_backward_chunked(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream,
+                                    int *launches);
+// The per-token kernel over the items a.seg_list names (all when null).
+cudaError_t launch_backward_segments(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream);
+cudaError_t launch_backward_combine(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream);
 // Adds the number of kernels it launched to *launches.
 cudaError_t launch_backward(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream, int *launches);
 

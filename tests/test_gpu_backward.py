@@ -30,7 +30,7 @@ def _store(x, dtype):
     return x if dtype == "f32" else synth.f32_to_bf16_bits(x)
 
 
-def _run(w, inp, *, seed=0, with_dfin=True, separate_shared=False, scale=1.0, pairs_only=None):
+def _run(w, inp, *, seed=0, with_dfin=True, separate_shared=False, scale=1.0, pairs_only=None, algo="auto"):
     """GPU and oracle gradients of <d_out, out> + <d_final, final_state>."""
     from oracle import backward as bw
     from sparse_state_linear_router_gb300 import binding
@@ -43,7 +43,7 @@ def _run(w, inp, *, seed=0, with_dfin=True, separate_shared=False, scale=1.0, pa
     if separate_shared:
         qs = _store(rng.normal(size=inp.q.shape) / np.sqrt(w.key_dim), w.dtype)
         ks = _store(rng.random(size=inp.k.shape) / w.key_dim, w.dtype)
-    cfg = H_.config_of(w, scale=scale)
+    cfg = H_.config_of(w, algo=algo, scale=scale)
     dv_ = lambda a: None if a is None else binding.to_device(a)  # noqa: E731
     t = {n: dv_(getattr(inp, n)) for n in ("q", "k", "v", "g", "logits")}
     cu = torch.from_numpy(inp.cu_seqlens).cuda()
@@ -98,13 +98,45 @@ CASES = {
 }
 
 
+def _algos(w):
+    """The chunked (tensor-core) form where it applies (bf16, c = 128), and the
+    per-token one everywhere."""
+    return ["recurrent", "chunked"] if (w.dtype == "bf16" and w.key_dim == 128) else ["recurrent"]
+
+
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_backward_matches_oracle(name):
     wname, lengths, over, kw = CASES[name]
     w = H_.workload_variant(wname, **over)
     inp = synth.make_forward_inputs(w, seed=3, lengths=lengths, with_init=True)
-    gpu, ref, _ = _run(w, inp, **kw)
-    _compare(gpu, ref, H_.tol_for(w))
+    for algo in _algos(w):
+        gpu, ref, _ = _run(w, inp, algo=algo, **kw)
+        _compare(gpu, ref, H_.tol_for(w))
+
+
+@pytest.mark.parametrize("dv", [128, 64])
+def test_backward_chunked_many_chunks(dv):
+    """Segments of several chunks with ragged tails, empty sequences and
+    separate shared q / k: the chunked form's scan over chunks and its
+    suffix sums of the gate gradient carry across chunk boundaries."""
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=4, top_k=2, value_dim=dv)
+    inp = synth.make_forward_inputs(w, seed=21, lengths=[700, 0, 300, 129], with_init=True)
+    gpu, ref, _ = _run(w, inp, algo="chunked", separate_shared=True, scale=0.75)
+    _compare(gpu, ref, H_.TOL_BF16)
+
+
+def test_backward_chunked_strong_gates():
+    """Log-gates of -5 on a run of rows push some chunks past the factorised
+    form's range (|G_m| or |G_l - G_m| > 64): those work items go to the
+    per-token kernel, the rest stay chunked, and every gradient matches."""
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=4, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=5, lengths=[400, 260], with_init=True)
+    g = synth.bf16_bits_to_f32(inp.g)
+    g[100:180, 0] = -5.0       # shared and routed segments of head 0 in sequence 0
+    g[500:520, 1] = -3.0       # a milder run in sequence 1, head 1
+    inp.g = synth.f32_to_bf16_bits(g.astype(np.float32))
+    gpu, ref, _ = _run(w, inp, algo="chunked")
+    _compare(gpu, ref, H_.TOL_BF16)
 
 
 def test_backward_skewed_routing_and_empty_segments():
