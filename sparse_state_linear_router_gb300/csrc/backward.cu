@@ -308,56 +308,56 @@ backward_segment_kernel(BackwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
 
 // Per (t, h): the fixed-order sums of the contribution slots, and the router
 // logits' gradient through the softmax over all N partitions.  One thread per
-// (t, h) row handles its logits; the c- and d-wide sums run four columns per
-// thread.
-template <typename T>
+// (t, h) row handles its logits; then the c- and d-wide sums run four columns
+// per thread, NC (= k + shared) slot loads issued before the sum.
+template <typename T, int NC>
 __global__ void __launch_bounds__(256)
 backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int32_t N, int32_t topk,
                         int32_t use_shared) {
-    const int ncon = topk + use_shared;
+    const int ncon = NC;
     const int c4 = c / 4, d4 = d / 4;
-    const int per_row = 1 + 4 * c4 + d4;  // logits, dq, dk, dg, dq_shared / dk_shared, dv
-    const int64_t total = rows * per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const bool sep_q = use_shared && a.qs, sep_k = use_shared && a.ks;
-    for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = x / per_row;
-        int part = (int)(x - row * per_row);
-        if (part == 0) {
-            // dlogits = e * (de - <e, de>): softmax of the stored logits in fp32
-            const T *lg = static_cast<const T *>(a.logits) + row * N;
-            float m = -INFINITY;
-            for (int i = 0; i < N; ++i) m = fmaxf(m, Elem<T>::load(lg + i));
-            float s = 0.f;
-            for (int i = 0; i < N; ++i) s += expf(Elem<T>::load(lg + i) - m);
-            const float inv = 1.f / s;
-            float ede = 0.f;
-            for (int j = 0; j < topk; ++j) {
-                const int i = a.topk_idx[row * topk + j];
-                ede += expf(Elem<T>::load(lg + i) - m) * inv * (a.de_c[(row * topk + j) * 2] + a.de_c[(row * topk + j) * 2 + 1]);
-            }
-            T *dl = static_cast<T *>(a.d_logits) + row * N;
-            for (int i = 0; i < N; ++i) {
-                float de = 0.f;
-                for (int j = 0; j < topk; ++j)
-                    if (a.topk_idx[row * topk + j] == i) de = a.de_c[(row * topk + j) * 2] + a.de_c[(row * topk + j) * 2 + 1];
-                const float e = expf(Elem<T>::load(lg + i) - m) * inv;
-                Elem<T>::store(dl + i, e * (de - ede));
-            }
-            continue;
+    for (int64_t row = gid; row < rows; row += stride) {
+        // dlogits = e * (de - <e, de>): softmax of the stored logits in fp32
+        const T *lg = static_cast<const T *>(a.logits) + row * N;
+        float m = -INFINITY;
+        for (int i = 0; i < N; ++i) m = fmaxf(m, Elem<T>::load(lg + i));
+        float s = 0.f;
+        for (int i = 0; i < N; ++i) s += expf(Elem<T>::load(lg + i) - m);
+        const float inv = 1.f / s;
+        float ede = 0.f;
+        for (int j = 0; j < topk; ++j) {
+            const int i = a.topk_idx[row * topk + j];
+            ede += expf(Elem<T>::load(lg + i) - m) * inv * (a.de_c[(row * topk + j) * 2] + a.de_c[(row * topk + j) * 2 + 1]);
         }
-        part -= 1;
+        T *dl = static_cast<T *>(a.d_logits) + row * N;
+        for (int i = 0; i < N; ++i) {
+            float de = 0.f;
+            for (int j = 0; j < topk; ++j)
+                if (a.topk_idx[row * topk + j] == i) de = a.de_c[(row * topk + j) * 2] + a.de_c[(row * topk + j) * 2 + 1];
+            const float e = expf(Elem<T>::load(lg + i) - m) * inv;
+            Elem<T>::store(dl + i, e * (de - ede));
+        }
+    }
+    const int per_row = 4 * c4 + d4;  // dq, dk, dg, dq_shared / dk_shared, dv
+    const int64_t total = rows * per_row;
+    for (int64_t x = gid; x < total; x += stride) {
+        const int64_t row = x / per_row;
+        const int part = (int)(x - row * per_row);
         const float *src;
         T *dst;
-        int width, cidx, lo, hi;  // slots lo .. hi - 1 summed
+        int width, cidx, hi;  // slots 0 .. hi - 1 summed
         const int kind = part < 4 * c4 ? part / c4 : 4;
         if (kind < 4) {
             cidx = 4 * (part % c4);
             width = c;
             // 0: dq (routed slots, plus the shared slot unless q_shared is separate),
             // 1: dk (likewise), 2: dg (all slots), 3: dq_shared / dk_shared
-            if (kind == 0) { src = a.dq_c; dst = static_cast<T *>(a.dq); lo = 0; hi = sep_q ? topk : ncon; }
-            else if (kind == 1) { src = a.dk_c; dst = static_cast<T *>(a.dk); lo = 0; hi = sep_k ? topk : ncon; }
-            else if (kind == 2) { src = a.dg_c; dst = static_cast<T *>(a.dg); lo = 0; hi = ncon; }
+            if (kind == 0) { src = a.dq_c; dst = static_cast<T *>(a.dq); hi = sep_q ? topk : ncon; }
+            else if (kind == 1) { src = a.dk_c; dst = static_cast<T *>(a.dk); hi = sep_k ? topk : ncon; }
+            else if (kind == 2) { src = a.dg_c; dst = static_cast<T *>(a.dg); hi = ncon; }
             else {
                 // the shared slot alone, into dq_shared and dk_shared when they are separate
                 if (sep_q) {
@@ -375,13 +375,18 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
             width = d;
             src = a.dv_c;
             dst = static_cast<T *>(a.dv);
-            lo = 0;
             hi = ncon;
         }
+        float4 p[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j)
+            p[j] = j < hi ? *reinterpret_cast<const float4 *>(src + (row * ncon + j) * width + cidx)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = lo; j < hi; ++j) {
-            const float4 p = *reinterpret_cast<const float4 *>(src + (row * ncon + j) * width + cidx);
-            acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            if (j >= hi) break;
+            acc.x += p[j].x; acc.y += p[j].y; acc.z += p[j].z; acc.w += p[j].w;
         }
         Elem<T>::store4(dst + row * width + cidx, acc);
     }
@@ -425,15 +430,27 @@ cudaError_t launch_backward_segments(const sse_config_t &cfg, const BackwardArgs
 cudaError_t launch_backward_combine(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream) {
     const int64_t rows = a.total_tokens * cfg.num_heads;
     if (rows == 0) return cudaSuccess;
-    const int per_row = 1 + 4 * (cfg.key_dim / 4) + cfg.value_dim / 4;
+    const int per_row = 4 * (cfg.key_dim / 4) + cfg.value_dim / 4;
     const unsigned blocks = (unsigned)std::min<int64_t>((rows * per_row + 255) / 256, 152 * 16);
-    if (cfg.dtype == SSE_BF16)
-        backward_combine_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(a, rows, cfg.key_dim, cfg.value_dim,
-                                                                          cfg.num_partitions, cfg.top_k,
-                                                                          cfg.use_shared);
-    else
-        backward_combine_kernel<float><<<blocks, 256, 0, stream>>>(a, rows, cfg.key_dim, cfg.value_dim,
-                                                                  cfg.num_partitions, cfg.top_k, cfg.use_shared);
+    const int ncon = cfg.top_k + cfg.use_shared;
+#define SSE_BCOMB(T, NC)                                                                                      \
+    case NC:                                                                                                  \
+        backward_combine_kernel<T, NC><<<blocks, 256, 0, stream>>>(a, rows, cfg.key_dim, cfg.value_dim,     \
+                                                                   cfg.num_partitions, cfg.top_k, cfg.use_shared); \
+        break
+#define SSE_BCOMB_ALL(T)                                                                                      \
+    switch (ncon) {                                                                                           \
+        SSE_BCOMB(T, 1); SSE_BCOMB(T, 2); SSE_BCOMB(T, 3); SSE_BCOMB(T, 4); SSE_BCOMB(T, 5);                 \
+        SSE_BCOMB(T, 6); SSE_BCOMB(T, 7); SSE_BCOMB(T, 8); SSE_BCOMB(T, 9);                                  \
+        default: return cudaErrorInvalidValue;                                                                \
+    }
+    if (cfg.dtype == SSE_BF16) {
+        SSE_BCOMB_ALL(__nv_bfloat16)
+    } else {
+        SSE_BCOMB_ALL(float)
+    }
+#undef SSE_BCOMB_ALL
+#undef SSE_BCOMB
     return cudaGetLastError();
 }
 

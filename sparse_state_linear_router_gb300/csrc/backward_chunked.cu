@@ -155,12 +155,34 @@ __device__ __forceinline__ void gate_half_sums(const unsigned char *tg, float *p
     part[half * kKey + col] = s;
 }
 
+constexpr int kPatchStride = 20;  // floats per row of a warp's store patch (16 used; rows stay 16-byte aligned)
+
+// A 32-row x 16-column block of fp32 values, one row per lane, goes out through
+// the warp's shared patch: each store instruction then writes 8 rows x 64
+// contiguous bytes instead of 32 rows x 16.  Row (lane / 4 + 8 kk) of the block
+// lands at base + sr[kk] * width + col0 (skipped when sr[kk] < 0).
+__device__ __forceinline__ void warp_put16(float *patch, int lane, const float (&v)[16], float *base, int width,
+                                           int col0, const int64_t (&sr)[4]) {
+    float4 *pr = reinterpret_cast<float4 *>(patch + lane * kPatchStride);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int rr = (lane >> 2) + 8 * kk, qd = lane & 3;
+        if (sr[kk] >= 0)
+            *reinterpret_cast<float4 *>(base + sr[kk] * width + col0 + 4 * qd) =
+                *reinterpret_cast<const float4 *>(patch + rr * kPatchStride + 4 * qd);
+    }
+    __syncwarp();
+}
+
 // Shared memory of the chunk kernels: tiles from a 1024-aligned base, then
 // row metadata, gate sums, the mbarrier and the TMEM address slot.
 struct ChunkSmem {
     unsigned char *tile[6];
     int *tok, *slotj;
-    float *e, *part, *gm, *gl, *de;
+    float *e, *part, *gm, *gl, *de, *patch;
     uint32_t bar;
     uint32_t *tslot;
 };
@@ -169,31 +191,34 @@ __device__ __forceinline__ ChunkSmem carve_smem(unsigned char *raw, int ntiles) 
     ChunkSmem c;
     for (int i = 0; i < 6; ++i) c.tile[i] = sm + (i < ntiles ? i : 0) * kTile;
     unsigned char *p = sm + ntiles * kTile;
-    c.tok = reinterpret_cast<int *>(p);
-    c.slotj = c.tok + kRows;
-    c.e = reinterpret_cast<float *>(c.slotj + kRows);
-    c.part = c.e + kRows;       // [2][kKey]
+    c.tok = reinterpret_cast<int *>(p);   // [2 buffers][kRows]
+    c.slotj = c.tok + 2 * kRows;          // [2][kRows]
+    c.e = reinterpret_cast<float *>(c.slotj + 2 * kRows);  // [2][kRows]
+    c.part = c.e + 2 * kRows;   // [2][kKey]
     c.gm = c.part + 2 * kKey;   // [kKey]
     c.gl = c.gm + kKey;         // [kKey]
     c.de = c.gl + kKey;         // [2 halves][2 (read, write)][kRows]
-    uint64_t *b = reinterpret_cast<uint64_t *>(c.de + 4 * kRows);
+    c.patch = c.de + 4 * kRows; // [8 warps][32][kPatchStride]
+    uint64_t *b = reinterpret_cast<uint64_t *>(c.patch + 8 * 32 * kPatchStride);
     c.bar = smem_u32(b);
     c.tslot = reinterpret_cast<uint32_t *>(b + 1);
     return c;
 }
 constexpr size_t chunk_smem_bytes(int ntiles) {
-    return 1024 + (size_t)ntiles * kTile + 3 * kRows * 4 + 4 * kKey * 4 + 4 * kRows * 4 + 16;
+    return 1024 + (size_t)ntiles * kTile + 6 * kRows * 4 + 4 * kKey * 4 + 4 * kRows * 4 +
+           8 * 32 * kPatchStride * 4 + 16;
 }
 
-// Row metadata of the chunk into shared memory (threads 0..127).
-__device__ __forceinline__ void chunk_meta(const BackwardArgs &a, const ChunkRef &r, int topk, const ChunkSmem &c) {
+// Row metadata of the chunk into metadata buffer mb (threads 0..127).
+__device__ __forceinline__ void chunk_meta(const BackwardArgs &a, const ChunkRef &r, int topk, const ChunkSmem &c,
+                                           int mb) {
     if (threadIdx.x < kRows) {
         int t, j;
         float e;
         row_meta(a, r, threadIdx.x, topk, t, e, j);
-        c.tok[threadIdx.x] = t;
-        c.e[threadIdx.x] = e;
-        c.slotj[threadIdx.x] = j;
+        c.tok[mb * kRows + threadIdx.x] = t;
+        c.e[mb * kRows + threadIdx.x] = e;
+        c.slotj[mb * kRows + threadIdx.x] = j;
     }
 }
 
@@ -245,16 +270,24 @@ bwd_chunk_sums_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v), *g = static_cast<const __nv_bfloat16 *>(a.g);
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.d_out);
     bool failed = false;
-    for (int64_t chunk = blockIdx.x; chunk < a.num_chunks; chunk += gridDim.x) {
-        ChunkRef r;
-        if (!locate_chunk(a, chunk, H, N, use_shared, r)) break;
-        chunk_meta(a, r, topk, c);
+    // metadata and row staging of chunk n + 1 are issued before chunk n's read-out
+    auto stage = [&](const ChunkRef &r, int mb) {
+        chunk_meta(a, r, topk, c, mb);
         __syncthreads();
-        stage_rows(tK, r.shared && ks ? ks : k, c.tok, H, r.h, kKey);
-        stage_rows(tQ, r.shared && qs ? qs : q, c.tok, H, r.h, kKey);
-        stage_rows(tG, g, c.tok, H, r.h, kKey);
-        stage_rows(tV, v, c.tok, H, r.h, DV);
-        stage_rows(tD, dout, c.tok, H, r.h, DV);
+        const int *tok = c.tok + mb * kRows;
+        stage_rows(tK, r.shared && ks ? ks : k, tok, H, r.h, kKey);
+        stage_rows(tQ, r.shared && qs ? qs : q, tok, H, r.h, kKey);
+        stage_rows(tG, g, tok, H, r.h, kKey);
+        stage_rows(tV, v, tok, H, r.h, DV);
+        stage_rows(tD, dout, tok, H, r.h, DV);
+    };
+    int64_t chunk = blockIdx.x;
+    ChunkRef r;
+    bool have = chunk < a.num_chunks && locate_chunk(a, chunk, H, N, use_shared, r);
+    int mb = 0;
+    if (have) stage(r, 0);
+    while (have) {
+        const float *ev = c.e + mb * kRows;
         cp_async_wait_all();
         __syncthreads();
         gate_half_sums(tG, c.part);
@@ -264,14 +297,19 @@ bwd_chunk_sums_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             const int col = tid & (kKey - 1), half = tid >> 7;
             const float gl = c.part[col] + c.part[kKey + col];
             float run = half ? c.part[col] : 0.f;
-            if (half == 0) a.gamma[chunk * kKey + col] = expf(gl);
+            if (half == 0) {
+                a.gamma[chunk * kKey + col] = expf(gl);
+                a.gml[chunk * 2 * kKey + col] = c.part[col];  // G_m: through the midpoint row
+                a.gml[chunk * 2 * kKey + kKey + col] = gl;
+            }
             for (int x = half * 64; x < half * 64 + 64; ++x) {
                 run += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tG + toff(x, col)));
-                const float e = c.e[x];
+                const float e = ev[x];
                 __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(tK + toff(x, col));
                 __nv_bfloat16 *pq = reinterpret_cast<__nv_bfloat16 *>(tQ + toff(x, col));
-                *pk = __float2bfloat16_rn(e * __bfloat162float(*pk) * expf(gl - run));
-                *pq = __float2bfloat16_rn(e * scale * __bfloat162float(*pq) * expf(run));
+                // factors rounded to bf16 with the products: fast exponentials suffice
+                *pk = __float2bfloat16_rn(e * __bfloat162float(*pk) * __expf(gl - run));
+                *pq = __float2bfloat16_rn(e * scale * __bfloat162float(*pq) * __expf(run));
             }
         }
         const bool ok = run_mma(c, phase, [&] {
@@ -288,32 +326,42 @@ bwd_chunk_sums_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             failed = true;
             break;
         }
+        const int64_t next = chunk + gridDim.x;
+        ChunkRef rn;
+        const bool have_next = next < a.num_chunks && locate_chunk(a, next, H, N, use_shared, rn);
+        if (have_next) stage(rn, mb ^ 1);
         {
             // lane quarter (warp % 4) holds state rows 32 (warp % 4) .. + 31, column half warp / 4
-            const int row = 32 * (warp & 3) + (tid & 31), hc = warp >> 2;
+            const int lane = tid & 31, hc = warp >> 2;
             const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-            float *U = a.ustate + (chunk * kKey + row) * DV, *W = a.wgrad + (chunk * kKey + row) * DV;
+            float *patch = c.patch + warp * 32 * kPatchStride;
+            int64_t sr[4];  // rows this lane stores: state rows of the chunk
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) sr[kk] = chunk * kKey + 32 * (warp & 3) + (lane >> 2) + 8 * kk;
             for (int c0 = hc * (DV / 2); c0 < (hc + 1) * (DV / 2); c0 += 32) {
-                uint32_t x[32];
-                tmem_ld32(tmem + lb + c0, x);
-                tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4 *>(U + c0 + i) =
-                        make_float4(__uint_as_float(x[i]), __uint_as_float(x[i + 1]), __uint_as_float(x[i + 2]),
-                                    __uint_as_float(x[i + 3]));
-                tmem_ld32(tmem + lb + 128 + c0, x);
-                tmem_wait_ld();
+                for (int m = 0; m < 2; ++m) {
+                    uint32_t x[32];
+                    tmem_ld32(tmem + lb + 128 * m + c0, x);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4 *>(W + c0 + i) =
-                        make_float4(__uint_as_float(x[i]), __uint_as_float(x[i + 1]), __uint_as_float(x[i + 2]),
-                                    __uint_as_float(x[i + 3]));
+                    for (int s16 = 0; s16 < 32; s16 += 16) {
+                        float v16[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v16[i] = __uint_as_float(x[s16 + i]);
+                        warp_put16(patch, lane, v16, m ? a.wgrad : a.ustate, DV, c0 + s16, sr);
+                    }
+                }
             }
         }
         fence_before();
-        __syncthreads();  // TMEM and the tiles are reused by the next chunk
+        __syncthreads();  // TMEM is reused by the next chunk
+        chunk = next;
+        r = rn;
+        have = have_next;
+        mb ^= 1;
     }
+    if (failed) cp_async_wait_all();  // no copy may still be writing shared memory when the CTA exits
     if (failed && tid == 0) atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
     __syncthreads();
     if (warp == 0) {
@@ -336,10 +384,12 @@ __device__ __forceinline__ void item_bhs(int u, int H, int N, int nshared, int &
     }
 }
 
-// ---- scan over chunks (in place) ---------------------------------------------
-// One thread per four elements of an item's c x d state: forward, U_j is
-// replaced by the state at chunk j's start; backward, W_j by dL/dS at its end.
-// Also rowsum(S_T * dL/dS_T) into fterm and dL/dS_0 into d_init.
+// ---- scan over chunks ---------------------------------------------------------
+// One thread per four elements of an item's c x d state: forward, the state
+// at chunk j's start, S' = diag(exp(G_m)) S_start; backward, dL/dS at its end,
+// dS' = diag(exp(G_l - G_m)) dS_end -- each written in bf16 straight into the
+// operand tile layout the gradient kernel copies in.  Also
+// rowsum(S_T * dL/dS_T) into fterm and dL/dS_0 into d_init.
 template <int DV>
 __global__ void __launch_bounds__(256)
 bwd_state_scan_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t use_shared) {
@@ -356,18 +406,35 @@ bwd_state_scan_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t use_shared) 
     const int64_t so = (((int64_t)b * H + h) * P + slot) * (int64_t)kKey * DV + (int64_t)row * DV + col;
     const int64_t cs = (int64_t)kKey * DV / 4;  // float4 stride between chunks
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 *U = reinterpret_cast<float4 *>(a.ustate + (cb * kKey + row) * DV + col);
-    float4 *W = reinterpret_cast<float4 *>(a.wgrad + (cb * kKey + row) * DV + col);
+    const float4 *U = reinterpret_cast<const float4 *>(a.ustate + (cb * kKey + row) * DV + col);
+    const float4 *W = reinterpret_cast<const float4 *>(a.wgrad + (cb * kKey + row) * DV + col);
     const float *gam = a.gamma + cb * kKey + row;
+    const float *gml = a.gml + cb * 2 * kKey + row;  // G_m at [j][0][row], G_l at [j][1][row]
+    const uint32_t toffs = toff(row, col);           // four bf16 in one 8-byte piece
+    unsigned char *sp = static_cast<unsigned char *>(a.sp_tiles) + cb * (int64_t)kTile + toffs;
+    unsigned char *dsp = static_cast<unsigned char *>(a.dsp_tiles) + cb * (int64_t)kTile + toffs;
+    auto put4 = [](unsigned char *p, float f, float4 x) {
+        *reinterpret_cast<uint2 *>(p) = make_uint2(pack2(f * x.x, f * x.y), pack2(f * x.z, f * x.w));
+    };
 
+    // eight chunks' loads in flight ahead of the dependent updates
+    constexpr int kAhead = 8;
     float4 S = a.init ? *reinterpret_cast<const float4 *>(a.init + so) : zero;
-    float4 x = nch > 0 ? U[0] : zero;
-    for (int j = 0; j < nch; ++j) {
-        const float4 xn = j + 1 < nch ? U[(j + 1) * cs] : zero;  // loaded ahead of the dependent update
-        const float gm = gam[(int64_t)j * kKey];
-        U[j * cs] = S;
-        S = make_float4(fmaf(gm, S.x, x.x), fmaf(gm, S.y, x.y), fmaf(gm, S.z, x.z), fmaf(gm, S.w, x.w));
-        x = xn;
+    for (int j0 = 0; j0 < nch; j0 += kAhead) {
+        float4 x[kAhead];
+        float gm[kAhead];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) {
+            x[i] = j0 + i < nch ? U[(j0 + i) * cs] : zero;
+            gm[i] = j0 + i < nch ? gam[(int64_t)(j0 + i) * kKey] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) {
+            if (j0 + i >= nch) break;
+            put4(sp + (int64_t)(j0 + i) * kTile, expf(gml[(int64_t)(j0 + i) * 2 * kKey]), S);
+            S = make_float4(fmaf(gm[i], S.x, x[i].x), fmaf(gm[i], S.y, x[i].y), fmaf(gm[i], S.z, x[i].z),
+                            fmaf(gm[i], S.w, x[i].w));
+        }
     }
     const float4 df = a.d_final ? *reinterpret_cast<const float4 *>(a.d_final + so) : zero;
     float pr = S.x * df.x + S.y * df.y + S.z * df.z + S.w * df.w;
@@ -376,13 +443,22 @@ bwd_state_scan_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t use_shared) 
     if (threadIdx.x % Q4 == 0) a.fterm[(int64_t)u * kKey + row] = pr;
 
     float4 dS = df;
-    x = nch > 0 ? W[(nch - 1) * cs] : zero;
-    for (int j = nch - 1; j >= 0; --j) {
-        const float4 xn = j > 0 ? W[(j - 1) * cs] : zero;
-        const float gm = gam[(int64_t)j * kKey];
-        W[j * cs] = dS;
-        dS = make_float4(fmaf(gm, dS.x, x.x), fmaf(gm, dS.y, x.y), fmaf(gm, dS.z, x.z), fmaf(gm, dS.w, x.w));
-        x = xn;
+    for (int j0 = nch - 1; j0 >= 0; j0 -= kAhead) {
+        float4 x[kAhead];
+        float gm[kAhead];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) {
+            x[i] = j0 - i >= 0 ? W[(j0 - i) * cs] : zero;
+            gm[i] = j0 - i >= 0 ? gam[(int64_t)(j0 - i) * kKey] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) {
+            if (j0 - i < 0) break;
+            const float *gj = gml + (int64_t)(j0 - i) * 2 * kKey;
+            put4(dsp + (int64_t)(j0 - i) * kTile, expf(gj[kKey] - gj[0]), dS);
+            dS = make_float4(fmaf(gm[i], dS.x, x[i].x), fmaf(gm[i], dS.y, x[i].y), fmaf(gm[i], dS.z, x[i].z),
+                             fmaf(gm[i], dS.w, x[i].w));
+        }
     }
     if (a.d_init) *reinterpret_cast<float4 *>(a.d_init + so) = dS;
 }
@@ -430,17 +506,26 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
     const int quarter = warp & 3, hc = warp >> 2, erow = 32 * quarter + lane;
     const uint32_t lb = (uint32_t)(32 * quarter) << 16;
     bool failed = false;
-    for (int64_t chunk = blockIdx.x; chunk < a.num_chunks; chunk += gridDim.x) {
-        ChunkRef r;
-        if (!locate_chunk(a, chunk, H, N, use_shared, r)) break;
-        chunk_meta(a, r, topk, c);
+    // metadata and row staging of chunk n + 1 are issued once chunk n's last
+    // products are done (every tile free), before its read-out
+    auto stage = [&](const ChunkRef &r, int mb) {
+        chunk_meta(a, r, topk, c, mb);
         __syncthreads();
-        const __nv_bfloat16 *qsrc = r.shared && qs ? qs : q, *ksrc = r.shared && ks ? ks : k;
-        stage_rows(tQ, qsrc, c.tok, H, r.h, kKey);
-        stage_rows(tK, ksrc, c.tok, H, r.h, kKey);
-        stage_rows(tA, g, c.tok, H, r.h, kKey);
-        stage_rows(tV, v, c.tok, H, r.h, DV);
-        stage_rows(tD, dout, c.tok, H, r.h, DV);
+        const int *tok = c.tok + mb * kRows;
+        stage_rows(tQ, r.shared && qs ? qs : q, tok, H, r.h, kKey);
+        stage_rows(tK, r.shared && ks ? ks : k, tok, H, r.h, kKey);
+        stage_rows(tA, g, tok, H, r.h, kKey);
+        stage_rows(tV, v, tok, H, r.h, DV);
+        stage_rows(tD, dout, tok, H, r.h, DV);
+    };
+    int64_t chunk = blockIdx.x;
+    ChunkRef r;
+    bool have = chunk < a.num_chunks && locate_chunk(a, chunk, H, N, use_shared, r);
+    int mb = 0;
+    if (have) stage(r, 0);
+    while (have) {
+        const int *tok = c.tok + mb * kRows, *sj = c.slotj + mb * kRows;
+        const float *ev = c.e + mb * kRows;
         cp_async_wait_all();
         __syncthreads();
         gate_half_sums(tA, c.part);
@@ -458,11 +543,11 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
             float run = half ? gm : 0.f;
             for (int x = half * 64; x < half * 64 + 64; ++x) {
                 run += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tA + toff(x, col)));
-                const float d = run - gm, e = c.e[x];
+                const float d = run - gm, e = ev[x];
                 __nv_bfloat16 *pq = reinterpret_cast<__nv_bfloat16 *>(tQ + toff(x, col));
                 __nv_bfloat16 *pk = reinterpret_cast<__nv_bfloat16 *>(tK + toff(x, col));
-                *pq = __float2bfloat16_rn(e * scale * __bfloat162float(*pq) * expf(d));
-                *pk = __float2bfloat16_rn(e * __bfloat162float(*pk) * expf(-d));
+                *pq = __float2bfloat16_rn(e * scale * __bfloat162float(*pq) * __expf(d));
+                *pk = __float2bfloat16_rn(e * __bfloat162float(*pk) * __expf(-d));
                 gs[x * kKey + col] = d;
             }
         }
@@ -525,23 +610,15 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
             failed = true;
             break;
         }
-        // S' = diag(exp(G_m)) S_start -> tile 0, dS' = diag(exp(G_l - G_m)) dS_end -> tile 4
+        // S' -> tile 0 and dS' -> tile 4: the scan wrote them in the tile layout
         {
-            const float *Ss = a.ustate + chunk * kKey * DV, *Ds = a.wgrad + chunk * kKey * DV;
-            for (int x = tid; x < kKey * DV / 8; x += kThr) {
-                const int row = x / (DV / 8), c8 = (x % (DV / 8)) * 8;
-                const float f1 = expf(c.gm[row]), f2 = expf(c.gl[row] - c.gm[row]);
-                const float4 s0 = *reinterpret_cast<const float4 *>(Ss + row * DV + c8);
-                const float4 s1 = *reinterpret_cast<const float4 *>(Ss + row * DV + c8 + 4);
-                const float4 d0 = *reinterpret_cast<const float4 *>(Ds + row * DV + c8);
-                const float4 d1 = *reinterpret_cast<const float4 *>(Ds + row * DV + c8 + 4);
-                *reinterpret_cast<uint4 *>(tQ + toff(row, c8)) =
-                    make_uint4(pack2(f1 * s0.x, f1 * s0.y), pack2(f1 * s0.z, f1 * s0.w), pack2(f1 * s1.x, f1 * s1.y),
-                               pack2(f1 * s1.z, f1 * s1.w));
-                *reinterpret_cast<uint4 *>(tA + toff(row, c8)) =
-                    make_uint4(pack2(f2 * d0.x, f2 * d0.y), pack2(f2 * d0.z, f2 * d0.w), pack2(f2 * d1.x, f2 * d1.y),
-                               pack2(f2 * d1.z, f2 * d1.w));
+            const unsigned char *sp = static_cast<const unsigned char *>(a.sp_tiles) + chunk * (int64_t)kTile;
+            const unsigned char *dsp = static_cast<const unsigned char *>(a.dsp_tiles) + chunk * (int64_t)kTile;
+            for (int x = tid; x < (int)(kTile / 16); x += kThr) {
+                cp_async16(smem_u32(tQ + 16 * x), sp + 16 * x, true);
+                cp_async16(smem_u32(tA + 16 * x), dsp + 16 * x, true);
             }
+            cp_async_wait_all();
         }
         // products 3: U += dO S'^T, DK += V dS'^T, DV += Kt dS'
         ok = run_mma(c, phase, [&] {
@@ -562,48 +639,73 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
             failed = true;
             break;
         }
-        // read-out: row erow of U, DK (columns of this warp's half) and DV
+        const int64_t next = chunk + gridDim.x;
+        ChunkRef rn;
+        const bool have_next = next < a.num_chunks && locate_chunk(a, next, H, N, use_shared, rn);
+        if (have_next) stage(rn, mb ^ 1);
+        // read-out: row erow of U, DK (columns of this warp's half) and DV; the
+        // slot rows of a warp's 32 rows are scattered, so every value goes out
+        // through the warp's store patch
         {
-            const int t = c.tok[erow], j = c.slotj[erow];
-            const float e = c.e[erow];
+            const int t = tok[erow];
+            const float e = ev[erow];
             const bool valid = t >= 0;
             const int64_t th = (int64_t)(valid ? t : 0) * H + r.h;
-            const int64_t srow = th * ncon + j;
             const __nv_bfloat16 *qrow = (r.shared && qs ? qs : q) + th * kKey;
             const __nv_bfloat16 *krow = (r.shared && ks ? ks : k) + th * kKey;
             const float *gsr = gs + erow * kKey;
+            float *patch = c.patch + warp * 32 * kPatchStride;
+            int64_t sr[4];  // slot rows this lane stores (-1 past the item's end)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int rr = 32 * quarter + (lane >> 2) + 8 * kk, tt = tok[rr];
+                sr[kk] = tt >= 0 ? ((int64_t)tt * H + r.h) * ncon + sj[rr] : -1;
+            }
             float de_r = 0.f, de_w = 0.f;
             for (int c0 = hc * 64; c0 < hc * 64 + 64; c0 += 32) {
+                // this block's q, k and G_r - G_m first: one load latency per block
+                uint4 q4[4] = {}, k4[4] = {};
+                float4 g4[8] = {};
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        q4[i] = __ldg(reinterpret_cast<const uint4 *>(qrow + c0 + 8 * i));
+                        k4[i] = __ldg(reinterpret_cast<const uint4 *>(krow + c0 + 8 * i));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) g4[i] = *reinterpret_cast<const float4 *>(gsr + c0 + 4 * i);
+                }
                 uint32_t xu[32], xk[32];
                 __syncwarp();  // the warp converged for its collective TMEM loads
                 tmem_ld32(tmem + lb + c0, xu);
                 tmem_ld32(tmem + lb + 128 + c0, xk);
                 tmem_wait_ld();
-                if (!valid) continue;
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    float qv[8], kv[8], dq[8], dk[8], xg[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(qrow + c0 + i)), qv);
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(krow + c0 + i)), kv);
+                for (int s16 = 0; s16 < 32; s16 += 16) {
+                    float dq[16], dk[16], xg[16];
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const float d = gsr[c0 + i + jj];
-                        const float u = expf(d) * __uint_as_float(xu[i + jj]);
-                        const float dK = expf(-d) * __uint_as_float(xk[i + jj]);
-                        dq[jj] = e * scale * u;
-                        dk[jj] = e * dK;
-                        xg[jj] = qv[jj] * dq[jj] - kv[jj] * dk[jj];
-                        de_r += scale * qv[jj] * u;
-                        de_w += kv[jj] * dK;
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float qv[8], kv[8];
+                        unpack8(q4[s16 / 8 + h8], qv);
+                        unpack8(k4[s16 / 8 + h8], kv);
+                        const float4 ga = g4[s16 / 4 + 2 * h8], gb = g4[s16 / 4 + 2 * h8 + 1];
+                        const float gd[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int x = 8 * h8 + jj;
+                            // fast exponentials: relative error ~1e-5 at |G_r - G_m| = 64, far below bf16's
+                            const float u = __expf(gd[jj]) * __uint_as_float(xu[s16 + x]);
+                            const float dK = __expf(-gd[jj]) * __uint_as_float(xk[s16 + x]);
+                            dq[x] = e * scale * u;
+                            dk[x] = e * dK;
+                            xg[x] = qv[jj] * dq[x] - kv[jj] * dk[x];
+                            de_r += scale * qv[jj] * u;
+                            de_w += kv[jj] * dK;
+                        }
                     }
-                    float *pq = a.dq_c + srow * kKey + c0 + i, *pk = a.dk_c + srow * kKey + c0 + i;
-                    float *pg = a.dg_c + srow * kKey + c0 + i;
-                    *reinterpret_cast<float4 *>(pq) = make_float4(dq[0], dq[1], dq[2], dq[3]);
-                    *reinterpret_cast<float4 *>(pq + 4) = make_float4(dq[4], dq[5], dq[6], dq[7]);
-                    *reinterpret_cast<float4 *>(pk) = make_float4(dk[0], dk[1], dk[2], dk[3]);
-                    *reinterpret_cast<float4 *>(pk + 4) = make_float4(dk[4], dk[5], dk[6], dk[7]);
-                    *reinterpret_cast<float4 *>(pg) = make_float4(xg[0], xg[1], xg[2], xg[3]);
-                    *reinterpret_cast<float4 *>(pg + 4) = make_float4(xg[4], xg[5], xg[6], xg[7]);
+                    warp_put16(patch, lane, dq, a.dq_c, kKey, c0 + s16, sr);
+                    warp_put16(patch, lane, dk, a.dk_c, kKey, c0 + s16, sr);
+                    warp_put16(patch, lane, xg, a.dg_c, kKey, c0 + s16, sr);
                 }
             }
             for (int c0 = hc * (DV / 2); c0 < (hc + 1) * (DV / 2); c0 += 32) {
@@ -611,27 +713,33 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
                 __syncwarp();
                 tmem_ld32(tmem + lb + 256 + c0, xv);
                 tmem_wait_ld();
-                if (!valid) continue;
-                float *pv = a.dv_c + srow * DV + c0;
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4 *>(pv + i) =
-                        make_float4(__uint_as_float(xv[i]), __uint_as_float(xv[i + 1]), __uint_as_float(xv[i + 2]),
-                                    __uint_as_float(xv[i + 3]));
+                for (int s16 = 0; s16 < 32; s16 += 16) {
+                    float v16[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v16[i] = __uint_as_float(xv[s16 + i]);
+                    warp_put16(patch, lane, v16, a.dv_c, DV, c0 + s16, sr);
+                }
             }
+            if (!valid) de_r = de_w = 0.f;
             c.de[(hc * 2) * kRows + erow] = de_r;
             c.de[(hc * 2 + 1) * kRows + erow] = de_w;
         }
         fence_before();
         __syncthreads();
         // router-weight terms of the routed rows: the two column halves, in a fixed order
-        if (!r.shared && tid < kRows && c.tok[tid] >= 0) {
-            const int64_t o = (((int64_t)c.tok[tid] * H + r.h) * topk + c.slotj[tid]) * 2;
+        if (!r.shared && tid < kRows && tok[tid] >= 0) {
+            const int64_t o = (((int64_t)tok[tid] * H + r.h) * topk + sj[tid]) * 2;
             a.de_c[o] = c.de[tid] + c.de[2 * kRows + tid];
             a.de_c[o + 1] = c.de[kRows + tid] + c.de[3 * kRows + tid];
         }
-        __syncthreads();  // TMEM, tiles and metadata are reused by the next chunk
+        __syncthreads();  // TMEM, the router-weight sums and this metadata buffer are reused
+        chunk = next;
+        r = rn;
+        have = have_next;
+        mb ^= 1;
     }
+    if (failed) cp_async_wait_all();  // no copy may still be writing shared memory when the CTA exits
     if (failed && tid == 0) atomicOr(a.flags, SSE_DEVICE_TIMEOUT);
     __syncthreads();
     if (warp == 0) {
@@ -698,11 +806,16 @@ bwd_dg_apply_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t 
         chunk_slot_rows(a, r, H, topk, ncon, srow);
         __syncthreads();
         float run = a.dgtot[chunk * kKey + threadIdx.x];
-        for (int x = kRows - 1; x >= 0; --x) {
-            if (srow[x] < 0) continue;
-            float *p = a.dg_c + srow[x] * kKey + threadIdx.x;
-            run += *p;
-            *p = run;
+        for (int x0 = kRows - 1; x0 >= 0; x0 -= 8) {  // eight rows' loads ahead of the running sum
+            float t[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t[i] = srow[x0 - i] >= 0 ? a.dg_c[srow[x0 - i] * kKey + threadIdx.x] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (srow[x0 - i] < 0) continue;
+                run += t[i];
+                a.dg_c[srow[x0 - i] * kKey + threadIdx.x] = run;
+            }
         }
         __syncthreads();
     }

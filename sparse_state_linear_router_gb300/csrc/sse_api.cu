@@ -334,7 +334,8 @@ struct BackwardLayout {
     // chunked form
     bool chunked;
     int64_t num_chunks;
-    float *ustate, *wgrad, *gamma, *gscratch, *fterm, *dgtot;
+    float *ustate, *wgrad, *gamma, *gml, *gscratch, *fterm, *dgtot;
+    void *sp_tiles, *dsp_tiles;
     int32_t *marks, *redo_list, *flags;
     size_t bytes;
 };
@@ -358,6 +359,9 @@ BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_
         L.ustate = cv.take<float>(nch * kc * dv);
         L.wgrad = cv.take<float>(nch * kc * dv);
         L.gamma = cv.take<float>(nch * kc);
+        L.gml = cv.take<float>(nch * 2 * kc);
+        L.sp_tiles = cv.take<unsigned char>(nch * sse::kChunkRows * 256);  // one 128 x 128 bf16 tile per chunk
+        L.dsp_tiles = cv.take<unsigned char>(nch * sse::kChunkRows * 256);
         L.dgtot = cv.take<float>(nch * kc);
         L.gscratch = cv.take<float>((size_t)sse::kBwdScratchCtas * sse::kChunkRows * kc);
         L.fterm = cv.take<float>(nitems * kc);
@@ -438,7 +442,8 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
     if (L.chunked) {
         a.pad_off = L.rb.pad_off;
         a.num_chunks = L.num_chunks;
-        a.ustate = L.ustate; a.wgrad = L.wgrad; a.gamma = L.gamma; a.gscratch = L.gscratch;
+        a.ustate = L.ustate; a.wgrad = L.wgrad; a.gamma = L.gamma; a.gml = L.gml; a.gscratch = L.gscratch;
+        a.sp_tiles = L.sp_tiles; a.dsp_tiles = L.dsp_tiles;
         a.fterm = L.fterm; a.dgtot = L.dgtot; a.marks = L.marks; a.redo_list = L.redo_list; a.flags = L.flags;
         e = sse::launch_backward_chunked(c, a, s, &launches);
         return e == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;

@@ -305,9 +305,12 @@ struct BackwardArgs {
     // Chunked (tensor-core) form, c = 128: buffers of backward_chunked.cu.
     const int32_t *pad_off;  // chunk-padded first row of each work item; chunk = row / 128
     int64_t num_chunks;      // upper bound of the chunks (launch size; items past the last exit)
-    float *ustate;           // [chunks, c, d]: K_hat^T V of the chunk, then the state at its start
-    float *wgrad;            // [chunks, c, d]: Q_hat^T dO of the chunk, then dL/dS at its end
+    float *ustate;           // [chunks, c, d]: K_hat^T V of the chunk
+    float *wgrad;            // [chunks, c, d]: Q_hat^T dO of the chunk
     float *gamma;            // [chunks, c]: exp(G_last), the chunk's decay of each state row
+    float *gml;              // [chunks, 2, c]: G_m and G_l of each state row
+    void *sp_tiles;          // [chunks, 32 KB]: S' = diag(exp(G_m)) S_start, bf16 in the operand tile layout
+    void *dsp_tiles;         // [chunks, 32 KB]: dS' = diag(exp(G_l - G_m)) dS_end, likewise
     float *gscratch;         // [kBwdScratchCtas, 128, c]: G_r - G_m of the chunk in flight, per CTA
     float *fterm;            // [items, c]: rowsum(S_T * dL/dS_T) of each work item
     float *dgtot;            // [chunks, c]: gate-gradient sums of each chunk, then of all later rows
