@@ -237,9 +237,23 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
  *   d_initial_state float32 [num_seqs, H, P, c, d], may be NULL (not written)
  * The routing is recomputed from router_logits.  Every (token, head) gets
  * one float32 contribution per selected partition and one from the shared
- * partition, summed in a fixed order (deterministic).  Computed token by token
- * in float32 on the CUDA cores (any shape the recurrent forward takes).
- * Workspace: sse_backward_workspace_size bytes (256-byte aligned).
+ * partition, summed in a fixed order (deterministic).
+ *
+ * Two computations, chosen by cfg->algo:
+ *  - chunked (SSE_ALGO_AUTO, SSE_ALGO_CHUNKED, SSE_ALGO_MASKED; bf16, c = 128,
+ *    d in {64, 128}): chunks of 128 grouped rows on the tensor cores -- each
+ *    chunk's state contributions, a scan over the chunks in float32, then the
+ *    chunk's gradient products (bf16 operands, float32 accumulation) with the
+ *    decay referenced to the chunk's midpoint row.  A work item with a chunk
+ *    whose summed log-gate leaves that form's range (|G_m| or |G_l - G_m| above
+ *    64) is recomputed token by token, as below.  SSE_ALGO_CHUNKED on another
+ *    shape returns SSE_ERR_UNSUPPORTED.
+ *  - recurrent (SSE_ALGO_RECURRENT, and AUTO / MASKED on other shapes): token
+ *    by token in float32 on the CUDA cores, any shape the recurrent forward
+ *    takes.
+ * Workspace: sse_backward_workspace_size bytes (256-byte aligned); the chunked
+ * form adds about 192 KB per chunk of 128 grouped rows (states, their
+ * gradients and the bf16 operand tiles) plus 16 MB of per-CTA scratch.
  * ------------------------------------------------------------------------- */
 size_t sse_backward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
 
