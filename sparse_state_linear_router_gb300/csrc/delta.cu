@@ -204,8 +204,11 @@ delta_segment_kernel(DeltaArgs a, int32_t H, int32_t c, int32_t N, int32_t topk,
 }
 
 // Decode: one CTA per (sequence, head).
+// Two CTAs per SM (at most 128 registers a thread): each holds one state in
+// registers between its load and its store, so the second CTA keeps HBM busy
+// through the first one's reductions.
 template <typename T, int D4>
-__global__ void __launch_bounds__(kDThreads)
+__global__ void __launch_bounds__(kDThreads, 2)
 delta_decode_kernel(DeltaDecodeArgs a, int32_t H, int32_t c, int32_t N, int32_t topk, int32_t use_shared,
                     float scale) {
     constexpr int R = kDThreads / D4;
