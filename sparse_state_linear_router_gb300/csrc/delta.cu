@@ -103,8 +103,10 @@ __device__ __forceinline__ float4 key_answer(const float4 (&st)[kDMaxRows], cons
     return acc;
 }
 
+// Two CTAs per SM (at most 128 registers a thread): the token-serial segments
+// are many (one CTA each), so more of them run at once.
 template <typename T, int D4>
-__global__ void __launch_bounds__(kDThreads)
+__global__ void __launch_bounds__(kDThreads, 2)
 delta_segment_kernel(DeltaArgs a, int32_t H, int32_t c, int32_t N, int32_t topk, int32_t use_shared, float scale) {
     constexpr int R = kDThreads / D4;
     constexpr int d = 4 * D4;
