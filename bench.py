@@ -876,6 +876,60 @@ def run_front_end(args):
     return 0
 
 
+def run_backward(args, N=4, L=8192):
+    """One JSON line for sse_backward alone at the operator shape of the
+    pages' Fig. 6 (8 heads, head dim 128, top-1 of N = 4, shared,
+    cu_seqlens = [0, L/2, L], bf16; d_out ~ N(0, 1), no final-state gradient):
+    tokens/s of the backward and its time per call."""
+    import dataclasses
+
+    import torch
+    from sparse_state_linear_router_gb300 import binding
+    ws, rank, local = _dist()
+    if ws > 1:
+        raise SystemExit("--part backward runs on one GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = dataclasses.replace(synth.WORKLOADS["layer_bf16"], name=f"fig6_N{N}", num_heads=8, num_partitions=N,
+                            top_k=1, lengths=(L // 2, L // 2), sigma_router=1.0)
+    x = synth.make_forward_inputs_device(w, seed=0, device=dev)
+    T, S = x["total_tokens"], x["num_seqs"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    d_out = torch.randn((T, w.num_heads, w.value_dim), generator=gen, device=dev).to(torch.bfloat16)
+    cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, N, 1, 1, 1.0, "bf16", args.algo)
+    bws = torch.empty(binding.sse_backward_workspace_size(cfg, T, S), dtype=torch.uint8, device=dev)
+
+    def call():
+        binding.backward(cfg, x["q"], x["k"], x["v"], x["g"], x["logits"], x["cu_seqlens"], d_out,
+                         want_d_initial_state=False, workspace=bws)
+    for _ in range(args.warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.15)
+        ev[0].record(stream)
+        for _ in range(args.steps):
+            call()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.15)
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    line = {
+        "metric": "SSE backward tokens/s at Fig. 6's operator shape on 1 GB300",
+        "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"backward, H8, c=d=128, top-1 of N={N}, shared, cu_seqlens=[0, {L // 2}, {L}], "
+                               "bf16 in, fp32 state and slots", "algo": args.algo},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -890,8 +944,9 @@ def main(argv=None):
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the forward-only timings of the other workloads (varlen, small, skewed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--part", choices=["both", "forward", "decode", "front_end"], default="both",
-                    help="time the whole step (default), one of its two calls, or the front end alone")
+    ap.add_argument("--part", choices=["both", "forward", "decode", "front_end", "backward"], default="both",
+                    help="time the whole step (default), one of its two calls, the front end alone, or the "
+                         "backward at Fig. 6's shape")
     ap.add_argument("--fwd-workload", choices=["layer_bf16", "varlen_bf16", "small_bf16"],
                     default=FWD_WORKLOAD, help="forward batch of the step")
     args = ap.parse_args(argv)
@@ -901,6 +956,8 @@ def main(argv=None):
         return run_reference(args)
     if args.part == "front_end":
         return run_front_end(args)
+    if args.part == "backward":
+        return run_backward(args)
     return run_native(args)
 
 
