@@ -95,6 +95,9 @@ CASES = {
     "k_equals_N": ("small_bf16", [150, 60], {"num_heads": 1, "num_partitions": 3, "top_k": 3}, {}),
     "c128_d128_no_dfin": ("layer_bf16", [257, 64], {"num_heads": 1, "num_partitions": 4}, {"with_dfin": False}),
     "c128_d64": ("layer_bf16", [130, 3], {"num_heads": 2, "value_dim": 64}, {}),
+    "c128_noshared_k3": ("layer_bf16", [260, 1, 0], {"num_heads": 2, "num_partitions": 6, "top_k": 3,
+                                                     "use_shared": 0}, {}),
+    "c128_k_equals_N": ("layer_bf16", [200, 57], {"num_heads": 1, "num_partitions": 3, "top_k": 3}, {"scale": 0.5}),
 }
 
 
