@@ -307,8 +307,9 @@ __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item
             s.base = a.cu_seqlens[s.b];
             s.len = a.cu_seqlens[s.b + 1] - s.base;
         } else {
-            s.base = a.seg_off[r];
-            s.len = a.seg_off[r + 1] - s.base;
+            // routing outputs of the kernels ahead in the chain: coherent (L2) loads
+            s.base = __ldcg(a.seg_off + r);
+            s.len = __ldcg(a.seg_off + r + 1) - s.base;
         }
     }
     return s;
@@ -349,10 +350,10 @@ __device__ __forceinline__ RowMeta row_meta(const ForwardArgs &a, const Segment 
             m.e = -1.f;
             const int64_t o = ((int64_t)m.t * H + seg.h) * topk;
             for (int j = 0; j < topk; ++j)
-                if (a.topk_idx[o + j] == seg.slot) m.e = a.topk_w[o + j];
+                if (__ldcg(a.topk_idx + o + j) == seg.slot) m.e = __ldcg(a.topk_w + o + j);
         } else {
-            m.t = a.perm_rec[seg.base + idx] / topk;
-            m.e = a.perm_e[seg.base + idx];
+            m.t = __ldcg(a.perm_rec + seg.base + idx) / topk;
+            m.e = __ldcg(a.perm_e + seg.base + idx);
         }
     }
     return m;
@@ -466,7 +467,7 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
                 int pad_base = 0;
                 if (!stop) {
                     seg = decode_segment<MASKED>(a, item, H, N, use_shared);
-                    pad_base = a.pad_off[item];
+                    pad_base = __ldcg(a.pad_off + item);
                 }
                 const int slot = sidx % kSegSlots;
                 bool ok = sidx < kSegSlots ||
@@ -1051,10 +1052,10 @@ segment_redo_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t u
     const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.g);
     __nv_bfloat16 *part = static_cast<__nv_bfloat16 *>(a.part_routed);
     for (int li = blockIdx.x; li < count; li += gridDim.x) {
-        const int item = a.redo_list[li];
+        const int item = __ldcg(a.redo_list + li);
         const Segment seg = decode_segment<MASKED>(a, item, H, N, use_shared);
         const int64_t state_off = (((int64_t)seg.b * H + seg.h) * P + seg.slot) * (int64_t)KC * DV;
-        const int64_t row0 = a.pad_off[item];
+        const int64_t row0 = __ldcg(a.pad_off + item);
         const __nv_bfloat16 *qsrc = seg.shared && a.qs ? static_cast<const __nv_bfloat16 *>(a.qs) : q;
         const __nv_bfloat16 *ksrc = seg.shared && a.ks ? static_cast<const __nv_bfloat16 *>(a.ks) : kk;
         float4 st[RPT];
@@ -1129,7 +1130,7 @@ segment_redo_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t u
 // rate; taking two or four pieces per thread was no faster, or slower).
 template <int NC>
 __global__ void __launch_bounds__(256)
-gather_combine_kernel(const __nv_bfloat16 *__restrict__ part, const int32_t *__restrict__ rec_pos, int64_t rows,
+gather_combine_kernel(const __nv_bfloat16 *part, const int32_t *rec_pos, int64_t rows,
                       int32_t d, __nv_bfloat16 *__restrict__ out) {
     griddep_launch_dependents();
     griddep_wait();
@@ -1141,11 +1142,11 @@ gather_combine_kernel(const __nv_bfloat16 *__restrict__ part, const int32_t *__r
         const int ch = (int)(x - row * cpr);
         int32_t pr[NC];
 #pragma unroll
-        for (int j = 0; j < NC; ++j) pr[j] = __ldg(rec_pos + row * NC + j);
+        for (int j = 0; j < NC; ++j) pr[j] = __ldcg(rec_pos + row * NC + j);
         uint4 pv[NC];
 #pragma unroll
         for (int j = 0; j < NC; ++j)
-            pv[j] = __ldcs(reinterpret_cast<const uint4 *>(part + (int64_t)pr[j] * d + ch * 8));
+            pv[j] = __ldcg(reinterpret_cast<const uint4 *>(part + (int64_t)pr[j] * d + ch * 8));
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
         for (int j = 0; j < NC; ++j) {

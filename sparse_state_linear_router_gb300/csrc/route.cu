@@ -93,7 +93,7 @@ __global__ void plan_blocks_kernel(const int32_t *__restrict__ cu, int32_t nseq,
 
 template <typename T, int NP>
 __global__ void __launch_bounds__(kRouteBlock)
-route_count_kernel(const T *__restrict__ logits, const int4 *__restrict__ blk_info, int32_t H, int32_t N,
+route_count_kernel(const T *__restrict__ logits, const int4 *blk_info, int32_t H, int32_t N,
                    int32_t k, int32_t vec, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                    int32_t *__restrict__ cnt, int32_t max_blocks) {
     __shared__ int hist[kMaxPartitions];
@@ -125,7 +125,7 @@ route_count_kernel(const T *__restrict__ logits, const int4 *__restrict__ blk_in
 }
 
 __global__ void __launch_bounds__(1024)
-scan_blocks_kernel(int32_t *__restrict__ cnt, int32_t max_blocks) {
+scan_blocks_kernel(int32_t *cnt, int32_t max_blocks) {
     griddep_launch_dependents();
     griddep_wait();
     int32_t *row = cnt + (int64_t)blockIdx.x * (max_blocks + 1);
@@ -155,8 +155,8 @@ __device__ __forceinline__ int routed_len(const int32_t *cnt, int32_t max_blocks
 // exclusive scan over the work items (shared segments, then routed ones) of
 // their lengths rounded up to whole chunks.
 __global__ void __launch_bounds__(1024)
-seg_off_kernel(const int32_t *__restrict__ cnt, int32_t max_blocks,
-               const int32_t *__restrict__ blk_prefix, const int32_t *__restrict__ cu, int32_t nseq,
+seg_off_kernel(const int32_t *cnt, int32_t max_blocks,
+               const int32_t *blk_prefix, const int32_t *__restrict__ cu, int32_t nseq,
                int32_t H, int32_t N, int32_t use_shared, int32_t *__restrict__ seg_off,
                int32_t *__restrict__ pad_off) {
     griddep_launch_dependents();
@@ -195,12 +195,12 @@ seg_off_kernel(const int32_t *__restrict__ cnt, int32_t max_blocks,
 }
 
 __global__ void __launch_bounds__(kRouteBlock)
-scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ cu, int32_t nseq,
-               const int32_t *__restrict__ blk_prefix, const int4 *__restrict__ blk_info,
-               const int32_t *__restrict__ cnt, int32_t max_blocks, const int32_t *__restrict__ seg_off, int32_t H,
-               int32_t N, int32_t k, int32_t use_shared, const float *__restrict__ topk_w, int32_t *__restrict__ perm,
+scatter_kernel(const int32_t *topk_idx, const int32_t *__restrict__ cu, int32_t nseq,
+               const int32_t *blk_prefix, const int4 *blk_info,
+               const int32_t *cnt, int32_t max_blocks, const int32_t *seg_off, int32_t H,
+               int32_t N, int32_t k, int32_t use_shared, const float *topk_w, int32_t *__restrict__ perm,
                int32_t *__restrict__ perm_rec, float *__restrict__ perm_e,
-               const int32_t *__restrict__ pad_off, int32_t *__restrict__ rec_pos) {
+               const int32_t *pad_off, int32_t *__restrict__ rec_pos) {
     constexpr int kWarps = kRouteBlock / 32;
     __shared__ uint32_t wmask[kWarps][kMaxPartitions];
     // per partition i: where this block's records of segment (b, h, i) start
@@ -318,9 +318,9 @@ masked_pad_kernel(const int32_t *__restrict__ cu, int32_t nseq, int32_t H, int32
 // Partial row of each contribution of (t, h): selected partition j of the
 // token, then the shared one.
 __global__ void __launch_bounds__(256)
-masked_recpos_kernel(const int32_t *__restrict__ cu, int32_t nseq, const int32_t *__restrict__ topk_idx,
+masked_recpos_kernel(const int32_t *__restrict__ cu, int32_t nseq, const int32_t *topk_idx,
                      int64_t total_tokens, int32_t H, int32_t N, int32_t k, int32_t use_shared,
-                     const int32_t *__restrict__ pad_off, int32_t *__restrict__ rec_pos) {
+                     const int32_t *pad_off, int32_t *__restrict__ rec_pos) {
     griddep_launch_dependents();
     griddep_wait();
     const int64_t rows = total_tokens * H;

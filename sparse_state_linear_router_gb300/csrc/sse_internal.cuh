@@ -26,7 +26,11 @@ constexpr int kChunkRows = 128;   // rows of a tensor-core chunk; output regions
 // early return, so that no grid of the chain completes before the one ahead
 // of it -- and calls griddep_launch_dependents() at its start, which lets the
 // next kernel be scheduled once all of this grid's CTAs are running.  Both are
-// no-ops for a kernel launched the ordinary way.
+// no-ops for a kernel launched the ordinary way.  What an earlier kernel of
+// the chain wrote is read with coherent loads only: no const __restrict__
+// pointer and no __ldg on it (the read-only cache path assumes data that does
+// not change during the reading kernel's lifetime, and a dependent kernel's
+// lifetime begins before its predecessor has finished writing).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {

@@ -161,3 +161,43 @@ def test_forward_state_carry_split(algo):
         assert H_.max_abs_rel(H_.to_numpy(both), H_.to_numpy(a["out"])) < H_.TOL_BF16
         # the two runs cut the sequence into different chunks (bf16 operands)
         assert H_.max_abs_rel(H_.to_numpy(p2["final_state"]), H_.to_numpy(a["final_state"])) < H_.TOL_BF16
+
+
+@pytest.mark.parametrize("algo,dv", [("chunked", 128), ("chunked", 64), ("recurrent", 128)])
+def test_backward_writes_only_its_outputs_and_ignores_workspace(algo, dv):
+    """sse_backward through the C ABI: every gradient inside canary guards,
+    the workspace filled with 0xFF bytes (the chunked form's d = 64 operand
+    tiles leave half of each tile unwritten: it must never be read), and the
+    results bit-identical to a call on a zero-filled workspace."""
+    from sparse_state_linear_router_gb300 import binding
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=4, value_dim=dv)
+    inp = synth.make_forward_inputs(w, seed=9, lengths=[300, 1, 0, 260], with_init=True)
+    T, S, H = inp.total_tokens, inp.num_seqs, w.num_heads
+    c, N, P = w.key_dim, w.num_partitions, w.num_slots
+    rng = np.random.default_rng(4)
+    cfg = H_.config_of(w, algo)
+    t = {n: binding.to_device(getattr(inp, n)) for n in ("q", "k", "v", "g", "logits")}
+    cu = torch.from_numpy(inp.cu_seqlens.astype(np.int32)).cuda()
+    init = torch.from_numpy(inp.init_state).cuda()
+    d_out = binding.to_device(synth.f32_to_bf16_bits(rng.normal(size=(T, H, dv)).astype(np.float32)))
+    d_fin = torch.from_numpy((rng.normal(size=(S, H, P, c, dv)) * 0.5).astype(np.float32)).cuda()
+    nbytes = binding.sse_backward_workspace_size(cfg, T, S)
+    ref = binding.backward(cfg, t["q"], t["k"], t["v"], t["g"], t["logits"], cu, d_out, initial_state=init,
+                           d_final_state=d_fin, workspace=torch.zeros(nbytes, dtype=torch.uint8, device="cuda"))
+    shapes = {"dq": ((T, H, c), torch.bfloat16), "dk": ((T, H, c), torch.bfloat16),
+              "dv": ((T, H, dv), torch.bfloat16), "dg": ((T, H, c), torch.bfloat16),
+              "dlogits": ((T, H, N), torch.bfloat16), "d_initial_state": ((S, H, P, c, dv), torch.float32)}
+    g = {n: _guarded(*shapes[n]) for n in shapes}
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    p = binding._ptr
+    st = binding.sse_backward(cfg, p(t["q"]), p(t["k"]), p(t["v"]), p(t["g"]), p(t["logits"]), None, None, p(cu), S,
+                              T, p(init), p(d_out), p(d_fin), p(g["dq"][0]), p(g["dk"][0]), p(g["dv"][0]),
+                              p(g["dg"][0]), p(g["dlogits"][0]), None, None, p(g["d_initial_state"][0]), p(ws),
+                              nbytes, binding._stream())
+    torch.cuda.synchronize()
+    assert st == binding.SSE_OK
+    bad = [n for n, (view, raw) in g.items() if not torch.equal(view, ref[n])]
+    nonfinite = {n: int((~torch.isfinite(view.float())).sum()) for n, (view, raw) in g.items()}
+    for n, (view, raw) in g.items():
+        assert _canaries_intact(raw, view.numel() * view.element_size()), n
+    assert not bad, (bad, nonfinite)
