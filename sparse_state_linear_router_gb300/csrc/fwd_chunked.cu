@@ -307,7 +307,7 @@ __device__ __forceinline__ Segment decode_segment(const ForwardArgs &a, int item
             s.base = a.cu_seqlens[s.b];
             s.len = a.cu_seqlens[s.b + 1] - s.base;
         } else {
-            // routing outputs of the kernels ahead in the chain: coherent (L2) loads
+            // routing outputs: L2 loads (see the routing kernels' dependent launches)
             s.base = __ldcg(a.seg_off + r);
             s.len = __ldcg(a.seg_off + r + 1) - s.base;
         }
@@ -383,7 +383,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     const int tid = threadIdx.x, warp = tid >> 5;
     const __nv_bfloat16 *gg = static_cast<const __nv_bfloat16 *>(a.g);
     const int P = N + use_shared;
-    griddep_launch_dependents();
 
     auto meta_tok = [&](int stage) { return reinterpret_cast<int *>(sm + Smem::META + stage * Smem::META_STAGE); };
     auto meta_e = [&](int stage) {
@@ -433,8 +432,6 @@ chunked_forward_kernel(ForwardArgs a, const __grid_constant__ CUtensorMap part_m
     __syncthreads();
     fence_after();
     const uint32_t tmem = *s_slot;
-    // everything above is on-chip; the routing's outputs are read from here on
-    griddep_wait();
 
     // The roles walk the same sequence of work items, each at its own pace: the
     // loader claims the items and posts them through the segment ring; every
@@ -1041,8 +1038,6 @@ segment_redo_kernel(ForwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t u
     __shared__ float s_red[R][DV];
     __shared__ int s_tok[kBatch];
     __shared__ float s_e[kBatch];
-    griddep_launch_dependents();
-    griddep_wait();
     const int tid = threadIdx.x, cq = tid % D4, rg = tid / D4, col = 4 * cq;
     const int count = *(volatile const int32_t *)(a.flags + 1);
     const int P = N + use_shared;
@@ -1132,8 +1127,6 @@ template <int NC>
 __global__ void __launch_bounds__(256)
 gather_combine_kernel(const __nv_bfloat16 *part, const int32_t *rec_pos, int64_t rows,
                       int32_t d, __nv_bfloat16 *__restrict__ out) {
-    griddep_launch_dependents();
-    griddep_wait();
     const int cpr = d / 8;
     const int64_t total = rows * cpr;
     for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
@@ -1197,7 +1190,6 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
     // the work counter (a.flags[2]) and the redo list's length (a.flags[1])
     // start at zero with the flags words, cleared by the caller before routing
     int32_t *counter = a.flags + 2;
-    cudaError_t e;
 
     // The partial buffer as a 2-D tensor [part_rows, DV] of bf16, stored in
     // boxes of 64 columns x one chunk of rows with the 128-byte swizzle.
@@ -1230,13 +1222,12 @@ cudaError_t launch_t(const sse_config_t &cfg, const ForwardArgs &a, cudaStream_t
         return cudaErrorInvalidValue;
 
     const int grid = (int)std::min<int64_t>(nseg, sms > 0 ? sms : 148);
-    e = launch_dependent(chunked_forward_kernel<KC, DV, MASKED>, dim3(grid), dim3(kThreads), kSmemBytes, stream, a,
-                         map, maps, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale,
-                         (int32_t)nseg, counter);
-    if (e != cudaSuccess) return e;
+    chunked_forward_kernel<KC, DV, MASKED><<<grid, kThreads, kSmemBytes, stream>>>(
+        a, map, maps, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale, (int32_t)nseg, counter);
     const int redo_grid = (int)std::min<int64_t>(nseg, 2 * (sms > 0 ? sms : 148));
-    return launch_dependent(segment_redo_kernel<KC, DV, MASKED>, dim3(redo_grid), dim3(256), 0, stream, a,
-                            cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
+    segment_redo_kernel<KC, DV, MASKED><<<redo_grid, 256, 0, stream>>>(a, cfg.num_heads, cfg.num_partitions,
+                                                                       cfg.top_k, cfg.use_shared, cfg.scale);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -1290,13 +1281,13 @@ cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a,
     const int32_t *rp = a.rec_pos;
     switch (ncon) {
 #define SSE_COMBINE(NC) \
-    case NC: return launch_dependent(gather_combine_kernel<NC>, dim3(blocks), dim3(256), 0, stream, part, rp, rows, \
-                                     cfg.value_dim, out)
+    case NC: gather_combine_kernel<NC><<<blocks, 256, 0, stream>>>(part, rp, rows, cfg.value_dim, out); break
         SSE_COMBINE(1); SSE_COMBINE(2); SSE_COMBINE(3); SSE_COMBINE(4); SSE_COMBINE(5);
         SSE_COMBINE(6); SSE_COMBINE(7); SSE_COMBINE(8); SSE_COMBINE(9);
 #undef SSE_COMBINE
         default: return cudaErrorInvalidValue;
     }
+    return cudaGetLastError();
 }
 
 }  // namespace sse

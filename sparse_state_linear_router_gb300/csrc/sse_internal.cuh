@@ -19,9 +19,11 @@ constexpr int kRouteLaunches = 5; // kernels launch_route issues when grouping
 constexpr int kChunkRows = 128;   // rows of a tensor-core chunk; output regions are padded to it
 
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch.  The forward's kernels are launched so that
-// each may start while the previous one in the stream is finishing (its CTAs
-// are scheduled and run their prologue early).  Every kernel of such a chain
+// Programmatic dependent launch.  The routing kernels after the first are
+// launched so that each may start while the previous one in the stream is
+// finishing (its CTAs are scheduled and run their prologue early).  (The
+// forward's later kernels launch the ordinary way: as dependents they made
+// the whole step 13 us slower.)  Every kernel of such a chain
 // calls griddep_wait() before it touches global memory -- and before any
 // early return, so that no grid of the chain completes before the one ahead
 // of it -- and calls griddep_launch_dependents() at its start, which lets the
