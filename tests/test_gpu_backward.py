@@ -170,3 +170,32 @@ def test_backward_layer_shape_sampled_pairs():
             assert err < H_.TOL_BF16, (b, h, n, err)
         err = H_.max_abs_rel(gpu["d_initial_state"][b:b + 1, h:h + 1], ref["d_initial_state"])
         assert err < H_.TOL_BF16, (b, h, "d_initial_state", err)
+
+
+def test_backward_fig6_shape_sampled_pairs():
+    """Fig. 6's operator shape ("Scaling Linear Attention with Sparse State
+    Expansion", section 2.6: 8 heads, head dim 128, top-1 of N = 4, shared,
+    cu_seqlens = [0, L/2, L]) at L = 2048: 256 chunks, more than the chunked
+    kernels' persistent CTAs, so each of them walks several chunks.  The
+    oracle recomputes three (sequence, head) pairs on their own rows."""
+    w = H_.workload_variant("layer_bf16", num_heads=8, num_partitions=4, top_k=1)
+    inp = synth.make_forward_inputs(w, seed=6, lengths=[1024, 1024], with_init=True)
+    S, H = inp.num_seqs, w.num_heads
+    pairs = [0, 11, S * H - 1]
+    gpu, _, refs = _run(w, inp, pairs_only=pairs, algo="chunked")
+    for b, h, t0, t1, ref in refs:
+        for n in ("dq", "dk", "dv", "dg", "dlogits"):
+            err = H_.max_abs_rel(gpu[n][t0:t1, h:h + 1], ref[n])
+            assert err < H_.TOL_BF16, (b, h, n, err)
+        err = H_.max_abs_rel(gpu["d_initial_state"][b:b + 1, h:h + 1], ref["d_initial_state"])
+        assert err < H_.TOL_BF16, (b, h, "d_initial_state", err)
+
+
+def test_backward_chunked_without_initial_state():
+    """No initial state and no final-state gradient (the usual training call):
+    the scan starts from zero states, the gate gradient's final term is zero,
+    and d_initial_state is the gradient of a zero initial state."""
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=4, top_k=2)
+    inp = synth.make_forward_inputs(w, seed=8, lengths=[333, 0, 140], with_init=False)
+    gpu, ref, _ = _run(w, inp, algo="chunked", with_dfin=False)
+    _compare(gpu, ref, H_.TOL_BF16)
