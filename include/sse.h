@@ -236,8 +236,9 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
  *                  query gradient is added into dq (likewise dk)
  *   d_initial_state float32 [num_seqs, H, P, c, d], may be NULL (not written)
  * The routing is recomputed from router_logits.  Every (token, head) gets
- * one float32 contribution per selected partition and one from the shared
- * partition, summed in a fixed order (deterministic).
+ * one contribution per selected partition and one from the shared
+ * partition (dq, dk, dv in cfg->dtype, d_log_gate in float32), summed in
+ * float32 in a fixed order (deterministic).
  *
  * Two computations, chosen by cfg->algo:
  *  - chunked (SSE_ALGO_AUTO, SSE_ALGO_CHUNKED, SSE_ALGO_MASKED; bf16, c = 128,

@@ -203,7 +203,7 @@ backward_segment_kernel(BackwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
         if (tid < c) {
             float u = 0.f;
             for (int x = 0; x < D4; ++x) u += s_rows[tid * D4P + x];
-            a.dq_c[slot_row * c + tid] = e * scale * u;
+            Elem<T>::store(static_cast<T *>(a.dq_c) + slot_row * c + tid, e * scale * u);
             a.dg_c[slot_row * c + tid] = e * s_q[tid] * u;  // Q * u, finished by the reverse sweep
             qu = s_q[tid] * u;
         }
@@ -282,7 +282,7 @@ backward_segment_kernel(BackwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
         if (tid < c) {
             float dkr = 0.f;
             for (int x = 0; x < D4; ++x) dkr += s_rows[tid * D4P + x];
-            a.dk_c[slot_row * c + tid] = e * dkr;
+            Elem<T>::store(static_cast<T *>(a.dk_c) + slot_row * c + tid, e * dkr);
             kdk = s_k[tid] * dkr;
             // dL/dG_t = Q_t * u_t - K_t * dK_t, summed from the last row down
             run += qu_row - e * kdk;
@@ -291,7 +291,7 @@ backward_segment_kernel(BackwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
         for (int cc = tid; cc < d; cc += kBwdThreads) {
             float s = 0.f;
             for (int r2 = 0; r2 < R; ++r2) s += s_cols[r2 * d + cc];
-            a.dv_c[slot_row * d + cc] = s;
+            Elem<T>::store(static_cast<T *>(a.dv_c) + slot_row * d + cc, s);
         }
         // its barrier also orders this row's reads of s_rows / s_cols before the next row's writes
         const float de_write = block_sum(kdk);
@@ -343,10 +343,12 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
     }
     const int per_row = 4 * c4 + d4;  // dq, dk, dg, dq_shared / dk_shared, dv
     const int64_t total = rows * per_row;
+    const T *sq = static_cast<const T *>(a.dq_c), *sk = static_cast<const T *>(a.dk_c);
+    const T *sv = static_cast<const T *>(a.dv_c);
     for (int64_t x = gid; x < total; x += stride) {
         const int64_t row = x / per_row;
         const int part = (int)(x - row * per_row);
-        const float *src;
+        const T *src = nullptr;  // dq, dk, dv slots (I/O type); dg slots are float32
         T *dst;
         int width, cidx, hi;  // slots 0 .. hi - 1 summed
         const int kind = part < 4 * c4 ? part / c4 : 4;
@@ -355,33 +357,34 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
             width = c;
             // 0: dq (routed slots, plus the shared slot unless q_shared is separate),
             // 1: dk (likewise), 2: dg (all slots), 3: dq_shared / dk_shared
-            if (kind == 0) { src = a.dq_c; dst = static_cast<T *>(a.dq); hi = sep_q ? topk : ncon; }
-            else if (kind == 1) { src = a.dk_c; dst = static_cast<T *>(a.dk); hi = sep_k ? topk : ncon; }
-            else if (kind == 2) { src = a.dg_c; dst = static_cast<T *>(a.dg); hi = ncon; }
+            if (kind == 0) { src = sq; dst = static_cast<T *>(a.dq); hi = sep_q ? topk : ncon; }
+            else if (kind == 1) { src = sk; dst = static_cast<T *>(a.dk); hi = sep_k ? topk : ncon; }
+            else if (kind == 2) { dst = static_cast<T *>(a.dg); hi = ncon; }
             else {
                 // the shared slot alone, into dq_shared and dk_shared when they are separate
-                if (sep_q) {
-                    const float4 p = *reinterpret_cast<const float4 *>(a.dq_c + (row * ncon + topk) * c + cidx);
-                    Elem<T>::store4(static_cast<T *>(a.dq_shared) + row * c + cidx, p);
-                }
-                if (sep_k) {
-                    const float4 p = *reinterpret_cast<const float4 *>(a.dk_c + (row * ncon + topk) * c + cidx);
-                    Elem<T>::store4(static_cast<T *>(a.dk_shared) + row * c + cidx, p);
-                }
+                if (sep_q)
+                    Elem<T>::store4(static_cast<T *>(a.dq_shared) + row * c + cidx,
+                                    Elem<T>::load4(sq + (row * ncon + topk) * c + cidx));
+                if (sep_k)
+                    Elem<T>::store4(static_cast<T *>(a.dk_shared) + row * c + cidx,
+                                    Elem<T>::load4(sk + (row * ncon + topk) * c + cidx));
                 continue;
             }
         } else {
             cidx = 4 * (part - 4 * c4);
             width = d;
-            src = a.dv_c;
+            src = sv;
             dst = static_cast<T *>(a.dv);
             hi = ncon;
         }
         float4 p[NC];
 #pragma unroll
-        for (int j = 0; j < NC; ++j)
-            p[j] = j < hi ? *reinterpret_cast<const float4 *>(src + (row * ncon + j) * width + cidx)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < NC; ++j) {
+            const int64_t o = (row * ncon + j) * width + cidx;
+            p[j] = j >= hi ? make_float4(0.f, 0.f, 0.f, 0.f)
+                   : src  ? Elem<T>::load4(src + o)
+                          : *reinterpret_cast<const float4 *>(a.dg_c + o);
+        }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < NC; ++j) {

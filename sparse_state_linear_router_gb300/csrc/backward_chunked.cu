@@ -33,10 +33,12 @@
 // queued for the per-token kernel, which recomputes all of its slots.
 //
 // Kernels (one stream, in order): chunk sums (tensor cores) -> scan (CUDA
-// cores, in place) -> chunk gradients (tensor cores) -> gate-gradient chunk
-// totals -> their suffix sums per item -> the reverse running sums -> the
-// per-token kernel on the queued items -> the per-token combine of
-// backward.cu.
+// cores, in place) -> chunk gradients (tensor cores; they also leave each
+// chunk's gate-gradient column totals) -> the totals' suffix sums per item ->
+// the reverse running sums -> the per-token kernel on the queued items -> the
+// per-token combine of backward.cu.  The dq, dk and dv slots are bf16 (each
+// value is one product, rounded once); the gate-gradient slots stay float32,
+// since the running sums accumulate in place.
 #include <algorithm>
 
 #include "sse_internal.cuh"
@@ -51,6 +53,7 @@ constexpr int kRows = kChunkRows;  // 128 rows per chunk
 constexpr int kKey = 128;          // c
 constexpr int kThr = 256;          // 8 warps: two per TMEM lane quarter
 constexpr uint32_t kTile = 128 * 256;
+static_assert(kThr - kRows == kKey, "the upper half of the CTA writes one chunk total per column");
 constexpr float kRange = 64.f;     // largest |G_m| and |G_l - G_m| the factorised form takes
 constexpr uint64_t kWait = 2000000000ull;
 
@@ -177,12 +180,32 @@ __device__ __forceinline__ void warp_put16(float *patch, int lane, const float (
     __syncwarp();
 }
 
+// A 32-row x 32-column block of bf16 values, one row per lane (16 packed
+// words), goes out through the same patch: 64 contiguous bytes per row, and
+// each store instruction writes 8 rows.  Row (lane / 4 + 8 kk) of the block
+// lands at base + sr[kk] * width + col0 (skipped when sr[kk] < 0).
+__device__ __forceinline__ void warp_put32_bf16(float *patch, int lane, const uint32_t (&w)[16], __nv_bfloat16 *base,
+                                                int width, int col0, const int64_t (&sr)[4]) {
+    uint4 *pr = reinterpret_cast<uint4 *>(patch + lane * kPatchStride);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int rr = (lane >> 2) + 8 * kk, qd = lane & 3;
+        if (sr[kk] >= 0)
+            *reinterpret_cast<uint4 *>(base + sr[kk] * width + col0 + 8 * qd) =
+                *reinterpret_cast<const uint4 *>(patch + rr * kPatchStride + 4 * qd);
+    }
+    __syncwarp();
+}
+
 // Shared memory of the chunk kernels: tiles from a 1024-aligned base, then
 // row metadata, gate sums, the mbarrier and the TMEM address slot.
 struct ChunkSmem {
     unsigned char *tile[6];
     int *tok, *slotj;
-    float *e, *part, *gm, *gl, *de, *patch;
+    float *e, *part, *gm, *gl, *de, *patch, *csum;
     uint32_t bar;
     uint32_t *tslot;
 };
@@ -199,14 +222,15 @@ __device__ __forceinline__ ChunkSmem carve_smem(unsigned char *raw, int ntiles) 
     c.gl = c.gm + kKey;         // [kKey]
     c.de = c.gl + kKey;         // [2 halves][2 (read, write)][kRows]
     c.patch = c.de + 4 * kRows; // [8 warps][32][kPatchStride]
-    uint64_t *b = reinterpret_cast<uint64_t *>(c.patch + 8 * 32 * kPatchStride);
+    c.csum = c.patch + 8 * 32 * kPatchStride;  // [4 lane quarters][kKey]
+    uint64_t *b = reinterpret_cast<uint64_t *>(c.csum + 4 * kKey);
     c.bar = smem_u32(b);
     c.tslot = reinterpret_cast<uint32_t *>(b + 1);
     return c;
 }
 constexpr size_t chunk_smem_bytes(int ntiles) {
     return 1024 + (size_t)ntiles * kTile + 6 * kRows * 4 + 4 * kKey * 4 + 4 * kRows * 4 +
-           8 * 32 * kPatchStride * 4 + 16;
+           8 * 32 * kPatchStride * 4 + 4 * kKey * 4 + 16;
 }
 
 // Row metadata of the chunk into metadata buffer mb (threads 0..127).
@@ -655,6 +679,8 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
             const __nv_bfloat16 *krow = (r.shared && ks ? ks : k) + th * kKey;
             const float *gsr = gs + erow * kKey;
             float *patch = c.patch + warp * 32 * kPatchStride;
+            __nv_bfloat16 *dq_c = static_cast<__nv_bfloat16 *>(a.dq_c), *dk_c = static_cast<__nv_bfloat16 *>(a.dk_c);
+            __nv_bfloat16 *dv_c = static_cast<__nv_bfloat16 *>(a.dv_c);
             int64_t sr[4];  // slot rows this lane stores (-1 past the item's end)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -680,6 +706,7 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
                 tmem_ld32(tmem + lb + c0, xu);
                 tmem_ld32(tmem + lb + 128 + c0, xk);
                 tmem_wait_ld();
+                uint32_t pq[16], pk[16];  // dq and dk of the block, packed bf16 pairs
 #pragma unroll
                 for (int s16 = 0; s16 < 32; s16 += 16) {
                     float dq[16], dk[16], xg[16];
@@ -703,23 +730,40 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
                             de_w += kv[jj] * dK;
                         }
                     }
-                    warp_put16(patch, lane, dq, a.dq_c, kKey, c0 + s16, sr);
-                    warp_put16(patch, lane, dk, a.dk_c, kKey, c0 + s16, sr);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        pq[s16 / 2 + i] = pack2(dq[2 * i], dq[2 * i + 1]);
+                        pk[s16 / 2 + i] = pack2(dk[2 * i], dk[2 * i + 1]);
+                    }
+                    if (!valid) {
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) xg[x] = 0.f;
+                    }
                     warp_put16(patch, lane, xg, a.dg_c, kKey, c0 + s16, sr);
+                    // the block's column sums over this warp's 32 rows, still in
+                    // the patch: lane (half, col) adds 16 rows, then the halves meet
+                    {
+                        const float *pc = patch + (lane >> 4) * 16 * kPatchStride + (lane & 15);
+                        float cs = 0.f;
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) cs += pc[x * kPatchStride];
+                        cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+                        if (lane < 16) c.csum[quarter * kKey + c0 + s16 + lane] = cs;
+                        __syncwarp();  // the patch is rewritten next
+                    }
                 }
+                warp_put32_bf16(patch, lane, pq, dq_c, kKey, c0, sr);
+                warp_put32_bf16(patch, lane, pk, dk_c, kKey, c0, sr);
             }
             for (int c0 = hc * (DV / 2); c0 < (hc + 1) * (DV / 2); c0 += 32) {
                 uint32_t xv[32];
                 __syncwarp();
                 tmem_ld32(tmem + lb + 256 + c0, xv);
                 tmem_wait_ld();
+                uint32_t pv[16];
 #pragma unroll
-                for (int s16 = 0; s16 < 32; s16 += 16) {
-                    float v16[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v16[i] = __uint_as_float(xv[s16 + i]);
-                    warp_put16(patch, lane, v16, a.dv_c, DV, c0 + s16, sr);
-                }
+                for (int i = 0; i < 16; ++i) pv[i] = pack2(__uint_as_float(xv[2 * i]), __uint_as_float(xv[2 * i + 1]));
+                warp_put32_bf16(patch, lane, pv, dv_c, DV, c0, sr);
             }
             if (!valid) de_r = de_w = 0.f;
             c.de[(hc * 2) * kRows + erow] = de_r;
@@ -732,6 +776,12 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
             const int64_t o = (((int64_t)tok[tid] * H + r.h) * topk + sj[tid]) * 2;
             a.de_c[o] = c.de[tid] + c.de[2 * kRows + tid];
             a.de_c[o + 1] = c.de[kRows + tid] + c.de[3 * kRows + tid];
+        }
+        // the chunk's total of q * dq - k * dk per column: the lane quarters in order
+        if (tid >= kRows) {
+            const int col = tid - kRows;
+            a.dgtot[chunk * kKey + col] =
+                ((c.csum[col] + c.csum[kKey + col]) + c.csum[2 * kKey + col]) + c.csum[3 * kKey + col];
         }
         __syncthreads();  // TMEM, the router-weight sums and this metadata buffer are reused
         chunk = next;
@@ -757,25 +807,6 @@ __device__ __forceinline__ void chunk_slot_rows(const BackwardArgs &a, const Chu
         float e;
         row_meta(a, r, threadIdx.x, topk, t, e, j);
         srow[threadIdx.x] = t >= 0 ? ((int64_t)t * H + r.h) * ncon + j : -1;
-    }
-}
-
-// dgtot[chunk][col] = the chunk's sum of the terms (one thread per column)
-__global__ void __launch_bounds__(kKey)
-bwd_dg_total_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared) {
-    __shared__ int64_t srow[kRows];
-    const int ncon = topk + use_shared;
-    for (int64_t chunk = blockIdx.x; chunk < a.num_chunks; chunk += gridDim.x) {
-        ChunkRef r;
-        if (!locate_chunk(a, chunk, H, N, use_shared, r)) break;
-        chunk_slot_rows(a, r, H, topk, ncon, srow);
-        __syncthreads();
-        float acc = 0.f;
-#pragma unroll 8
-        for (int x = 0; x < kRows; ++x)
-            if (srow[x] >= 0) acc += a.dg_c[srow[x] * kKey + threadIdx.x];
-        a.dgtot[chunk * kKey + threadIdx.x] = acc;
-        __syncthreads();
     }
 }
 
@@ -848,12 +879,11 @@ cudaError_t launch_chunked_t(const sse_config_t &cfg, const BackwardArgs &a, cud
         bwd_chunk_sums_kernel<DV><<<grid, kThr, chunk_smem_bytes(5), stream>>>(a, H, N, topk, us, cfg.scale);
         bwd_state_scan_kernel<DV><<<dim3(nitems, kKey * DV / 4 / 256), 256, 0, stream>>>(a, H, N, us);
         bwd_chunk_grads_kernel<DV><<<grid, kThr, chunk_smem_bytes(6), stream>>>(a, H, N, topk, us, cfg.scale);
-        bwd_dg_total_kernel<<<grid_dg, kKey, 0, stream>>>(a, H, N, topk, us);
         bwd_dg_suffix_kernel<<<nitems, kKey, 0, stream>>>(a);
         bwd_dg_apply_kernel<<<grid_dg, kKey, 0, stream>>>(a, H, N, topk, us);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        *launches += 6;
+        *launches += 5;
         // items whose gates left the factorised form's range: the per-token kernel
         BackwardArgs b = a;
         b.seg_list = a.redo_list;

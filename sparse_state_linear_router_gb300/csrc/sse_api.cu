@@ -330,7 +330,8 @@ sse_status_t sse_decode_step(const sse_config_t *cfg, const void *q, const void 
 namespace {
 struct BackwardLayout {
     RouteBuffers rb;
-    float *dq_c, *dk_c, *dg_c, *dv_c, *de_c;
+    void *dq_c, *dk_c, *dv_c;  // I/O type
+    float *dg_c, *de_c;
     // chunked form
     bool chunked;
     int64_t num_chunks;
@@ -370,10 +371,11 @@ BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_
         L.flags = cv.take<int32_t>(64);
     }
     const size_t slots = (size_t)T * c.num_heads * (c.top_k + c.use_shared);
-    L.dq_c = cv.take<float>(slots * c.key_dim);
-    L.dk_c = cv.take<float>(slots * c.key_dim);
+    const size_t esz = c.dtype == SSE_BF16 ? 2 : 4;
+    L.dq_c = cv.take<unsigned char>(slots * c.key_dim * esz);
+    L.dk_c = cv.take<unsigned char>(slots * c.key_dim * esz);
     L.dg_c = cv.take<float>(slots * c.key_dim);
-    L.dv_c = cv.take<float>(slots * c.value_dim);
+    L.dv_c = cv.take<unsigned char>(slots * c.value_dim * esz);
     L.de_c = cv.take<float>((size_t)T * c.num_heads * c.top_k * 2);
     L.bytes = (cv.off + 255) & ~size_t(255);
     return L;

@@ -291,8 +291,8 @@ cudaError_t launch_gather_combine(const sse_config_t &cfg, const ForwardArgs &a,
 int64_t chunked_part_rows(const sse_config_t &cfg, int64_t total_tokens, int32_t num_seqs);
 
 // Backward (backward.cu): pointers as in sse_backward, plus the routing of
-// the forward (recomputed) and the float32 contribution slots
-// [T, H, k + shared, width] of every (token, head) that the per-token pass sums.
+// the forward (recomputed) and the contribution slots [T, H, k + shared, width]
+// of every (token, head) that the combine pass sums.
 struct BackwardArgs {
     const void *q, *k, *v, *g, *logits, *qs, *ks, *d_out;
     const int32_t *cu_seqlens;
@@ -303,7 +303,10 @@ struct BackwardArgs {
     float *d_init;
     const int32_t *seg_off, *perm_rec, *topk_idx;
     const float *perm_e;
-    float *dq_c, *dk_c, *dg_c, *dv_c;  // contribution slots
+    // contribution slots: dq, dk and dv in the I/O type (each a single product
+    // or sum, rounded once), dg in float32 (it holds reverse running sums)
+    void *dq_c, *dk_c, *dv_c;
+    float *dg_c;
     float *de_c;                       // [T, H, k, 2] router-weight gradient of each selected partition (read, write)
     // Per-token kernel restricted to a list of work items (shared (b, h) first,
     // then routed (b, h, i)): item seg_list[x] for x < *seg_count.  Null: all.
