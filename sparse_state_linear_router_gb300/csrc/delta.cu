@@ -16,12 +16,15 @@
 //
 // Forward: one CTA per (sequence, head, partition) segment of the grouping
 // (section 2.6, varlen schedule) and per shared (sequence, head), walking its
-// rows in time order with the c x d state in registers; read-outs go to the
-// float32 partial slots that launch_combine sums (the recurrent path's).
+// rows in time order with the c x d state in registers (delta_cols_kernel for
+// c = 128 and d in {64, 128}, delta_segment_kernel for the other shapes);
+// read-outs go to the float32 partial slots that launch_combine sums (the
+// recurrent path's).
 // Decode: one CTA per (sequence, head) routes the token (warp-level softmax
 // and top-k) and updates only the k + 1 selected states in place.
 #include <algorithm>
 
+#include "f32x2.cuh"
 #include "sse_internal.cuh"
 
 namespace sse {
@@ -205,6 +208,255 @@ delta_segment_kernel(DeltaArgs a, int32_t H, int32_t c, int32_t N, int32_t topk,
     }
 }
 
+// Sum over the 16 lanes that share lane bit 4 of CB per-lane values (one per
+// column), scattered: after halving steps on lane bits 3, 2, ... each lane
+// holds one column's sum, column `owned` of the CB (from the lane's top bits),
+// and the remaining steps add lanes that hold the same column -- both sides of
+// every addition get the same operands, so the lanes agree bit for bit.
+template <int CB>
+__device__ __forceinline__ float reduce_scatter16(const float (&x)[CB], int rg, int &owned) {
+    float a[CB];
+#pragma unroll
+    for (int j = 0; j < CB; ++j) a[j] = x[j];
+    owned = 0;
+#pragma unroll
+    for (int m = 8, h = CB / 2; m >= 1; m >>= 1, h >>= 1) {
+        if (h >= 1) {
+            const bool hi = (rg & m) != 0;
+#pragma unroll
+            for (int j = 0; j < h; ++j) {
+                const float send = hi ? a[j] : a[j + h];
+                const float keep = hi ? a[j + h] : a[j];
+                a[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+            owned += hi ? h : 0;
+        } else {
+            a[0] += __shfl_xor_sync(0xffffffffu, a[0], m);
+        }
+    }
+    return a[0];
+}
+
+// Forward for c = 128 and d in {64, 128}: warp w holds columns
+// [w d / 8, (w + 1) d / 8) of the state; lane (cg, rg) = (lane / 16, lane % 16)
+// holds rows 8 rg .. 8 rg + 7 x CB = d / 16 columns from w d / 8 + cg CB.  A
+// row then reads 8 k and 8 q values per thread from shared memory (k and q
+// skewed by 4 floats per 32 rows, so that the 8 row groups of a quarter warp
+// hit 8 distinct bank quads); the column sums w = k S and q S are register
+// sums over the thread's 8 rows plus a reduce-scatter over the 16 row groups
+// (lane shuffles), and u = e beta (v - alpha w) goes back to the warp's lanes
+// through a per-warp shared buffer.  Column pairs go through the packed
+// float32 pipe (each lane the scalar operation).
+//
+// One CTA barrier per row: the next row's q, k and v are written into the
+// other half of a double buffer right after it, while the three rows after
+// that are in flight in registers (the loop is unrolled by three so that no
+// register slot is copied while its loads are pending).  A routed item's
+// records come in blocks of 32 rows through shared memory (warp 0 loads block
+// m + 1 at row 32 m and stores it at row 32 m + 16), so that no row's input
+// loads wait on its record.
+//
+// Measured on the layer shape (8 x 4096 tokens, H16, N8, top-2, shared):
+// 8.45 ms against 10.7 ms for delta_segment_kernel.  The kernel issues on
+// about 45 % of cycles with two warps per scheduler, stalled mostly on
+// fixed-latency dependencies; neither half-width CTAs at two per SM, nor a
+// recurrence arranged to take the reduction off the row-to-row path (w_{n+1}
+// = alpha_n k_{n+1} S_{n-1} + (k_{n+1} . k_n) u_n), nor scalar instead of
+// packed arithmetic was faster (9.5 - 10.0 ms).
+template <typename T, int D>
+__global__ void __launch_bounds__(kDThreads, 1)
+delta_cols_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared, float scale) {
+    constexpr int C = 128, CB = D / 16, CP = CB / 2, WC = D / 8;
+    constexpr int CS = C + C / 8;  // skewed k / q row
+    __shared__ __align__(16) float s_k[2][CS], s_q[2][CS], s_v[2][D];
+    __shared__ __align__(16) float s_u[8][2][WC];  // per warp, by row parity
+    __shared__ float s_sc[2][3];                   // alpha, e * beta, e * scale of the row
+    __shared__ int64_t s_dst[2];                   // first element of the row's read-out slot
+    __shared__ int s_rec[2][32];                   // records of rows 32 m .. 32 m + 31 in s_rec[m % 2]
+    const T *q = static_cast<const T *>(a.q);
+    const T *kk = static_cast<const T *>(a.k);
+    const T *v = static_cast<const T *>(a.v);
+    const T *la = static_cast<const T *>(a.log_alpha);
+    const T *bt = static_cast<const T *>(a.beta);
+    const int nshared = use_shared ? a.num_seqs * H : 0;
+    const int P = N + use_shared;
+    const bool is_shared = (int)blockIdx.x < nshared;
+    int b, h, slot, len, base;
+    if (is_shared) {
+        b = blockIdx.x / H;
+        h = blockIdx.x % H;
+        slot = N;
+        base = a.cu_seqlens[b];
+        len = a.cu_seqlens[b + 1] - base;
+    } else {
+        const int s = blockIdx.x - nshared;
+        slot = s % N;
+        h = (s / N) % H;
+        b = s / (N * H);
+        base = a.seg_off[s];
+        len = a.seg_off[s + 1] - base;
+    }
+    const T *qsrc = is_shared && a.qs ? static_cast<const T *>(a.qs) : q;
+    const T *ksrc = is_shared && a.ks ? static_cast<const T *>(a.ks) : kk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rg = lane & 15, cg = lane >> 4;
+    const int col0 = warp * WC + cg * CB;     // first of the thread's CB columns
+    const int kofs = 8 * rg + 4 * (rg >> 2);  // its 8 rows in the skewed k / q rows
+    const int64_t state_off = (((int64_t)b * H + h) * P + slot) * (int64_t)C * D;
+    if (len == 0 && a.init == a.final_state) return;
+    F2 st[8][CP];  // rows 8 rg + i, column pairs from col0
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int j4 = 0; j4 < CB / 4; ++j4) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a.init) x = *reinterpret_cast<const float4 *>(a.init + state_off + (int64_t)(8 * rg + i) * D + col0 + 4 * j4);
+            st[i][2 * j4] = f2(x.x, x.y);
+            st[i][2 * j4 + 1] = f2(x.z, x.w);
+        }
+    }
+    // one row's inputs as raw elements: q, k (threads < c), v (threads < d)
+    struct Raw { T q, k, v, la, b; float e; int64_t dst; };
+    auto fetch = [&](int n) -> Raw {
+        int t, jj;
+        Raw x{};
+        if (is_shared) {
+            t = base + n;
+            jj = 0;
+            x.e = 1.f;
+        } else {
+            const int rec = s_rec[(n >> 5) & 1][n & 31];
+            t = rec / topk;
+            jj = rec - t * topk;
+            x.e = a.topk_w[((int64_t)t * H + h) * topk + jj];
+        }
+        const int64_t th = (int64_t)t * H + h;
+        if (tid < C) {
+            x.q = qsrc[th * C + tid];
+            x.k = ksrc[th * C + tid];
+        }
+        if (tid < D) x.v = v[th * D + tid];
+        x.la = la[th];
+        x.b = bt[th];
+        x.dst = is_shared ? th * D : (th * topk + jj) * D;
+        return x;
+    };
+    auto put = [&](const Raw &x, int buf) {
+        if (tid < C) {
+            const int r = tid + 4 * (tid >> 5);
+            s_q[buf][r] = to_f32(x.q);
+            s_k[buf][r] = to_f32(x.k);
+        }
+        if (tid < D) s_v[buf][tid] = to_f32(x.v);
+        if (tid == 0) {
+            s_sc[buf][0] = expf(to_f32(x.la));
+            s_sc[buf][1] = x.e * to_f32(x.b);
+            s_sc[buf][2] = x.e * scale;
+            s_dst[buf] = x.dst;
+        }
+    };
+    float *out = is_shared ? a.part_shared : a.part_routed;
+    int rec_next = 0;
+    if (!is_shared && tid < 32) {
+        if (tid < len) s_rec[0][tid] = a.perm_rec[base + tid];
+    }
+    __syncthreads();
+    auto compute = [&](int cb) {
+        const float *kb = s_k[cb] + kofs, *qb = s_q[cb] + kofs;
+        const float alpha = s_sc[cb][0], eb = s_sc[cb][1], qf = s_sc[cb][2];
+        const float4 ka = *reinterpret_cast<const float4 *>(kb), kz = *reinterpret_cast<const float4 *>(kb + 4);
+        const float kr[8] = {ka.x, ka.y, ka.z, ka.w, kz.x, kz.y, kz.z, kz.w};
+        F2 wp[CP];
+#pragma unroll
+        for (int j = 0; j < CP; ++j) wp[j] = f2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const F2 k2 = f2(kr[i], kr[i]);
+#pragma unroll
+            for (int j = 0; j < CP; ++j) wp[j] = fma2(k2, st[i][j], wp[j]);
+        }
+        float wl[CB];
+#pragma unroll
+        for (int j = 0; j < CP; ++j) {
+            const float2 x = f2_get(wp[j]);
+            wl[2 * j] = x.x;
+            wl[2 * j + 1] = x.y;
+        }
+        int own;
+        const float w = reduce_scatter16<CB>(wl, rg, own);
+        // u of the owned column, to every lane of the column group
+        float *su = s_u[warp][cb];
+        if ((rg & (16 / CB - 1)) == 0) su[cg * CB + own] = eb * (s_v[cb][col0 + own] - alpha * w);
+        __syncwarp();
+        F2 u2[CP];
+#pragma unroll
+        for (int j4 = 0; j4 < CB / 4; ++j4) {
+            const float4 x = *reinterpret_cast<const float4 *>(su + cg * CB + 4 * j4);
+            u2[2 * j4] = f2(x.x, x.y);
+            u2[2 * j4 + 1] = f2(x.z, x.w);
+        }
+        const float4 qa = *reinterpret_cast<const float4 *>(qb), qz = *reinterpret_cast<const float4 *>(qb + 4);
+        const float qr[8] = {qa.x, qa.y, qa.z, qa.w, qz.x, qz.y, qz.z, qz.w};
+        // S <- alpha S + k u, then the read-out q S after the step
+        const F2 a2 = f2(alpha, alpha);
+#pragma unroll
+        for (int j = 0; j < CP; ++j) wp[j] = f2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const F2 k2 = f2(kr[i], kr[i]), q2 = f2(qr[i], qr[i]);
+#pragma unroll
+            for (int j = 0; j < CP; ++j) {
+                st[i][j] = fma2(k2, u2[j], mul2(a2, st[i][j]));
+                wp[j] = fma2(q2, st[i][j], wp[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < CP; ++j) {
+            const float2 x = f2_get(wp[j]);
+            wl[2 * j] = x.x;
+            wl[2 * j + 1] = x.y;
+        }
+        const float o = reduce_scatter16<CB>(wl, rg, own);
+        if ((rg & (16 / CB - 1)) == 0) out[s_dst[cb] + col0 + own] = qf * o;
+    };
+    auto step = [&](int n, Raw &slot) {
+        const int cb = n & 1;
+        // row n's buffer is complete; every thread has finished row n - 1,
+        // which read the other buffer
+        __syncthreads();
+        if (!is_shared && tid < 32) {
+            const int nb = n + 32 - (n & 31) + tid;  // row tid of the next block
+            if ((n & 31) == 0 && nb < len) rec_next = a.perm_rec[base + nb];
+            if ((n & 31) == 16 && nb < len) s_rec[((n >> 5) + 1) & 1][tid] = rec_next;
+        }
+        if (n + 1 < len) {
+            put(slot, cb ^ 1);
+            if (n + 4 < len) slot = fetch(n + 4);
+        }
+        compute(cb);
+    };
+    Raw ra{}, rb{}, rc{};
+    if (len > 0) put(fetch(0), 0);
+    if (len > 1) ra = fetch(1);
+    if (len > 2) rb = fetch(2);
+    if (len > 3) rc = fetch(3);
+    for (int n = 0; n < len; n += 3) {
+        step(n, ra);
+        if (n + 1 < len) step(n + 1, rb);
+        if (n + 2 < len) step(n + 2, rc);
+    }
+    if (a.final_state) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int j4 = 0; j4 < CB / 4; ++j4) {
+                const float2 lo = f2_get(st[i][2 * j4]), hi = f2_get(st[i][2 * j4 + 1]);
+                *reinterpret_cast<float4 *>(a.final_state + state_off + (int64_t)(8 * rg + i) * D + col0 + 4 * j4) =
+                    make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+    }
+}
+
 // Decode: one CTA per (sequence, head).
 // Two CTAs per SM (at most 128 registers a thread): each holds one state in
 // registers between its load and its store, so the second CTA keeps HBM busy
@@ -279,6 +531,13 @@ cudaError_t launch_fwd_t(const sse_config_t &cfg, const DeltaArgs &a, cudaStream
     const size_t smem = sizeof(float) * (2 * c + 3 * d + R * d);
     const int64_t nseg = (int64_t)a.num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
     if (nseg == 0) return cudaSuccess;
+    if constexpr (4 * D4 == 64 || 4 * D4 == 128) {
+        if (c == 128) {
+            delta_cols_kernel<T, 4 * D4><<<(unsigned)nseg, kDThreads, 0, stream>>>(
+                a, cfg.num_heads, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
+            return cudaGetLastError();
+        }
+    }
     delta_segment_kernel<T, D4><<<(unsigned)nseg, kDThreads, smem, stream>>>(
         a, cfg.num_heads, c, cfg.num_partitions, cfg.top_k, cfg.use_shared, cfg.scale);
     return cudaGetLastError();
