@@ -306,16 +306,68 @@ backward_segment_kernel(BackwardArgs a, int32_t H, int32_t c, int32_t N, int32_t
     }
 }
 
+// G consecutive elements (G = 4: 8-byte bf16 / 16-byte float accesses; G = 8:
+// 16-byte bf16 / two 16-byte float accesses) as float32.
+template <typename T, int G> struct Cols;
+template <typename T> struct Cols<T, 4> {
+    static __device__ __forceinline__ void load(const T *p, float (&x)[4]) {
+        const float4 y = Elem<T>::load4(p);
+        x[0] = y.x; x[1] = y.y; x[2] = y.z; x[3] = y.w;
+    }
+    static __device__ __forceinline__ void store(T *p, const float (&x)[4]) {
+        Elem<T>::store4(p, make_float4(x[0], x[1], x[2], x[3]));
+    }
+};
+template <typename T> struct Cols<T, 8> {
+    static __device__ __forceinline__ void load(const T *p, float (&x)[8]) {
+        if constexpr (sizeof(T) == 2) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = __uint_as_float(w[i] << 16);
+                x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+        } else {
+            const float4 y0 = Elem<T>::load4(p), y1 = Elem<T>::load4(p + 4);
+            x[0] = y0.x; x[1] = y0.y; x[2] = y0.z; x[3] = y0.w;
+            x[4] = y1.x; x[5] = y1.y; x[6] = y1.z; x[7] = y1.w;
+        }
+    }
+    static __device__ __forceinline__ void store(T *p, const float (&x)[8]) {
+        if constexpr (sizeof(T) == 2) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+                w[i] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            Elem<T>::store4(p, make_float4(x[0], x[1], x[2], x[3]));
+            Elem<T>::store4(p + 4, make_float4(x[4], x[5], x[6], x[7]));
+        }
+    }
+};
+template <int G>
+__device__ __forceinline__ void load_f32(const float *p, float (&x)[G]) {
+#pragma unroll
+    for (int i = 0; i < G; i += 4) {
+        const float4 y = *reinterpret_cast<const float4 *>(p + i);
+        x[i] = y.x; x[i + 1] = y.y; x[i + 2] = y.z; x[i + 3] = y.w;
+    }
+}
+
 // Per (t, h): the fixed-order sums of the contribution slots, and the router
 // logits' gradient through the softmax over all N partitions.  One thread per
-// (t, h) row handles its logits; then the c- and d-wide sums run four columns
+// (t, h) row handles its logits; then the c- and d-wide sums run G columns
 // per thread, NC (= k + shared) slot loads issued before the sum.
-template <typename T, int NC>
+template <typename T, int NC, int G>
 __global__ void __launch_bounds__(256)
 backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int32_t N, int32_t topk,
                         int32_t use_shared) {
     const int ncon = NC;
-    const int c4 = c / 4, d4 = d / 4;
+    const int cg = c / G, dg = d / G;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t gid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const bool sep_q = use_shared && a.qs, sep_k = use_shared && a.ks;
@@ -341,7 +393,7 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
             Elem<T>::store(dl + i, e * (de - ede));
         }
     }
-    const int per_row = 4 * c4 + d4;  // dq, dk, dg, dq_shared / dk_shared, dv
+    const int per_row = 4 * cg + dg;  // dq, dk, dg, dq_shared / dk_shared, dv
     const int64_t total = rows * per_row;
     const T *sq = static_cast<const T *>(a.dq_c), *sk = static_cast<const T *>(a.dk_c);
     const T *sv = static_cast<const T *>(a.dv_c);
@@ -351,9 +403,9 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
         const T *src = nullptr;  // dq, dk, dv slots (I/O type); dg slots are float32
         T *dst;
         int width, cidx, hi;  // slots 0 .. hi - 1 summed
-        const int kind = part < 4 * c4 ? part / c4 : 4;
+        const int kind = part < 4 * cg ? part / cg : 4;
         if (kind < 4) {
-            cidx = 4 * (part % c4);
+            cidx = G * (part % cg);
             width = c;
             // 0: dq (routed slots, plus the shared slot unless q_shared is separate),
             // 1: dk (likewise), 2: dg (all slots), 3: dq_shared / dk_shared
@@ -362,36 +414,47 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
             else if (kind == 2) { dst = static_cast<T *>(a.dg); hi = ncon; }
             else {
                 // the shared slot alone, into dq_shared and dk_shared when they are separate
-                if (sep_q)
-                    Elem<T>::store4(static_cast<T *>(a.dq_shared) + row * c + cidx,
-                                    Elem<T>::load4(sq + (row * ncon + topk) * c + cidx));
-                if (sep_k)
-                    Elem<T>::store4(static_cast<T *>(a.dk_shared) + row * c + cidx,
-                                    Elem<T>::load4(sk + (row * ncon + topk) * c + cidx));
+                float y[G];
+                if (sep_q) {
+                    Cols<T, G>::load(sq + (row * ncon + topk) * c + cidx, y);
+                    Cols<T, G>::store(static_cast<T *>(a.dq_shared) + row * c + cidx, y);
+                }
+                if (sep_k) {
+                    Cols<T, G>::load(sk + (row * ncon + topk) * c + cidx, y);
+                    Cols<T, G>::store(static_cast<T *>(a.dk_shared) + row * c + cidx, y);
+                }
                 continue;
             }
         } else {
-            cidx = 4 * (part - 4 * c4);
+            cidx = G * (part - 4 * cg);
             width = d;
             src = sv;
             dst = static_cast<T *>(a.dv);
             hi = ncon;
         }
-        float4 p[NC];
+        float p[NC][G];
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
             const int64_t o = (row * ncon + j) * width + cidx;
-            p[j] = j >= hi ? make_float4(0.f, 0.f, 0.f, 0.f)
-                   : src  ? Elem<T>::load4(src + o)
-                          : *reinterpret_cast<const float4 *>(a.dg_c + o);
+            if (j >= hi) {
+#pragma unroll
+                for (int i = 0; i < G; ++i) p[j][i] = 0.f;
+            } else if (src) {
+                Cols<T, G>::load(src + o, p[j]);
+            } else {
+                load_f32<G>(a.dg_c + o, p[j]);
+            }
         }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float acc[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) acc[i] = 0.f;
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
             if (j >= hi) break;
-            acc.x += p[j].x; acc.y += p[j].y; acc.z += p[j].z; acc.w += p[j].w;
+#pragma unroll
+            for (int i = 0; i < G; ++i) acc[i] += p[j][i];
         }
-        Elem<T>::store4(dst + row * width + cidx, acc);
+        Cols<T, G>::store(dst + row * width + cidx, acc);
     }
 }
 
@@ -430,31 +493,37 @@ cudaError_t launch_backward_segments(const sse_config_t &cfg, const BackwardArgs
     return cfg.dtype == SSE_BF16 ? dispatch_d<__nv_bfloat16>(cfg, a, stream) : dispatch_d<float>(cfg, a, stream);
 }
 
+// Eight columns per thread where every row and output is 16-byte aligned,
+// four otherwise.
+template <typename T, int G>
+cudaError_t launch_combine_g(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream) {
+    const int64_t rows = a.total_tokens * cfg.num_heads;
+    const int per_row = 4 * (cfg.key_dim / G) + cfg.value_dim / G;
+    const unsigned blocks = (unsigned)std::min<int64_t>((rows * per_row + 255) / 256, 152 * 16);
+#define SSE_BCOMB(NC)                                                                                         \
+    case NC:                                                                                                  \
+        backward_combine_kernel<T, NC, G><<<blocks, 256, 0, stream>>>(a, rows, cfg.key_dim, cfg.value_dim,  \
+                                                                      cfg.num_partitions, cfg.top_k,          \
+                                                                      cfg.use_shared);                        \
+        break
+    switch (cfg.top_k + cfg.use_shared) {
+        SSE_BCOMB(1); SSE_BCOMB(2); SSE_BCOMB(3); SSE_BCOMB(4); SSE_BCOMB(5);
+        SSE_BCOMB(6); SSE_BCOMB(7); SSE_BCOMB(8); SSE_BCOMB(9);
+        default: return cudaErrorInvalidValue;
+    }
+#undef SSE_BCOMB
+    return cudaGetLastError();
+}
+
 cudaError_t launch_backward_combine(const sse_config_t &cfg, const BackwardArgs &a, cudaStream_t stream) {
     const int64_t rows = a.total_tokens * cfg.num_heads;
     if (rows == 0) return cudaSuccess;
-    const int per_row = 4 * (cfg.key_dim / 4) + cfg.value_dim / 4;
-    const unsigned blocks = (unsigned)std::min<int64_t>((rows * per_row + 255) / 256, 152 * 16);
-    const int ncon = cfg.top_k + cfg.use_shared;
-#define SSE_BCOMB(T, NC)                                                                                      \
-    case NC:                                                                                                  \
-        backward_combine_kernel<T, NC><<<blocks, 256, 0, stream>>>(a, rows, cfg.key_dim, cfg.value_dim,     \
-                                                                   cfg.num_partitions, cfg.top_k, cfg.use_shared); \
-        break
-#define SSE_BCOMB_ALL(T)                                                                                      \
-    switch (ncon) {                                                                                           \
-        SSE_BCOMB(T, 1); SSE_BCOMB(T, 2); SSE_BCOMB(T, 3); SSE_BCOMB(T, 4); SSE_BCOMB(T, 5);                 \
-        SSE_BCOMB(T, 6); SSE_BCOMB(T, 7); SSE_BCOMB(T, 8); SSE_BCOMB(T, 9);                                  \
-        default: return cudaErrorInvalidValue;                                                                \
-    }
-    if (cfg.dtype == SSE_BF16) {
-        SSE_BCOMB_ALL(__nv_bfloat16)
-    } else {
-        SSE_BCOMB_ALL(float)
-    }
-#undef SSE_BCOMB_ALL
-#undef SSE_BCOMB
-    return cudaGetLastError();
+    auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool g8 = cfg.key_dim % 8 == 0 && cfg.value_dim % 8 == 0 && al16(a.dq) && al16(a.dk) && al16(a.dv) &&
+                    al16(a.dg) && (!a.dq_shared || al16(a.dq_shared)) && (!a.dk_shared || al16(a.dk_shared));
+    if (cfg.dtype == SSE_BF16)
+        return g8 ? launch_combine_g<__nv_bfloat16, 8>(cfg, a, stream) : launch_combine_g<__nv_bfloat16, 4>(cfg, a, stream);
+    return g8 ? launch_combine_g<float, 8>(cfg, a, stream) : launch_combine_g<float, 4>(cfg, a, stream);
 }
 
 bool backward_supported(const sse_config_t &cfg) {
