@@ -268,7 +268,7 @@ __device__ __forceinline__ bool run_mma(const ChunkSmem &c, uint32_t &phase, F i
 }
 
 // ---- chunk sums ---------------------------------------------------------
-// U_j = K_hat^T V and W_j = Q_hat^T dO of every chunk (fp32, [c][d] each) and
+// U_j = K_hat^T V and W_j = Q_hat^T dO of every chunk (bf16, [c][d] each) and
 // gamma_j = exp(G_l).  Persistent CTAs walk the chunks; per chunk: stage the
 // raw q, k, g, v, dO rows; per-column gate sums in two halves; K_hat, Q_hat in
 // place; two products (M = c, K = the chunk's rows, N = d) into TMEM; read-out.
@@ -365,16 +365,12 @@ bwd_chunk_sums_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
             for (int c0 = hc * (DV / 2); c0 < (hc + 1) * (DV / 2); c0 += 32) {
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-                    uint32_t x[32];
+                    uint32_t x[32], w[16];
                     tmem_ld32(tmem + lb + 128 * m + c0, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int s16 = 0; s16 < 32; s16 += 16) {
-                        float v16[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v16[i] = __uint_as_float(x[s16 + i]);
-                        warp_put16(patch, lane, v16, m ? a.wgrad : a.ustate, DV, c0 + s16, sr);
-                    }
+                    for (int i = 0; i < 16; ++i) w[i] = pack2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+                    warp_put32_bf16(patch, lane, w, m ? a.wgrad : a.ustate, DV, c0, sr);
                 }
             }
         }
@@ -428,10 +424,14 @@ bwd_state_scan_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t use_shared) 
     const int64_t cb = a.pad_off[u] / kRows;
     const int nch = (a.pad_off[u + 1] - a.pad_off[u]) / kRows;
     const int64_t so = (((int64_t)b * H + h) * P + slot) * (int64_t)kKey * DV + (int64_t)row * DV + col;
-    const int64_t cs = (int64_t)kKey * DV / 4;  // float4 stride between chunks
+    const int64_t cs = (int64_t)kKey * DV / 4;  // stride between chunks, in four-element pieces
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 *U = reinterpret_cast<const float4 *>(a.ustate + (cb * kKey + row) * DV + col);
-    const float4 *W = reinterpret_cast<const float4 *>(a.wgrad + (cb * kKey + row) * DV + col);
+    const uint2 *U = reinterpret_cast<const uint2 *>(a.ustate + (cb * kKey + row) * DV + col);
+    const uint2 *W = reinterpret_cast<const uint2 *>(a.wgrad + (cb * kKey + row) * DV + col);
+    auto f4 = [](uint2 u) {
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    };
     const float *gam = a.gamma + cb * kKey + row;
     const float *gml = a.gml + cb * 2 * kKey + row;  // G_m at [j][0][row], G_l at [j][1][row]
     const uint32_t toffs = toff(row, col);           // four bf16 in one 8-byte piece
@@ -449,7 +449,7 @@ bwd_state_scan_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t use_shared) 
         float gm[kAhead];
 #pragma unroll
         for (int i = 0; i < kAhead; ++i) {
-            x[i] = j0 + i < nch ? U[(j0 + i) * cs] : zero;
+            x[i] = j0 + i < nch ? f4(U[(j0 + i) * cs]) : zero;
             gm[i] = j0 + i < nch ? gam[(int64_t)(j0 + i) * kKey] : 0.f;
         }
 #pragma unroll
@@ -472,7 +472,7 @@ bwd_state_scan_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t use_shared) 
         float gm[kAhead];
 #pragma unroll
         for (int i = 0; i < kAhead; ++i) {
-            x[i] = j0 - i >= 0 ? W[(j0 - i) * cs] : zero;
+            x[i] = j0 - i >= 0 ? f4(W[(j0 - i) * cs]) : zero;
             gm[i] = j0 - i >= 0 ? gam[(int64_t)(j0 - i) * kKey] : 0.f;
         }
 #pragma unroll

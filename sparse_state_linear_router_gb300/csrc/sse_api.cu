@@ -335,7 +335,8 @@ struct BackwardLayout {
     // chunked form
     bool chunked;
     int64_t num_chunks;
-    float *ustate, *wgrad, *gamma, *gml, *gscratch, *fterm, *dgtot;
+    __nv_bfloat16 *ustate, *wgrad;
+    float *gamma, *gml, *gscratch, *fterm, *dgtot;
     void *sp_tiles, *dsp_tiles;
     int32_t *marks, *redo_list, *flags;
     size_t bytes;
@@ -357,8 +358,8 @@ BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_
         L.num_chunks = sse::chunked_part_rows(grouped, T, S) / sse::kChunkRows;
         const size_t nch = (size_t)L.num_chunks, kc = (size_t)c.key_dim, dv = (size_t)c.value_dim;
         const size_t nitems = (size_t)S * c.num_heads * (c.num_partitions + c.use_shared);
-        L.ustate = cv.take<float>(nch * kc * dv);
-        L.wgrad = cv.take<float>(nch * kc * dv);
+        L.ustate = cv.take<__nv_bfloat16>(nch * kc * dv);
+        L.wgrad = cv.take<__nv_bfloat16>(nch * kc * dv);
         L.gamma = cv.take<float>(nch * kc);
         L.gml = cv.take<float>(nch * 2 * kc);
         L.sp_tiles = cv.take<unsigned char>(nch * sse::kChunkRows * 256);  // one 128 x 128 bf16 tile per chunk

@@ -314,8 +314,8 @@ struct BackwardArgs {
     // Chunked (tensor-core) form, c = 128: buffers of backward_chunked.cu.
     const int32_t *pad_off;  // chunk-padded first row of each work item; chunk = row / 128
     int64_t num_chunks;      // upper bound of the chunks (launch size; items past the last exit)
-    float *ustate;           // [chunks, c, d]: K_hat^T V of the chunk
-    float *wgrad;            // [chunks, c, d]: Q_hat^T dO of the chunk
+    __nv_bfloat16 *ustate;   // [chunks, c, d]: K_hat^T V of the chunk (bf16; the scan sums in fp32)
+    __nv_bfloat16 *wgrad;    // [chunks, c, d]: Q_hat^T dO of the chunk (likewise)
     float *gamma;            // [chunks, c]: exp(G_last), the chunk's decay of each state row
     float *gml;              // [chunks, 2, c]: G_m and G_l of each state row
     void *sp_tiles;          // [chunks, 32 KB]: S' = diag(exp(G_m)) S_start, bf16 in the operand tile layout

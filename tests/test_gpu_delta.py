@@ -47,6 +47,10 @@ CASES = {
     "noshared_k3": ("small_bf16", [180], {"num_heads": 1, "num_partitions": 6, "top_k": 3, "use_shared": 0}),
     "c128_d128": ("layer_bf16", [257, 64], {"num_heads": 2}),
     "c128_d64": ("layer_bf16", [130, 3], {"num_heads": 2, "value_dim": 64}),
+    # segments of hundreds of rows: many 32-row record blocks and wraps of the
+    # row pipeline of the c = 128 kernel
+    "c128_long": ("layer_bf16", [1500, 0, 700], {"num_heads": 1, "num_partitions": 4, "top_k": 1}),
+    "c128_d64_long": ("layer_bf16", [901], {"num_heads": 1, "value_dim": 64, "num_partitions": 2, "top_k": 1}),
 }
 
 
@@ -62,8 +66,9 @@ def test_delta_forward_matches_oracle(name):
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < tol
 
 
-def test_delta_scale_separate_shared_and_untouched_states():
-    w = H_.workload_variant("small_bf16", num_heads=2, num_partitions=6, top_k=2)
+@pytest.mark.parametrize("wname,over", [("small_bf16", {"num_heads": 2}), ("layer_bf16", {"num_heads": 1})])
+def test_delta_scale_separate_shared_and_untouched_states(wname, over):
+    w = H_.workload_variant(wname, num_partitions=6, top_k=2, **over)
     inp = synth.make_delta_inputs(w, seed=5, lengths=[200, 41], with_init=True)
     inp.logits[..., 4:] = synth.f32_to_bf16_bits(np.full(inp.logits[..., 4:].shape, -60.0, np.float32))
     rng = np.random.default_rng(6)
