@@ -34,9 +34,9 @@
 //
 // Kernels (one stream, in order): chunk sums (tensor cores) -> scan (CUDA
 // cores, in place) -> chunk gradients (tensor cores; they also leave each
-// chunk's gate-gradient column totals) -> the totals' suffix sums per item ->
-// the reverse running sums -> the per-token kernel on the queued items -> the
-// per-token combine of backward.cu.  The dq, dk and dv slots are bf16 (each
+// chunk's gate-gradient column totals) -> the reverse running sums (each
+// chunk starting from the totals of its item's later chunks) -> the per-token
+// kernel on the queued items -> the per-token combine of backward.cu.  The dq, dk and dv slots are bf16 (each
 // value is one product, rounded once); the gate-gradient slots stay float32,
 // since the running sums accumulate in place.
 #include <algorithm>
@@ -810,23 +810,9 @@ __device__ __forceinline__ void chunk_slot_rows(const BackwardArgs &a, const Chu
     }
 }
 
-// per item, over its chunks from the last: dgtot becomes the sum of every
-// later chunk's terms plus rowsum(S_T * dL/dS_T)
-__global__ void __launch_bounds__(kKey) bwd_dg_suffix_kernel(BackwardArgs a) {
-    const int u = blockIdx.x, col = threadIdx.x;
-    const int64_t cb = a.pad_off[u] / kRows;
-    const int nch = (a.pad_off[u + 1] - a.pad_off[u]) / kRows;
-    float carry = a.fterm[(int64_t)u * kKey + col];
-    for (int j = nch - 1; j >= 0; --j) {
-        float *p = a.dgtot + (cb + j) * kKey + col;
-        const float x = *p;
-        *p = carry;
-        carry += x;
-    }
-}
-
-// inside each chunk, from its last row: dg_c = carry + the terms of this and
-// every later row
+// Inside each chunk, from its last row: dg_c = carry + the terms of this and
+// every later row, where the chunk's carry is rowsum(S_T * dL/dS_T) plus the
+// column totals of the item's later chunks, added from the last chunk down.
 __global__ void __launch_bounds__(kKey)
 bwd_dg_apply_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared) {
     __shared__ int64_t srow[kRows];
@@ -835,8 +821,11 @@ bwd_dg_apply_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_t 
         ChunkRef r;
         if (!locate_chunk(a, chunk, H, N, use_shared, r)) break;
         chunk_slot_rows(a, r, H, topk, ncon, srow);
+        const int64_t cb = a.pad_off[r.item] / kRows;
+        const int nch = (a.pad_off[r.item + 1] - a.pad_off[r.item]) / kRows;
+        float run = a.fterm[(int64_t)r.item * kKey + threadIdx.x];
+        for (int j = nch - 1; j > r.n; --j) run += a.dgtot[(cb + j) * kKey + threadIdx.x];
         __syncthreads();
-        float run = a.dgtot[chunk * kKey + threadIdx.x];
         for (int x0 = kRows - 1; x0 >= 0; x0 -= 8) {  // eight rows' loads ahead of the running sum
             float t[8];
 #pragma unroll
@@ -879,11 +868,10 @@ cudaError_t launch_chunked_t(const sse_config_t &cfg, const BackwardArgs &a, cud
         bwd_chunk_sums_kernel<DV><<<grid, kThr, chunk_smem_bytes(5), stream>>>(a, H, N, topk, us, cfg.scale);
         bwd_state_scan_kernel<DV><<<dim3(nitems, kKey * DV / 4 / 256), 256, 0, stream>>>(a, H, N, us);
         bwd_chunk_grads_kernel<DV><<<grid, kThr, chunk_smem_bytes(6), stream>>>(a, H, N, topk, us, cfg.scale);
-        bwd_dg_suffix_kernel<<<nitems, kKey, 0, stream>>>(a);
         bwd_dg_apply_kernel<<<grid_dg, kKey, 0, stream>>>(a, H, N, topk, us);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        *launches += 5;
+        *launches += 4;
         // items whose gates left the factorised form's range: the per-token kernel
         BackwardArgs b = a;
         b.seg_list = a.redo_list;

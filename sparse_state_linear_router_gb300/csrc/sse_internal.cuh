@@ -322,7 +322,7 @@ struct BackwardArgs {
     void *dsp_tiles;         // [chunks, 32 KB]: dS' = diag(exp(G_l - G_m)) dS_end, likewise
     float *gscratch;         // [kBwdScratchCtas, 128, c]: G_r - G_m of the chunk in flight, per CTA
     float *fterm;            // [items, c]: rowsum(S_T * dL/dS_T) of each work item
-    float *dgtot;            // [chunks, c]: gate-gradient sums of each chunk, then of all later rows
+    float *dgtot;            // [chunks, c]: gate-gradient column totals of each chunk
     int32_t *marks;          // [items]: item queued for the per-token kernel (gate range)
     int32_t *redo_list;      // [items] and its length in flags[1]
     int32_t *flags;          // [0]: device-check flags, [1]: entries of redo_list
