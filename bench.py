@@ -323,6 +323,34 @@ def describe_decode(w):
             f"N{w.num_partitions}, top-{w.top_k}{', shared' if w.use_shared else ''}, fp32 states resident)")
 
 
+def graph_replay_ms(call, reps=50):
+    """Mean time of one replay of a CUDA graph holding call(stream) (captured
+    after two warm-up calls on a side stream), CUDA events around `reps`
+    back-to-back replays."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            call(side.cuda_stream)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / reps
+
+
 def time_forward_variants(args, dev, peaks):
     """Forward-only timings of the other forward workloads, reported beside
     the step (not part of `value`): the long-context varlen batch (16
@@ -403,6 +431,14 @@ def time_forward_variants(args, dev, peaks):
                          "algorithmic_bytes": fb, "algorithmic_flops": ff},
             "device_status": st, "device_flags": flags,
         }
+        if wname == "small_bf16" and bias is None:
+            # the launch-bound shape replayed as one CUDA graph of the same call
+            g_ms = graph_replay_ms(lambda s: binding._check(
+                binding.sse_forward(cfg, P_(x["q"]), P_(x["k"]), P_(x["v"]), P_(x["g"]), P_(x["logits"]), None,
+                                    None, P_(x["cu_seqlens"]), S, T, P_(x["init"]), P_(fin), P_(out), None, None,
+                                    P_(wsp), wsp.numel(), s), "sse_forward"))
+            res[key]["graph_ms"] = g_ms
+            res[key]["graph_tokens_per_s"] = T / (g_ms * 1e-3)
         del x, out, fin, wsp
         torch.cuda.empty_cache()
     return res
