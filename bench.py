@@ -496,6 +496,28 @@ def time_fwd_bwd_fig6(args, dev, L=8192):
     return res
 
 
+def delta_inputs(w, T, dev, seed=None, gen=None):
+    """One batch of T tokens for the delta rule, drawn on the device: unit
+    keys, q = N(0,1)/sqrt(c), v = N(0,1), log_alpha = logsigmoid(N(0,1))/16
+    and beta = sigmoid(N(0,1)) per (token, head), router logits N(0, sigma_r);
+    bf16.  `gen` (a torch generator) continues a stream; else one is seeded."""
+    import torch
+    if gen is None:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+
+    def normal(*shape):
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+    H, c, d, N = w.num_heads, w.key_dim, w.value_dim, w.num_partitions
+    k = normal(T, H, c)
+    return {"q": (normal(T, H, c) / np.sqrt(c)).to(torch.bfloat16),
+            "k": (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16),
+            "v": normal(T, H, d).to(torch.bfloat16),
+            "la": (torch.nn.functional.logsigmoid(normal(T, H)) / 16).to(torch.bfloat16),
+            "b": torch.sigmoid(normal(T, H)).to(torch.bfloat16),
+            "lg": (normal(T, H, N) * w.sigma_router).to(torch.bfloat16)}
+
+
 def time_delta(args, dev):
     """SSE on the gated delta rule (CUDA cores): the forward on the layer
     workload's shape (8 x 4096 tokens, H16, c=d=128, N8, top-2, shared) and
@@ -508,19 +530,6 @@ def time_delta(args, dev):
     stream = torch.cuda.current_stream(dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(3)
-
-    def normal(*shape):
-        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
-
-    def inputs(w, T):
-        H, c, d, N = w.num_heads, w.key_dim, w.value_dim, w.num_partitions
-        k = normal(T, H, c)
-        return {"q": (normal(T, H, c) / np.sqrt(c)).to(torch.bfloat16),
-                "k": (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16),
-                "v": normal(T, H, d).to(torch.bfloat16),
-                "la": (torch.nn.functional.logsigmoid(normal(T, H)) / 16).to(torch.bfloat16),
-                "b": torch.sigmoid(normal(T, H)).to(torch.bfloat16),
-                "lg": (normal(T, H, N) * w.sigma_router).to(torch.bfloat16)}
 
     def timed(fn, reps):
         fn()
@@ -536,7 +545,7 @@ def time_delta(args, dev):
     res = {}
     w = synth.WORKLOADS["layer_bf16"]
     T = sum(w.lengths)
-    x = inputs(w, T)
+    x = delta_inputs(w, T, dev, gen=gen)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(w.lengths)]).astype(np.int32), device=dev)
     cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k, 1, 1.0, "bf16")
     ws = torch.empty(binding.load().sse_delta_forward_workspace_size(binding.ctypes.byref(cfg), T, len(w.lengths)),
@@ -548,7 +557,7 @@ def time_delta(args, dev):
     del x, ws
     w = synth.WORKLOADS["decode_bf16"]
     B = w.decode_batch
-    x = inputs(w, B)
+    x = delta_inputs(w, B, dev, gen=gen)
     cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k, 1, 1.0, "bf16")
     state = torch.zeros((B, w.num_heads, w.num_slots, w.key_dim, w.value_dim), dtype=torch.float32, device=dev)
     ms = timed(lambda: binding.delta_decode_step(cfg, state, x["q"], x["k"], x["v"], x["la"], x["b"], x["lg"]), 10)
@@ -919,6 +928,54 @@ def run_front_end(args):
     return 0
 
 
+def run_delta(args):
+    """One JSON line for sse_delta_forward alone (SSE on the gated delta rule,
+    section 7d of the design notes) on the layer workload's shape, inputs as
+    time_delta draws them: tokens/s of the forward and its time per call."""
+    import torch
+    from sparse_state_linear_router_gb300 import binding
+    ws, rank, local = _dist()
+    if ws > 1:
+        raise SystemExit("--part delta runs on one GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS["layer_bf16"]
+    T = sum(w.lengths)
+    x = delta_inputs(w, T, dev, seed=3)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(w.lengths)]).astype(np.int32), device=dev)
+    cfg = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k, 1, 1.0, "bf16")
+    wsp = torch.empty(binding.load().sse_delta_forward_workspace_size(binding.ctypes.byref(cfg), T, len(w.lengths)),
+                      dtype=torch.uint8, device=dev)
+
+    def call():
+        binding.delta_forward(cfg, x["q"], x["k"], x["v"], x["la"], x["b"], x["lg"], cu, workspace=wsp)
+    for _ in range(args.warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        time.sleep(0.15)
+        ev[0].record(stream)
+        for _ in range(args.steps):
+            call()
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.15)
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    line = {
+        "metric": "SSE on the gated delta rule: forward tokens/s on 1 GB300",
+        "value": T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "delta-rule forward, 8 x 4096 tokens, H16, c=d=128, N8, top-2, shared, "
+                               "bf16 in, fp32 state"},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_backward(args, N=4, L=8192):
     """One JSON line for sse_backward alone at the operator shape of the
     pages' Fig. 6 (8 heads, head dim 128, top-1 of N = 4, shared,
@@ -987,9 +1044,10 @@ def main(argv=None):
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the forward-only timings of the other workloads (varlen, small, skewed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--part", choices=["both", "forward", "decode", "front_end", "backward"], default="both",
-                    help="time the whole step (default), one of its two calls, the front end alone, or the "
-                         "backward at Fig. 6's shape")
+    ap.add_argument("--part", choices=["both", "forward", "decode", "front_end", "backward", "delta"],
+                    default="both",
+                    help="time the whole step (default), one of its two calls, the front end alone, the "
+                         "backward at Fig. 6's shape, or the delta-rule forward on the layer shape")
     ap.add_argument("--fwd-workload", choices=["layer_bf16", "varlen_bf16", "small_bf16"],
                     default=FWD_WORKLOAD, help="forward batch of the step")
     args = ap.parse_args(argv)
@@ -1001,6 +1059,8 @@ def main(argv=None):
         return run_front_end(args)
     if args.part == "backward":
         return run_backward(args)
+    if args.part == "delta":
+        return run_delta(args)
     return run_native(args)
 
 
