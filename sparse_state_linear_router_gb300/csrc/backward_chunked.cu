@@ -41,6 +41,7 @@
 // since the running sums accumulate in place.
 #include <algorithm>
 
+#include "chunk_tiles.cuh"
 #include "sse_internal.cuh"
 #include "umma.cuh"
 
@@ -48,6 +49,7 @@ namespace sse {
 namespace {
 
 using namespace umma;
+using namespace tiles;
 
 constexpr int kRows = kChunkRows;  // 128 rows per chunk
 constexpr int kKey = 128;          // c
@@ -56,14 +58,6 @@ constexpr uint32_t kTile = 128 * 256;
 static_assert(kThr - kRows == kKey, "the upper half of the CTA writes one chunk total per column");
 constexpr float kRange = 64.f;     // largest |G_m| and |G_l - G_m| the factorised form takes
 constexpr uint64_t kWait = 2000000000ull;
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-// byte offset of element (row, col) of a 128-row bf16 tile of up to 128
-// columns: two 64-column atoms per 8-row group, 128-byte swizzle
-__device__ __forceinline__ uint32_t toff(int row, int col) { return sw128_offset(row, col, 2); }
 
 // The work item and chunk of global chunk index `chunk` (items own the
 // chunk-padded row ranges pad_off[u] .. pad_off[u + 1]).  Returns false past
@@ -126,27 +120,6 @@ __device__ __forceinline__ void row_meta(const BackwardArgs &a, const ChunkRef &
     }
 }
 
-// Rows of a [T * H, width] bf16 tensor into a swizzled tile by 16-byte
-// asynchronous copies (zero-filled for token -1: nothing is read there), all
-// threads of the CTA; the caller waits with cp_async_wait_all().
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void stage_rows(unsigned char *tile, const __nv_bfloat16 *src, const int *tok, int H, int h,
-                                           int width) {
-    const int pieces = width / 8;
-    for (int x = threadIdx.x; x < kRows * pieces; x += blockDim.x) {
-        const int r = x / pieces, c8 = x - r * pieces;
-        const int t = tok[r];
-        const __nv_bfloat16 *p = t >= 0 ? src + ((int64_t)t * H + h) * width + c8 * 8 : src;
-        cp_async16(smem_u32(tile + toff(r, c8 * 8)), p, t >= 0);
-    }
-}
-
 // Per-column gate sums of a staged g tile: thread (col, half) sums rows
 // half * 64 .. half * 64 + 63 of column col into part[half][col].
 __device__ __forceinline__ void gate_half_sums(const unsigned char *tg, float *part) {
@@ -156,48 +129,6 @@ __device__ __forceinline__ void gate_half_sums(const unsigned char *tg, float *p
     for (int x = half * 64; x < half * 64 + 64; ++x)
         s += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tg + toff(x, col)));
     part[half * kKey + col] = s;
-}
-
-constexpr int kPatchStride = 20;  // floats per row of a warp's store patch (16 used; rows stay 16-byte aligned)
-
-// A 32-row x 16-column block of fp32 values, one row per lane, goes out through
-// the warp's shared patch: each store instruction then writes 8 rows x 64
-// contiguous bytes instead of 32 rows x 16.  Row (lane / 4 + 8 kk) of the block
-// lands at base + sr[kk] * width + col0 (skipped when sr[kk] < 0).
-__device__ __forceinline__ void warp_put16(float *patch, int lane, const float (&v)[16], float *base, int width,
-                                           int col0, const int64_t (&sr)[4]) {
-    float4 *pr = reinterpret_cast<float4 *>(patch + lane * kPatchStride);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    __syncwarp();
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int rr = (lane >> 2) + 8 * kk, qd = lane & 3;
-        if (sr[kk] >= 0)
-            *reinterpret_cast<float4 *>(base + sr[kk] * width + col0 + 4 * qd) =
-                *reinterpret_cast<const float4 *>(patch + rr * kPatchStride + 4 * qd);
-    }
-    __syncwarp();
-}
-
-// A 32-row x 32-column block of bf16 values, one row per lane (16 packed
-// words), goes out through the same patch: 64 contiguous bytes per row, and
-// each store instruction writes 8 rows.  Row (lane / 4 + 8 kk) of the block
-// lands at base + sr[kk] * width + col0 (skipped when sr[kk] < 0).
-__device__ __forceinline__ void warp_put32_bf16(float *patch, int lane, const uint32_t (&w)[16], __nv_bfloat16 *base,
-                                                int width, int col0, const int64_t (&sr)[4]) {
-    uint4 *pr = reinterpret_cast<uint4 *>(patch + lane * kPatchStride);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    __syncwarp();
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int rr = (lane >> 2) + 8 * kk, qd = lane & 3;
-        if (sr[kk] >= 0)
-            *reinterpret_cast<uint4 *>(base + sr[kk] * width + col0 + 8 * qd) =
-                *reinterpret_cast<const uint4 *>(patch + rr * kPatchStride + 4 * qd);
-    }
-    __syncwarp();
 }
 
 // Shared memory of the chunk kernels: tiles from a 1024-aligned base, then

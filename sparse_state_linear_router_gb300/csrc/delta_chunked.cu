@@ -1,0 +1,571 @@
+// delta_chunked.cu -- SSE on the gated delta rule in chunked form on the
+// tensor cores, for bf16 tokens and c = d = 128 (the recurrence and its
+// reading are those of delta.cu: "Scaling Linear Attention with Sparse State
+// Expansion", close-reading notes section 2.1 eq. 6 and section 6; DeltaNet's
+// update, "动态线性注意力" section 2.1 eq. 4).
+//
+// One work item (a routed segment or a shared (sequence, head)) is a sequence
+// of rows t with key k_t, value v_t, query factor qf_t = e_t scale, writing
+// strength b_t = e_t beta_t and decay alpha_t (e_t: the router weight, 1 for
+// the shared partition).  With w_t = k_t S_{t-1} (row vectors, S is c x d):
+//   u_t = b_t (v_t - alpha_t w_t),  S_t = alpha_t S_{t-1} + k_t^T u_t,
+//   o_t = qf_t q_t S_t.
+// In a chunk of 128 rows starting from the state S0, with G_t the running sum
+// of log alpha from the chunk's first row through row t, gamma_t = exp(G_t)
+// and Gamma_ts = exp(G_t - G_s) (s <= t, so every factor is at most 1):
+//   alpha_t w_t = gamma_t k_t S0 + sum_{s<t} Gamma_ts (k_t . k_s) u_s,
+// so the chunk's u rows solve a unit lower-triangular system:
+//   (I + L) U = diag(b) (V - diag(gamma) K S0),  L_ts = b_t Gamma_ts (k_t . k_s), s < t,
+//   U = T R,  T = (I + L)^-1 diag(b),  R = V - diag(gamma) (K S0);
+//   O = diag(qf gamma) Q S0 + (tril(Q K^T) . Gamma . qf) U;
+//   S_end = gamma_last S0 + (diag(gamma_last / gamma) K)^T U.
+// Per chunk: three rounds of tcgen05 products (K K^T, Q K^T, K S0; then
+// (qf gamma Q) S0 and T R; then P U and the state update), the inverse of
+// I + L in float32 on the CUDA cores (16 x 16 blocks: the diagonal blocks by
+// forward substitution, one warp each, then the block columns from the
+// right), and the passes between them over TMEM rows.  The state stays in
+// TMEM in float32 for the whole item; its bf16 copy is the operand of K S0
+// and Q S0.  Read-outs go to the float32 partial slots that launch_combine
+// sums, like the token-serial kernels of delta.cu.
+#include <algorithm>
+
+#include "chunk_tiles.cuh"
+#include "sse_internal.cuh"
+#include "umma.cuh"
+
+namespace sse {
+namespace {
+
+using namespace umma;
+using namespace tiles;
+
+constexpr int kRows = kChunkRows;  // 128 rows per chunk
+constexpr int kC = 128, kD = 128;  // key and value dimensions
+constexpr int kThr = 256;          // 8 warps: two per TMEM lane quarter
+constexpr uint32_t kTile = 128 * 256;
+constexpr int kNB = kRows / 16;               // 16-row blocks of the chunk
+constexpr int kBS = 16 * 17;                  // floats per stored 16 x 16 block (rows padded to 17)
+constexpr int kNBlk = kNB * (kNB + 1) / 2;    // lower blocks, diagonal included
+constexpr uint64_t kWait = 2000000000ull;
+
+__device__ __forceinline__ int blkidx(int I, int K) { return I * (I + 1) / 2 + K; }
+
+// Shared memory: five operand tiles from a 1024-aligned base, the lower
+// blocks of I + L (then of its inverse), per-row metadata, the warps' store
+// patches, the mbarrier and the TMEM address slot.
+struct DSmem {
+    unsigned char *tQ, *tK, *tV, *tS, *tT;
+    float *blk;
+    int *tok, *slotj;
+    float *G, *b, *qf, *red, *patch;
+    uint32_t bar;
+    uint32_t *tslot;
+    int *item;
+};
+__device__ __forceinline__ DSmem carve(unsigned char *raw) {
+    unsigned char *sm = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+    DSmem c;
+    c.tQ = sm;
+    c.tK = sm + kTile;
+    c.tV = sm + 2 * kTile;
+    c.tS = sm + 3 * kTile;
+    c.tT = sm + 4 * kTile;
+    c.blk = reinterpret_cast<float *>(sm + 5 * kTile);  // [kNBlk][kBS]
+    c.tok = reinterpret_cast<int *>(c.blk + kNBlk * kBS);
+    c.slotj = c.tok + kRows;
+    c.G = reinterpret_cast<float *>(c.slotj + kRows);
+    c.b = c.G + kRows;
+    c.qf = c.b + kRows;
+    c.red = c.qf + kRows;   // [8]
+    c.patch = c.red + 8;    // [8 warps][32][kPatchStride], 16-byte aligned
+    uint64_t *bar = reinterpret_cast<uint64_t *>(c.patch + 8 * 32 * kPatchStride);
+    c.bar = smem_u32(bar);
+    c.tslot = reinterpret_cast<uint32_t *>(bar + 1);
+    c.item = reinterpret_cast<int *>(c.tslot + 1);
+    return c;
+}
+constexpr size_t delta_smem_bytes() {
+    return 1024 + 5 * (size_t)kTile + (size_t)kNBlk * kBS * 4 + 2 * kRows * 4 + 3 * kRows * 4 + 8 * 4 +
+           8 * 32 * kPatchStride * 4 + 16 + 16;
+}
+
+// One elected thread issues the products, commits them to the CTA's mbarrier
+// and every thread waits (bounded).  Shared-memory operands written by the
+// generic proxy before the call are made visible to the tensor core first.
+// Returns false, in every thread, when the wait ran out.
+template <typename F>
+__device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue) {
+    fence_proxy_async();
+    fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        fence_after();
+        issue();
+        commit(c.bar);
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(c.bar, phase, kWait);
+    phase ^= 1u;
+    fence_after();
+    return __syncthreads_and(ok) != 0;
+}
+
+__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// 8 consecutive bf16 of a tile row (16 bytes) <-> float32
+__device__ __forceinline__ void ld8(const unsigned char *p, float (&f)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void st8(unsigned char *p, const float (&f)[8]) {
+    *reinterpret_cast<uint4 *>(p) =
+        make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+__global__ void __launch_bounds__(kThr, 1)
+delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t use_shared, float scale,
+                     int32_t num_items, int32_t *flags) {
+    extern __shared__ unsigned char smem_raw[];
+    const DSmem c = carve(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // TMEM lane quarter (warp % 4) = rows, column half = warp / 4
+    const int quarter = warp & 3, hc = warp >> 2, erow = 32 * quarter + lane;
+    const uint32_t lb = (uint32_t)(32 * quarter) << 16;
+    if (warp == 0) tmem_alloc(smem_u32(c.tslot), 512);
+    if (tid == 0) {
+        mbar_init(c.bar, 1);
+        mbar_fence_init();
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *c.tslot;
+    const uint32_t tA1 = tmem, tA2 = tmem + 128, tO = tmem + 256, tSt = tmem + 384;
+    uint32_t phase = 0;
+    bool failed = false;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q), *k = static_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *qs = static_cast<const __nv_bfloat16 *>(a.qs), *ks = static_cast<const __nv_bfloat16 *>(a.ks);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
+    const __nv_bfloat16 *la = static_cast<const __nv_bfloat16 *>(a.log_alpha);
+    const __nv_bfloat16 *bt = static_cast<const __nv_bfloat16 *>(a.beta);
+    const int nshared = use_shared ? a.num_seqs * H : 0;
+    const int P = N + use_shared;
+    int32_t *counter = flags + 1;
+    float *patch = c.patch + warp * 32 * kPatchStride;
+
+    for (;;) {
+        if (tid == 0) *c.item = atomicAdd(counter, 1);
+        __syncthreads();
+        const int item = *c.item;
+        __syncthreads();  // the slot is written again by the next claim
+        if (item >= num_items) break;
+        int b, h, slot, base, len;
+        const bool shared = item < nshared;
+        if (shared) {
+            b = item / H;
+            h = item % H;
+            slot = N;
+            base = a.cu_seqlens[b];
+            len = a.cu_seqlens[b + 1] - base;
+        } else {
+            const int s = item - nshared;
+            slot = s % N;
+            h = (s / N) % H;
+            b = s / (N * H);
+            base = a.seg_off[s];
+            len = a.seg_off[s + 1] - base;
+        }
+        const int64_t state_off = (((int64_t)b * H + h) * P + slot) * (int64_t)kC * kD;
+        if (len == 0) {
+            // nothing to apply: the final state is the initial one
+            if (a.final_state && a.final_state != a.init)
+                for (int x = tid; x < kC * kD / 4; x += kThr)
+                    reinterpret_cast<float4 *>(a.final_state + state_off)[x] =
+                        a.init ? reinterpret_cast<const float4 *>(a.init + state_off)[x]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
+        const __nv_bfloat16 *qsrc = shared && qs ? qs : q, *ksrc = shared && ks ? ks : k;
+        // the initial state into TMEM (row = lane of the quarter, this warp's column half)
+        for (int g = 0; g < 2; ++g) {
+            const int col0 = 64 * hc + 32 * g;
+            uint32_t x[32];
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4) {
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (a.init)
+                    y = *reinterpret_cast<const float4 *>(a.init + state_off + (int64_t)erow * kD + col0 + 4 * i4);
+                x[4 * i4] = __float_as_uint(y.x);
+                x[4 * i4 + 1] = __float_as_uint(y.y);
+                x[4 * i4 + 2] = __float_as_uint(y.z);
+                x[4 * i4 + 3] = __float_as_uint(y.w);
+            }
+            __syncwarp();
+            tmem_st32(tSt + lb + col0, x);
+        }
+        tmem_wait_st();
+
+        const int nch = (len + kRows - 1) / kRows;
+        for (int ch = 0; ch < nch; ++ch) {
+            // ---- row metadata and the running log-decay G (inclusive) ----
+            __syncthreads();  // the previous chunk's read-out is done with the metadata
+            float lg = 0.f;
+            if (tid < kRows) {
+                const int idx = ch * kRows + tid;
+                int t = -1, jj = 0;
+                float e = 0.f, beta = 0.f;
+                if (idx < len) {
+                    if (shared) {
+                        t = base + idx;
+                        e = 1.f;
+                    } else {
+                        const int rec = a.perm_rec[base + idx];
+                        t = rec / topk;
+                        jj = rec - t * topk;
+                        e = a.topk_w[((int64_t)t * H + h) * topk + jj];
+                    }
+                    const int64_t th = (int64_t)t * H + h;
+                    lg = bf(la + th);
+                    beta = bf(bt + th);
+                }
+                c.tok[tid] = t;
+                c.slotj[tid] = jj;
+                c.b[tid] = e * beta;
+                c.qf[tid] = e * scale;
+            }
+            // inclusive scan of lg over rows 0..127 (warps 0..3)
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, lg, o);
+                if (lane >= o) lg += y;
+            }
+            if (lane == 31) c.red[warp] = lg;
+            __syncthreads();
+            if (tid < kRows) {
+                for (int w2 = 0; w2 < warp; ++w2) lg += c.red[w2];
+                c.G[tid] = lg;
+            }
+            __syncthreads();
+            // ---- stage q, k, v rows; meanwhile the state's bf16 copy and the decay of the chunk ----
+            stage_rows(c.tQ, qsrc, c.tok, H, h, kC);
+            stage_rows(c.tK, ksrc, c.tok, H, h, kC);
+            stage_rows(c.tV, v, c.tok, H, h, kD);
+            {
+                const float gC = __expf(c.G[kRows - 1]);
+                for (int g = 0; g < 2; ++g) {
+                    const int col0 = 64 * hc + 32 * g;
+                    uint32_t x[32];
+                    __syncwarp();
+                    tmem_ld32(tSt + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float f[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(x[8 * j8 + i]);
+                        st8(c.tS + toff(erow, col0 + 8 * j8), f);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(gC * __uint_as_float(x[i]));
+                    tmem_st32(tSt + lb + col0, x);
+                }
+                tmem_wait_st();
+            }
+            cp_async_wait_all();
+            // ---- products 1: A1 = K K^T, A2 = Q K^T, Y = K S0 ----
+            bool ok = run_mma(c, phase, [&] {
+                constexpr uint32_t idT = idesc_bf16(128, 128, 0, 0), idS = idesc_bf16(128, kD, 0, 1);
+                for (int k16 = 0; k16 < kC; k16 += 16) {
+                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
+                    mma_bf16(tA1, desc_sw128(smem_u32(c.tK) + ko, 16, 2048), desc_sw128(smem_u32(c.tK) + ko, 16, 2048),
+                             idT, k16 > 0);
+                    mma_bf16(tA2, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tK) + ko, 16, 2048),
+                             idT, k16 > 0);
+                    mma_bf16(tO, desc_sw128(smem_u32(c.tK) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
+                             idS, k16 > 0);
+                }
+            });
+            if (!ok) {
+                failed = true;
+                break;
+            }
+            // ---- L blocks from A1; R = V - gamma Y in place of V; Q scaled by qf gamma in place ----
+            {
+                const int t = erow;
+                const float Gt = c.G[t], bt_ = c.b[t], gt = __expf(Gt), qg = c.qf[t] * gt;
+                for (int g = 0; g < 2; ++g) {
+                    const int col0 = 64 * hc + 32 * g;
+                    uint32_t x[32];
+                    __syncwarp();
+                    tmem_ld32(tA1 + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int s = col0 + i;
+                        if (s < t)
+                            c.blk[blkidx(t >> 4, s >> 4) * kBS + (t & 15) * 17 + (s & 15)] =
+                                bt_ * __expf(Gt - c.G[s]) * __uint_as_float(x[i]);
+                    }
+                    __syncwarp();
+                    tmem_ld32(tO + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float f[8];
+                        unsigned char *pv = c.tV + toff(t, col0 + 8 * j8);
+                        ld8(pv, f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] -= gt * __uint_as_float(x[8 * j8 + i]);
+                        st8(pv, f);
+                        unsigned char *pq = c.tQ + toff(t, col0 + 8 * j8);
+                        ld8(pq, f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] *= qg;
+                        st8(pq, f);
+                    }
+                }
+            }
+            __syncthreads();
+            // ---- the inverse of I + L: diagonal blocks, one warp each ----
+            {
+                float *bd = c.blk + blkidx(warp, warp) * kBS;
+                float x[16];  // column `lane` of the block's inverse
+#pragma unroll
+                for (int r = 0; r < 16; ++r) x[r] = r == lane ? 1.f : 0.f;
+#pragma unroll
+                for (int r = 1; r < 16; ++r) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < r; ++kk) acc = fmaf(bd[r * 17 + kk], x[kk], acc);
+                    if (r > lane) x[r] = -acc;  // rows above the diagonal keep 0, the diagonal 1
+                }
+                __syncwarp();
+                if (lane < 16) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) bd[r * 17 + lane] = x[r];
+                }
+            }
+            __syncthreads();
+            // ---- block columns from the right: X[I][J] = -(sum_{K=J+1..I} X[I][K] L[K][J]) X[J][J] ----
+            {
+                const int r = tid >> 4, cc = tid & 15;
+                for (int J = kNB - 2; J >= 0; --J) {
+                    float z[kNB];
+#pragma unroll
+                    for (int I = 1; I < kNB; ++I) {
+                        z[I] = 0.f;
+                        if (I > J) {
+                            float acc = 0.f;
+                            for (int K = J + 1; K <= I; ++K) {
+                                const float *xr = c.blk + blkidx(I, K) * kBS + r * 17;
+                                const float *lc = c.blk + blkidx(K, J) * kBS + cc;
+#pragma unroll
+                                for (int m = 0; m < 16; ++m) acc = fmaf(xr[m], lc[m * 17], acc);
+                            }
+                            z[I] = acc;
+                        }
+                    }
+                    __syncthreads();  // every read of L[K][J] is done
+#pragma unroll
+                    for (int I = 1; I < kNB; ++I)
+                        if (I > J) c.blk[blkidx(I, J) * kBS + r * 17 + cc] = z[I];
+                    __syncthreads();
+                    const float *xd = c.blk + blkidx(J, J) * kBS + cc;
+#pragma unroll
+                    for (int I = 1; I < kNB; ++I) {
+                        if (I > J) {
+                            const float *zr = c.blk + blkidx(I, J) * kBS + r * 17;
+                            float acc = 0.f;
+#pragma unroll
+                            for (int m = 0; m < 16; ++m) acc = fmaf(zr[m], xd[m * 17], acc);
+                            z[I] = -acc;
+                        }
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int I = 1; I < kNB; ++I)
+                        if (I > J) c.blk[blkidx(I, J) * kBS + r * 17 + cc] = z[I];
+                    __syncthreads();
+                }
+            }
+            // ---- T = X diag(b) as a bf16 tile (rows t, columns s; zero above the diagonal) ----
+            {
+                const int t = erow;
+                for (int s0 = 64 * hc; s0 < 64 * hc + 64; s0 += 8) {
+                    float f[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int s = s0 + i;
+                        f[i] = (s >> 4) <= (t >> 4)
+                                   ? c.blk[blkidx(t >> 4, s >> 4) * kBS + (t & 15) * 17 + (s & 15)] * c.b[s]
+                                   : 0.f;
+                    }
+                    st8(c.tT + toff(t, s0), f);
+                }
+            }
+            // ---- products 2: Z = (qf gamma Q) S0 into O, U = T R ----
+            ok = run_mma(c, phase, [&] {
+                constexpr uint32_t idS = idesc_bf16(128, kD, 0, 1);
+                for (int k16 = 0; k16 < kC; k16 += 16) {
+                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
+                    mma_bf16(tO, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
+                             idS, k16 > 0);
+                }
+                for (int k16 = 0; k16 < kRows; k16 += 16) {
+                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
+                    mma_bf16(tA1, desc_sw128(smem_u32(c.tT) + ko, 16, 2048), desc_sw128(smem_u32(c.tV) + ro, 1024, 2048),
+                             idS, k16 > 0);
+                }
+            });
+            if (!ok) {
+                failed = true;
+                break;
+            }
+            // ---- U -> bf16 in place of R; P = tril(Q K^T) Gamma qf in place of T; K scaled by
+            //      gamma_last / gamma in place ----
+            {
+                const int t = erow;
+                const float Gt = c.G[t], qft = c.qf[t], GC = c.G[kRows - 1];
+                const float kf = __expf(GC - Gt);
+                for (int g = 0; g < 2; ++g) {
+                    const int col0 = 64 * hc + 32 * g;
+                    uint32_t x[32];
+                    __syncwarp();
+                    tmem_ld32(tA1 + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float f[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(x[8 * j8 + i]);
+                        st8(c.tV + toff(t, col0 + 8 * j8), f);
+                    }
+                    __syncwarp();
+                    tmem_ld32(tA2 + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float f[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int s = col0 + 8 * j8 + i;
+                            f[i] = s <= t ? qft * __expf(Gt - c.G[s]) * __uint_as_float(x[8 * j8 + i]) : 0.f;
+                        }
+                        st8(c.tT + toff(t, col0 + 8 * j8), f);
+                        unsigned char *pk = c.tK + toff(t, col0 + 8 * j8);
+                        ld8(pk, f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] *= kf;
+                        st8(pk, f);
+                    }
+                }
+            }
+            // ---- products 3: O += P U, S += (K gamma_last / gamma)^T U ----
+            ok = run_mma(c, phase, [&] {
+                constexpr uint32_t idP = idesc_bf16(128, kD, 0, 1), idU = idesc_bf16(128, kD, 1, 1);
+                for (int k16 = 0; k16 < kRows; k16 += 16) {
+                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
+                    mma_bf16(tO, desc_sw128(smem_u32(c.tT) + ko, 16, 2048), desc_sw128(smem_u32(c.tV) + ro, 1024, 2048),
+                             idP, 1);
+                    mma_bf16(tSt, desc_sw128(smem_u32(c.tK) + ro, 1024, 2048),
+                             desc_sw128(smem_u32(c.tV) + ro, 1024, 2048), idU, 1);
+                }
+            });
+            if (!ok) {
+                failed = true;
+                break;
+            }
+            // ---- read-out: rows of O to the partial slots ----
+            {
+                int64_t sr[4];  // slot rows this lane stores (-1 past the item's end)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int rr = 32 * quarter + (lane >> 2) + 8 * kk, tt = c.tok[rr];
+                    const int64_t th = (int64_t)tt * H + h;
+                    sr[kk] = tt < 0 ? -1 : shared ? th : th * topk + c.slotj[rr];
+                }
+                float *dst = shared ? a.part_shared : a.part_routed;
+                for (int g = 0; g < 2; ++g) {
+                    const int col0 = 64 * hc + 32 * g;
+                    uint32_t x[32];
+                    __syncwarp();
+                    tmem_ld32(tO + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int s16 = 0; s16 < 32; s16 += 16) {
+                        float f[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(x[s16 + i]);
+                        warp_put16(patch, lane, f, dst, kD, col0 + s16, sr);
+                    }
+                }
+            }
+            fence_before();
+        }
+        if (failed) break;
+        // ---- the final state out of TMEM ----
+        __syncthreads();
+        fence_after();
+        if (a.final_state) {
+            for (int g = 0; g < 2; ++g) {
+                const int col0 = 64 * hc + 32 * g;
+                uint32_t x[32];
+                __syncwarp();
+                tmem_ld32(tSt + lb + col0, x);
+                tmem_wait_ld();
+                float *row = a.final_state + state_off + (int64_t)erow * kD + col0;
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4)
+                    reinterpret_cast<float4 *>(row)[i4] =
+                        make_float4(__uint_as_float(x[4 * i4]), __uint_as_float(x[4 * i4 + 1]),
+                                    __uint_as_float(x[4 * i4 + 2]), __uint_as_float(x[4 * i4 + 3]));
+            }
+        }
+        fence_before();
+        __syncthreads();  // TMEM's state columns are loaded again by the next item
+        fence_after();
+    }
+    if (failed) cp_async_wait_all();  // no copy may still be writing shared memory when the CTA exits
+    if (failed && tid == 0) atomicOr(flags, SSE_DEVICE_TIMEOUT);
+    __syncthreads();
+    if (warp == 0) {
+        fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool delta_chunked_supported(const sse_config_t &cfg) {
+    return cfg.dtype == SSE_BF16 && cfg.key_dim == kC && cfg.value_dim == kD;
+}
+
+cudaError_t launch_delta_chunked(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream) {
+    int32_t *flags = a.flags;
+    if (!flags) return cudaErrorInvalidValue;
+    static bool attr_set = false;  // benign race: every caller sets the same value
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(delta_chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)delta_smem_bytes());
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int nitems = a.num_seqs * cfg.num_heads * (cfg.num_partitions + cfg.use_shared);
+    cudaError_t e = cudaMemsetAsync(flags, 0, 2 * sizeof(int32_t), stream);
+    if (e != cudaSuccess || nitems == 0) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = std::max(1, std::min(nitems, sms > 0 ? sms : 148));
+    delta_chunked_kernel<<<grid, kThr, delta_smem_bytes(), stream>>>(a, cfg.num_heads, cfg.num_partitions,
+                                                                     cfg.top_k, cfg.use_shared, cfg.scale, nitems,
+                                                                     flags);
+    return cudaGetLastError();
+}
+
+}  // namespace sse

@@ -457,6 +457,7 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
 
 namespace {
 struct DeltaLayout {
+    int32_t *flags;  // status words first (sse_read_device_status reads word 0)
     RouteBuffers rb;
     float *part_routed, *part_shared;
     size_t bytes;
@@ -465,6 +466,7 @@ struct DeltaLayout {
 DeltaLayout carve_delta(void *ws, const sse_config_t &c, int64_t T, int32_t S, int32_t *topk_idx, float *topk_w) {
     Carver cv(ws);
     DeltaLayout L{};
+    L.flags = cv.take<int32_t>(64);
     L.rb = carve_route(cv, c, T, S, topk_idx, topk_w, nullptr, nullptr, true, true);
     L.part_routed = cv.take<float>((size_t)T * c.num_heads * c.top_k * c.value_dim);
     L.part_shared = c.use_shared ? cv.take<float>((size_t)T * c.num_heads * c.value_dim) : nullptr;
@@ -519,6 +521,7 @@ sse_status_t sse_delta_forward(const sse_config_t *cfg, const void *q, const voi
     a.topk_w = L.rb.topk_w;
     a.part_routed = L.part_routed;
     a.part_shared = L.part_shared;
+    a.flags = L.flags;
     if (sse::launch_delta_forward(c, a, s) != cudaSuccess) return SSE_ERR_CUDA;
     sse::ForwardArgs fa{};
     fa.total_tokens = total_tokens;

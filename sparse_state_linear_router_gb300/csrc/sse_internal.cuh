@@ -356,6 +356,7 @@ struct DeltaArgs {
     const int32_t *seg_off, *perm_rec;
     const float *topk_w;
     float *part_routed, *part_shared;
+    int32_t *flags;  // status words of the chunked form: [0] device flags, [1] work counter
 };
 struct DeltaDecodeArgs {
     const void *q, *k, *v, *log_alpha, *beta, *logits, *qs, *ks;
@@ -367,6 +368,9 @@ struct DeltaDecodeArgs {
 };
 bool delta_supported(const sse_config_t &cfg);
 cudaError_t launch_delta_forward(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream);
+// Chunked delta-rule forward on the tensor cores (delta_chunked.cu): bf16, c = d = 128.
+bool delta_chunked_supported(const sse_config_t &cfg);
+cudaError_t launch_delta_chunked(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream);
 cudaError_t launch_delta_decode(const sse_config_t &cfg, const DeltaDecodeArgs &a, cudaStream_t stream);
 
 bool decode_supported(const sse_config_t &cfg);

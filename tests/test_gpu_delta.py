@@ -20,9 +20,9 @@ def _lib():
     binding.load()
 
 
-def _gpu(w, inp, scale=1.0, qs=None, ks=None):
+def _gpu(w, inp, scale=1.0, qs=None, ks=None, algo="auto"):
     from sparse_state_linear_router_gb300 import binding
-    cfg = H_.config_of(w, scale=scale)
+    cfg = H_.config_of(w, algo, scale=scale)
     t = {n: binding.to_device(getattr(inp, n)) for n in ("q", "k", "v", "log_alpha", "beta", "logits")}
     cu = torch.from_numpy(inp.cu_seqlens).cuda()
     init = None if inp.init_state is None else torch.from_numpy(inp.init_state).cuda()
@@ -54,27 +54,39 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_delta_forward_matches_oracle(name):
+def _algos(name):
+    """Both forms where the chunked tensor-core one applies (bf16, c = d = 128):
+    auto takes it, recurrent keeps the token-serial kernel."""
+    wname, _, over = CASES[name]
+    w = H_.workload_variant(wname, **over)
+    if w.dtype == "bf16" and w.key_dim == 128 and w.value_dim == 128:
+        return ["auto", "recurrent"]
+    return ["auto"]
+
+
+@pytest.mark.parametrize("name,algo", [(n, a) for n in sorted(CASES) for a in _algos(n)])
+def test_delta_forward_matches_oracle(name, algo):
     wname, lengths, over = CASES[name]
     w = H_.workload_variant(wname, **over)
     inp = synth.make_delta_inputs(w, seed=4, lengths=lengths, with_init=True)
-    gpu, ref = _gpu(w, inp), _ref(w, inp)
+    gpu, ref = _gpu(w, inp, algo=algo), _ref(w, inp)
     assert np.array_equal(gpu["topk_idx"], ref["topk_idx"])
     tol = H_.tol_for(w)
     assert H_.max_abs_rel(gpu["out"], ref["out"]) < tol
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < tol
 
 
-@pytest.mark.parametrize("wname,over", [("small_bf16", {"num_heads": 2}), ("layer_bf16", {"num_heads": 1})])
-def test_delta_scale_separate_shared_and_untouched_states(wname, over):
+@pytest.mark.parametrize("wname,over,algo", [("small_bf16", {"num_heads": 2}, "auto"),
+                                             ("layer_bf16", {"num_heads": 1}, "auto"),
+                                             ("layer_bf16", {"num_heads": 1}, "recurrent")])
+def test_delta_scale_separate_shared_and_untouched_states(wname, over, algo):
     w = H_.workload_variant(wname, num_partitions=6, top_k=2, **over)
     inp = synth.make_delta_inputs(w, seed=5, lengths=[200, 41], with_init=True)
     inp.logits[..., 4:] = synth.f32_to_bf16_bits(np.full(inp.logits[..., 4:].shape, -60.0, np.float32))
     rng = np.random.default_rng(6)
     qs = synth.f32_to_bf16_bits((rng.normal(size=inp.q.shape) / 8).astype(np.float32))
     ks = synth.f32_to_bf16_bits((rng.normal(size=inp.k.shape) / 11).astype(np.float32))
-    gpu, ref = _gpu(w, inp, 0.6, qs, ks), _ref(w, inp, 0.6, qs, ks)
+    gpu, ref = _gpu(w, inp, 0.6, qs, ks, algo=algo), _ref(w, inp, 0.6, qs, ks)
     assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
     assert np.array_equal(gpu["final_state"][:, :, 4:6], inp.init_state[:, :, 4:6])
