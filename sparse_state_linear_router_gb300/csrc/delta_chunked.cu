@@ -44,15 +44,17 @@ constexpr int kC = 128, kD = 128;  // key and value dimensions
 constexpr int kThr = 256;          // 8 warps: two per TMEM lane quarter
 constexpr uint32_t kTile = 128 * 256;
 constexpr int kNB = kRows / 16;               // 16-row blocks of the chunk
-constexpr int kBS = 16 * 17;                  // floats per stored 16 x 16 block (rows padded to 17)
+constexpr int kRS = 20;                       // floats per stored block row (16 used; rows 16-byte aligned)
+constexpr int kBS = 16 * kRS;                 // floats per stored 16 x 16 block
 constexpr int kNBlk = kNB * (kNB + 1) / 2;    // lower blocks, diagonal included
 constexpr uint64_t kWait = 2000000000ull;
 
 __device__ __forceinline__ int blkidx(int I, int K) { return I * (I + 1) / 2 + K; }
 
 // Shared memory: five operand tiles from a 1024-aligned base, the lower
-// blocks of I + L (then of its inverse), per-row metadata, the warps' store
-// patches, the mbarrier and the TMEM address slot.
+// blocks of I + L (then of its inverse), per-row metadata, the mbarrier and
+// the TMEM address slot.  The warps' store patches of the read-out use the
+// T / P tile, free by then (the next chunk's rows are landing in Q, K, V).
 struct DSmem {
     unsigned char *tQ, *tK, *tV, *tS, *tT;
     float *blk;
@@ -77,16 +79,15 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     c.b = c.G + kRows;
     c.qf = c.b + kRows;
     c.red = c.qf + kRows;   // [8]
-    c.patch = c.red + 8;    // [8 warps][32][kPatchStride], 16-byte aligned
-    uint64_t *bar = reinterpret_cast<uint64_t *>(c.patch + 8 * 32 * kPatchStride);
+    c.patch = reinterpret_cast<float *>(c.tT);  // [8 warps][32][kPatchStride] in the T / P tile
+    uint64_t *bar = reinterpret_cast<uint64_t *>(c.red + 8);
     c.bar = smem_u32(bar);
     c.tslot = reinterpret_cast<uint32_t *>(bar + 1);
     c.item = reinterpret_cast<int *>(c.tslot + 1);
     return c;
 }
 constexpr size_t delta_smem_bytes() {
-    return 1024 + 5 * (size_t)kTile + (size_t)kNBlk * kBS * 4 + 2 * kRows * 4 + 3 * kRows * 4 + 8 * 4 +
-           8 * 32 * kPatchStride * 4 + 16 + 16;
+    return 1024 + 5 * (size_t)kTile + (size_t)kNBlk * kBS * 4 + 2 * kRows * 4 + 3 * kRows * 4 + 8 * 4 + 16 + 16;
 }
 
 // One elected thread issues the products, commits them to the CTA's mbarrier
@@ -210,10 +211,10 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
         }
         tmem_wait_st();
 
-        const int nch = (len + kRows - 1) / kRows;
-        for (int ch = 0; ch < nch; ++ch) {
-            // ---- row metadata and the running log-decay G (inclusive) ----
-            __syncthreads();  // the previous chunk's read-out is done with the metadata
+        // row metadata and the running log-decay G (inclusive) of chunk ch, then
+        // its q, k, v rows by asynchronous copies (waited for before products 1)
+        auto prepare = [&](int ch) {
+            __syncthreads();  // every reader of the metadata and of the Q, K, V tiles is done
             float lg = 0.f;
             if (tid < kRows) {
                 const int idx = ch * kRows + tid;
@@ -251,10 +252,14 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 c.G[tid] = lg;
             }
             __syncthreads();
-            // ---- stage q, k, v rows; meanwhile the state's bf16 copy and the decay of the chunk ----
             stage_rows(c.tQ, qsrc, c.tok, H, h, kC);
             stage_rows(c.tK, ksrc, c.tok, H, h, kC);
             stage_rows(c.tV, v, c.tok, H, h, kD);
+        };
+        const int nch = (len + kRows - 1) / kRows;
+        prepare(0);
+        for (int ch = 0; ch < nch; ++ch) {
+            // ---- the state's bf16 copy and the decay of the chunk, while the rows land ----
             {
                 const float gC = __expf(c.G[kRows - 1]);
                 for (int g = 0; g < 2; ++g) {
@@ -305,11 +310,16 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     tmem_ld32(tA1 + lb + col0, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int s = col0 + i;
-                        if (s < t)
-                            c.blk[blkidx(t >> 4, s >> 4) * kBS + (t & 15) * 17 + (s & 15)] =
-                                bt_ * __expf(Gt - c.G[s]) * __uint_as_float(x[i]);
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(c.G + col0 + 4 * i4);
+                        const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int s = col0 + 4 * i4 + i;
+                            if (s < t)
+                                c.blk[blkidx(t >> 4, s >> 4) * kBS + (t & 15) * kRS + (s & 15)] =
+                                    bt_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]);
+                        }
                     }
                     __syncwarp();
                     tmem_ld32(tO + lb + col0, x);
@@ -330,7 +340,20 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     }
                 }
             }
+            // ---- products 2a, issued now and waited for after the inverse: Z = (qf gamma Q) S0 into O ----
+            fence_proxy_async();
+            fence_before();
             __syncthreads();
+            if (tid == 0) {
+                fence_after();
+                constexpr uint32_t idS = idesc_bf16(128, kD, 0, 1);
+                for (int k16 = 0; k16 < kC; k16 += 16) {
+                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
+                    mma_bf16(tO, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
+                             idS, k16 > 0);
+                }
+                commit(c.bar);
+            }
             // ---- the inverse of I + L: diagonal blocks, one warp each ----
             {
                 float *bd = c.blk + blkidx(warp, warp) * kBS;
@@ -341,55 +364,63 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 for (int r = 1; r < 16; ++r) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int kk = 0; kk < r; ++kk) acc = fmaf(bd[r * 17 + kk], x[kk], acc);
+                    for (int kk = 0; kk < r; ++kk) acc = fmaf(bd[r * kRS + kk], x[kk], acc);
                     if (r > lane) x[r] = -acc;  // rows above the diagonal keep 0, the diagonal 1
                 }
                 __syncwarp();
                 if (lane < 16) {
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) bd[r * 17 + lane] = x[r];
+                    for (int r = 0; r < 16; ++r) bd[r * kRS + lane] = x[r];
                 }
             }
             __syncthreads();
             // ---- block columns from the right: X[I][J] = -(sum_{K=J+1..I} X[I][K] L[K][J]) X[J][J] ----
+            // thread (r, cc): element (r, cc) of every block of column J; a column of
+            // L[K][J] (or of X[J][J]) stays in registers while the rows of the X
+            // blocks it meets come in as 16-byte vectors
             {
                 const int r = tid >> 4, cc = tid & 15;
+                auto row_dot = [&](const float *row, const float (&col)[16]) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        const float4 x4 = *reinterpret_cast<const float4 *>(row + 4 * m4);
+                        acc = fmaf(x4.x, col[4 * m4], acc);
+                        acc = fmaf(x4.y, col[4 * m4 + 1], acc);
+                        acc = fmaf(x4.z, col[4 * m4 + 2], acc);
+                        acc = fmaf(x4.w, col[4 * m4 + 3], acc);
+                    }
+                    return acc;
+                };
                 for (int J = kNB - 2; J >= 0; --J) {
                     float z[kNB];
 #pragma unroll
-                    for (int I = 1; I < kNB; ++I) {
-                        z[I] = 0.f;
-                        if (I > J) {
-                            float acc = 0.f;
-                            for (int K = J + 1; K <= I; ++K) {
-                                const float *xr = c.blk + blkidx(I, K) * kBS + r * 17;
-                                const float *lc = c.blk + blkidx(K, J) * kBS + cc;
+                    for (int I = 0; I < kNB; ++I) z[I] = 0.f;
+                    for (int K = J + 1; K < kNB; ++K) {
+                        float lcol[16];
+                        const float *lc = c.blk + blkidx(K, J) * kBS + cc;
 #pragma unroll
-                                for (int m = 0; m < 16; ++m) acc = fmaf(xr[m], lc[m * 17], acc);
-                            }
-                            z[I] = acc;
-                        }
+                        for (int m = 0; m < 16; ++m) lcol[m] = lc[m * kRS];
+#pragma unroll
+                        for (int I = 1; I < kNB; ++I)
+                            if (I >= K) z[I] += row_dot(c.blk + blkidx(I, K) * kBS + r * kRS, lcol);
                     }
                     __syncthreads();  // every read of L[K][J] is done
 #pragma unroll
                     for (int I = 1; I < kNB; ++I)
-                        if (I > J) c.blk[blkidx(I, J) * kBS + r * 17 + cc] = z[I];
+                        if (I > J) c.blk[blkidx(I, J) * kBS + r * kRS + cc] = z[I];
                     __syncthreads();
+                    float xcol[16];
                     const float *xd = c.blk + blkidx(J, J) * kBS + cc;
 #pragma unroll
-                    for (int I = 1; I < kNB; ++I) {
-                        if (I > J) {
-                            const float *zr = c.blk + blkidx(I, J) * kBS + r * 17;
-                            float acc = 0.f;
+                    for (int m = 0; m < 16; ++m) xcol[m] = xd[m * kRS];
 #pragma unroll
-                            for (int m = 0; m < 16; ++m) acc = fmaf(zr[m], xd[m * 17], acc);
-                            z[I] = -acc;
-                        }
-                    }
+                    for (int I = 1; I < kNB; ++I)
+                        if (I > J) z[I] = -row_dot(c.blk + blkidx(I, J) * kBS + r * kRS, xcol);
                     __syncthreads();
 #pragma unroll
                     for (int I = 1; I < kNB; ++I)
-                        if (I > J) c.blk[blkidx(I, J) * kBS + r * 17 + cc] = z[I];
+                        if (I > J) c.blk[blkidx(I, J) * kBS + r * kRS + cc] = z[I];
                     __syncthreads();
                 }
             }
@@ -398,24 +429,33 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 const int t = erow;
                 for (int s0 = 64 * hc; s0 < 64 * hc + 64; s0 += 8) {
                     float f[8];
+                    if ((s0 >> 4) <= (t >> 4)) {
+                        const float *xr = c.blk + blkidx(t >> 4, s0 >> 4) * kBS + (t & 15) * kRS + (s0 & 15);
+                        const float4 x0 = *reinterpret_cast<const float4 *>(xr);
+                        const float4 x1 = *reinterpret_cast<const float4 *>(xr + 4);
+                        const float4 b0 = *reinterpret_cast<const float4 *>(c.b + s0);
+                        const float4 b1 = *reinterpret_cast<const float4 *>(c.b + s0 + 4);
+                        f[0] = x0.x * b0.x; f[1] = x0.y * b0.y; f[2] = x0.z * b0.z; f[3] = x0.w * b0.w;
+                        f[4] = x1.x * b1.x; f[5] = x1.y * b1.y; f[6] = x1.z * b1.z; f[7] = x1.w * b1.w;
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int s = s0 + i;
-                        f[i] = (s >> 4) <= (t >> 4)
-                                   ? c.blk[blkidx(t >> 4, s >> 4) * kBS + (t & 15) * 17 + (s & 15)] * c.b[s]
-                                   : 0.f;
+                        for (int i = 0; i < 8; ++i) f[i] = 0.f;
                     }
                     st8(c.tT + toff(t, s0), f);
                 }
             }
-            // ---- products 2: Z = (qf gamma Q) S0 into O, U = T R ----
+            // ---- products 2b: U = T R (after products 2a have completed) ----
+            {
+                const bool zok = mbar_wait_bounded(c.bar, phase, kWait);
+                phase ^= 1u;
+                fence_after();
+                if (!__syncthreads_and(zok)) {
+                    failed = true;
+                    break;
+                }
+            }
             ok = run_mma(c, phase, [&] {
                 constexpr uint32_t idS = idesc_bf16(128, kD, 0, 1);
-                for (int k16 = 0; k16 < kC; k16 += 16) {
-                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
-                    mma_bf16(tO, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
-                             idS, k16 > 0);
-                }
                 for (int k16 = 0; k16 < kRows; k16 += 16) {
                     const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
                     mma_bf16(tA1, desc_sw128(smem_u32(c.tT) + ko, 16, 2048), desc_sw128(smem_u32(c.tV) + ro, 1024, 2048),
@@ -451,10 +491,13 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
 #pragma unroll
                     for (int j8 = 0; j8 < 4; ++j8) {
                         float f[8];
+                        const float4 g0 = *reinterpret_cast<const float4 *>(c.G + col0 + 8 * j8);
+                        const float4 g1 = *reinterpret_cast<const float4 *>(c.G + col0 + 8 * j8 + 4);
+                        const float gs[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int s = col0 + 8 * j8 + i;
-                            f[i] = s <= t ? qft * __expf(Gt - c.G[s]) * __uint_as_float(x[8 * j8 + i]) : 0.f;
+                            f[i] = s <= t ? qft * __expf(Gt - gs[i]) * __uint_as_float(x[8 * j8 + i]) : 0.f;
                         }
                         st8(c.tT + toff(t, col0 + 8 * j8), f);
                         unsigned char *pk = c.tK + toff(t, col0 + 8 * j8);
@@ -480,7 +523,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 failed = true;
                 break;
             }
-            // ---- read-out: rows of O to the partial slots ----
+            // ---- read-out: rows of O to the partial slots, while the next chunk's rows land ----
             {
                 int64_t sr[4];  // slot rows this lane stores (-1 past the item's end)
 #pragma unroll
@@ -489,6 +532,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     const int64_t th = (int64_t)tt * H + h;
                     sr[kk] = tt < 0 ? -1 : shared ? th : th * topk + c.slotj[rr];
                 }
+                if (ch + 1 < nch) prepare(ch + 1);
                 float *dst = shared ? a.part_shared : a.part_routed;
                 for (int g = 0; g < 2; ++g) {
                     const int col0 = 64 * hc + 32 * g;
