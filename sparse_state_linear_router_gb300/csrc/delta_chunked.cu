@@ -52,12 +52,13 @@ constexpr uint64_t kWait = 2000000000ull;
 __device__ __forceinline__ int blkidx(int I, int K) { return I * (I + 1) / 2 + K; }
 
 // Shared memory: five operand tiles from a 1024-aligned base, the lower
-// blocks of I + L (then of its inverse), per-row metadata, the mbarrier and
+// blocks of I + L (then of its inverse) and a scratch block per block row for
+// the inverse's sums, per-row metadata, the mbarrier and
 // the TMEM address slot.  The warps' store patches of the read-out use the
 // T / P tile, free by then (the next chunk's rows are landing in Q, K, V).
 struct DSmem {
     unsigned char *tQ, *tK, *tV, *tS, *tT;
-    float *blk;
+    float *blk, *zs;
     int *tok, *slotj;
     float *G, *b, *qf, *red, *patch;
     uint32_t bar;
@@ -73,7 +74,8 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     c.tS = sm + 3 * kTile;
     c.tT = sm + 4 * kTile;
     c.blk = reinterpret_cast<float *>(sm + 5 * kTile);  // [kNBlk][kBS]
-    c.tok = reinterpret_cast<int *>(c.blk + kNBlk * kBS);
+    c.zs = c.blk + kNBlk * kBS;                          // [kNB][kBS] sums of the block inverse
+    c.tok = reinterpret_cast<int *>(c.zs + kNB * kBS);
     c.slotj = c.tok + kRows;
     c.G = reinterpret_cast<float *>(c.slotj + kRows);
     c.b = c.G + kRows;
@@ -87,7 +89,8 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     return c;
 }
 constexpr size_t delta_smem_bytes() {
-    return 1024 + 5 * (size_t)kTile + (size_t)kNBlk * kBS * 4 + 2 * kRows * 4 + 3 * kRows * 4 + 8 * 4 + 16 + 16;
+    return 1024 + 5 * (size_t)kTile + (size_t)(kNBlk + kNB) * kBS * 4 + 2 * kRows * 4 + 3 * kRows * 4 + 8 * 4 + 16 +
+           16;
 }
 
 // One elected thread issues the products, commits them to the CTA's mbarrier
@@ -375,52 +378,43 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
             }
             __syncthreads();
             // ---- block columns from the right: X[I][J] = -(sum_{K=J+1..I} X[I][K] L[K][J]) X[J][J] ----
-            // thread (r, cc): element (r, cc) of every block of column J; a column of
-            // L[K][J] (or of X[J][J]) stays in registers while the rows of the X
-            // blocks it meets come in as 16-byte vectors
+            // thread (r, cc): element (r, cc) of every block of column J.  For each
+            // K a column of L[K][J] stays in registers while the rows of the X
+            // blocks below it come in as 16-byte vectors; the sums Z_I gather in
+            // a scratch block per I, since L[I][J] is read until every Z is done
             {
                 const int r = tid >> 4, cc = tid & 15;
                 auto row_dot = [&](const float *row, const float (&col)[16]) {
-                    float acc = 0.f;
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
 #pragma unroll
                     for (int m4 = 0; m4 < 4; ++m4) {
                         const float4 x4 = *reinterpret_cast<const float4 *>(row + 4 * m4);
-                        acc = fmaf(x4.x, col[4 * m4], acc);
-                        acc = fmaf(x4.y, col[4 * m4 + 1], acc);
-                        acc = fmaf(x4.z, col[4 * m4 + 2], acc);
-                        acc = fmaf(x4.w, col[4 * m4 + 3], acc);
+                        a0 = fmaf(x4.x, col[4 * m4], a0);
+                        a1 = fmaf(x4.y, col[4 * m4 + 1], a1);
+                        a2 = fmaf(x4.z, col[4 * m4 + 2], a2);
+                        a3 = fmaf(x4.w, col[4 * m4 + 3], a3);
                     }
-                    return acc;
+                    return (a0 + a1) + (a2 + a3);
                 };
+                float *zme = c.zs + r * kRS + cc;  // this thread's element of scratch block I at zme[I * kBS]
                 for (int J = kNB - 2; J >= 0; --J) {
-                    float z[kNB];
-#pragma unroll
-                    for (int I = 0; I < kNB; ++I) z[I] = 0.f;
                     for (int K = J + 1; K < kNB; ++K) {
                         float lcol[16];
                         const float *lc = c.blk + blkidx(K, J) * kBS + cc;
 #pragma unroll
                         for (int m = 0; m < 16; ++m) lcol[m] = lc[m * kRS];
-#pragma unroll
-                        for (int I = 1; I < kNB; ++I)
-                            if (I >= K) z[I] += row_dot(c.blk + blkidx(I, K) * kBS + r * kRS, lcol);
+                        for (int I = K; I < kNB; ++I) {
+                            const float d = row_dot(c.blk + blkidx(I, K) * kBS + r * kRS, lcol);
+                            zme[I * kBS] = K == J + 1 ? d : zme[I * kBS] + d;
+                        }
                     }
-                    __syncthreads();  // every read of L[K][J] is done
-#pragma unroll
-                    for (int I = 1; I < kNB; ++I)
-                        if (I > J) c.blk[blkidx(I, J) * kBS + r * kRS + cc] = z[I];
-                    __syncthreads();
+                    __syncthreads();  // every Z of column J is complete and every read of L[K][J] done
                     float xcol[16];
                     const float *xd = c.blk + blkidx(J, J) * kBS + cc;
 #pragma unroll
                     for (int m = 0; m < 16; ++m) xcol[m] = xd[m * kRS];
-#pragma unroll
-                    for (int I = 1; I < kNB; ++I)
-                        if (I > J) z[I] = -row_dot(c.blk + blkidx(I, J) * kBS + r * kRS, xcol);
-                    __syncthreads();
-#pragma unroll
-                    for (int I = 1; I < kNB; ++I)
-                        if (I > J) c.blk[blkidx(I, J) * kBS + r * kRS + cc] = z[I];
+                    for (int I = J + 1; I < kNB; ++I)
+                        c.blk[blkidx(I, J) * kBS + r * kRS + cc] = -row_dot(c.zs + I * kBS + r * kRS, xcol);
                     __syncthreads();
                 }
             }
