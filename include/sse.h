@@ -283,11 +283,20 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
  * keys (DeltaNet takes unit keys).
  *
  *   log_alpha, beta   [total_tokens, H] (decode: [batch, H]) in cfg->dtype
- *   everything else   as sse_forward / sse_decode_step (cfg->algo ignored)
- * Computed token by token in float32 on the CUDA cores; read-outs summed per
+ *   everything else   as sse_forward / sse_decode_step
+ * Forward, two computations chosen by cfg->algo:
+ *  - chunked (every algo but SSE_ALGO_RECURRENT; bf16, c = d = 128): chunks
+ *    of 128 rows on the tensor cores -- the chunk's write strengths solved as
+ *    a unit lower-triangular system (its inverse in float32), bf16 operands,
+ *    float32 accumulation and a float32 state held on chip for each segment;
+ *  - token by token in float32 on the CUDA cores (SSE_ALGO_RECURRENT and every
+ *    other shape).
+ * The decode step is token by token in float32.  Read-outs are summed per
  * (token, head) in a fixed order.  Shapes: d in {16, 32, 64, 128, 256},
  * c <= 256 (and c <= 4 * 256 * 16 / d).  Workspace (forward only):
- * sse_delta_forward_workspace_size bytes, 256-byte aligned.
+ * sse_delta_forward_workspace_size bytes, 256-byte aligned; its first word is
+ * the status word sse_read_device_status reads (SSE_DEVICE_TIMEOUT when a
+ * bounded wait of the chunked form ran out).
  * ------------------------------------------------------------------------- */
 size_t sse_delta_forward_workspace_size(const sse_config_t *cfg, int64_t total_tokens, int32_t num_seqs);
 
