@@ -22,8 +22,9 @@
 // Per chunk: three rounds of tcgen05 products (K K^T, Q K^T, K S0; then
 // (qf gamma Q) S0 and T R; then P U and the state update), the inverse of
 // I + L in float32 on the CUDA cores (16 x 16 blocks: the diagonal blocks by
-// forward substitution, one warp each, then the block columns from the
-// right), and the passes between them over TMEM rows.  The state stays in
+// forward substitution, one warp each; each 64-row half by its block columns
+// from the right; the lower-left quadrant as -X_B (L_BA X_A), register-blocked
+// 64 x 64 products), and the passes between them over TMEM rows.  The state stays in
 // TMEM in float32 for the whole item; its bf16 copy is the operand of K S0
 // and Q S0.  Read-outs go to the float32 partial slots that launch_combine
 // sums, like the token-serial kernels of delta.cu.
@@ -377,13 +378,15 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 }
             }
             __syncthreads();
-            // ---- block columns from the right: X[I][J] = -(sum_{K=J+1..I} X[I][K] L[K][J]) X[J][J] ----
-            // thread (r, cc): element (r, cc) of every block of column J.  For each
-            // K a column of L[K][J] stays in registers while the rows of the X
-            // blocks below it come in as 16-byte vectors; the sums Z_I gather in
+            // ---- each 64-row half from its diagonal blocks: block columns from the right,
+            //      X[I][J] = -(sum_{K=J+1..I} X[I][K] L[K][J]) X[J][J] ----
+            // the two halves at once, 128 threads each; thread (rr, cc) holds
+            // elements (rr, cc) and (rr + 8, cc) of every block of column J.  For
+            // each K a column of L[K][J] stays in registers while the rows of the
+            // X blocks below it come in as 16-byte vectors; the sums Z_I gather in
             // a scratch block per I, since L[I][J] is read until every Z is done
             {
-                const int r = tid >> 4, cc = tid & 15;
+                const int B0 = 4 * (tid >> 7), rr = (tid >> 4) & 7, cc = tid & 15;
                 auto row_dot = [&](const float *row, const float (&col)[16]) {
                     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
 #pragma unroll
@@ -396,27 +399,88 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     }
                     return (a0 + a1) + (a2 + a3);
                 };
-                float *zme = c.zs + r * kRS + cc;  // this thread's element of scratch block I at zme[I * kBS]
-                for (int J = kNB - 2; J >= 0; --J) {
-                    for (int K = J + 1; K < kNB; ++K) {
+                float *z0 = c.zs + rr * kRS + cc;  // this thread's elements of scratch block I: z0[I kBS], z0[I kBS + 8 kRS]
+                for (int J = 2; J >= 0; --J) {
+                    for (int K = J + 1; K < 4; ++K) {
                         float lcol[16];
-                        const float *lc = c.blk + blkidx(K, J) * kBS + cc;
+                        const float *lc = c.blk + blkidx(B0 + K, B0 + J) * kBS + cc;
 #pragma unroll
                         for (int m = 0; m < 16; ++m) lcol[m] = lc[m * kRS];
-                        for (int I = K; I < kNB; ++I) {
-                            const float d = row_dot(c.blk + blkidx(I, K) * kBS + r * kRS, lcol);
-                            zme[I * kBS] = K == J + 1 ? d : zme[I * kBS] + d;
+                        for (int I = K; I < 4; ++I) {
+                            const float *xb = c.blk + blkidx(B0 + I, B0 + K) * kBS + rr * kRS;
+                            const float d0 = row_dot(xb, lcol), d1 = row_dot(xb + 8 * kRS, lcol);
+                            float *z = z0 + (B0 + I) * kBS;
+                            z[0] = K == J + 1 ? d0 : z[0] + d0;
+                            z[8 * kRS] = K == J + 1 ? d1 : z[8 * kRS] + d1;
                         }
                     }
                     __syncthreads();  // every Z of column J is complete and every read of L[K][J] done
                     float xcol[16];
-                    const float *xd = c.blk + blkidx(J, J) * kBS + cc;
+                    const float *xd = c.blk + blkidx(B0 + J, B0 + J) * kBS + cc;
 #pragma unroll
                     for (int m = 0; m < 16; ++m) xcol[m] = xd[m * kRS];
-                    for (int I = J + 1; I < kNB; ++I)
-                        c.blk[blkidx(I, J) * kBS + r * kRS + cc] = -row_dot(c.zs + I * kBS + r * kRS, xcol);
+                    for (int I = J + 1; I < 4; ++I) {
+                        float *xo = c.blk + blkidx(B0 + I, B0 + J) * kBS + rr * kRS + cc;
+                        const float *zr = c.zs + (B0 + I) * kBS + rr * kRS;
+                        xo[0] = -row_dot(zr, xcol);
+                        xo[8 * kRS] = -row_dot(zr + 8 * kRS, xcol);
+                    }
                     __syncthreads();
                 }
+            }
+            // ---- the lower-left quadrant, 64 x 64: X_BA = -X_B (L_BA X_A) ----
+            // thread: rows m0 .. m0 + 3 x columns n0 .. n0 + 3 of the quadrant; per
+            // step of the inner dimension four values of a column and a 16-byte
+            // piece of a row feed sixteen multiply-adds; X_A and X_B are lower
+            // triangular (their diagonal blocks hold zeros above the diagonal)
+            {
+                const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
+                auto at = [&](int row, int col) -> float * {  // element (row, col) of the lower block storage
+                    return c.blk + blkidx(row >> 4, col >> 4) * kBS + (row & 15) * kRS + (col & 15);
+                };
+                float acc[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+                for (int kk = n0; kk < 64; ++kk) {  // Y = L_BA X_A: X_A[kk][n] = 0 for kk < n
+                    const float4 b4 = *reinterpret_cast<const float4 *>(at(kk, n0));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float av = *at(64 + m0 + i, kk);
+                        acc[i][0] = fmaf(av, b4.x, acc[i][0]);
+                        acc[i][1] = fmaf(av, b4.y, acc[i][1]);
+                        acc[i][2] = fmaf(av, b4.z, acc[i][2]);
+                        acc[i][3] = fmaf(av, b4.w, acc[i][3]);
+                    }
+                }
+                __syncthreads();  // every read of L_BA is done: Y goes in its place
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
+                        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                __syncthreads();
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+                for (int kk = 0; kk < m0 + 4; ++kk) {  // X_B Y: X_B[m][kk] = 0 for kk > m
+                    const float4 y4 = *reinterpret_cast<const float4 *>(at(64 + kk, n0));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float av = *at(64 + m0 + i, 64 + kk);
+                        acc[i][0] = fmaf(av, y4.x, acc[i][0]);
+                        acc[i][1] = fmaf(av, y4.y, acc[i][1]);
+                        acc[i][2] = fmaf(av, y4.z, acc[i][2]);
+                        acc[i][3] = fmaf(av, y4.w, acc[i][3]);
+                    }
+                }
+                __syncthreads();  // every read of Y is done: X_BA goes in its place
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
+                        make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
+                __syncthreads();
             }
             // ---- T = X diag(b) as a bf16 tile (rows t, columns s; zero above the diagonal) ----
             {
