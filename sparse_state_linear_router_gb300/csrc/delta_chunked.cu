@@ -46,7 +46,7 @@ constexpr int kThr = 256;          // 8 warps: two per TMEM lane quarter
 constexpr uint32_t kTile = 128 * 256;
 constexpr int kNB = kRows / 16;               // 16-row blocks of the chunk
 constexpr int kRS = 20;                       // floats per stored block row (16 used; rows 16-byte aligned)
-constexpr int kBS = 16 * kRS;                 // floats per stored 16 x 16 block
+constexpr int kBS = 16 * kRS + 4;             // floats per stored 16 x 16 block (+4: consecutive blocks 4 banks apart)
 constexpr int kNBlk = kNB * (kNB + 1) / 2;    // lower blocks, diagonal included
 constexpr uint64_t kWait = 2000000000ull;
 
@@ -429,58 +429,67 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 }
             }
             // ---- the lower-left quadrant, 64 x 64: X_BA = -X_B (L_BA X_A) ----
-            // thread: rows m0 .. m0 + 3 x columns n0 .. n0 + 3 of the quadrant; per
-            // step of the inner dimension four values of a column and a 16-byte
-            // piece of a row feed sixteen multiply-adds; X_A and X_B are lower
-            // triangular (their diagonal blocks hold zeros above the diagonal)
+            // a thread's 4 x 4 outputs; per step of the inner dimension four values
+            // of a column and a 16-byte piece of a row feed sixteen multiply-adds.
+            // X_A and X_B are lower triangular (their diagonal blocks hold zeros
+            // above the diagonal), so each product's inner range ends at the
+            // thread's columns (L_BA X_A) or rows (X_B Y); the threads of a warp
+            // share those bounds, so no warp runs the full range
             {
-                const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);
                 auto at = [&](int row, int col) -> float * {  // element (row, col) of the lower block storage
                     return c.blk + blkidx(row >> 4, col >> 4) * kBS + (row & 15) * kRS + (col & 15);
                 };
                 float acc[4][4];
+                {
+                    const int n0 = 4 * (tid >> 4), m0 = 4 * (tid & 15);  // columns warp-shared
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-                for (int kk = n0; kk < 64; ++kk) {  // Y = L_BA X_A: X_A[kk][n] = 0 for kk < n
-                    const float4 b4 = *reinterpret_cast<const float4 *>(at(kk, n0));
+                        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 2
+                    for (int kk = n0; kk < 64; ++kk) {  // Y = L_BA X_A: X_A[kk][n] = 0 for kk < n
+                        const float4 b4 = *reinterpret_cast<const float4 *>(at(kk, n0));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float av = *at(64 + m0 + i, kk);
-                        acc[i][0] = fmaf(av, b4.x, acc[i][0]);
-                        acc[i][1] = fmaf(av, b4.y, acc[i][1]);
-                        acc[i][2] = fmaf(av, b4.z, acc[i][2]);
-                        acc[i][3] = fmaf(av, b4.w, acc[i][3]);
+                        for (int i = 0; i < 4; ++i) {
+                            const float av = *at(64 + m0 + i, kk);
+                            acc[i][0] = fmaf(av, b4.x, acc[i][0]);
+                            acc[i][1] = fmaf(av, b4.y, acc[i][1]);
+                            acc[i][2] = fmaf(av, b4.z, acc[i][2]);
+                            acc[i][3] = fmaf(av, b4.w, acc[i][3]);
+                        }
                     }
+                    __syncthreads();  // every read of L_BA is done: Y goes in its place
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
+                            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                    __syncthreads();
                 }
-                __syncthreads();  // every read of L_BA is done: Y goes in its place
+                {
+                    const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);  // rows warp-shared
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
-                        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-                __syncthreads();
+                    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 2
+                    for (int kk = 0; kk < m0 + 4; ++kk) {  // X_B Y: X_B[m][kk] = 0 for kk > m
+                        const float4 y4 = *reinterpret_cast<const float4 *>(at(64 + kk, n0));
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-                for (int kk = 0; kk < m0 + 4; ++kk) {  // X_B Y: X_B[m][kk] = 0 for kk > m
-                    const float4 y4 = *reinterpret_cast<const float4 *>(at(64 + kk, n0));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float av = *at(64 + m0 + i, 64 + kk);
-                        acc[i][0] = fmaf(av, y4.x, acc[i][0]);
-                        acc[i][1] = fmaf(av, y4.y, acc[i][1]);
-                        acc[i][2] = fmaf(av, y4.z, acc[i][2]);
-                        acc[i][3] = fmaf(av, y4.w, acc[i][3]);
+                        for (int i = 0; i < 4; ++i) {
+                            const float av = *at(64 + m0 + i, 64 + kk);
+                            acc[i][0] = fmaf(av, y4.x, acc[i][0]);
+                            acc[i][1] = fmaf(av, y4.y, acc[i][1]);
+                            acc[i][2] = fmaf(av, y4.z, acc[i][2]);
+                            acc[i][3] = fmaf(av, y4.w, acc[i][3]);
+                        }
                     }
-                }
-                __syncthreads();  // every read of Y is done: X_BA goes in its place
+                    __syncthreads();  // every read of Y is done: X_BA goes in its place
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
-                        make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
-                __syncthreads();
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
+                            make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
+                    __syncthreads();
+                }
             }
             // ---- T = X diag(b) as a bf16 tile (rows t, columns s; zero above the diagonal) ----
             {
