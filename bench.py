@@ -552,8 +552,15 @@ def time_delta(args, dev):
                      dtype=torch.uint8, device=dev)
     ms = timed(lambda: binding.delta_forward(cfg, x["q"], x["k"], x["v"], x["la"], x["b"], x["lg"], cu,
                                              workspace=ws), 3)
-    res["forward_layer_shape"] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3),
+    res["forward_layer_shape"] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3), "form": "chunked (tensor cores)",
                                   "workload": "8 x 4096 tokens, H16, c=d=128, N8, top-2, shared, bf16"}
+    cfg_r = binding.make_config(w.num_heads, w.key_dim, w.value_dim, w.num_partitions, w.top_k, 1, 1.0, "bf16",
+                                "recurrent")
+    ms = timed(lambda: binding.delta_forward(cfg_r, x["q"], x["k"], x["v"], x["la"], x["b"], x["lg"], cu,
+                                             workspace=ws), 3)
+    res["forward_layer_shape_token_serial"] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3),
+                                               "form": "token by token (CUDA cores)",
+                                               "workload": "8 x 4096 tokens, H16, c=d=128, N8, top-2, shared, bf16"}
     del x, ws
     w = synth.WORKLOADS["decode_bf16"]
     B = w.decode_batch
