@@ -23,8 +23,8 @@
 // (qf gamma Q) S0 and T R; then P U and the state update), the inverse of
 // I + L in float32 on the CUDA cores (16 x 16 blocks: the diagonal blocks by
 // forward substitution, one warp each; each 64-row half by its block columns
-// from the right; the lower-left quadrant as -X_B (L_BA X_A), register-blocked
-// 64 x 64 products), and the passes between them over TMEM rows.  The state stays in
+// from the right; the lower-left quadrant as -X_B (L_BA X_A), two 64 x 64
+// products on the tensor cores), and the passes between them over TMEM rows.  The state stays in
 // TMEM in float32 for the whole item; its bf16 copy is the operand of K S0
 // and Q S0.  Read-outs go to the float32 partial slots that launch_combine
 // sums, like the token-serial kernels of delta.cu.
@@ -428,68 +428,99 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     __syncthreads();
                 }
             }
-            // ---- the lower-left quadrant, 64 x 64: X_BA = -X_B (L_BA X_A) ----
-            // a thread's 4 x 4 outputs; per step of the inner dimension four values
-            // of a column and a 16-byte piece of a row feed sixteen multiply-adds.
-            // X_A and X_B are lower triangular (their diagonal blocks hold zeros
-            // above the diagonal), so each product's inner range ends at the
-            // thread's columns (L_BA X_A) or rows (X_B Y); the threads of a warp
-            // share those bounds, so no warp runs the full range
+            // ---- the lower-left quadrant, 64 x 64: X_BA = -X_B (L_BA X_A), on the tensor cores ----
+            // products 2a are done first, so the state's bf16 tile is free; the
+            // T tile and the state tile hold the bf16 operands (rows 0..63; the A
+            // operands' rows 64..127 only feed output rows that are never read),
+            // TMEM columns 0..63 and 64..127 (free until U) the two products
             {
-                auto at = [&](int row, int col) -> float * {  // element (row, col) of the lower block storage
-                    return c.blk + blkidx(row >> 4, col >> 4) * kBS + (row & 15) * kRS + (col & 15);
+                const bool zok = mbar_wait_bounded(c.bar, phase, kWait);
+                phase ^= 1u;
+                fence_after();
+                if (!__syncthreads_and(zok)) {
+                    failed = true;
+                    break;
+                }
+                // element (row, col) of the lower block storage (zero above the block diagonal)
+                auto ld8f = [&](int row, int col, float (&f)[8]) {
+                    if ((row >> 4) < (col >> 4)) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+                        return;
+                    }
+                    const float *p = c.blk + blkidx(row >> 4, col >> 4) * kBS + (row & 15) * kRS + (col & 15);
+                    const float4 x0 = *reinterpret_cast<const float4 *>(p), x1 = *reinterpret_cast<const float4 *>(p + 4);
+                    f[0] = x0.x; f[1] = x0.y; f[2] = x0.z; f[3] = x0.w;
+                    f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
                 };
-                float acc[4][4];
-                {
-                    const int n0 = 4 * (tid >> 4), m0 = 4 * (tid & 15);  // columns warp-shared
+                const int er = tid >> 2, ec = (tid & 3) * 16;  // this thread's row and 16 columns of a 64 x 64 operand
+                // L_BA (A, K-major: rows m, columns k) into the T tile; X_A (B, MN-major: rows k, columns n) into the state tile
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 2
-                    for (int kk = n0; kk < 64; ++kk) {  // Y = L_BA X_A: X_A[kk][n] = 0 for kk < n
-                        const float4 b4 = *reinterpret_cast<const float4 *>(at(kk, n0));
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float av = *at(64 + m0 + i, kk);
-                            acc[i][0] = fmaf(av, b4.x, acc[i][0]);
-                            acc[i][1] = fmaf(av, b4.y, acc[i][1]);
-                            acc[i][2] = fmaf(av, b4.z, acc[i][2]);
-                            acc[i][3] = fmaf(av, b4.w, acc[i][3]);
-                        }
-                    }
-                    __syncthreads();  // every read of L_BA is done: Y goes in its place
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
-                            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-                    __syncthreads();
+                for (int h8 = 0; h8 < 16; h8 += 8) {
+                    float f[8];
+                    ld8f(64 + er, ec + h8, f);
+                    st8(c.tT + toff(er, ec + h8), f);
+                    ld8f(er, ec + h8, f);
+                    st8(c.tS + toff(er, ec + h8), f);
                 }
-                {
-                    const int m0 = 4 * (tid >> 4), n0 = 4 * (tid & 15);  // rows warp-shared
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-#pragma unroll 2
-                    for (int kk = 0; kk < m0 + 4; ++kk) {  // X_B Y: X_B[m][kk] = 0 for kk > m
-                        const float4 y4 = *reinterpret_cast<const float4 *>(at(64 + kk, n0));
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float av = *at(64 + m0 + i, 64 + kk);
-                            acc[i][0] = fmaf(av, y4.x, acc[i][0]);
-                            acc[i][1] = fmaf(av, y4.y, acc[i][1]);
-                            acc[i][2] = fmaf(av, y4.z, acc[i][2]);
-                            acc[i][3] = fmaf(av, y4.w, acc[i][3]);
-                        }
-                    }
-                    __syncthreads();  // every read of Y is done: X_BA goes in its place
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        *reinterpret_cast<float4 *>(at(64 + m0 + i, n0)) =
-                            make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
-                    __syncthreads();
+                ok = run_mma(c, phase, [&] {
+                    constexpr uint32_t id = idesc_bf16(128, 64, 0, 1);
+                    for (int k16 = 0; k16 < 64; k16 += 16)
+                        mma_bf16(tA1, desc_sw128(smem_u32(c.tT) + k16 * 2, 16, 2048),
+                                 desc_sw128(smem_u32(c.tS) + (k16 / 8) * 2048, 1024, 2048), id, k16 > 0);
+                });
+                if (!ok) {
+                    failed = true;
+                    break;
                 }
+                // Y (rows 0..63 of TMEM columns 0..63) into the state tile as the B operand; X_B into the T tile
+                if (quarter < 2) {
+                    uint32_t x[32];
+                    const int col0 = 32 * hc;
+                    tmem_ld32(tA1 + lb + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float f[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(x[8 * j8 + i]);
+                        st8(c.tS + toff(erow, col0 + 8 * j8), f);
+                    }
+                }
+#pragma unroll
+                for (int h8 = 0; h8 < 16; h8 += 8) {
+                    float f[8];
+                    ld8f(64 + er, 64 + ec + h8, f);
+                    st8(c.tT + toff(er, ec + h8), f);
+                }
+                ok = run_mma(c, phase, [&] {
+                    constexpr uint32_t id = idesc_bf16(128, 64, 0, 1);
+                    for (int k16 = 0; k16 < 64; k16 += 16)
+                        mma_bf16(tA1 + 64, desc_sw128(smem_u32(c.tT) + k16 * 2, 16, 2048),
+                                 desc_sw128(smem_u32(c.tS) + (k16 / 8) * 2048, 1024, 2048), id, k16 > 0);
+                });
+                if (!ok) {
+                    failed = true;
+                    break;
+                }
+                // X_BA = -(X_B Y) into the lower-left quadrant of the block storage
+                if (quarter < 2) {
+                    uint32_t x[32];
+                    const int col0 = 32 * hc;
+                    tmem_ld32(tA1 + lb + 64 + col0, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const int n = col0 + 4 * j4;
+                        float *p = c.blk + blkidx((64 + erow) >> 4, n >> 4) * kBS + (erow & 15) * kRS + (n & 15);
+                        *reinterpret_cast<float4 *>(p) =
+                            make_float4(-__uint_as_float(x[4 * j4]), -__uint_as_float(x[4 * j4 + 1]),
+                                        -__uint_as_float(x[4 * j4 + 2]), -__uint_as_float(x[4 * j4 + 3]));
+                    }
+                }
+                fence_before();
+                __syncthreads();
+                fence_after();
             }
             // ---- T = X diag(b) as a bf16 tile (rows t, columns s; zero above the diagonal) ----
             {
@@ -511,16 +542,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     st8(c.tT + toff(t, s0), f);
                 }
             }
-            // ---- products 2b: U = T R (after products 2a have completed) ----
-            {
-                const bool zok = mbar_wait_bounded(c.bar, phase, kWait);
-                phase ^= 1u;
-                fence_after();
-                if (!__syncthreads_and(zok)) {
-                    failed = true;
-                    break;
-                }
-            }
+            // ---- products 2b: U = T R ----
             ok = run_mma(c, phase, [&] {
                 constexpr uint32_t idS = idesc_bf16(128, kD, 0, 1);
                 for (int k16 = 0; k16 < kRows; k16 += 16) {

@@ -51,6 +51,8 @@ CASES = {
     # row pipeline of the c = 128 kernel
     "c128_long": ("layer_bf16", [1500, 0, 700], {"num_heads": 1, "num_partitions": 4, "top_k": 1}),
     "c128_d64_long": ("layer_bf16", [901], {"num_heads": 1, "value_dim": 64, "num_partitions": 2, "top_k": 1}),
+    # one sequence of the layer shape's length: 32 chunks carry the state
+    "c128_4096": ("layer_bf16", [4096], {"num_heads": 1, "num_partitions": 4, "top_k": 1}),
 }
 
 
