@@ -595,8 +595,7 @@ bool delta_supported(const sse_config_t &cfg) {
 // The chunked tensor-core form (delta_chunked.cu) unless the token-serial one
 // is asked for (SSE_ALGO_RECURRENT) or the shape has no chunked form.
 cudaError_t launch_delta_forward(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream) {
-    if (cfg.algo != SSE_ALGO_RECURRENT && delta_chunked_supported(cfg) && a.flags)
-        return launch_delta_chunked(cfg, a, stream);
+    if (delta_chunked_partials_bf16(cfg)) return launch_delta_chunked(cfg, a, stream);
     return cfg.dtype == SSE_BF16 ? fwd_dispatch<__nv_bfloat16>(cfg, a, stream) : fwd_dispatch<float>(cfg, a, stream);
 }
 

@@ -26,8 +26,9 @@
 // from the right; the lower-left quadrant as -X_B (L_BA X_A), two 64 x 64
 // products on the tensor cores), and the passes between them over TMEM rows.  The state stays in
 // TMEM in float32 for the whole item; its bf16 copy is the operand of K S0
-// and Q S0.  Read-outs go to the float32 partial slots that launch_combine
-// sums, like the token-serial kernels of delta.cu.
+// and Q S0.  Read-outs go to bf16 partial slots ([T, H, k, d] and [T, H, d],
+// the layout of the token-serial kernels' float32 ones) that launch_combine
+// sums in float32.
 #include <algorithm>
 
 #include "chunk_tiles.cuh"
@@ -622,20 +623,17 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     sr[kk] = tt < 0 ? -1 : shared ? th : th * topk + c.slotj[rr];
                 }
                 if (ch + 1 < nch) prepare(ch + 1);
-                float *dst = shared ? a.part_shared : a.part_routed;
+                // bf16 partial rows (the combine sums them in float32)
+                __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(shared ? a.part_shared : a.part_routed);
                 for (int g = 0; g < 2; ++g) {
                     const int col0 = 64 * hc + 32 * g;
-                    uint32_t x[32];
+                    uint32_t x[32], w[16];
                     __syncwarp();
                     tmem_ld32(tO + lb + col0, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int s16 = 0; s16 < 32; s16 += 16) {
-                        float f[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(x[s16 + i]);
-                        warp_put16(patch, lane, f, dst, kD, col0 + s16, sr);
-                    }
+                    for (int i = 0; i < 16; ++i) w[i] = pack2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+                    warp_put32_bf16(patch, lane, w, dst, kD, col0, sr);
                 }
             }
             fence_before();

@@ -528,7 +528,7 @@ sse_status_t sse_delta_forward(const sse_config_t *cfg, const void *q, const voi
     fa.out = out;
     fa.part_routed = L.part_routed;
     fa.part_shared = L.part_shared;
-    fa.part_bf16 = 0;
+    fa.part_bf16 = sse::delta_chunked_partials_bf16(c) ? 1 : 0;  // the chunked form writes bf16 partials
     return sse::launch_combine(c, fa, s) == cudaSuccess ? SSE_OK : SSE_ERR_CUDA;
 }
 

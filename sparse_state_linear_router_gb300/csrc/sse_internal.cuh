@@ -371,6 +371,10 @@ cudaError_t launch_delta_forward(const sse_config_t &cfg, const DeltaArgs &a, cu
 // Chunked delta-rule forward on the tensor cores (delta_chunked.cu): bf16, c = d = 128.
 bool delta_chunked_supported(const sse_config_t &cfg);
 cudaError_t launch_delta_chunked(const sse_config_t &cfg, const DeltaArgs &a, cudaStream_t stream);
+// Whether sse_delta_forward takes the chunked form (which writes bf16 partial rows).
+inline bool delta_chunked_partials_bf16(const sse_config_t &cfg) {
+    return cfg.algo != SSE_ALGO_RECURRENT && delta_chunked_supported(cfg);
+}
 cudaError_t launch_delta_decode(const sse_config_t &cfg, const DeltaDecodeArgs &a, cudaStream_t stream);
 
 bool decode_supported(const sse_config_t &cfg);
