@@ -13,11 +13,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsse.so")
-# Checked build for the failure-detection test: fwd_chunked.cu compiled with
-# -DSSE_FAULT_INJECT (short bounded waits, a switch that withholds one
-# barrier arrival), linked with the same objects as libsse.so.
+# Checked build for the failure-detection test: the persistent tensor-core
+# kernels compiled with -DSSE_FAULT_INJECT (short bounded waits, a switch
+# that withholds one barrier arrival or one product round), linked with the
+# same objects as libsse.so otherwise.
 LIB_CHECKED = os.path.join(BUILD, "libsse_checked.so")
-CHECKED_SRC = "fwd_chunked.cu"
+CHECKED_SRCS = ("fwd_chunked.cu", "delta_chunked.cu")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -62,14 +63,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 print(r.stdout + r.stderr)
         return obj
 
-    checked_src = os.path.join(CSRC, CHECKED_SRC)
-    jobs = [(src, False) for src in srcs] + [(checked_src, True)]
+    checked_srcs = [os.path.join(CSRC, n) for n in CHECKED_SRCS]
+    jobs = [(src, False) for src in srcs] + [(src, True) for src in checked_srcs]
     # the largest translation units first, so the parallel compile ends sooner
     jobs.sort(key=lambda j: -os.path.getsize(j[0]))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
         done = dict(zip(jobs, ex.map(compile_one, jobs)))
     objs = [done[(src, False)] for src in srcs]
-    checked_objs = [done[(checked_src, True)] if src == checked_src else done[(src, False)] for src in srcs]
+    checked_objs = [done[(src, src in checked_srcs)] for src in srcs]
     for lib, lib_objs in ((LIB, objs), (LIB_CHECKED, checked_objs)):
         if force or _stale(lib, lib_objs):
             tmp = lib + ".tmp.%d" % os.getpid()

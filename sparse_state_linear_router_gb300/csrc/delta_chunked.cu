@@ -49,7 +49,17 @@ constexpr int kNB = kRows / 16;               // 16-row blocks of the chunk
 constexpr int kRS = 20;                       // floats per stored block row (16 used; rows 16-byte aligned)
 constexpr int kBS = 16 * kRS + 4;             // floats per stored 16 x 16 block (+4: consecutive blocks 4 banks apart)
 constexpr int kNBlk = kNB * (kNB + 1) / 2;    // lower blocks, diagonal included
+#ifdef SSE_FAULT_INJECT
+// Checked build (libsse_checked.so, for the failure-detection test only):
+// every bounded wait gives up after 50 ms, and g_delta_fault_mode = 1 makes
+// CTA 0 issue neither the first product round of its first chunk nor its
+// commit, so that the wait on it runs out and the kernel takes its abort path
+// (SSE_DEVICE_TIMEOUT, TMEM freed) with no product in flight.
+__device__ int g_delta_fault_mode = 0;
+constexpr uint64_t kWait = 50000000ull;
+#else
 constexpr uint64_t kWait = 2000000000ull;
+#endif
 
 __device__ __forceinline__ int blkidx(int I, int K) { return I * (I + 1) / 2 + K; }
 
@@ -100,11 +110,11 @@ constexpr size_t delta_smem_bytes() {
 // generic proxy before the call are made visible to the tensor core first.
 // Returns false, in every thread, when the wait ran out.
 template <typename F>
-__device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue) {
+__device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue, bool withhold = false) {
     fence_proxy_async();
     fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !withhold) {
         fence_after();
         issue();
         commit(c.bar);
@@ -163,6 +173,9 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
     const int P = N + use_shared;
     int32_t *counter = flags + 1;
     float *patch = c.patch + warp * 32 * kPatchStride;
+#ifdef SSE_FAULT_INJECT
+    bool first_chunk = true;  // of this CTA (the checked build's fault switch)
+#endif
 
     for (;;) {
         if (tid == 0) *c.item = atomicAdd(counter, 1);
@@ -288,6 +301,12 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
             }
             cp_async_wait_all();
             // ---- products 1: A1 = K K^T, A2 = Q K^T, Y = K S0 ----
+#ifdef SSE_FAULT_INJECT
+            const bool withhold = g_delta_fault_mode == 1 && blockIdx.x == 0 && first_chunk;
+            first_chunk = false;
+#else
+            const bool withhold = false;
+#endif
             bool ok = run_mma(c, phase, [&] {
                 constexpr uint32_t idT = idesc_bf16(128, 128, 0, 0), idS = idesc_bf16(128, kD, 0, 1);
                 for (int k16 = 0; k16 < kC; k16 += 16) {
@@ -299,7 +318,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     mma_bf16(tO, desc_sw128(smem_u32(c.tK) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
                              idS, k16 > 0);
                 }
-            });
+            }, withhold);
             if (!ok) {
                 failed = true;
                 break;
@@ -700,3 +719,12 @@ cudaError_t launch_delta_chunked(const sse_config_t &cfg, const DeltaArgs &a, cu
 }
 
 }  // namespace sse
+
+#ifdef SSE_FAULT_INJECT
+// Checked build only: sets the fault mode read by delta_chunked_kernel (0 =
+// none, 1 = CTA 0 withholds its first product round).  Returns the CUDA error
+// of the copy.
+extern "C" int sse_debug_set_delta_fault(int mode) {
+    return (int)cudaMemcpyToSymbol(sse::g_delta_fault_mode, &mode, sizeof(int));
+}
+#endif

@@ -1,14 +1,15 @@
-"""Failure detection of the tensor-core forward, exercised without a GPU
+"""Failure detection of the tensor-core forwards, exercised without a GPU
 fault (marked gpu).
 
-The checked build (libsse_checked.so: fwd_chunked.cu with -DSSE_FAULT_INJECT)
-gives every bounded wait of the kernel a 50 ms limit and has a switch that
-makes CTA 0's transform warps withhold one barrier arrival ("Qt / Kt
-written" of its first chunk).  The waits on it then run out; the kernel's
-roles stop together, free their tensor memory and return; the host reads
-SSE_ERR_DEVICE_TIMEOUT.  The next call on the same workspace and stream, with
-the switch off, must be correct.  Nothing traps, faults or waits without a
-limit."""
+The checked build (libsse_checked.so: fwd_chunked.cu and delta_chunked.cu
+with -DSSE_FAULT_INJECT) gives every bounded wait of those kernels a 50 ms
+limit and has a switch per kernel: CTA 0's transform warps withhold one
+barrier arrival ("Qt / Kt written" of its first chunk), or CTA 0 of the
+delta-rule kernel issues neither its first product round nor its commit.
+The waits then run out; the kernel stops, frees its tensor memory and
+returns; the host reads SSE_ERR_DEVICE_TIMEOUT.  The next call on the same
+workspace and stream, with the switch off, must be correct.  Nothing traps,
+faults or waits without a limit."""
 import ctypes
 import os
 
@@ -43,8 +44,15 @@ def checked():
     lib.sse_get_last_device_error.argtypes = [P, P]
     lib.sse_debug_set_fault.restype = ctypes.c_int
     lib.sse_debug_set_fault.argtypes = [ctypes.c_int]
+    lib.sse_debug_set_delta_fault.restype = ctypes.c_int
+    lib.sse_debug_set_delta_fault.argtypes = [ctypes.c_int]
+    lib.sse_delta_forward_workspace_size.restype = sz
+    lib.sse_delta_forward_workspace_size.argtypes = [cfgp, i64, i32]
+    lib.sse_delta_forward.restype = ctypes.c_int
+    lib.sse_delta_forward.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, i32, i64, P, P, P, P, P, P, sz, P]
     yield lib
     lib.sse_debug_set_fault(0)
+    lib.sse_debug_set_delta_fault(0)
 
 
 def test_timeout_is_reported_and_the_next_call_is_correct(checked):
@@ -87,3 +95,43 @@ def test_timeout_is_reported_and_the_next_call_is_correct(checked):
     assert H_.max_abs_rel(H_.to_numpy(out), ref["out"]) < H_.TOL_BF16
     assert H_.max_abs_rel(H_.to_numpy(fin), ref["final_state"]) < H_.TOL_BF16
     assert np.all(np.isfinite(H_.to_numpy(out)))
+
+
+def test_delta_timeout_is_reported_and_the_next_call_is_correct(checked):
+    from oracle import delta as dl
+    from sparse_state_linear_router_gb300 import binding
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=4, top_k=2)
+    inp = synth.make_delta_inputs(w, seed=11, lengths=[300, 129, 77], with_init=True)
+    cfg = H_.config_of(w)  # the chunked form (bf16, c = d = 128)
+    T, S, H = inp.total_tokens, inp.num_seqs, w.num_heads
+    t = {n: binding.to_device(getattr(inp, n)) for n in ("q", "k", "v", "log_alpha", "beta", "logits")}
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    init = torch.from_numpy(inp.init_state).cuda()
+    out = torch.empty((T, H, w.value_dim), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty((S, H, w.num_slots, w.key_dim, w.value_dim), dtype=torch.float32, device="cuda")
+    nbytes = checked.sse_delta_forward_workspace_size(ctypes.byref(cfg), T, S)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = binding._stream()
+
+    def call():
+        st = checked.sse_delta_forward(ctypes.byref(cfg), t["q"].data_ptr(), t["k"].data_ptr(), t["v"].data_ptr(),
+                                       t["log_alpha"].data_ptr(), t["beta"].data_ptr(), t["logits"].data_ptr(),
+                                       None, None, cu.data_ptr(), S, T, init.data_ptr(), fin.data_ptr(),
+                                       out.data_ptr(), None, None, ws.data_ptr(), nbytes, stream)
+        assert st == binding.SSE_OK
+        flags = ctypes.c_int32(0)
+        status = checked.sse_read_device_status(ws.data_ptr(), ctypes.byref(flags), stream)
+        return status, flags.value
+
+    assert checked.sse_debug_set_delta_fault(1) == 0
+    status, flags = call()          # returns: CTA 0 gave up its wait and exited
+    assert status == binding.SSE_ERR_DEVICE_TIMEOUT, (status, flags)
+    assert flags & binding.SSE_DEVICE_TIMEOUT
+
+    assert checked.sse_debug_set_delta_fault(0) == 0
+    status, flags = call()          # same workspace and stream, no fault
+    assert status == binding.SSE_OK and flags == 0, (status, flags)
+    ref = dl.delta_forward(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.logits, inp.cu_seqlens,
+                           top_k=w.top_k, use_shared=w.use_shared, scale=1.0, initial_state=inp.init_state)
+    assert H_.max_abs_rel(H_.to_numpy(out), ref["out"]) < H_.TOL_BF16
+    assert H_.max_abs_rel(H_.to_numpy(fin), ref["final_state"]) < H_.TOL_BF16
