@@ -49,6 +49,12 @@ constexpr int kNB = kRows / 16;               // 16-row blocks of the chunk
 constexpr int kRS = 20;                       // floats per stored block row (16 used; rows 16-byte aligned)
 constexpr int kBS = 16 * kRS + 4;             // floats per stored 16 x 16 block (+4: consecutive blocks 4 banks apart)
 constexpr int kNBlk = kNB * (kNB + 1) / 2;    // lower blocks, diagonal included
+// Gamma_ts = exp(G_t - G_s) is formed as exp(G_t - G_m) exp(G_m - G_s) around
+// the chunk's midpoint row m when every |G - G_m| of the chunk is at most
+// kFacRange (each factor then stays within float32, their product is at most
+// 1); a chunk with stronger decay takes one exponential per element.
+constexpr int kMidRow = kRows / 2 - 1;
+constexpr float kFacRange = 60.f;
 #ifdef SSE_FAULT_INJECT
 // Checked build (libsse_checked.so, for the failure-detection test only):
 // every bounded wait gives up after 50 ms, and g_delta_fault_mode = 1 makes
@@ -72,7 +78,7 @@ struct DSmem {
     unsigned char *tQ, *tK, *tV, *tS, *tT;
     float *blk, *zs;
     int *tok, *slotj;
-    float *G, *b, *qf, *red, *patch;
+    float *G, *b, *qf, *ec, *red, *patch;
     uint32_t bar;
     uint32_t *tslot;
     int *item;
@@ -92,7 +98,8 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     c.G = reinterpret_cast<float *>(c.slotj + kRows);
     c.b = c.G + kRows;
     c.qf = c.b + kRows;
-    c.red = c.qf + kRows;   // [8]
+    c.ec = c.qf + kRows;    // exp(G_m - G_s) of the chunk's rows s (the column factors of Gamma)
+    c.red = c.ec + kRows;   // [8]
     c.patch = reinterpret_cast<float *>(c.tT);  // [8 warps][32][kPatchStride] in the T / P tile
     uint64_t *bar = reinterpret_cast<uint64_t *>(c.red + 8);
     c.bar = smem_u32(bar);
@@ -101,7 +108,7 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     return c;
 }
 constexpr size_t delta_smem_bytes() {
-    return 1024 + 5 * (size_t)kTile + (size_t)(kNBlk + kNB) * kBS * 4 + 2 * kRows * 4 + 3 * kRows * 4 + 8 * 4 + 16 +
+    return 1024 + 5 * (size_t)kTile + (size_t)(kNBlk + kNB) * kBS * 4 + 2 * kRows * 4 + 4 * kRows * 4 + 8 * 4 + 16 +
            16;
 }
 
@@ -263,13 +270,18 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 const float y = __shfl_up_sync(0xffffffffu, lg, o);
                 if (lane >= o) lg += y;
             }
-            if (lane == 31) c.red[warp] = lg;
+            if (lane == 31) c.red[warp] = lg;  // warps 4..7 write zeros: red[7] starts clear
             __syncthreads();
             if (tid < kRows) {
                 for (int w2 = 0; w2 < warp; ++w2) lg += c.red[w2];
                 c.G[tid] = lg;
             }
             __syncthreads();
+            if (tid < kRows) {  // read after the next barrier, with red[7]'s range flag (zeroed by the scan)
+                const float dG = c.G[kMidRow] - c.G[tid];
+                c.ec[tid] = __expf(dG);
+                if (!(fabsf(dG) <= kFacRange)) c.red[7] = 1.f;
+            }
             stage_rows(c.tQ, qsrc, c.tok, H, h, kC);
             stage_rows(c.tK, ksrc, c.tok, H, h, kC);
             stage_rows(c.tV, v, c.tok, H, h, kD);
@@ -324,25 +336,44 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 break;
             }
             // ---- L blocks from A1; R = V - gamma Y in place of V; Q scaled by qf gamma in place ----
+            const float Gm = c.G[kMidRow];
+            const bool fac = c.red[7] == 0.f;  // every |G - G_m| of the chunk within kFacRange (uniform)
             {
                 const int t = erow;
                 const float Gt = c.G[t], bt_ = c.b[t], gt = __expf(Gt), qg = c.qf[t] * gt;
+                const float ber = bt_ * __expf(Gt - Gm);  // b_t exp(G_t - G_m)
                 for (int g = 0; g < 2; ++g) {
                     const int col0 = 64 * hc + 32 * g;
                     uint32_t x[32];
                     __syncwarp();
                     tmem_ld32(tA1 + lb + col0, x);
                     tmem_wait_ld();
+                    float *lrow = c.blk + (t & 15) * kRS;
+                    if (fac) {
 #pragma unroll
-                    for (int i4 = 0; i4 < 8; ++i4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(c.G + col0 + 4 * i4);
-                        const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 e4 = *reinterpret_cast<const float4 *>(c.ec + col0 + 4 * i4);
+                            const float es[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int s = col0 + 4 * i4 + i;
-                            if (s < t)
-                                c.blk[blkidx(t >> 4, s >> 4) * kBS + (t & 15) * kRS + (s & 15)] =
-                                    bt_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]);
+                            for (int i = 0; i < 4; ++i) {
+                                const int s = col0 + 4 * i4 + i;
+                                if (s < t)
+                                    lrow[blkidx(t >> 4, s >> 4) * kBS + (s & 15)] =
+                                        ber * es[i] * __uint_as_float(x[4 * i4 + i]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(c.G + col0 + 4 * i4);
+                            const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int s = col0 + 4 * i4 + i;
+                                if (s < t)
+                                    lrow[blkidx(t >> 4, s >> 4) * kBS + (s & 15)] =
+                                        bt_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]);
+                            }
                         }
                     }
                     __syncwarp();
@@ -581,6 +612,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 const int t = erow;
                 const float Gt = c.G[t], qft = c.qf[t], GC = c.G[kRows - 1];
                 const float kf = __expf(GC - Gt);
+                const float qer = qft * __expf(Gt - Gm);  // qf_t exp(G_t - G_m)
                 for (int g = 0; g < 2; ++g) {
                     const int col0 = 64 * hc + 32 * g;
                     uint32_t x[32];
@@ -600,13 +632,24 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
 #pragma unroll
                     for (int j8 = 0; j8 < 4; ++j8) {
                         float f[8];
-                        const float4 g0 = *reinterpret_cast<const float4 *>(c.G + col0 + 8 * j8);
-                        const float4 g1 = *reinterpret_cast<const float4 *>(c.G + col0 + 8 * j8 + 4);
-                        const float gs[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                        if (fac) {
+                            const float4 e0 = *reinterpret_cast<const float4 *>(c.ec + col0 + 8 * j8);
+                            const float4 e1 = *reinterpret_cast<const float4 *>(c.ec + col0 + 8 * j8 + 4);
+                            const float es[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int s = col0 + 8 * j8 + i;
-                            f[i] = s <= t ? qft * __expf(Gt - gs[i]) * __uint_as_float(x[8 * j8 + i]) : 0.f;
+                            for (int i = 0; i < 8; ++i) {
+                                const int s = col0 + 8 * j8 + i;
+                                f[i] = s <= t ? qer * es[i] * __uint_as_float(x[8 * j8 + i]) : 0.f;
+                            }
+                        } else {
+                            const float4 g0 = *reinterpret_cast<const float4 *>(c.G + col0 + 8 * j8);
+                            const float4 g1 = *reinterpret_cast<const float4 *>(c.G + col0 + 8 * j8 + 4);
+                            const float gs[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int s = col0 + 8 * j8 + i;
+                                f[i] = s <= t ? qft * __expf(Gt - gs[i]) * __uint_as_float(x[8 * j8 + i]) : 0.f;
+                            }
                         }
                         st8(c.tT + toff(t, col0 + 8 * j8), f);
                         unsigned char *pk = c.tK + toff(t, col0 + 8 * j8);

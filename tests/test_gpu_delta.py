@@ -78,6 +78,24 @@ def test_delta_forward_matches_oracle(name, algo):
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < tol
 
 
+@pytest.mark.parametrize("algo", ["auto", "recurrent"])
+def test_delta_forward_strong_and_mild_decay(algo):
+    """Chunks whose summed log-decay spans more than 60 either side of their
+    midpoint (log-gates of -1.5 on every row of the first 300 tokens) beside
+    chunks of the mild recipe: the chunked form forms their decay factors one
+    element at a time, the others around the midpoint; both must match."""
+    w = H_.workload_variant("layer_bf16", num_heads=2, num_partitions=4, top_k=1)
+    inp = synth.make_delta_inputs(w, seed=8, lengths=[700, 260], with_init=True)
+    la = synth.bf16_bits_to_f32(inp.log_alpha)
+    la[:300] = -1.5
+    la[760:800] = -4.0
+    inp.log_alpha = synth.f32_to_bf16_bits(la)
+    gpu, ref = _gpu(w, inp, algo=algo), _ref(w, inp)
+    assert np.array_equal(gpu["topk_idx"], ref["topk_idx"])
+    assert H_.max_abs_rel(gpu["out"], ref["out"]) < H_.TOL_BF16
+    assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < H_.TOL_BF16
+
+
 @pytest.mark.parametrize("wname,over,algo", [("small_bf16", {"num_heads": 2}, "auto"),
                                              ("layer_bf16", {"num_heads": 1}, "auto"),
                                              ("layer_bf16", {"num_heads": 1}, "recurrent")])
