@@ -451,25 +451,34 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     return (a0 + a1) + (a2 + a3);
                 };
                 float *z0 = c.zs + rr * kRS + cc;  // this thread's elements of scratch block I: z0[I kBS], z0[I kBS + 8 kRS]
+#pragma unroll
                 for (int J = 2; J >= 0; --J) {
+                    float za[4][2];  // this thread's two elements of Z_I, I = J+1..3
+#pragma unroll
                     for (int K = J + 1; K < 4; ++K) {
                         float lcol[16];
                         const float *lc = c.blk + blkidx(B0 + K, B0 + J) * kBS + cc;
 #pragma unroll
                         for (int m = 0; m < 16; ++m) lcol[m] = lc[m * kRS];
+#pragma unroll
                         for (int I = K; I < 4; ++I) {
                             const float *xb = c.blk + blkidx(B0 + I, B0 + K) * kBS + rr * kRS;
                             const float d0 = row_dot(xb, lcol), d1 = row_dot(xb + 8 * kRS, lcol);
-                            float *z = z0 + (B0 + I) * kBS;
-                            z[0] = K == J + 1 ? d0 : z[0] + d0;
-                            z[8 * kRS] = K == J + 1 ? d1 : z[8 * kRS] + d1;
+                            za[I][0] = K == J + 1 ? d0 : za[I][0] + d0;
+                            za[I][1] = K == J + 1 ? d1 : za[I][1] + d1;
                         }
+                    }
+#pragma unroll
+                    for (int I = J + 1; I < 4; ++I) {
+                        z0[(B0 + I) * kBS] = za[I][0];
+                        z0[(B0 + I) * kBS + 8 * kRS] = za[I][1];
                     }
                     __syncthreads();  // every Z of column J is complete and every read of L[K][J] done
                     float xcol[16];
                     const float *xd = c.blk + blkidx(B0 + J, B0 + J) * kBS + cc;
 #pragma unroll
                     for (int m = 0; m < 16; ++m) xcol[m] = xd[m * kRS];
+#pragma unroll
                     for (int I = J + 1; I < 4; ++I) {
                         float *xo = c.blk + blkidx(B0 + I, B0 + J) * kBS + rr * kRS + cc;
                         const float *zr = c.zs + (B0 + I) * kBS + rr * kRS;
