@@ -133,7 +133,56 @@ __device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue
     return __syncthreads_and(ok) != 0;
 }
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+// Loads kept where they are written (volatile: the compiler neither sinks them
+// towards their use nor merges them), for metadata fetched a phase or a chunk
+// before it is needed.
+__device__ __forceinline__ int ld_early_s32(const int32_t *p) {
+    int v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_early_f32(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_early_bf16(const __nv_bfloat16 *p) {
+    unsigned short u;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
+    return __uint_as_float((uint32_t)u << 16);
+}
+
+// The chunk's q, k and v rows (128 x 128 bf16 each) into their swizzled
+// tiles by 16-byte asynchronous copies (zero-filled for rows past the item's
+// end): thread tid copies piece tid % 16 of rows tid / 16 + 16 i, i = 0..7,
+// whose tile offsets differ by 16 rows = two 8-row groups = 4096 bytes.
+__device__ __forceinline__ void stage_qkv(const DSmem &c, const __nv_bfloat16 *qsrc, const __nv_bfloat16 *ksrc,
+                                          const __nv_bfloat16 *v, int H, int h) {
+    const int r0 = threadIdx.x >> 4, c8 = threadIdx.x & 15;
+    const uint32_t o0 = toff(r0, c8 * 8);
+    int64_t src[8];
+    bool ok[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int t = c.tok[r0 + 16 * i];
+        ok[i] = t >= 0;
+        src[i] = ok[i] ? ((int64_t)t * H + h) * 128 + c8 * 8 : 0;
+    }
+    const uint32_t dq = smem_u32(c.tQ) + o0, dk = smem_u32(c.tK) + o0, dv = smem_u32(c.tV) + o0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        cp_async16(dq + 4096 * i, qsrc + src[i], ok[i]);
+        cp_async16(dk + 4096 * i, ksrc + src[i], ok[i]);
+        cp_async16(dv + 4096 * i, v + src[i], ok[i]);
+    }
+}
+
+// L2 prefetch of one 256-byte bf16 row of 128 elements (two 128-byte lines; no
+// completion to wait for)
+__device__ __forceinline__ void prefetch_row_l2(const __nv_bfloat16 *row) {
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(row));
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(row + 64));
+}
 
 // 8 consecutive bf16 of a tile row (16 bytes) <-> float32
 __device__ __forceinline__ void ld8(const unsigned char *p, float (&f)[8]) {
@@ -236,33 +285,51 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
         }
         tmem_wait_st();
 
-        // row metadata and the running log-decay G (inclusive) of chunk ch, then
-        // its q, k, v rows by asynchronous copies (waited for before products 1)
+        // Row tid's metadata of the next chunk, fetched a chunk ahead in two
+        // steps so that no warp waits on a dependent load: the grouped record
+        // first, then (a few phases later) the token's router weight, gates and
+        // an L2 prefetch of its q, k, v rows, which the copies of prepare then
+        // find in L2.
+        int nrec = 0, nt = -1, njj = 0;
+        float ne = 0.f, nbeta = 0.f, nlg = 0.f;
+        auto fetch_rec = [&](int ch) {
+            const int idx = ch * kRows + tid;
+            if (!shared && tid < kRows && idx < len) nrec = ld_early_s32(a.perm_rec + base + idx);
+        };
+        auto fetch_rest = [&](int ch) {
+            const int idx = ch * kRows + tid;
+            nt = -1;
+            njj = 0;
+            ne = nbeta = nlg = 0.f;
+            if (tid < kRows && idx < len) {
+                if (shared) {
+                    nt = base + idx;
+                    ne = 1.f;
+                } else {
+                    nt = nrec / topk;
+                    njj = nrec - nt * topk;
+                    ne = ld_early_f32(a.topk_w + ((int64_t)nt * H + h) * topk + njj);
+                }
+                const int64_t th = (int64_t)nt * H + h;
+                nlg = ld_early_bf16(la + th);
+                nbeta = ld_early_bf16(bt + th);
+                prefetch_row_l2(qsrc + th * kC);
+                prefetch_row_l2(ksrc + th * kC);
+                prefetch_row_l2(v + th * kD);
+            }
+        };
+        // row metadata (fetched ahead) and the running log-decay G (inclusive)
+        // of chunk ch, then its q, k, v rows by asynchronous copies (waited for
+        // before products 1)
         auto prepare = [&](int ch) {
             __syncthreads();  // every reader of the metadata and of the Q, K, V tiles is done
             float lg = 0.f;
             if (tid < kRows) {
-                const int idx = ch * kRows + tid;
-                int t = -1, jj = 0;
-                float e = 0.f, beta = 0.f;
-                if (idx < len) {
-                    if (shared) {
-                        t = base + idx;
-                        e = 1.f;
-                    } else {
-                        const int rec = a.perm_rec[base + idx];
-                        t = rec / topk;
-                        jj = rec - t * topk;
-                        e = a.topk_w[((int64_t)t * H + h) * topk + jj];
-                    }
-                    const int64_t th = (int64_t)t * H + h;
-                    lg = bf(la + th);
-                    beta = bf(bt + th);
-                }
-                c.tok[tid] = t;
-                c.slotj[tid] = jj;
-                c.b[tid] = e * beta;
-                c.qf[tid] = e * scale;
+                c.tok[tid] = nt;
+                c.slotj[tid] = njj;
+                c.b[tid] = ne * nbeta;
+                c.qf[tid] = ne * scale;
+                lg = nlg;
             }
             // inclusive scan of lg over rows 0..127 (warps 0..3)
 #pragma unroll
@@ -282,11 +349,11 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 c.ec[tid] = __expf(dG);
                 if (!(fabsf(dG) <= kFacRange)) c.red[7] = 1.f;
             }
-            stage_rows(c.tQ, qsrc, c.tok, H, h, kC);
-            stage_rows(c.tK, ksrc, c.tok, H, h, kC);
-            stage_rows(c.tV, v, c.tok, H, h, kD);
+            stage_qkv(c, qsrc, ksrc, v, H, h);
         };
         const int nch = (len + kRows - 1) / kRows;
+        fetch_rec(0);
+        fetch_rest(0);
         prepare(0);
         for (int ch = 0; ch < nch; ++ch) {
             // ---- the state's bf16 copy and the decay of the chunk, while the rows land ----
@@ -312,6 +379,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 tmem_wait_st();
             }
             cp_async_wait_all();
+            if (ch + 1 < nch) fetch_rec(ch + 1);
             // ---- products 1: A1 = K K^T, A2 = Q K^T, Y = K S0 ----
 #ifdef SSE_FAULT_INJECT
             const bool withhold = g_delta_fault_mode == 1 && blockIdx.x == 0 && first_chunk;
@@ -409,6 +477,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 }
                 commit(c.bar);
             }
+            if (ch + 1 < nch) fetch_rest(ch + 1);
             // ---- the inverse of I + L: diagonal blocks, one warp each ----
             {
                 float *bd = c.blk + blkidx(warp, warp) * kBS;
