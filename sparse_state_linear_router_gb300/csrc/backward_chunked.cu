@@ -230,11 +230,8 @@ bwd_chunk_sums_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32_
         chunk_meta(a, r, topk, c, mb);
         __syncthreads();
         const int *tok = c.tok + mb * kRows;
-        stage_rows(tK, r.shared && ks ? ks : k, tok, H, r.h, kKey);
-        stage_rows(tQ, r.shared && qs ? qs : q, tok, H, r.h, kKey);
-        stage_rows(tG, g, tok, H, r.h, kKey);
-        stage_rows(tV, v, tok, H, r.h, DV);
-        stage_rows(tD, dout, tok, H, r.h, DV);
+        stage_rows_n<kKey, 3>({tK, tQ, tG}, {r.shared && ks ? ks : k, r.shared && qs ? qs : q, g}, tok, H, r.h);
+        stage_rows_n<DV, 2>({tV, tD}, {v, dout}, tok, H, r.h);
     };
     int64_t chunk = blockIdx.x;
     ChunkRef r;
@@ -467,11 +464,8 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
         chunk_meta(a, r, topk, c, mb);
         __syncthreads();
         const int *tok = c.tok + mb * kRows;
-        stage_rows(tQ, r.shared && qs ? qs : q, tok, H, r.h, kKey);
-        stage_rows(tK, r.shared && ks ? ks : k, tok, H, r.h, kKey);
-        stage_rows(tA, g, tok, H, r.h, kKey);
-        stage_rows(tV, v, tok, H, r.h, DV);
-        stage_rows(tD, dout, tok, H, r.h, DV);
+        stage_rows_n<kKey, 3>({tQ, tK, tA}, {r.shared && qs ? qs : q, r.shared && ks ? ks : k, g}, tok, H, r.h);
+        stage_rows_n<DV, 2>({tV, tD}, {v, dout}, tok, H, r.h);
     };
     int64_t chunk = blockIdx.x;
     ChunkRef r;

@@ -23,9 +23,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // columns: two 64-column atoms per 8-row group, 128-byte swizzle
 __device__ __forceinline__ uint32_t toff(int row, int col) { return sw128_offset(row, col, 2); }
 
-// Rows of a [T * H, width] bf16 tensor into a swizzled tile by 16-byte
-// asynchronous copies (zero-filled for token -1: nothing is read there), all
-// threads of the CTA; the caller waits with cp_async_wait_all().
+// 16-byte asynchronous copies into shared memory (zero-filled when !valid:
+// nothing is read there); the caller waits with cp_async_wait_all().
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0)
                  : "memory");
@@ -33,14 +32,36 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
-__device__ __forceinline__ void stage_rows(unsigned char *tile, const __nv_bfloat16 *src, const int *tok, int H, int h,
-                                           int width) {
-    const int pieces = width / 8;
-    for (int x = threadIdx.x; x < kChunkRows * pieces; x += blockDim.x) {
-        const int r = x / pieces, c8 = x - r * pieces;
-        const int t = tok[r];
-        const __nv_bfloat16 *p = t >= 0 ? src + ((int64_t)t * H + h) * width + c8 * 8 : src;
-        cp_async16(smem_u32(tile + toff(r, c8 * 8)), p, t >= 0);
+
+// The 128 rows tok[0..127] of NT [T * H, W] bf16 tensors (W = 64 or 128) into
+// their swizzled tiles by 16-byte asynchronous copies, zero-filled for token
+// -1, by a CTA of exactly 256 threads; the caller waits with
+// cp_async_wait_all().  Thread x copies piece x % (W / 8) of rows
+// x / (W / 8) + (256 / (W / 8)) i: one token lookup per row serves all NT
+// tensors, and the tile offsets of a thread's rows step by whole 8-row groups
+// (the swizzle of row r depends on r % 8 only), so the pass is a few
+// instructions per copy.
+template <int W, int NT>
+__device__ __forceinline__ void stage_rows_n(unsigned char *const (&tiles)[NT], const __nv_bfloat16 *const (&srcs)[NT],
+                                             const int *tok, int H, int h) {
+    static_assert(W == 64 || W == 128, "row width");
+    constexpr int kPieces = W / 8, kRowsPerPass = 256 / kPieces, kPasses = kChunkRows / kRowsPerPass;
+    constexpr uint32_t kStep = (kRowsPerPass / 8) * 2048;  // bytes between a thread's rows
+    const int r0 = threadIdx.x / kPieces, c8 = threadIdx.x % kPieces;
+    const uint32_t o0 = toff(r0, c8 * 8);
+    int64_t src[kPasses];
+    bool ok[kPasses];
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+        const int t = tok[r0 + kRowsPerPass * i];
+        ok[i] = t >= 0;
+        src[i] = ok[i] ? ((int64_t)t * H + h) * W + c8 * 8 : 0;
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const uint32_t d = smem_u32(tiles[n]) + o0;
+#pragma unroll
+        for (int i = 0; i < kPasses; ++i) cp_async16(d + kStep * i, srcs[n] + src[i], ok[i]);
     }
 }
 

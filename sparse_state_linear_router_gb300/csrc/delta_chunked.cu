@@ -152,31 +152,6 @@ __device__ __forceinline__ float ld_early_bf16(const __nv_bfloat16 *p) {
     return __uint_as_float((uint32_t)u << 16);
 }
 
-// The chunk's q, k and v rows (128 x 128 bf16 each) into their swizzled
-// tiles by 16-byte asynchronous copies (zero-filled for rows past the item's
-// end): thread tid copies piece tid % 16 of rows tid / 16 + 16 i, i = 0..7,
-// whose tile offsets differ by 16 rows = two 8-row groups = 4096 bytes.
-__device__ __forceinline__ void stage_qkv(const DSmem &c, const __nv_bfloat16 *qsrc, const __nv_bfloat16 *ksrc,
-                                          const __nv_bfloat16 *v, int H, int h) {
-    const int r0 = threadIdx.x >> 4, c8 = threadIdx.x & 15;
-    const uint32_t o0 = toff(r0, c8 * 8);
-    int64_t src[8];
-    bool ok[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int t = c.tok[r0 + 16 * i];
-        ok[i] = t >= 0;
-        src[i] = ok[i] ? ((int64_t)t * H + h) * 128 + c8 * 8 : 0;
-    }
-    const uint32_t dq = smem_u32(c.tQ) + o0, dk = smem_u32(c.tK) + o0, dv = smem_u32(c.tV) + o0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        cp_async16(dq + 4096 * i, qsrc + src[i], ok[i]);
-        cp_async16(dk + 4096 * i, ksrc + src[i], ok[i]);
-        cp_async16(dv + 4096 * i, v + src[i], ok[i]);
-    }
-}
-
 // L2 prefetch of one 256-byte bf16 row of 128 elements (two 128-byte lines; no
 // completion to wait for)
 __device__ __forceinline__ void prefetch_row_l2(const __nv_bfloat16 *row) {
@@ -349,7 +324,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 c.ec[tid] = __expf(dG);
                 if (!(fabsf(dG) <= kFacRange)) c.red[7] = 1.f;
             }
-            stage_qkv(c, qsrc, ksrc, v, H, h);
+            stage_rows_n<128, 3>({c.tQ, c.tK, c.tV}, {qsrc, ksrc, v}, c.tok, H, h);
         };
         const int nch = (len + kRows - 1) / kRows;
         fetch_rec(0);
