@@ -113,11 +113,16 @@ constexpr size_t delta_smem_bytes() {
 }
 
 // One elected thread issues the products, commits them to the CTA's mbarrier
-// and every thread waits (bounded).  Shared-memory operands written by the
-// generic proxy before the call are made visible to the tensor core first.
-// Returns false, in every thread, when the wait ran out.
-template <typename F>
-__device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue, bool withhold = false) {
+// and every thread runs `during` (work that touches neither the products'
+// operands nor their results) and then waits (bounded).  Shared-memory
+// operands written by the generic proxy before the call are made visible to
+// the tensor core first.  Returns false, in every thread, when the wait ran out.
+struct NoWork {
+    __device__ void operator()() const {}
+};
+template <typename F, typename D = NoWork>
+__device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue, bool withhold = false,
+                                        D during = D()) {
     fence_proxy_async();
     fence_before();
     __syncthreads();
@@ -127,6 +132,7 @@ __device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue
         commit(c.bar);
     }
     __syncwarp();
+    during();
     const bool ok = mbar_wait_bounded(c.bar, phase, kWait);
     phase ^= 1u;
     fence_after();
@@ -260,11 +266,11 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
         }
         tmem_wait_st();
 
-        // Row tid's metadata of the next chunk, fetched a chunk ahead in two
-        // steps so that no warp waits on a dependent load: the grouped record
-        // first, then (a few phases later) the token's router weight, gates and
-        // an L2 prefetch of its q, k, v rows, which the copies of prepare then
-        // find in L2.
+        // Row tid's metadata, fetched ahead in two steps so that no warp waits
+        // on a dependent load: the grouped record two chunks ahead, then (a
+        // chunk later, while the first products run) the token's router weight,
+        // gates and an L2 prefetch of its q, k, v rows, which the copies of
+        // prepare then find in L2.
         int nrec = 0, nt = -1, njj = 0;
         float ne = 0.f, nbeta = 0.f, nlg = 0.f;
         auto fetch_rec = [&](int ch) {
@@ -330,6 +336,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
         fetch_rec(0);
         fetch_rest(0);
         prepare(0);
+        if (nch > 1) fetch_rec(1);
         for (int ch = 0; ch < nch; ++ch) {
             // ---- the state's bf16 copy and the decay of the chunk, while the rows land ----
             {
@@ -354,7 +361,6 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 tmem_wait_st();
             }
             cp_async_wait_all();
-            if (ch + 1 < nch) fetch_rec(ch + 1);
             // ---- products 1: A1 = K K^T, A2 = Q K^T, Y = K S0 ----
 #ifdef SSE_FAULT_INJECT
             const bool withhold = g_delta_fault_mode == 1 && blockIdx.x == 0 && first_chunk;
@@ -373,7 +379,10 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     mma_bf16(tO, desc_sw128(smem_u32(c.tK) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
                              idS, k16 > 0);
                 }
-            }, withhold);
+            }, withhold, [&] {
+                if (ch + 1 < nch) fetch_rest(ch + 1);  // uses the record fetched a chunk ago
+                if (ch + 2 < nch) fetch_rec(ch + 2);
+            });
             if (!ok) {
                 failed = true;
                 break;
@@ -452,7 +461,6 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 }
                 commit(c.bar);
             }
-            if (ch + 1 < nch) fetch_rest(ch + 1);
             // ---- the inverse of I + L: diagonal blocks, one warp each ----
             {
                 float *bd = c.blk + blkidx(warp, warp) * kBS;
