@@ -400,33 +400,29 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     __syncwarp();
                     tmem_ld32(tA1 + lb + col0, x);
                     tmem_wait_ld();
+                    // row t of the lower blocks, four columns per 16-byte store (rows of
+                    // a warp 80 bytes apart: conflict-free); the entries on and above the
+                    // diagonal of a diagonal block are written as zeros (never read)
                     float *lrow = c.blk + (t & 15) * kRS;
-                    if (fac) {
 #pragma unroll
-                        for (int i4 = 0; i4 < 8; ++i4) {
-                            const float4 e4 = *reinterpret_cast<const float4 *>(c.ec + col0 + 4 * i4);
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const int s0 = col0 + 4 * i4;
+                        if ((s0 >> 4) > (t >> 4)) continue;  // a block above the diagonal: not stored
+                        float l[4];
+                        if (fac) {
+                            const float4 e4 = *reinterpret_cast<const float4 *>(c.ec + s0);
                             const float es[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int s = col0 + 4 * i4 + i;
-                                if (s < t)
-                                    lrow[blkidx(t >> 4, s >> 4) * kBS + (s & 15)] =
-                                        ber * es[i] * __uint_as_float(x[4 * i4 + i]);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int i4 = 0; i4 < 8; ++i4) {
-                            const float4 g4 = *reinterpret_cast<const float4 *>(c.G + col0 + 4 * i4);
+                            for (int i = 0; i < 4; ++i) l[i] = s0 + i < t ? ber * es[i] * __uint_as_float(x[4 * i4 + i]) : 0.f;
+                        } else {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(c.G + s0);
                             const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int s = col0 + 4 * i4 + i;
-                                if (s < t)
-                                    lrow[blkidx(t >> 4, s >> 4) * kBS + (s & 15)] =
-                                        bt_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]);
-                            }
+                            for (int i = 0; i < 4; ++i)
+                                l[i] = s0 + i < t ? bt_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]) : 0.f;
                         }
+                        *reinterpret_cast<float4 *>(lrow + blkidx(t >> 4, s0 >> 4) * kBS + (s0 & 15)) =
+                            make_float4(l[0], l[1], l[2], l[3]);
                     }
                     __syncwarp();
                     tmem_ld32(tO + lb + col0, x);
