@@ -393,7 +393,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
             {
                 const int t = erow;
                 const float Gt = c.G[t], bt_ = c.b[t], gt = __expf(Gt), qg = c.qf[t] * gt;
-                const float ber = bt_ * __expf(Gt - Gm);  // b_t exp(G_t - G_m)
+                const float erm = __expf(Gt - Gm), ber = bt_ * erm;  // exp(G_t - G_m), b_t exp(G_t - G_m)
                 for (int g = 0; g < 2; ++g) {
                     const int col0 = 64 * hc + 32 * g;
                     uint32_t x[32];
@@ -402,8 +402,12 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     tmem_wait_ld();
                     // row t of the lower blocks, four columns per 16-byte store (rows of
                     // a warp 80 bytes apart: conflict-free); the entries on and above the
-                    // diagonal of a diagonal block are written as zeros (never read)
+                    // diagonal of a diagonal block are written as zeros (never read).  The
+                    // lower-left quadrant (t >= 64, s < 64) holds M_ts = Gamma_ts (k_t . k_s),
+                    // L without its row factor b_t: only the quadrant's products read it.
                     float *lrow = c.blk + (t & 15) * kRS;
+                    const bool mq = t >= 64 && col0 < 64;  // uniform in the warp
+                    const float rf = mq ? erm : ber, bf_ = mq ? 1.f : bt_;
 #pragma unroll
                     for (int i4 = 0; i4 < 8; ++i4) {
                         const int s0 = col0 + 4 * i4;
@@ -413,13 +417,13 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                             const float4 e4 = *reinterpret_cast<const float4 *>(c.ec + s0);
                             const float es[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) l[i] = s0 + i < t ? ber * es[i] * __uint_as_float(x[4 * i4 + i]) : 0.f;
+                            for (int i = 0; i < 4; ++i) l[i] = s0 + i < t ? rf * es[i] * __uint_as_float(x[4 * i4 + i]) : 0.f;
                         } else {
                             const float4 g4 = *reinterpret_cast<const float4 *>(c.G + s0);
                             const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
-                                l[i] = s0 + i < t ? bt_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]) : 0.f;
+                                l[i] = s0 + i < t ? bf_ * __expf(Gt - gs[i]) * __uint_as_float(x[4 * i4 + i]) : 0.f;
                         }
                         *reinterpret_cast<float4 *>(lrow + blkidx(t >> 4, s0 >> 4) * kBS + (s0 & 15)) =
                             make_float4(l[0], l[1], l[2], l[3]);
@@ -536,11 +540,18 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     __syncthreads();
                 }
             }
-            // ---- the lower-left quadrant, 64 x 64: X_BA = -X_B (L_BA X_A), on the tensor cores ----
-            // products 2a are done first, so the state's bf16 tile is free; the
-            // T tile and the state tile hold the bf16 operands (rows 0..63; the A
-            // operands' rows 64..127 only feed output rows that are never read),
-            // TMEM columns 0..63 and 64..127 (free until U) the two products
+            // ---- T = X diag(b) as the bf16 tile of U = T R (rows t, columns s), its lower-left
+            //      quadrant on the tensor cores ----
+            // With L_BA = diag(b_B) M_BA, the quadrant of T is
+            //   T_BA = X_BA diag(b_A) = -X_B L_BA X_A diag(b_A) = -T_BB (M_BA T_AA):
+            // T_AA = X_A diag(b_A) and T_BB = X_B diag(b_B) go to their places in the
+            // T tile (the upper-right quadrant zero), M_BA to the state tile (free:
+            // products 2a are done); W = M_BA T_AA (T_AA read in place as the
+            // MN-major B operand) into TMEM columns 0..63, W back to the state tile,
+            // then T_BB W with the T tile's columns 64..127 as the A operand (its
+            // rows 0..63 are the zero quadrant), rows 64..127 of TMEM columns
+            // 64..127, negated into the lower-left quadrant.  Rows 64..127 of the
+            // first product's A operand only feed output rows that are never read.
             {
                 const bool zok = mbar_wait_bounded(c.bar, phase, kWait);
                 phase ^= 1u;
@@ -561,27 +572,40 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     f[0] = x0.x; f[1] = x0.y; f[2] = x0.z; f[3] = x0.w;
                     f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
                 };
-                const int er = tid >> 2, ec = (tid & 3) * 16;  // this thread's row and 16 columns of a 64 x 64 operand
-                // L_BA (A, K-major: rows m, columns k) into the T tile; X_A (B, MN-major: rows k, columns n) into the state tile
+                auto scale_b = [&](int col, float (&f)[8]) {
+                    const float4 b0 = *reinterpret_cast<const float4 *>(c.b + col);
+                    const float4 b1 = *reinterpret_cast<const float4 *>(c.b + col + 4);
+                    f[0] *= b0.x; f[1] *= b0.y; f[2] *= b0.z; f[3] *= b0.w;
+                    f[4] *= b1.x; f[5] *= b1.y; f[6] *= b1.z; f[7] *= b1.w;
+                };
+                const int er = tid >> 2, ec = (tid & 3) * 16;  // this thread's row and 16 columns of a 64 x 64 quadrant
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8) {
+                    const int cq = ec + h8;
                     float f[8];
-                    ld8f(64 + er, ec + h8, f);
-                    st8(c.tT + toff(er, ec + h8), f);
-                    ld8f(er, ec + h8, f);
-                    st8(c.tS + toff(er, ec + h8), f);
+                    ld8f(64 + er, cq, f);  // M_BA: A operand, K-major
+                    st8(c.tS + toff(er, cq), f);
+                    ld8f(er, cq, f);  // T_AA
+                    scale_b(cq, f);
+                    st8(c.tT + toff(er, cq), f);
+                    ld8f(64 + er, 64 + cq, f);  // T_BB
+                    scale_b(64 + cq, f);
+                    st8(c.tT + toff(64 + er, 64 + cq), f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+                    st8(c.tT + toff(er, 64 + cq), f);  // T_AB = 0
                 }
                 ok = run_mma(c, phase, [&] {
                     constexpr uint32_t id = idesc_bf16(128, 64, 0, 1);
                     for (int k16 = 0; k16 < 64; k16 += 16)
-                        mma_bf16(tA1, desc_sw128(smem_u32(c.tT) + k16 * 2, 16, 2048),
-                                 desc_sw128(smem_u32(c.tS) + (k16 / 8) * 2048, 1024, 2048), id, k16 > 0);
+                        mma_bf16(tA1, desc_sw128(smem_u32(c.tS) + k16 * 2, 16, 2048),
+                                 desc_sw128(smem_u32(c.tT) + (k16 / 8) * 2048, 1024, 2048), id, k16 > 0);
                 });
                 if (!ok) {
                     failed = true;
                     break;
                 }
-                // Y (rows 0..63 of TMEM columns 0..63) into the state tile as the B operand; X_B into the T tile
+                // W (rows 0..63 of TMEM columns 0..63) into the state tile as the B operand
                 if (quarter < 2) {
                     uint32_t x[32];
                     const int col0 = 32 * hc;
@@ -595,59 +619,29 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                         st8(c.tS + toff(erow, col0 + 8 * j8), f);
                     }
                 }
-#pragma unroll
-                for (int h8 = 0; h8 < 16; h8 += 8) {
-                    float f[8];
-                    ld8f(64 + er, 64 + ec + h8, f);
-                    st8(c.tT + toff(er, ec + h8), f);
-                }
                 ok = run_mma(c, phase, [&] {
                     constexpr uint32_t id = idesc_bf16(128, 64, 0, 1);
                     for (int k16 = 0; k16 < 64; k16 += 16)
-                        mma_bf16(tA1 + 64, desc_sw128(smem_u32(c.tT) + k16 * 2, 16, 2048),
+                        mma_bf16(tA1 + 64, desc_sw128(smem_u32(c.tT) + 1024 + k16 * 2, 16, 2048),
                                  desc_sw128(smem_u32(c.tS) + (k16 / 8) * 2048, 1024, 2048), id, k16 > 0);
                 });
                 if (!ok) {
                     failed = true;
                     break;
                 }
-                // X_BA = -(X_B Y) into the lower-left quadrant of the block storage
-                if (quarter < 2) {
+                // T_BA = -(T_BB W) into the lower-left quadrant of the T tile
+                if (quarter >= 2) {
                     uint32_t x[32];
                     const int col0 = 32 * hc;
                     tmem_ld32(tA1 + lb + 64 + col0, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const int n = col0 + 4 * j4;
-                        float *p = c.blk + blkidx((64 + erow) >> 4, n >> 4) * kBS + (erow & 15) * kRS + (n & 15);
-                        *reinterpret_cast<float4 *>(p) =
-                            make_float4(-__uint_as_float(x[4 * j4]), -__uint_as_float(x[4 * j4 + 1]),
-                                        -__uint_as_float(x[4 * j4 + 2]), -__uint_as_float(x[4 * j4 + 3]));
-                    }
-                }
-                fence_before();
-                __syncthreads();
-                fence_after();
-            }
-            // ---- T = X diag(b) as a bf16 tile (rows t, columns s; zero above the diagonal) ----
-            {
-                const int t = erow;
-                for (int s0 = 64 * hc; s0 < 64 * hc + 64; s0 += 8) {
-                    float f[8];
-                    if ((s0 >> 4) <= (t >> 4)) {
-                        const float *xr = c.blk + blkidx(t >> 4, s0 >> 4) * kBS + (t & 15) * kRS + (s0 & 15);
-                        const float4 x0 = *reinterpret_cast<const float4 *>(xr);
-                        const float4 x1 = *reinterpret_cast<const float4 *>(xr + 4);
-                        const float4 b0 = *reinterpret_cast<const float4 *>(c.b + s0);
-                        const float4 b1 = *reinterpret_cast<const float4 *>(c.b + s0 + 4);
-                        f[0] = x0.x * b0.x; f[1] = x0.y * b0.y; f[2] = x0.z * b0.z; f[3] = x0.w * b0.w;
-                        f[4] = x1.x * b1.x; f[5] = x1.y * b1.y; f[6] = x1.z * b1.z; f[7] = x1.w * b1.w;
-                    } else {
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        float f[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+                        for (int i = 0; i < 8; ++i) f[i] = -__uint_as_float(x[8 * j8 + i]);
+                        st8(c.tT + toff(erow, col0 + 8 * j8), f);
                     }
-                    st8(c.tT + toff(t, s0), f);
                 }
             }
             // ---- products 2b: U = T R ----
