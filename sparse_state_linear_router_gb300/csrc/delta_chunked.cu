@@ -481,63 +481,109 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 }
             }
             __syncthreads();
-            // ---- each 64-row half from its diagonal blocks: block columns from the right,
-            //      X[I][J] = -(sum_{K=J+1..I} X[I][K] L[K][J]) X[J][J] ----
-            // the two halves at once, 128 threads each; thread (rr, cc) holds
-            // elements (rr, cc) and (rr + 8, cc) of every block of column J.  For
-            // each K a column of L[K][J] stays in registers while the rows of the
-            // X blocks below it come in as 16-byte vectors; the sums Z_I gather in
-            // a scratch block per I, since L[I][J] is read until every Z is done
+            // ---- each 64-row half from its diagonal blocks D, by doubling ----
+            // (A) the four 32-row pairs: X[2p+1][2p] = -D[2p+1] (L[2p+1][2p] D[2p]);
+            // (B) in each half (blocks B0..B0+3) the 32 x 32 lower-left block:
+            //     X_BA = -X_B (L_BA X_A), X_A, X_B the pairs' 32-row inverses.
+            // Every stage keeps all 256 threads busy on a register tile of four
+            // columns (one or two rows), reading 16-byte vectors: the left
+            // factor's row and the right factor's rows; the intermediate products
+            // go to the scratch blocks.  The lower block storage of a pair (the
+            // one of X_A, X_B) is zero above its block diagonal, so those terms
+            // are skipped.
             {
-                const int B0 = 4 * (tid >> 7), rr = (tid >> 4) & 7, cc = tid & 15;
-                auto row_dot = [&](const float *row, const float (&col)[16]) {
-                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // four independent chains
+                auto ld4 = [&](const float *p) { return *reinterpret_cast<const float4 *>(p); };
+                auto fma4 = [&](float a, const float4 &x, float (&acc)[4]) {
+                    acc[0] = fmaf(a, x.x, acc[0]);
+                    acc[1] = fmaf(a, x.y, acc[1]);
+                    acc[2] = fmaf(a, x.z, acc[2]);
+                    acc[3] = fmaf(a, x.w, acc[3]);
+                };
+                // acc += row (16 values at lrow) times the 16 x 4 column strip at rcol (rows kRS apart)
+                // (all loads issued before the products: one round of shared-memory latency)
+                auto strip = [&](const float *lrow, const float *rcol, float (&acc)[4]) {
+                    float4 l[4], x[16];
+#pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) l[m4] = ld4(lrow + 4 * m4);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) x[m] = ld4(rcol + m * kRS);
 #pragma unroll
                     for (int m4 = 0; m4 < 4; ++m4) {
-                        const float4 x4 = *reinterpret_cast<const float4 *>(row + 4 * m4);
-                        a0 = fmaf(x4.x, col[4 * m4], a0);
-                        a1 = fmaf(x4.y, col[4 * m4 + 1], a1);
-                        a2 = fmaf(x4.z, col[4 * m4 + 2], a2);
-                        a3 = fmaf(x4.w, col[4 * m4 + 3], a3);
+                        fma4(l[m4].x, x[4 * m4], acc);
+                        fma4(l[m4].y, x[4 * m4 + 1], acc);
+                        fma4(l[m4].z, x[4 * m4 + 2], acc);
+                        fma4(l[m4].w, x[4 * m4 + 3], acc);
                     }
-                    return (a0 + a1) + (a2 + a3);
                 };
-                float *z0 = c.zs + rr * kRS + cc;  // this thread's elements of scratch block I: z0[I kBS], z0[I kBS + 8 kRS]
+                // the same for two rows sharing the strip (each strip vector read once)
+                auto strip2 = [&](const float *lrow0, const float *lrow1, const float *rcol, float (&acc0)[4],
+                                  float (&acc1)[4]) {
+                    float4 l0[4], l1[4], x[16];
 #pragma unroll
-                for (int J = 2; J >= 0; --J) {
-                    float za[4][2];  // this thread's two elements of Z_I, I = J+1..3
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        l0[m4] = ld4(lrow0 + 4 * m4);
+                        l1[m4] = ld4(lrow1 + 4 * m4);
+                    }
 #pragma unroll
-                    for (int K = J + 1; K < 4; ++K) {
-                        float lcol[16];
-                        const float *lc = c.blk + blkidx(B0 + K, B0 + J) * kBS + cc;
+                    for (int m = 0; m < 16; ++m) x[m] = ld4(rcol + m * kRS);
 #pragma unroll
-                        for (int m = 0; m < 16; ++m) lcol[m] = lc[m * kRS];
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        const float a0[4] = {l0[m4].x, l0[m4].y, l0[m4].z, l0[m4].w};
+                        const float a1[4] = {l1[m4].x, l1[m4].y, l1[m4].z, l1[m4].w};
 #pragma unroll
-                        for (int I = K; I < 4; ++I) {
-                            const float *xb = c.blk + blkidx(B0 + I, B0 + K) * kBS + rr * kRS;
-                            const float d0 = row_dot(xb, lcol), d1 = row_dot(xb + 8 * kRS, lcol);
-                            za[I][0] = K == J + 1 ? d0 : za[I][0] + d0;
-                            za[I][1] = K == J + 1 ? d1 : za[I][1] + d1;
+                        for (int i = 0; i < 4; ++i) {
+                            fma4(a0[i], x[4 * m4 + i], acc0);
+                            fma4(a1[i], x[4 * m4 + i], acc1);
                         }
                     }
+                };
+                auto st4 = [&](float *p, const float (&v)[4], float sgn) {
+                    *reinterpret_cast<float4 *>(p) = make_float4(sgn * v[0], sgn * v[1], sgn * v[2], sgn * v[3]);
+                };
+                {
+                    // (A) thread: pair P, row rr, columns 4 c4 .. 4 c4 + 3
+                    const int P = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+                    float *lo = c.blk + blkidx(2 * P + 1, 2 * P) * kBS;
+                    float *w = c.zs + P * kBS;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    strip(lo + rr * kRS, c.blk + blkidx(2 * P, 2 * P) * kBS + c4, acc);  // L D[2p]
+                    st4(w + rr * kRS + c4, acc, 1.f);
+                    __syncthreads();
+                    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+                    strip(c.blk + blkidx(2 * P + 1, 2 * P + 1) * kBS + rr * kRS, w + c4, acc2);  // D[2p+1] W
+                    st4(lo + rr * kRS + c4, acc2, -1.f);
+                    __syncthreads();
+                }
+                {
+                    // (B) thread: half h, rows r of blocks B0+2 and B0+3, columns cj .. cj+3
+                    // of block column B0 + jb (a warp shares jb)
+                    const int h2 = tid >> 7, u = tid & 127, r = u & 15, c4 = u >> 4, jb = c4 >> 2, cj = (c4 & 3) * 4;
+                    const int B0 = 4 * h2;
+                    float *w = c.zs + 4 * h2 * kBS;  // W[i][j], i, j in {0, 1}: block 2 i + j
+                    {
+                        float a2[4] = {0.f, 0.f, 0.f, 0.f}, a3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int I = J + 1; I < 4; ++I) {
-                        z0[(B0 + I) * kBS] = za[I][0];
-                        z0[(B0 + I) * kBS + 8 * kRS] = za[I][1];
-                    }
-                    __syncthreads();  // every Z of column J is complete and every read of L[K][J] done
-                    float xcol[16];
-                    const float *xd = c.blk + blkidx(B0 + J, B0 + J) * kBS + cc;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) xcol[m] = xd[m * kRS];
-#pragma unroll
-                    for (int I = J + 1; I < 4; ++I) {
-                        float *xo = c.blk + blkidx(B0 + I, B0 + J) * kBS + rr * kRS + cc;
-                        const float *zr = c.zs + (B0 + I) * kBS + rr * kRS;
-                        xo[0] = -row_dot(zr, xcol);
-                        xo[8 * kRS] = -row_dot(zr + 8 * kRS, xcol);
+                        for (int kb = 0; kb < 2; ++kb) {
+                            if (kb < jb) continue;  // X_A's block (0, 1) is zero
+                            strip2(c.blk + blkidx(B0 + 2, B0 + kb) * kBS + r * kRS,
+                                   c.blk + blkidx(B0 + 3, B0 + kb) * kBS + r * kRS,
+                                   c.blk + blkidx(B0 + kb, B0 + jb) * kBS + cj, a2, a3);
+                        }
+                        st4(w + jb * kBS + r * kRS + cj, a2, 1.f);
+                        st4(w + (2 + jb) * kBS + r * kRS + cj, a3, 1.f);
                     }
                     __syncthreads();
+                    {
+                        // X_B's block (0, 1) is zero: row block 2 takes W[0] only
+                        float a2[4] = {0.f, 0.f, 0.f, 0.f}, a3[4] = {0.f, 0.f, 0.f, 0.f};
+                        const float *w0 = w + jb * kBS + cj, *w1 = w + (2 + jb) * kBS + cj;
+                        strip2(c.blk + blkidx(B0 + 2, B0 + 2) * kBS + r * kRS,
+                               c.blk + blkidx(B0 + 3, B0 + 2) * kBS + r * kRS, w0, a2, a3);
+                        strip(c.blk + blkidx(B0 + 3, B0 + 3) * kBS + r * kRS, w1, a3);
+                        st4(c.blk + blkidx(B0 + 2, B0 + jb) * kBS + r * kRS + cj, a2, -1.f);
+                        st4(c.blk + blkidx(B0 + 3, B0 + jb) * kBS + r * kRS + cj, a3, -1.f);
+                    }
+                    // read by the quadrant after its first barrier
                 }
             }
             // ---- T = X diag(b) as the bf16 tile of U = T R (rows t, columns s), its lower-left
