@@ -79,7 +79,7 @@ struct DSmem {
     float *blk, *zs;
     int *tok, *slotj;
     float *G, *b, *qf, *ec, *red, *patch;
-    uint32_t bar;
+    uint32_t bar, bar2;  // the products' mbarrier; the one of Q K^T (waited for a few phases later)
     uint32_t *tslot;
     int *item;
 };
@@ -103,22 +103,28 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     c.patch = reinterpret_cast<float *>(c.tT);  // [8 warps][32][kPatchStride] in the T / P tile
     uint64_t *bar = reinterpret_cast<uint64_t *>(c.red + 8);
     c.bar = smem_u32(bar);
-    c.tslot = reinterpret_cast<uint32_t *>(bar + 1);
+    c.bar2 = smem_u32(bar + 1);
+    c.tslot = reinterpret_cast<uint32_t *>(bar + 2);
     c.item = reinterpret_cast<int *>(c.tslot + 1);
     return c;
 }
 constexpr size_t delta_smem_bytes() {
-    return 1024 + 5 * (size_t)kTile + (size_t)(kNBlk + kNB) * kBS * 4 + 2 * kRows * 4 + 4 * kRows * 4 + 8 * 4 + 16 +
+    return 1024 + 5 * (size_t)kTile + (size_t)(kNBlk + kNB) * kBS * 4 + 2 * kRows * 4 + 4 * kRows * 4 + 8 * 4 + 24 +
            16;
 }
 
-// One elected thread issues the products, commits them to the CTA's mbarrier
-// and every thread runs `during` (work that touches neither the products'
-// operands nor their results) and then waits (bounded).  Shared-memory
-// operands written by the generic proxy before the call are made visible to
-// the tensor core first.  Returns false, in every thread, when the wait ran out.
+// One elected thread (kIssuer: every product and commit of the CTA comes
+// from it, and it is outside the row-metadata warps, so that its issue -- which
+// waits while the tensor core's queue is full -- delays no other work) issues
+// the products and commits them to the CTA's mbarrier; every thread runs
+// `during` (work that touches neither the products' operands nor their
+// results; false = a failed wait of its own) and then waits (bounded).
+// Shared-memory operands written by the generic proxy before the call are
+// made visible to the tensor core first.  Returns false, in every thread, when
+// a wait ran out.
+constexpr int kIssuer = 128;
 struct NoWork {
-    __device__ void operator()() const {}
+    __device__ bool operator()() const { return true; }
 };
 template <typename F, typename D = NoWork>
 __device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue, bool withhold = false,
@@ -126,14 +132,14 @@ __device__ __forceinline__ bool run_mma(const DSmem &c, uint32_t &phase, F issue
     fence_proxy_async();
     fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && !withhold) {
+    if (threadIdx.x == kIssuer && !withhold) {
         fence_after();
         issue();
         commit(c.bar);
     }
     __syncwarp();
-    during();
-    const bool ok = mbar_wait_bounded(c.bar, phase, kWait);
+    const bool dok = during();
+    const bool ok = mbar_wait_bounded(c.bar, phase, kWait) && dok;
     phase ^= 1u;
     fence_after();
     return __syncthreads_and(ok) != 0;
@@ -192,6 +198,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
     if (warp == 0) tmem_alloc(smem_u32(c.tslot), 512);
     if (tid == 0) {
         mbar_init(c.bar, 1);
+        mbar_init(c.bar2, 1);
         mbar_fence_init();
     }
     fence_before();
@@ -199,8 +206,8 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
     fence_after();
     const uint32_t tmem = *c.tslot;
     const uint32_t tA1 = tmem, tA2 = tmem + 128, tO = tmem + 256, tSt = tmem + 384;
-    uint32_t phase = 0;
-    bool failed = false;
+    uint32_t phase = 0, phase2 = 0;
+    bool failed = false, a2pend = false;  // a2pend: a chunk's Q K^T committed and not yet waited for
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q), *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *qs = static_cast<const __nv_bfloat16 *>(a.qs), *ks = static_cast<const __nv_bfloat16 *>(a.ks);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
@@ -361,7 +368,8 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 tmem_wait_st();
             }
             cp_async_wait_all();
-            // ---- products 1: A1 = K K^T, A2 = Q K^T, Y = K S0 ----
+            // ---- products 1: A1 = K K^T, Y = K S0, waited for now; A2 = Q K^T on the second
+            //      mbarrier, waited for before the P pass (the raw Q tile stays untouched) ----
 #ifdef SSE_FAULT_INJECT
             const bool withhold = g_delta_fault_mode == 1 && blockIdx.x == 0 && first_chunk;
             first_chunk = false;
@@ -374,20 +382,30 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
                     mma_bf16(tA1, desc_sw128(smem_u32(c.tK) + ko, 16, 2048), desc_sw128(smem_u32(c.tK) + ko, 16, 2048),
                              idT, k16 > 0);
-                    mma_bf16(tA2, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tK) + ko, 16, 2048),
-                             idT, k16 > 0);
                     mma_bf16(tO, desc_sw128(smem_u32(c.tK) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
                              idS, k16 > 0);
                 }
             }, withhold, [&] {
                 if (ch + 1 < nch) fetch_rest(ch + 1);  // uses the record fetched a chunk ago
                 if (ch + 2 < nch) fetch_rec(ch + 2);
+                return true;
             });
+            if (ok && tid == kIssuer && !withhold) {  // A2, queued behind nothing: it runs under the pass below
+                fence_after();
+                constexpr uint32_t idT = idesc_bf16(128, 128, 0, 0);
+                for (int k16 = 0; k16 < kC; k16 += 16) {
+                    const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2;
+                    mma_bf16(tA2, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tK) + ko, 16, 2048),
+                             idT, k16 > 0);
+                }
+                commit(c.bar2);
+            }
+            a2pend = ok && !withhold;
             if (!ok) {
                 failed = true;
                 break;
             }
-            // ---- L blocks from A1; R = V - gamma Y in place of V; Q scaled by qf gamma in place ----
+            // ---- L blocks from A1; R = V - gamma Y in place of V; Q scaled by qf gamma into the T tile ----
             const float Gm = c.G[kMidRow];
             const bool fac = c.red[7] == 0.f;  // every |G - G_m| of the chunk within kFacRange (uniform)
             {
@@ -439,11 +457,10 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] -= gt * __uint_as_float(x[8 * j8 + i]);
                         st8(pv, f);
-                        unsigned char *pq = c.tQ + toff(t, col0 + 8 * j8);
-                        ld8(pq, f);
+                        ld8(c.tQ + toff(t, col0 + 8 * j8), f);
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[i] *= qg;
-                        st8(pq, f);
+                        st8(c.tT + toff(t, col0 + 8 * j8), f);
                     }
                 }
             }
@@ -451,12 +468,12 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
             fence_proxy_async();
             fence_before();
             __syncthreads();
-            if (tid == 0) {
+            if (tid == kIssuer) {
                 fence_after();
                 constexpr uint32_t idS = idesc_bf16(128, kD, 0, 1);
                 for (int k16 = 0; k16 < kC; k16 += 16) {
                     const uint32_t ko = (k16 / 64) * 1024 + (k16 % 64) * 2, ro = (k16 / 8) * 2048;
-                    mma_bf16(tO, desc_sw128(smem_u32(c.tQ) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
+                    mma_bf16(tO, desc_sw128(smem_u32(c.tT) + ko, 16, 2048), desc_sw128(smem_u32(c.tS) + ro, 1024, 2048),
                              idS, k16 > 0);
                 }
                 commit(c.bar);
@@ -698,6 +715,13 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     mma_bf16(tA1, desc_sw128(smem_u32(c.tT) + ko, 16, 2048), desc_sw128(smem_u32(c.tV) + ro, 1024, 2048),
                              idS, k16 > 0);
                 }
+            }, false, [&] {  // A2 = Q K^T (long done by now) for the P pass below
+                const bool a2ok = mbar_wait_bounded(c.bar2, phase2, kWait);
+                if (a2ok) {
+                    phase2 ^= 1u;
+                    a2pend = false;
+                }
+                return a2ok;
             });
             if (!ok) {
                 failed = true;
@@ -821,6 +845,7 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
         fence_after();
     }
     if (failed) cp_async_wait_all();  // no copy may still be writing shared memory when the CTA exits
+    if (failed && a2pend) (void)mbar_wait_bounded(c.bar2, phase2, kWait);  // nor a product TMEM when it is freed
     if (failed && tid == 0) atomicOr(flags, SSE_DEVICE_TIMEOUT);
     __syncthreads();
     if (warp == 0) {
