@@ -122,7 +122,7 @@ constexpr size_t delta_smem_bytes() {
 // Shared-memory operands written by the generic proxy before the call are
 // made visible to the tensor core first.  Returns false, in every thread, when
 // a wait ran out.
-constexpr int kIssuer = 128;
+constexpr int kIssuer = 144;  // warp 4, lane 16
 struct NoWork {
     __device__ bool operator()() const { return true; }
 };
@@ -478,8 +478,9 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                 }
                 commit(c.bar);
             }
-            // ---- the inverse of I + L: diagonal blocks, one warp each ----
-            {
+            // ---- the inverse of I + L: diagonal blocks, one warp each (lanes 0..15, one
+            //      column each; lane 16 of warp 4 is the issuer, still queueing products 2a) ----
+            if (lane < 16) {
                 float *bd = c.blk + blkidx(warp, warp) * kBS;
                 float x[16];  // column `lane` of the block's inverse
 #pragma unroll
@@ -491,11 +492,9 @@ delta_chunked_kernel(DeltaArgs a, int32_t H, int32_t N, int32_t topk, int32_t us
                     for (int kk = 0; kk < r; ++kk) acc = fmaf(bd[r * kRS + kk], x[kk], acc);
                     if (r > lane) x[r] = -acc;  // rows above the diagonal keep 0, the diagonal 1
                 }
-                __syncwarp();
-                if (lane < 16) {
+                __syncwarp(0x0000ffffu);  // every read of the block's L is done
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) bd[r * kRS + lane] = x[r];
-                }
+                for (int r = 0; r < 16; ++r) bd[r * kRS + lane] = x[r];
             }
             __syncthreads();
             // ---- each 64-row half from its diagonal blocks D, by doubling ----
