@@ -397,15 +397,27 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
     const int64_t total = rows * per_row;
     const T *sq = static_cast<const T *>(a.dq_c), *sk = static_cast<const T *>(a.dk_c);
     const T *sv = static_cast<const T *>(a.dv_c);
+    // (row, part) of element x: 32-bit unsigned division when every index fits,
+    // a 64-bit one (emulated, several times slower) otherwise
+    const bool idx32 = total <= (int64_t)0xffffffffu;
     for (int64_t x = gid; x < total; x += stride) {
-        const int64_t row = x / per_row;
-        const int part = (int)(x - row * per_row);
+        int64_t row;
+        uint32_t part;
+        if (idx32) {
+            const uint32_t xr = (uint32_t)x, r32 = xr / (uint32_t)per_row;
+            row = r32;
+            part = xr - r32 * (uint32_t)per_row;
+        } else {
+            row = x / per_row;
+            part = (uint32_t)(x - row * per_row);
+        }
         const T *src = nullptr;  // dq, dk, dv slots (I/O type); dg slots are float32
         T *dst;
         int width, cidx, hi;  // slots 0 .. hi - 1 summed
-        const int kind = part < 4 * cg ? part / cg : 4;
+        const uint32_t ucg = (uint32_t)cg;
+        const int kind = part < 4 * ucg ? (int)(part / ucg) : 4;
         if (kind < 4) {
-            cidx = G * (part % cg);
+            cidx = G * (int)(part % ucg);
             width = c;
             // 0: dq (routed slots, plus the shared slot unless q_shared is separate),
             // 1: dk (likewise), 2: dg (all slots), 3: dq_shared / dk_shared
@@ -426,7 +438,7 @@ backward_combine_kernel(BackwardArgs a, int64_t rows, int32_t c, int32_t d, int3
                 continue;
             }
         } else {
-            cidx = G * (part - 4 * cg);
+            cidx = G * (int)(part - 4 * ucg);
             width = d;
             src = sv;
             dst = static_cast<T *>(a.dv);
