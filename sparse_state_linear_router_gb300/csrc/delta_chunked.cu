@@ -19,16 +19,21 @@
 //   U = T R,  T = (I + L)^-1 diag(b),  R = V - diag(gamma) (K S0);
 //   O = diag(qf gamma) Q S0 + (tril(Q K^T) . Gamma . qf) U;
 //   S_end = gamma_last S0 + (diag(gamma_last / gamma) K)^T U.
-// Per chunk: three rounds of tcgen05 products (K K^T, Q K^T, K S0; then
-// (qf gamma Q) S0 and T R; then P U and the state update), the inverse of
-// I + L in float32 on the CUDA cores (16 x 16 blocks: the diagonal blocks by
-// forward substitution, one warp each; each 64-row half by its block columns
-// from the right; the lower-left quadrant as -X_B (L_BA X_A), two 64 x 64
-// products on the tensor cores), and the passes between them over TMEM rows.  The state stays in
-// TMEM in float32 for the whole item; its bf16 copy is the operand of K S0
-// and Q S0.  Read-outs go to bf16 partial slots ([T, H, k, d] and [T, H, d],
-// the layout of the token-serial kernels' float32 ones) that launch_combine
-// sums in float32.
+// Per chunk, tcgen05 products (K K^T and K S0; Q K^T, waited for later;
+// (qf gamma Q) S0; the lower-left quadrant of T; T R; then P U and the state
+// update), all issued by one thread, and between them passes over TMEM rows
+// and the inverse X of I + L in float32 on the CUDA cores: the diagonal
+// 16 x 16 blocks D by forward substitution, each 64-row half by doubling
+// (X_10 = -D_1 L_10 D_0 for the four 32-row pairs, then -X_B L_BA X_A for
+// each half's 32 x 32 lower-left block).  T = X diag(b) is built as a bf16
+// tile whose lower-left 64 x 64 quadrant is -T_BB (M_BA T_AA), M = L without
+// its row factor b, two products on the tensor cores.  Gamma_ts is formed as
+// exp(G_t - G_m) exp(G_m - G_s) around the chunk's midpoint row m when that
+// stays within float32, else per element.  The state stays in TMEM in
+// float32 for the whole item; its bf16 copy is the operand of K S0 and Q S0.
+// Read-outs go to bf16 partial slots ([T, H, k, d] and [T, H, d], the layout
+// of the token-serial kernels' float32 ones) that launch_combine sums in
+// float32.
 #include <algorithm>
 
 #include "chunk_tiles.cuh"
@@ -70,8 +75,8 @@ constexpr uint64_t kWait = 2000000000ull;
 __device__ __forceinline__ int blkidx(int I, int K) { return I * (I + 1) / 2 + K; }
 
 // Shared memory: five operand tiles from a 1024-aligned base, the lower
-// blocks of I + L (then of its inverse) and a scratch block per block row for
-// the inverse's sums, per-row metadata, the mbarrier and
+// blocks of I + L (then of its inverse), eight scratch blocks for the
+// inverse's intermediate products, per-row metadata, the mbarrier and
 // the TMEM address slot.  The warps' store patches of the read-out use the
 // T / P tile, free by then (the next chunk's rows are landing in Q, K, V).
 struct DSmem {
@@ -92,7 +97,7 @@ __device__ __forceinline__ DSmem carve(unsigned char *raw) {
     c.tS = sm + 3 * kTile;
     c.tT = sm + 4 * kTile;
     c.blk = reinterpret_cast<float *>(sm + 5 * kTile);  // [kNBlk][kBS]
-    c.zs = c.blk + kNBlk * kBS;                          // [kNB][kBS] sums of the block inverse
+    c.zs = c.blk + kNBlk * kBS;                          // [kNB][kBS] products inside the doubling stages
     c.tok = reinterpret_cast<int *>(c.zs + kNB * kBS);
     c.slotj = c.tok + kRows;
     c.G = reinterpret_cast<float *>(c.slotj + kRows);
