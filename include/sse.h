@@ -287,8 +287,9 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
  * Forward, two computations chosen by cfg->algo:
  *  - chunked (every algo but SSE_ALGO_RECURRENT; bf16, c = d = 128): chunks
  *    of 128 rows on the tensor cores -- the chunk's write strengths solved as
- *    a unit lower-triangular system (its inverse in float32), bf16 operands,
- *    float32 accumulation and a float32 state held on chip for each segment;
+ *    a unit lower-triangular system (its inverse in float32 up to 64-row
+ *    blocks, the rest by bf16 tensor-core products), bf16 operands, float32
+ *    accumulation and a float32 state held on chip for each segment;
  *  - token by token in float32 on the CUDA cores (SSE_ALGO_RECURRENT and every
  *    other shape).
  * The decode step is token by token in float32.  Read-outs are summed per
