@@ -78,6 +78,33 @@ def test_delta_forward_matches_oracle(name, algo):
     assert H_.max_abs_rel(gpu["final_state"], ref["final_state"]) < tol
 
 
+def test_delta_full_size_sampled_pairs():
+    """The layer shape the benchmark times (8 x 4096 tokens, H16, c = d = 128,
+    N8, top-2, shared, random initial states) in one call of the chunked form;
+    the oracle recomputes a sample of (sequence, head) pairs, each from its own
+    slice of the inputs (heads and sequences are independent), and the routing
+    of those rows is compared exactly."""
+    import dataclasses
+    w = synth.WORKLOADS["layer_bf16"]
+    inp = synth.make_delta_inputs(w, seed=11, with_init=True)
+    gpu = _gpu(w, inp)
+    S, H = len(inp.cu_seqlens) - 1, w.num_heads
+    rng = np.random.default_rng(321)
+    pairs = sorted(set(rng.choice(S * H, size=3, replace=False).tolist()) | {S * H - 1})
+    for p in pairs:
+        b, h = divmod(int(p), H)
+        t0, t1 = int(inp.cu_seqlens[b]), int(inp.cu_seqlens[b + 1])
+        sub = dataclasses.replace(
+            inp, q=inp.q[t0:t1, h:h + 1], k=inp.k[t0:t1, h:h + 1], v=inp.v[t0:t1, h:h + 1],
+            log_alpha=inp.log_alpha[t0:t1, h:h + 1], beta=inp.beta[t0:t1, h:h + 1],
+            logits=inp.logits[t0:t1, h:h + 1], cu_seqlens=np.array([0, t1 - t0], dtype=np.int32),
+            init_state=inp.init_state[b:b + 1, h:h + 1])
+        ref = _ref(w, sub)
+        assert np.array_equal(gpu["topk_idx"][t0:t1, h], ref["topk_idx"][:, 0])
+        assert H_.max_abs_rel(gpu["out"][t0:t1, h], ref["out"][:, 0]) < H_.TOL_BF16
+        assert H_.max_abs_rel(gpu["final_state"][b, h], ref["final_state"][0, 0]) < H_.TOL_BF16
+
+
 @pytest.mark.parametrize("algo", ["auto", "recurrent"])
 def test_delta_forward_strong_and_mild_decay(algo):
     """Chunks whose summed log-decay spans more than 60 either side of their
