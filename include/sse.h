@@ -352,8 +352,8 @@ sse_status_t sse_front_end(const sse_config_t *cfg, int32_t hidden, int64_t tota
                            void *workspace, size_t workspace_bytes, sse_stream_t stream);
 
 /* Device-side status bits (bit mask), written by the kernels into the first
- * word of the workspace of sse_forward and sse_front_end (each call clears
- * them first).
+ * word of the workspace of sse_forward, sse_backward, sse_delta_forward and
+ * sse_front_end (each call clears them first).
  *   SSE_DEVICE_TIMEOUT      error: a bounded wait on the tensor-core pipeline
  *                           expired; the affected segments stopped early and
  *                           the call's results are invalid
@@ -363,8 +363,8 @@ sse_status_t sse_front_end(const sse_config_t *cfg, int32_t hidden, int64_t tota
  *                           (results valid) */
 enum { SSE_DEVICE_TIMEOUT = 2, SSE_DEVICE_RECOMPUTED = 4 };
 
-/* Reads the device-status bits of the last sse_forward or sse_front_end that
- * used `workspace`.  Synchronizes `stream`.  *flags receives the bit mask.
+/* Reads the device-status bits of the last sse_forward, sse_backward,
+ * sse_delta_forward or sse_front_end that used `workspace`.  Synchronizes `stream`.  *flags receives the bit mask.
  * Returns SSE_ERR_DEVICE_TIMEOUT if the timeout bit is set, SSE_ERR_DEVICE for
  * any other error bit, SSE_OK otherwise (informational bits included), and
  * SSE_ERR_CUDA if the copy fails. */

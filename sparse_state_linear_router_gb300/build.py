@@ -18,7 +18,7 @@ LIB = os.path.join(BUILD, "libsse.so")
 # that withholds one barrier arrival or one product round), linked with the
 # same objects as libsse.so otherwise.
 LIB_CHECKED = os.path.join(BUILD, "libsse_checked.so")
-CHECKED_SRCS = ("fwd_chunked.cu", "delta_chunked.cu")
+CHECKED_SRCS = ("fwd_chunked.cu", "delta_chunked.cu", "backward_chunked.cu")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -57,7 +57,18 @@ constexpr int kThr = 256;          // 8 warps: two per TMEM lane quarter
 constexpr uint32_t kTile = 128 * 256;
 static_assert(kThr - kRows == kKey, "the upper half of the CTA writes one chunk total per column");
 constexpr float kRange = 64.f;     // largest |G_m| and |G_l - G_m| the factorised form takes
+#ifdef SSE_FAULT_INJECT
+// Checked build (libsse_checked.so, for the failure-detection test only):
+// every bounded wait gives up after 50 ms, and g_bwd_fault_mode = 1 makes
+// CTA 0 of the gradient kernel issue neither the first product round of its
+// first chunk nor its commit, so that the wait on it runs out and the kernel
+// takes its abort path (SSE_DEVICE_TIMEOUT, TMEM freed) with no product in
+// flight.
+__device__ int g_bwd_fault_mode = 0;
+constexpr uint64_t kWait = 50000000ull;
+#else
 constexpr uint64_t kWait = 2000000000ull;
+#endif
 
 // The work item and chunk of global chunk index `chunk` (items own the
 // chunk-padded row ranges pad_off[u] .. pad_off[u + 1]).  Returns false past
@@ -177,16 +188,17 @@ __device__ __forceinline__ void chunk_meta(const BackwardArgs &a, const ChunkRef
     }
 }
 
-// One elected thread issues the products through `issue`, commits them to the
-// CTA's mbarrier and every thread waits (bounded).  Shared-memory operands
-// written by the generic proxy before the call are made visible to the tensor
-// core first.  Returns false, in every thread, when the wait ran out.
+// One elected thread issues the products through `issue` (unless `withhold`:
+// the checked build's fault switch), commits them to the CTA's mbarrier and
+// every thread waits (bounded).  Shared-memory operands written by the
+// generic proxy before the call are made visible to the tensor core first.
+// Returns false, in every thread, when the wait ran out.
 template <typename F>
-__device__ __forceinline__ bool run_mma(const ChunkSmem &c, uint32_t &phase, F issue) {
+__device__ __forceinline__ bool run_mma(const ChunkSmem &c, uint32_t &phase, F issue, bool withhold = false) {
     fence_proxy_async();
     fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !withhold) {
         fence_after();
         issue();
         commit(c.bar);
@@ -458,6 +470,9 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
     const int quarter = warp & 3, hc = warp >> 2, erow = 32 * quarter + lane;
     const uint32_t lb = (uint32_t)(32 * quarter) << 16;
     bool failed = false;
+#ifdef SSE_FAULT_INJECT
+    bool first_chunk = true;  // of this CTA (the checked build's fault switch)
+#endif
     // metadata and row staging of chunk n + 1 are issued once chunk n's last
     // products are done (every tile free), before its read-out
     auto stage = [&](const ChunkRef &r, int mb) {
@@ -506,6 +521,12 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
             a.redo_list[atomicAdd(a.flags + 1, 1)] = r.item;
         }
         // products 1: A = Qt Kt^T, P = dO V^T
+#ifdef SSE_FAULT_INJECT
+        const bool withhold = g_bwd_fault_mode == 1 && blockIdx.x == 0 && first_chunk;
+        first_chunk = false;
+#else
+        const bool withhold = false;
+#endif
         bool ok = run_mma(c, phase, [&] {
             constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
             for (int k16 = 0; k16 < kKey; k16 += 16) {
@@ -518,7 +539,7 @@ bwd_chunk_grads_kernel(BackwardArgs a, int32_t H, int32_t N, int32_t topk, int32
                 mma_bf16(tmem + 128, desc_sw128(smem_u32(tD) + ko, 16, 2048), desc_sw128(smem_u32(tV) + ko, 16, 2048),
                          id, k16 > 0);
             }
-        });
+        }, withhold);
         if (!ok) {
             failed = true;
             break;
@@ -827,3 +848,12 @@ cudaError_t launch_backward_chunked(const sse_config_t &cfg, const BackwardArgs 
 }
 
 }  // namespace sse
+
+#ifdef SSE_FAULT_INJECT
+// Checked build only: sets the fault mode read by bwd_chunk_grads_kernel (0 =
+// none, 1 = CTA 0 withholds its first product round).  Returns the CUDA error
+// of the copy.
+extern "C" int sse_debug_set_bwd_fault(int mode) {
+    return (int)cudaMemcpyToSymbol(sse::g_bwd_fault_mode, &mode, sizeof(int));
+}
+#endif

@@ -338,7 +338,8 @@ struct BackwardLayout {
     __nv_bfloat16 *ustate, *wgrad;
     float *gamma, *gml, *gscratch, *fterm, *dgtot;
     void *sp_tiles, *dsp_tiles;
-    int32_t *marks, *redo_list, *flags;
+    int32_t *marks, *redo_list;
+    int32_t *flags;  // status words first (sse_read_device_status reads word 0), both forms
     size_t bytes;
 };
 
@@ -350,6 +351,7 @@ bool use_chunked_backward(const sse_config_t &c) {
 BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_t S) {
     Carver cv(ws);
     BackwardLayout L{};
+    L.flags = cv.take<int32_t>(64);
     L.chunked = use_chunked_backward(c);
     L.rb = carve_route(cv, c, T, S, nullptr, nullptr, nullptr, nullptr, true, true, L.chunked);
     if (L.chunked) {
@@ -369,7 +371,6 @@ BackwardLayout carve_backward(void *ws, const sse_config_t &c, int64_t T, int32_
         L.fterm = cv.take<float>(nitems * kc);
         L.marks = cv.take<int32_t>(nitems);
         L.redo_list = cv.take<int32_t>(nitems);
-        L.flags = cv.take<int32_t>(64);
     }
     const size_t slots = (size_t)T * c.num_heads * (c.top_k + c.use_shared);
     const size_t esz = c.dtype == SSE_BF16 ? 2 : 4;
@@ -421,6 +422,7 @@ sse_status_t sse_backward(const sse_config_t *cfg, const void *q, const void *k,
     if (num_seqs == 0) return SSE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     BackwardLayout L = carve_backward(workspace, c, total_tokens, num_seqs);
+    if (cudaMemsetAsync(L.flags, 0, 64 * sizeof(int32_t), s) != cudaSuccess) return SSE_ERR_CUDA;
     cudaError_t e = sse::launch_route(c, router_logits, cu_seqlens, num_seqs, total_tokens, L.rb, true, s);
     if (e != cudaSuccess) return SSE_ERR_CUDA;
     sse::BackwardArgs a{};
